@@ -1,0 +1,273 @@
+/*
+ * mnb_oracle.c -- the CPU oracle for the block-quantized MatMulNBits product
+ * with an optional rank-r LoRA term.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or calls
+ * this file: only the tests, the package smoke check and the benchmark's
+ * CPU-baseline leg do.  It shares no code, header, table or helper with the
+ * CUDA library.
+ *
+ * What it computes is the plain definition, written out step by step, in
+ * IEEE binary64 ("fp64") so that every intermediate that is exact in the
+ * definition is exact here too:
+ *
+ *   w[n,k] = (q[n,k] - zp[n, k/bs]) * scale[n, k/bs]                  (dequant)
+ *   t[m,r] = sum_k x[m,k] * A[k,r]                                     (LoRA down)
+ *   y[m,n] = sum_k x[m,k] * w[n,k]  +  sum_r t[m,r] * B[n,r]           (base + LoRA up)
+ *   Y[m,n] = fp16_round_to_nearest_even(y[m,n])
+ *
+ * Sources, cited by page title and section:
+ *  - "[WebGPU] Fuse rank-32 quantized LoRA with MatMulNBits" (onnxruntime pull
+ *    request 33370), commit message that adds the opt-in MatMulNBitsLoRA
+ *    operator: INT4 / block-32 base weights, FP16 rank-32 adapters, the output
+ *    is base + T * Bt^T with T = X * A, an empty adapter runs the base
+ *    projection only, B is read in its transposed [N, r] layout.
+ *  - Same page, "Description": the fused operator covers the base projection,
+ *    the LoRA down and up projections and the residual addition.
+ *  - "Fuse DQ->MatMulNBits for shared initializers and skip outer-scope
+ *    weights" (onnxruntime pull request 33800), "Description" and the repro
+ *    under "Motivation and Context": DequantizeLinear(w_q, w_scale, w_zp)
+ *    followed by MatMul is the computation MatMulNBits replaces, i.e. the
+ *    dequant map is (q - zp) * scale and the weight is used transposed.
+ *
+ * Readings where the pages leave a step open (each is listed in the design doc):
+ *  - INT4 packing: two 4-bit codes per byte along K; element k = 2j sits in
+ *    the low nibble (bits 0..3) of byte j of the block, k = 2j + 1 in the
+ *    high nibble.  INT8: one code per byte.
+ *  - Zero points: one unsigned byte per (row, block), used as given; when no
+ *    array is passed the default is 2^(bits-1) (8 for INT4, 128 for INT8).
+ *  - T is kept exact (fp64) here; the fused GPU path rounds T to FP16 as the
+ *    pages do.  mnb_ref_run can also round T first (round_t = 1).
+ *
+ * Everything is plain loops; OpenMP only splits independent output rows.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------------
+ * IEEE 754 binary16 <-> binary64, written from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits; exponent field 0
+ * holds the subnormals m * 2^-24, field 31 holds inf / NaN.
+ * ------------------------------------------------------------------------- */
+
+double mnb_ref_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);
+    } else if (e == 31) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp((double)(1024 + f), e - 15 - 10);
+    }
+    return sign ? -v : v;
+}
+
+/* Round a non-negative real m to the nearest integer, ties to the even one. */
+static double round_half_even(double m)
+{
+    double fl = floor(m);
+    double d = m - fl; /* exact: m and fl share the exponent range used here */
+    if (d > 0.5) return fl + 1.0;
+    if (d < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+uint16_t mnb_ref_f64_to_f16(double v)
+{
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (isnan(v)) return (uint16_t)(sign | 0x7e00u);
+    /* 65520 is the midpoint between the largest finite value 65504 (odd
+     * fraction 0x3ff) and 2^16; the tie goes to the even neighbour, i.e. to
+     * infinity. */
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: a = m * 2^-24 with m real in [0, 1024) */
+        double m = round_half_even(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)m); /* m == 1024 is the smallest normal */
+    }
+    int e2;
+    (void)frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;               /* 2^E <= a < 2^(E+1), E in [-14, 15] */
+    double m = round_half_even(ldexp(a, 10 - E)); /* significand in [1024, 2048] */
+    if (m == 2048.0) { m = 1024.0; E += 1; }
+    if (E > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)((int)m - 1024));
+}
+
+/* ---------------------------------------------------------------------------
+ * Packing of the quantized codes.  Wq is [N, K/bs, bs*bits/8] bytes, i.e.
+ * each output row n holds its K codes in order along K.
+ * ------------------------------------------------------------------------- */
+
+static int check_shape(int64_t N, int64_t K, int bits, int bs)
+{
+    if (N < 0 || K < 0) return -1;
+    if (bits != 4 && bits != 8) return -2;
+    if (bs <= 0 || (bs * bits) % 8 != 0) return -2;
+    if (K % bs != 0) return -2;
+    return 0;
+}
+
+/* code q[n,k] read from the packed weight bytes */
+static int code_at(const uint8_t* Wq, int64_t K, int bits, int64_t n, int64_t k)
+{
+    if (bits == 8) return Wq[n * K + k];
+    uint8_t byte = Wq[n * (K / 2) + k / 2];
+    return (k % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+}
+
+int mnb_ref_unpack(const uint8_t* Wq, int64_t N, int64_t K, int bits, int bs, uint8_t* q)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) q[n * K + k] = (uint8_t)code_at(Wq, K, bits, n, k);
+    return 0;
+}
+
+int mnb_ref_pack(const uint8_t* q, int64_t N, int64_t K, int bits, int bs, uint8_t* Wq)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    if (bits == 8) {
+        memcpy(Wq, q, (size_t)(N * K));
+        return 0;
+    }
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < K / 2; ++j) {
+            uint8_t lo = q[n * K + 2 * j] & 0x0f, hi = q[n * K + 2 * j + 1] & 0x0f;
+            Wq[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Dequantization: w = (q - zp) * scale, one (scale, zp) per row and block.
+ * The product of an integer of at most 9 bits and an 11-bit significand is
+ * exact in binary64.
+ * ------------------------------------------------------------------------- */
+
+static double dequant_at(const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                         int64_t K, int bits, int bs, int64_t n, int64_t k)
+{
+    int64_t nb = K / bs, b = k / bs;
+    int q = code_at(Wq, K, bits, n, k);
+    int z = zp ? (int)zp[n * nb + b] : (1 << (bits - 1));
+    double s = mnb_ref_f16_to_f64(scales[n * nb + b]);
+    return (double)(q - z) * s;
+}
+
+int mnb_ref_dequant(const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                    int64_t N, int64_t K, int bits, int bs, double* W)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) W[n * K + k] = dequant_at(Wq, scales, zp, K, bits, bs, n, k);
+    return 0;
+}
+
+/* The dequantized weight rounded once to binary16 (what a kernel that stages
+ * FP16 weights for a tensor-core product must hold, bit for bit). */
+int mnb_ref_dequant_f16(const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                        int64_t N, int64_t K, int bits, int bs, uint16_t* W16)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            W16[n * K + k] = mnb_ref_f64_to_f16(dequant_at(Wq, scales, zp, K, bits, bs, n, k));
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * LoRA down projection T = X * A, X [Mt, K] fp16, A [K, r] fp16, T fp64.
+ * ------------------------------------------------------------------------- */
+
+int mnb_ref_lora_down(const uint16_t* X, const uint16_t* A, int64_t Mt, int64_t K, int r, double* T)
+{
+    if (Mt < 0 || K < 0 || r < 0) return -1;
+    for (int64_t m = 0; m < Mt; ++m)
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += mnb_ref_f16_to_f64(X[m * K + k]) * mnb_ref_f16_to_f64(A[k * r + j]);
+            T[m * r + j] = acc;
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * The whole operation.  X [Mt, K] fp16 (Mt = batch * M rows, every row is an
+ * independent product), Wq / scales / zp as above, A [K, rank] and B [N, rank]
+ * fp16 or NULL (rank 0 = empty adapter = base only).
+ * Outputs (any may be NULL):
+ *   Y16   [Mt, N]  fp16 bits of round-to-nearest-even(y)
+ *   Y64   [Mt, N]  y in binary64
+ *   bound [Mt, N]  sum_k |x w| + sum_r |t B|, the scale of the FP16
+ *                  tolerance |y_gpu - y| <= 1e-3 * bound + 1e-3
+ * round_t = 1 rounds each t[m,r] to fp16 before the up projection (the
+ * pages' FP16 intermediate); 0 keeps it exact.
+ * ------------------------------------------------------------------------- */
+
+int mnb_ref_run(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                const uint16_t* A, const uint16_t* B, int rank,
+                int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                uint16_t* Y16, double* Y64, double* bound)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    if (Mt < 0 || rank < 0) return -1;
+    if (rank > 0 && (!A || !B)) return -1;
+
+    double* T = NULL;
+    if (rank > 0) {
+        T = (double*)malloc(sizeof(double) * (size_t)(Mt > 0 ? Mt : 1) * (size_t)rank);
+        if (!T) return -3;
+        mnb_ref_lora_down(X, A, Mt, K, rank, T);
+        if (round_t)
+            for (int64_t i = 0; i < Mt * rank; ++i) T[i] = mnb_ref_f16_to_f64(mnb_ref_f64_to_f16(T[i]));
+    }
+
+    int64_t total = Mt * N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < total; ++i) {
+        int64_t m = i / N, n = i % N;
+        double acc = 0.0, mag = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double p = mnb_ref_f16_to_f64(X[m * K + k]) * dequant_at(Wq, scales, zp, K, bits, bs, n, k);
+            acc += p;
+            mag += fabs(p);
+        }
+        for (int j = 0; j < rank; ++j) {
+            double p = T[m * rank + j] * mnb_ref_f16_to_f64(B[n * rank + j]);
+            acc += p;
+            mag += fabs(p);
+        }
+        if (Y64) Y64[i] = acc;
+        if (bound) bound[i] = mag;
+        if (Y16) Y16[i] = mnb_ref_f64_to_f16(acc);
+    }
+    free(T);
+    return 0;
+}
+
+/* Threads the parallel loop above will use. */
+int mnb_ref_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
