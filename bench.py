@@ -1,0 +1,466 @@
+"""Benchmark of the block-quantized MatMulNBits hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mnb|reference] [--sweep]
+
+Headline (one JSON line on rank 0): the decode call -- M = 1, K = N = 4096,
+INT4 block-32 weights with explicit uint8 zero points and a rank-32 FP16 LoRA
+adapter -- as weight-stream GB/s (every byte the call must move: packed codes,
+scales, zero points, adapter A and B, X and Y) against the HBM roofline.  One
+step = one mnb_run call (LoRA down kernel + decode kernel).  The prefill call
+(M = 1024, same K, N, default zero point, rank 32) is reported in the same line
+as TFLOP/s against the dense FP16 tensor roofline.
+
+Inputs are seeded synthetic data of those shapes.  Each step reads its own copy
+of the weights, rotating over enough copies to exceed 4x the L2 size, so no
+step finds its weights in L2.  Steps are captured in CUDA graphs and timed with
+CUDA events on the capture stream; SM clocks are sampled with nvidia-smi while
+the GPU is busy.  `--impl reference` times the CPU oracle (the reference arm).
+Under torchrun every rank runs an independent replica on its own GPU (the
+operation has no exchange step); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "M=1 weight-stream GB/s vs HBM peak; M=1024 TFLOP/s vs FP16 tensor peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+DECODE = dict(M=1, K=4096, N=4096, bits=4, rank=32)
+PREFILL = dict(M=1024, K=4096, N=4096, bits=4, rank=32)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def decode_bytes(M, K, N, bits, rank, zp=True):
+    nb = K // 32
+    b = N * K * bits // 8 + N * nb * 2 + (N * nb if zp else 0)
+    if rank:
+        b += K * rank * 2 + N * rank * 2
+    return b + M * K * 2 + M * N * 2
+
+
+def prefill_flops(M, K, N, rank):
+    return 2.0 * M * N * K + (2.0 * M * rank * (K + N) if rank else 0.0)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            bf = d.get("bf16_tflops")
+            if hbm and bf:
+                return float(hbm), float(bf), float(d.get("bf16_tflops_sustained") or bf), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel sources
+    are unchanged since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path)).get(kernel_key)
+        if not d:
+            return None
+        if source_sha(d["sources"]) != d["source_sha"]:
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is busy."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Workload:
+    """Rotating device copies of one seeded problem (weights, adapter, X, Y, T)."""
+
+    def __init__(self, torch, mnb, synth, cfg, copies, seed_offset=0, zp=True):
+        self.torch, self.mnb = torch, mnb
+        self.cfg = cfg
+        M, K, N, bits, rank = cfg["M"], cfg["K"], cfg["N"], cfg["bits"], cfg["rank"]
+        inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=synth.SEED_BASE + 1 + seed_offset,
+                                zp_range=(0, 15) if zp else None, rank=rank)
+        self.inp = inp
+
+        def dev(a):
+            if a is None:
+                return None
+            if a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
+            return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+        base = dict(X=dev(inp.X), Wq=dev(inp.Wq), S=dev(inp.scales), Z=dev(inp.zp), A=dev(inp.A), B=dev(inp.B))
+        self.copies = []
+        for i in range(copies):
+            c = {k: (None if v is None else v.clone()) for k, v in base.items()}
+            c["Y"] = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+            c["T"] = torch.empty((M, rank), dtype=torch.float16, device="cuda") if rank else None
+            self.copies.append(c)
+        self.h = mnb.mnb_create(N, K, bits, 32, 32, 0, 0)
+
+    def step(self, i, rank=None):
+        c = self.copies[i % len(self.copies)]
+        rank = self.cfg["rank"] if rank is None else rank
+        self.mnb.mnb_run(self.h, c["X"], c["Wq"], c["S"], c["Z"], c["A"] if rank else None,
+                         c["B"] if rank else None, rank, c["Y"], c["T"] if rank else None, 1, self.cfg["M"])
+
+    def graph(self, start, n, rank=None):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step(start, rank)  # warm the capture stream once outside the graph
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(start, start + n):
+                self.step(i, rank)
+        return g
+
+    def close(self):
+        self.mnb.mnb_destroy(self.h)
+
+
+def time_graphs(torch, graphs, barrier=None):
+    """Replay (graph, times) pairs between two events on the current stream."""
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    e0.record(st)
+    for g, times in graphs:
+        for _ in range(times):
+            g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def timed_steps(torch, wl, steps, warmup, rank=None, chunk=1000, barrier=None):
+    """Warm up with `warmup` steps, then time exactly `steps` steps (graph replays)."""
+    G = min(chunk, steps)
+    g_full = wl.graph(0, G, rank)
+    rem = steps % G
+    g_rem = wl.graph(G, rem, rank) if rem else None
+    w_graph = wl.graph(0, min(warmup, G), rank)
+    for _ in range(max(1, math.ceil(warmup / max(1, min(warmup, G))))):
+        w_graph.replay()
+    torch.cuda.synchronize()
+    plan = [(g_full, steps // G)] + ([(g_rem, 1)] if g_rem else [])
+    return time_graphs(torch, plan, barrier)
+
+
+def e2e_decode(torch, wl, steps):
+    """Through the public call with host buffers: pinned X -> device, mnb_run,
+    Y -> pinned host, every step; one sync at the end."""
+    M, K, N = wl.cfg["M"], wl.cfg["K"], wl.cfg["N"]
+    x_host = torch.from_numpy(wl.inp.X.view(np.float16).copy()).pin_memory()
+    y_host = torch.empty((1, M, N), dtype=torch.float16).pin_memory()
+    st = torch.cuda.current_stream()
+    for i in range(3):
+        wl.copies[i % len(wl.copies)]["X"].copy_(x_host, non_blocking=True)
+        wl.step(i)
+        y_host.copy_(wl.copies[i % len(wl.copies)]["Y"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(steps):
+        c = wl.copies[i % len(wl.copies)]
+        c["X"].copy_(x_host, non_blocking=True)
+        wl.step(i)
+        y_host.copy_(c["Y"], non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3, M * K * 2, M * N * 2
+
+
+def run_gpu_arm(args, dist_ctx):
+    import torch
+
+    from block_quantized_matmul_matmulnbits_gb300 import mnb, synth
+
+    rank_id, world, barrier, reduce_max = dist_ctx
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    mnb.lib()
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    hbm_peak, bf16_peak, bf16_sus, peak_src = load_peaks()
+
+    cfg = DECODE
+    step_bytes = decode_bytes(cfg["M"], cfg["K"], cfg["N"], cfg["bits"], cfg["rank"])
+    copies = max(8, math.ceil(4 * l2 / step_bytes))
+    wl = Workload(torch, mnb, synth, cfg, copies)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    only = args.only
+    nan = float("nan")
+    t_decode = t_base = t_e2e = nan
+    h2d = d2h = 0
+    e2e_steps = min(args.steps, 2000)
+    base_bytes = decode_bytes(cfg["M"], cfg["K"], cfg["N"], cfg["bits"], 0)
+    if only in ("all", "decode"):
+        t_decode = reduce_max(timed_steps(torch, wl, args.steps, args.warmup, barrier=barrier))
+    if only in ("all", "decode_base"):
+        # the decode kernel alone (empty adapter), same rotation, for the per-kernel roofline
+        t_base = reduce_max(timed_steps(torch, wl, args.steps, args.warmup, rank=0, barrier=barrier))
+    sampler.stop()
+    clocks = sampler.summary()
+
+    if only == "all":
+        t_e2e, h2d, d2h = e2e_decode(torch, wl, e2e_steps)
+        t_e2e = reduce_max(t_e2e)
+    wl.close()
+    del wl
+    torch.cuda.empty_cache()
+
+    # prefill leg
+    prefill = None
+    try:
+        if only not in ("all", "prefill"):
+            raise RuntimeError(f"skipped (--only {only})")
+        pc = PREFILL
+        pbytes = decode_bytes(pc["M"], pc["K"], pc["N"], pc["bits"], pc["rank"], zp=False)
+        pcopies = max(4, math.ceil(2 * l2 / pbytes))
+        pwl = Workload(torch, mnb, synth, pc, pcopies, seed_offset=1, zp=False)
+        psteps = max(10, min(args.steps // 20, 400))
+        t_p = reduce_max(timed_steps(torch, pwl, psteps, max(3, args.warmup // 20), barrier=barrier))
+        fl = prefill_flops(pc["M"], pc["K"], pc["N"], pc["rank"])
+        tflops = fl * psteps / t_p / 1e12 * world
+        per_tf = fl * psteps / t_p / 1e12
+        prefill = {
+            "value": round(tflops, 2), "unit": "TFLOP/s", "steps": psteps,
+            "ms_per_step": round(t_p / psteps * 1e3, 4),
+            "config": {"workload": "prefill GEMM M=1024 K=4096 N=4096 INT4 block-32, default zero point 8, "
+                                   "rank-32 FP16 LoRA epilogue", "M": 1024, "K": 4096, "N": 4096, "bits": 4,
+                       "rank": 32, "l2": f"rotating {pcopies} weight+X copies"},
+            "roofline": {"bound": "tensor", "achieved": round(per_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(per_tf / bf16_peak, 4), "traffic": ncu_traffic("gemm"),
+                         "peak_source": f"{peak_src} bf16 burst (fp16 dense rate = bf16 rate)"},
+        }
+        pwl.close()
+    except Exception as e:  # the prefill kernel may be unavailable on this build
+        prefill = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+    def rate(nbytes, steps, t):
+        return nbytes * steps / t / 1e9 if t == t and t > 0 else None
+
+    def rnd(x, n=2):
+        return None if x is None else round(x, n)
+
+    gbs = step_bytes * args.steps / t_decode / 1e9 * world
+    per_gbs = step_bytes * args.steps / t_decode / 1e9
+    base_gbs = base_bytes * args.steps / t_base / 1e9
+    e2e_gbs = step_bytes * e2e_steps / t_e2e / 1e9 * world
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_decode / args.steps * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded)",
+        "config": {"workload": "decode GEMV M=1 K=4096 N=4096 INT4 block-32, explicit uint8 zero points, "
+                               "rank-32 FP16 LoRA (A,B ~ N(0,0.02))", "M": 1, "K": 4096, "N": 4096, "bits": 4,
+                   "rank": 32, "bytes_per_step": step_bytes,
+                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                         f"({copies * step_bytes / 2 ** 20:.0f} MiB vs {l2 / 2 ** 20:.0f} MiB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(per_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(per_gbs / hbm_peak, 4), "traffic": ncu_traffic("decode"),
+                     "kernel": "decode pass (lora_down + PDL-overlapped gemv), per mnb_run call",
+                     "peak_source": f"{peak_src} HBM copy bandwidth"},
+        "decode_base_only": {"value": round(base_gbs, 2), "unit": "GB/s", "bytes_per_step": base_bytes,
+                             "ms_per_step": round(t_base / args.steps * 1e3, 6),
+                             "frac": round(base_gbs / hbm_peak, 4), "traffic": ncu_traffic("decode_base")},
+        "prefill": prefill,
+        "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": round(t_e2e / e2e_steps * 1e3, 5)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_decode_sample(target_s):
+    import oracle
+    from block_quantized_matmul_matmulnbits_gb300 import synth
+    cfg = DECODE
+    inp = synth.decode_4096(rank=cfg["rank"])
+    step_bytes = decode_bytes(cfg["M"], cfg["K"], cfg["N"], cfg["bits"], cfg["rank"])
+    oracle.run(inp.X2d, inp.Wq[:64], inp.scales[:64], inp.zp[:64], inp.A, inp.B[:64], 64, cfg["K"], 4)  # warm
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, cfg["N"], cfg["K"], cfg["bits"])
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s:
+            break
+    return {"value": round(step_bytes * n / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{n} full decode calls (M=1, K=N=4096, INT4, rank 32) in {dt:.1f} s"}, n, dt, step_bytes
+
+
+def run_reference_arm(args):
+    cpu, n, dt, step_bytes = oracle_decode_sample(max(5.0, min(60.0, 0.01 * args.steps)))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cpu["value"], "unit": "GB/s", "n_gpus": 1,
+        "steps": n, "warmup": 0, "ms_per_step": round(dt / n * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": "decode GEMV M=1 K=4096 N=4096 INT4 block-32, explicit uint8 zero points, "
+                               "rank-32 FP16 LoRA (A,B ~ N(0,0.02))", "M": 1, "K": 4096, "N": 4096, "bits": 4,
+                   "rank": 32, "bytes_per_step": step_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": cpu["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- distribution
+
+def make_dist_ctx():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, None, (lambda x: x)
+    import torch
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dist.init_process_group(backend=backend)
+    dev = torch.device("cuda") if backend == "nccl" else torch.device("cpu")
+
+    def barrier():
+        dist.barrier()
+
+    def reduce_max(x):
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return dist.get_rank(), world, barrier, reduce_max
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", choices=["mnb", "reference"], default="mnb")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", choices=["all", "decode", "decode_base", "prefill"], default="all",
+                    help="run one leg only (for profiling); the printed line then lacks the other legs")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference_arm(args)), flush=True)
+        return 0
+
+    ctx = make_dist_ctx()
+    line = run_gpu_arm(args, ctx)
+    if ctx[0] == 0:
+        if not args.no_cpu_baseline and ctx[1] == 1 and args.only == "all":
+            line["cpu_baseline"] = oracle_decode_sample(args.cpu_seconds)[0]
+        print(json.dumps(line), flush=True)
+    if ctx[1] > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

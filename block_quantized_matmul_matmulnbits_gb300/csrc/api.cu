@@ -1,0 +1,344 @@
+// api.cu -- the C ABI of libmnb (include/mnb.h): validation, the per-call
+// dispatcher and the kernel launches.
+//
+// Dispatch follows the auto mode of "[WebGPU] Fuse rank-32 quantized LoRA with
+// MatMulNBits" (onnxruntime PR 33370, commit message adding MatMulNBitsLoRA):
+// chosen on every invocation from X's per-matrix row dimension M, independent
+// of the batch size, with forced overrides kept for comparisons.  Few rows go
+// to the weight-streaming decode kernel, more rows to the tensor-core prefill
+// kernel; the threshold is a handle property (default 16).
+//
+// A non-empty adapter adds the LoRA down kernel first (normal stream order)
+// and launches the matmul kernel after it with programmatic stream
+// serialization, so the matmul streams weights while T is produced and waits
+// (griddepcontrol.wait) only before it reads T.  Nothing here allocates or
+// synchronizes, so mnb_run can be captured in a CUDA graph.
+#include <mutex>
+#include <new>
+
+#include "mnb_internal.h"
+
+namespace mnb {
+// The library's device status word (one per device context; kernels receive
+// its address).  See mnb_sync_status.
+__device__ unsigned int g_status = 0u;
+}  // namespace mnb
+
+struct mnb_handle_s {
+    mnb_desc d;
+    int last_route;
+};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_init_mu;
+bool g_prepared[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+bool aligned16(const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_desc(const mnb_desc* d) {
+    if (!d) return MNB_ERR_ARG;
+    if (d->N < 0 || d->K < 0) return MNB_ERR_ARG;
+    if (d->N > (int64_t)INT32_MAX || d->K > (int64_t)INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
+    if (d->bits != 4 && d->bits != 8) return MNB_ERR_UNSUPPORTED;
+    if (d->block_size != 32) return MNB_ERR_UNSUPPORTED;
+    if (d->K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (d->max_rank != 0 && d->max_rank != 32) return MNB_ERR_UNSUPPORTED;
+    if (d->mode < MNB_MODE_AUTO || d->mode > MNB_MODE_FORCE_GEMM) return MNB_ERR_ARG;
+    return MNB_OK;
+}
+
+// One-time per-device setup: SM count and kernel attributes.  Returns MNB_OK
+// and the device's SM count, or MNB_ERR_NO_DEVICE / MNB_ERR_CUDA.
+int device_setup(int* sm_count, unsigned int** status = nullptr) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return MNB_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_init_mu);
+    if (!g_prepared[dev]) {
+        int major = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return MNB_ERR_NO_DEVICE;
+        }
+        if (major != 10) return MNB_ERR_NO_DEVICE;  // built for sm_103a only
+        void* st = nullptr;
+        if (mnb::gemv_prepare() != cudaSuccess || mnb::gemm_prepare() != cudaSuccess ||
+            mnb::lora_down_prepare() != cudaSuccess ||
+            cudaGetSymbolAddress(&st, mnb::g_status) != cudaSuccess) {
+            cudaGetLastError();
+            return MNB_ERR_CUDA;
+        }
+        g_status_ptr[dev] = static_cast<unsigned int*>(st);
+        g_sm_count[dev] = sms;
+        g_prepared[dev] = true;
+    }
+    *sm_count = g_sm_count[dev];
+    if (status) *status = g_status_ptr[dev];
+    return MNB_OK;
+}
+
+int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Decode-kernel geometry: balanced row ranges, one CTA per SM, up to 16 warps.
+void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p, int* maxseg_out) {
+    const int64_t N = d.N;
+    const int rowbytes = (int)(d.K * d.bits / 8);
+    const int steps = cdiv(rowbytes, 64);
+    const int tok = Mt <= 8 ? 8 : 16;
+    int ctas = sms > 0 ? sms : 1;
+    int R, warps, maxseg;
+    for (;;) {
+        R = cdiv(N, ctas);
+        const int RT = cdiv(R, 16);
+        const int64_t items = (int64_t)RT * steps;
+        warps = (int)(items < 16 ? (items > 0 ? items : 1) : 16);
+        const int64_t per = (items + warps - 1) / warps;
+        maxseg = (int)((per + steps - 1) / (steps > 0 ? steps : 1)) + 1;
+        if (mnb::gemv_smem_bytes(warps, maxseg, tok) <= (size_t)mnb::kGemvMaxSmem || R <= 16) break;
+        ctas *= 2;  // too many rows per CTA for the reduction buffer: spread over more CTAs
+    }
+    p->route = MNB_ROUTE_GEMV;
+    p->grid_x = cdiv(N, R);
+    p->grid_y = cdiv(Mt, tok);
+    p->block_threads = warps * 32;
+    p->rows_per_cta = R;
+    p->k_splits = 0;
+    p->tokens_per_cta = tok;
+    *maxseg_out = maxseg;
+}
+
+// Prefill-kernel geometry: 128 weight rows x up to 256 token rows per tile,
+// one persistent CTA per SM.
+void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
+    const int tok = mnb::gemm_token_tile((int)Mt);
+    const int ntiles = cdiv(d.N, 128) * cdiv(Mt, tok);
+    p->route = MNB_ROUTE_GEMM;
+    p->grid_x = ntiles < sms ? ntiles : (sms > 0 ? sms : 1);
+    p->grid_y = 1;
+    p->block_threads = mnb::gemm_threads();
+    p->rows_per_cta = 128;
+    p->k_splits = 0;
+    p->tokens_per_cta = tok;
+}
+
+int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p, int* maxseg) {
+    *p = mnb_plan_info{};
+    *maxseg = 0;
+    const int64_t Mt = batch * M;
+    if (Mt == 0 || d.N == 0) {
+        p->route = MNB_ROUTE_NONE;
+        return MNB_OK;
+    }
+    if (d.K == 0) {
+        p->route = MNB_ROUTE_FILL;
+        return MNB_OK;
+    }
+    const int thr = d.gemv_max_m > 0 ? d.gemv_max_m : 16;
+    int route = M <= thr ? MNB_ROUTE_GEMV : MNB_ROUTE_GEMM;
+    if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
+    if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
+    if (route == MNB_ROUTE_GEMV)
+        plan_gemv(d, Mt, sms, p, maxseg);
+    else
+        plan_gemm(d, Mt, sms, p);
+    p->lora_kernel = rank > 0 ? 1 : 0;
+    return MNB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mnb_create(const mnb_desc* desc, mnb_handle* out) {
+    if (!out) return MNB_ERR_ARG;
+    *out = nullptr;
+    const int rc = validate_desc(desc);
+    if (rc != MNB_OK) return rc;
+    mnb_handle h = new (std::nothrow) mnb_handle_s;
+    if (!h) return MNB_ERR_ARG;
+    h->d = *desc;
+    h->last_route = MNB_ROUTE_NONE;
+    *out = h;
+    return MNB_OK;
+}
+
+void mnb_destroy(mnb_handle h) { delete h; }
+
+int mnb_last_route(mnb_handle h) { return h ? h->last_route : MNB_ROUTE_NONE; }
+
+int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_count, mnb_plan_info* out) {
+    if (!h || !out || batch < 0 || M < 0) return MNB_ERR_ARG;
+    if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
+    if (rank != 0 && rank != 32) return MNB_ERR_UNSUPPORTED;
+    if (rank > h->d.max_rank) return MNB_ERR_ARG;
+    int sms = sm_count;
+    if (sms <= 0) {
+        const int rc = device_setup(&sms);
+        if (rc != MNB_OK) return rc;
+    }
+    int maxseg;
+    return make_plan(h->d, batch, M, rank, sms, out, &maxseg);
+}
+
+int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+            const void* B, int32_t rank, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
+    if (!h || batch < 0 || M < 0) return MNB_ERR_ARG;
+    const mnb_desc& d = h->d;
+    if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
+    const int64_t Mt = batch * M;
+    if (Mt > 0 && d.N > 0 && Mt * d.N > ((int64_t)1 << 40)) return MNB_ERR_UNSUPPORTED;
+    // empty adapter: rank 0, or both adapter pointers NULL
+    if (rank != 0 && rank != 32) return MNB_ERR_UNSUPPORTED;
+    if (A == nullptr && B == nullptr) rank = 0;
+    if (rank > 0) {
+        if (rank > d.max_rank) return MNB_ERR_ARG;
+        if (!A || !B || !T_ws) return MNB_ERR_ARG;
+    }
+    if (Mt > 0 && d.N > 0) {
+        if (!Y) return MNB_ERR_ARG;
+        if (d.K > 0 && (!X || !Wq || !scales)) return MNB_ERR_ARG;
+    }
+    if (!aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zp) || !aligned16(Y) ||
+        (rank > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(T_ws))))
+        return MNB_ERR_ALIGN;
+
+    mnb_plan_info p;
+    int maxseg = 0;
+    int sms = 0;
+    unsigned int* status = nullptr;
+    if (Mt > 0 && d.N > 0) {
+        const int rc = device_setup(&sms, &status);
+        if (rc != MNB_OK) return rc;
+    }
+    make_plan(d, batch, M, rank, sms, &p, &maxseg);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+
+    if (p.route == MNB_ROUTE_NONE) {
+        h->last_route = MNB_ROUTE_NONE;
+        return MNB_OK;
+    }
+    if (p.route == MNB_ROUTE_FILL) {
+        e = mnb::fill_zero_launch(static_cast<__half*>(Y), (size_t)Mt * (size_t)d.N, st);
+        if (e == cudaSuccess && rank > 0) e = mnb::fill_zero_launch(static_cast<__half*>(T_ws), (size_t)Mt * 32, st);
+        if (e != cudaSuccess) return MNB_ERR_CUDA;
+        h->last_route = MNB_ROUTE_FILL;
+        return MNB_OK;
+    }
+
+    const __half* Xh = static_cast<const __half*>(X);
+    __half* Th = static_cast<__half*>(T_ws);
+    if (rank > 0) {
+        e = mnb::lora_down_launch(Xh, static_cast<const __half*>(A), Th, (int)Mt, (int)d.K, st);
+        if (e != cudaSuccess) return MNB_ERR_CUDA;
+    }
+    if (p.route == MNB_ROUTE_GEMV) {
+        mnb::GemvArgs a;
+        a.X = Xh;
+        a.Wq = static_cast<const uint8_t*>(Wq);
+        a.S = static_cast<const __half*>(scales);
+        a.Z = static_cast<const uint8_t*>(zp);
+        a.T = Th;
+        a.B = static_cast<const __half*>(B);
+        a.Y = static_cast<__half*>(Y);
+        a.Mt = (int)Mt;
+        a.N = (int)d.N;
+        a.K = (int)d.K;
+        a.rows_per_cta = p.rows_per_cta;
+        a.maxseg = maxseg;
+        a.rank = rank;
+        e = mnb::gemv_launch(a, p, d.bits, rank > 0, st);
+    } else {
+        mnb::GemmArgs a;
+        a.X = Xh;
+        a.Wq = static_cast<const uint8_t*>(Wq);
+        a.S = static_cast<const __half*>(scales);
+        a.Z = static_cast<const uint8_t*>(zp);
+        a.T = Th;
+        a.B = static_cast<const __half*>(B);
+        a.Y = static_cast<__half*>(Y);
+        a.Mt = (int)Mt;
+        a.N = (int)d.N;
+        a.K = (int)d.K;
+        a.bits = d.bits;
+        a.rank = rank;
+        a.status = status;
+        e = mnb::gemm_launch(a, p, rank > 0, st);
+        if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return MNB_ERR_CUDA;
+    h->last_route = p.route;
+    return MNB_OK;
+}
+
+int mnb_sync_status(mnb_handle h, void* stream) {
+    if (!h) return MNB_ERR_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MNB_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, mnb::g_status, sizeof(v)) != cudaSuccess) return MNB_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(mnb::g_status, &zero, sizeof(zero)) != cudaSuccess) return MNB_ERR_CUDA;
+    return (v & mnb::kStatusTimeout) ? MNB_ERR_DEVICE_TIMEOUT : MNB_OK;
+}
+
+const char* mnb_status_str(int code) {
+    switch (code) {
+        case MNB_OK: return "MNB_OK";
+        case MNB_ERR_ARG: return "MNB_ERR_ARG: invalid argument";
+        case MNB_ERR_UNSUPPORTED: return "MNB_ERR_UNSUPPORTED: unsupported bits/block/K/rank";
+        case MNB_ERR_ALIGN: return "MNB_ERR_ALIGN: pointer not 16-byte aligned";
+        case MNB_ERR_CUDA: return "MNB_ERR_CUDA: CUDA runtime error";
+        case MNB_ERR_DEVICE_TIMEOUT: return "MNB_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+        case MNB_ERR_NO_DEVICE: return "MNB_ERR_NO_DEVICE: no sm_100-family GPU is current";
+        default: return "MNB_ERR_UNKNOWN";
+    }
+}
+
+int mnb_dequant(const void* Wq, const void* scales, const void* zp, int64_t N, int64_t K, int32_t bits,
+                int32_t block_size, void* W16, int32_t variant, void* stream) {
+    if (N < 0 || K < 0 || variant < 0 || variant > 1) return MNB_ERR_ARG;
+    if (bits != 4 && bits != 8) return MNB_ERR_UNSUPPORTED;
+    if (block_size != 32 || K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (N > INT32_MAX || K > INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
+    if (N == 0 || K == 0) return MNB_OK;
+    if (!Wq || !scales || !W16) return MNB_ERR_ARG;
+    if (!aligned16(Wq) || !aligned16(scales) || !aligned16(zp) || !aligned16(W16)) return MNB_ERR_ALIGN;
+    int sms;
+    const int rc = device_setup(&sms);
+    if (rc != MNB_OK) return rc;
+    const cudaError_t e = mnb::dequant_launch(static_cast<const uint8_t*>(Wq), static_cast<const __half*>(scales),
+                                              static_cast<const uint8_t*>(zp), (int)N, (int)K, bits,
+                                              static_cast<__half*>(W16), variant,
+                                              reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MNB_OK : MNB_ERR_CUDA;
+}
+
+int mnb_lora_down(const void* X, const void* A, void* T, int64_t Mt, int64_t K, int32_t rank, void* stream) {
+    if (Mt < 0 || K < 0) return MNB_ERR_ARG;
+    if (rank != 32 || K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (Mt > INT32_MAX || K > INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
+    if (Mt == 0) return MNB_OK;
+    if (!T) return MNB_ERR_ARG;
+    if (!aligned16(X) || !aligned16(A) || !aligned16(T)) return MNB_ERR_ALIGN;
+    int sms;
+    const int rc = device_setup(&sms);
+    if (rc != MNB_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        return mnb::fill_zero_launch(static_cast<__half*>(T), (size_t)Mt * 32, st) == cudaSuccess ? MNB_OK
+                                                                                                   : MNB_ERR_CUDA;
+    }
+    if (!X || !A) return MNB_ERR_ARG;
+    const cudaError_t e = mnb::lora_down_launch(static_cast<const __half*>(X), static_cast<const __half*>(A),
+                                                static_cast<__half*>(T), (int)Mt, (int)K, st);
+    return e == cudaSuccess ? MNB_OK : MNB_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// aux_kernels.cu -- the two small kernels around the matmuls.
+//
+//  * fill_zero: K == 0 leaves every sum empty, so the output keeps its logical
+//    shape and holds zeros -- the empty packed weight rule of "[WebGPU] Fuse
+//    rank-32 quantized LoRA with MatMulNBits" (onnxruntime PR 33370, commit
+//    message on empty packed weights: the WebGPU side records a fill dispatch
+//    so that graph replay rewrites the output).
+//  * dequant: the dequantization step on its own, W16 = fp16((q - zp) * scale),
+//    the DequantizeLinear weight map of "Fuse DQ->MatMulNBits for shared
+//    initializers and skip outer-scope weights" (onnxruntime PR 33800,
+//    Description).  It runs the exact device helpers of the matmul kernels
+//    (variant 0: natural order, variant 1: the decode kernel's pair-interleaved
+//    INT4 order, un-permuted on store) so their bits can be checked one by one.
+#include "common.cuh"
+#include "mnb_internal.h"
+
+namespace mnb {
+
+namespace {
+
+__global__ void fill_zero_kernel(uint4* __restrict__ y16, size_t n16, __half* __restrict__ tail, size_t ntail) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) y16[i] = make_uint4(0, 0, 0, 0);
+    if (blockIdx.x == 0)
+        for (size_t i = threadIdx.x; i < ntail; i += blockDim.x) tail[i] = __float2half_rn(0.f);
+}
+
+template <int BITS>
+__global__ void dequant_kernel(const uint8_t* __restrict__ Wq, const __half* __restrict__ S,
+                               const uint8_t* __restrict__ Z, int N, int K, __half* __restrict__ W16,
+                               int variant) {
+    const int rowbytes = K * BITS / 8;
+    const int chunks = rowbytes / 16;  // 16 packed bytes per thread
+    const long long total = (long long)N * chunks;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    const int n = (int)(i / chunks), c = (int)(i % chunks);
+    const int nblk = K / 32;
+    const int blk = c * 16 / (32 * BITS / 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(Wq + (size_t)n * rowbytes + (size_t)c * 16);
+    const uint16_t sbits = reinterpret_cast<const uint16_t*>(S)[(size_t)n * nblk + blk];
+    const uint32_t zp = Z ? Z[(size_t)n * nblk + blk] : (1u << (BITS - 1));
+    const DqConst dc = dq_const(zp, sbits);
+    const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    const int k0 = c * 16 * 8 / BITS;
+    uint32_t out[16];  // up to 32 halfs as half2 words
+    if constexpr (BITS == 4) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t d[4];
+            if (variant == 0) {
+                dq_int4_natural(words[w], dc, d);
+                out[4 * w + 0] = d[0];
+                out[4 * w + 1] = d[1];
+                out[4 * w + 2] = d[2];
+                out[4 * w + 3] = d[3];
+            } else {
+                dq_int4_interleaved(words[w], dc, d);  // (k0,k4) (k1,k5) (k2,k6) (k3,k7)
+                out[4 * w + 0] = prmt(d[0], d[1], 0x5410u);  // (k0, k1)
+                out[4 * w + 1] = prmt(d[2], d[3], 0x5410u);  // (k2, k3)
+                out[4 * w + 2] = prmt(d[0], d[1], 0x7632u);  // (k4, k5)
+                out[4 * w + 3] = prmt(d[2], d[3], 0x7632u);  // (k6, k7)
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)n * K + k0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            uint32_t d[2];
+            dq_int8_natural(words[w], dc, d);
+            out[2 * w] = d[0];
+            out[2 * w + 1] = d[1];
+        }
+        uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)n * K + k0);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+}
+
+}  // namespace
+
+cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st) {
+    const size_t n16 = count / 8, ntail = count % 8;
+    size_t blocks = (n16 + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 4096) blocks = 4096;
+    fill_zero_kernel<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<uint4*>(Y), n16, Y + n16 * 8, ntail);
+    return cudaGetLastError();
+}
+
+cudaError_t dequant_launch(const uint8_t* Wq, const __half* S, const uint8_t* Z, int N, int K, int bits,
+                           __half* W16, int variant, cudaStream_t st) {
+    const long long total = (long long)N * (K * bits / 8 / 16);
+    if (total == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((total + 255) / 256);
+    if (bits == 4)
+        dequant_kernel<4><<<blocks, 256, 0, st>>>(Wq, S, Z, N, K, W16, variant);
+    else
+        dequant_kernel<8><<<blocks, 256, 0, st>>>(Wq, S, Z, N, K, W16, variant);
+    return cudaGetLastError();
+}
+
+}  // namespace mnb

@@ -1,0 +1,142 @@
+// common.cuh -- device helpers shared by the libmnb kernels (sm_103a).
+//
+// The dequantization helpers implement w = (q - zp) * scale with exactly one
+// rounding to FP16, the weight map of DequantizeLinear in "Fuse
+// DQ->MatMulNBits for shared initializers and skip outer-scope weights"
+// (onnxruntime PR 33800, Description).  How:
+//   * a code q (< 2^bits) is placed in the low fraction bits of the FP16
+//     value 1024 (bits 0x6400), giving exactly 1024 + q (or 1024 + 16 q when
+//     the code sits in the upper nibble of a byte);
+//   * subtracting 1024 + zp (or, for the x16 form, multiplying by 1/16 and
+//     adding -(64 + zp) in one fused step) yields q - zp exactly: every
+//     operand and result is an integer below 2048 in magnitude;
+//   * one multiply by the FP16 scale rounds once, to nearest even.
+// All half2 arithmetic is issued with explicit .rn PTX so that no contraction
+// can merge the exact subtraction into the rounded multiply.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace mnb {
+
+
+// ---------------------------------------------------------------- bit tricks
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
+    uint32_t d;  // (a & mask) | magic
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(magic));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t hfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+constexpr uint32_t kMagic1024x2 = 0x64006400u;  // half2(1024, 1024)
+constexpr uint32_t kHalf960x2 = 0x63806380u;    // half2(960, 960)
+constexpr uint32_t kSixteenthX2 = 0x2C002C00u;  // half2(1/16, 1/16)
+constexpr uint32_t kOneSixteenth = 0x2C003C00u; // half2(lo = 1, hi = 1/16)
+
+// Per-block constants of the dequant: c0 = half2(1024 + zp), c1 = half2(-(64 + zp)),
+// s2 = half2(scale).  zp < 1024, so 1024 + zp is the bit pattern 0x6400 | zp.
+struct DqConst {
+    uint32_t c0, c1, s2;
+};
+
+__device__ __forceinline__ DqConst dq_const(uint32_t zp, uint16_t scale_bits) {
+    DqConst c;
+    c.c0 = kMagic1024x2 | (zp * 0x00010001u);
+    c.c1 = hsub2_rn(kHalf960x2, c.c0);  // 960 - (1024 + zp), exact
+    c.s2 = (uint32_t)scale_bits * 0x00010001u;
+    return c;
+}
+
+// INT4, pair-interleaved order (decode kernel).  Word w holds codes k0..k7
+// (k0 in bits 0..3).  Output half2s: d0 = (w_k0, w_k4), d1 = (w_k1, w_k5),
+// d2 = (w_k2, w_k6), d3 = (w_k3, w_k7).
+__device__ __forceinline__ void dq_int4_interleaved(uint32_t w, const DqConst& c, uint32_t d[4]) {
+    const uint32_t w8 = w >> 8;
+    const uint32_t h0 = lop3_and_or(w, 0x000F000Fu, kMagic1024x2);   // 1024 + (k0, k4)
+    const uint32_t h1 = lop3_and_or(w, 0x00F000F0u, kMagic1024x2);   // 1024 + 16 (k1, k5)
+    const uint32_t h2 = lop3_and_or(w8, 0x000F000Fu, kMagic1024x2);  // 1024 + (k2, k6)
+    const uint32_t h3 = lop3_and_or(w8, 0x00F000F0u, kMagic1024x2);  // 1024 + 16 (k3, k7)
+    d[0] = hmul2_rn(hsub2_rn(h0, c.c0), c.s2);
+    d[1] = hmul2_rn(hfma2_rn(h1, kSixteenthX2, c.c1), c.s2);
+    d[2] = hmul2_rn(hsub2_rn(h2, c.c0), c.s2);
+    d[3] = hmul2_rn(hfma2_rn(h3, kSixteenthX2, c.c1), c.s2);
+}
+
+// INT4, natural order (prefill kernel, K-major FP16 operand).  Output half2s:
+// d[j] = (w_k{2j}, w_k{2j+1}).  Byte j is copied to both halves, its low
+// nibble read as 1024 + q in the low half and its high nibble as 1024 + 16 q
+// in the high half; one fused step with per-half constants removes both.
+__device__ __forceinline__ void dq_int4_natural(uint32_t w, const DqConst& c, uint32_t d[4]) {
+    // per-half offset (lo: -(1024 + zp), hi: -(64 + zp))
+    const uint32_t off = prmt(c.c0 ^ 0x80008000u, c.c1, 0x7610u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t t = prmt(w, 0u, 0x4040u | (uint32_t)j | ((uint32_t)j << 8));
+        const uint32_t h = lop3_and_or(t, 0x00F0000Fu, kMagic1024x2);
+        d[j] = hmul2_rn(hfma2_rn(h, kOneSixteenth, off), c.s2);
+    }
+}
+
+// INT8, natural order.  Word w holds codes k0..k3.  d0 = (w_k0, w_k1), d1 = (w_k2, w_k3).
+__device__ __forceinline__ void dq_int8_natural(uint32_t w, const DqConst& c, uint32_t d[2]) {
+    const uint32_t h01 = prmt(w, 0x64646464u, 0x4140u);  // bytes [q0, 0x64, q1, 0x64]
+    const uint32_t h23 = prmt(w, 0x64646464u, 0x4342u);  // bytes [q2, 0x64, q3, 0x64]
+    d[0] = hmul2_rn(hsub2_rn(h01, c.c0), c.s2);
+    d[1] = hmul2_rn(hsub2_rn(h23, c.c0), c.s2);
+}
+
+// ---------------------------------------------------------------- tensor ops
+
+// D = A(16x16, row) * B(16x8, col) + C, FP16 inputs, FP32 accumulate.
+__device__ __forceinline__ void mma_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- launch ordering
+
+// Programmatic dependent launch: allow the next kernel on the stream to start.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding kernel on the stream has completed and its writes
+// are visible (returns at once when this grid was not launched dependently).
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+}  // namespace mnb

@@ -1,0 +1,188 @@
+// lora_down.cu -- the LoRA down projection T = fp16(X * A), X [Mt, K], A [K, 32].
+//
+// This is "T" of both fused paths in "[WebGPU] Fuse rank-32 quantized LoRA with
+// MatMulNBits" (onnxruntime PR 33370, commit message adding MatMulNBitsLoRA):
+// fuse_up computes T first and the base GEMM adds T * Bt^T in its epilogue;
+// fuse_down pairs T with the decode GEMV.  T is kept as an FP16 intermediate
+// ("preserving FP16 rounding").
+//
+// Design (sm_103a): K is split across the CTAs of one thread-block cluster
+// (up to 8).  Each CTA stages its slices of A and X in padded shared memory
+// with every 16-byte copy in flight at once (A, a weight, before the
+// griddepcontrol.wait on the producer of X; X after it), runs ldmatrix-fed
+// mma.sync m16n8k16 over 64 token rows x 32 ranks with FP32 accumulators, and
+// leaves its partial in shared memory.  After a
+// cluster barrier every CTA finishes an interleaved share of the outputs,
+// adding the partials of all CTAs in rank order through distributed shared
+// memory, rounds once to FP16 and stores T.  No atomics, so T is bitwise
+// reproducible.  The kernel
+// signals programmatic launch completion on entry so that the matmul kernel
+// queued after it can start streaming weights at once.
+#include "common.cuh"
+#include "mnb_internal.h"
+
+namespace mnb {
+
+namespace {
+
+constexpr int kTok = 64;        // token rows per CTA (4 warps x 16)
+constexpr int kPiece = 512;     // K columns staged per pass (one pass when K <= 8 * 512)
+constexpr int kPitchA = 40;     // halfs per staged A row (32 + 8 pad: conflict-free ldmatrix)
+constexpr int kPitchX = kPiece + 8;  // halfs per staged X row (pad: conflict-free ldmatrix)
+constexpr int kMaxCluster = 8;
+constexpr int kLoraSmem = kPiece * kPitchA * 2 + kTok * kPitchX * 2 + kTok * 32 * 4;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load from the shared memory of CTA `rank` of this cluster.  Volatile keeps
+// it after the cluster barrier (also volatile); having no memory clobber lets
+// the loads of one output be issued back to back.
+__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+    return v;
+}
+
+// 16-byte global -> shared copy; src_bytes == 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict__ X, const __half* __restrict__ A,
+                                                         __half* __restrict__ T, int Mt, int K, int nsplit) {
+    extern __shared__ __align__(16) unsigned char lds_raw[];
+    __half* As = reinterpret_cast<__half*>(lds_raw);                          // [kPiece][kPitchA]
+    __half* Xs = As + kPiece * kPitchA;                                       // [kTok][kPitchX]
+    float* part = reinterpret_cast<float*>(Xs + kTok * kPitchX);              // [kTok][32]
+
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_rank();
+    const int tokb = blockIdx.y * kTok;  // first token row of this CTA
+    const int ntok = min(kTok, Mt - tokb);
+    const int nch = K / 16;
+    const int c0 = (int)((long long)rank * nch / nsplit), c1 = (int)((long long)(rank + 1) * nch / nsplit);
+
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+
+    bool waited = false;
+    for (int kb = 16 * c0; kb < 16 * c1; kb += kPiece) {
+        const int klen = min(kPiece, 16 * c1 - kb);
+        // A (a weight) first, then X once the producer of X has finished.
+        for (int idx = tid; idx < klen * 4; idx += blockDim.x) {
+            const int row = idx >> 2, c = idx & 3;
+            cp_async16(smem_u32(&As[row * kPitchA + c * 8]), A + (size_t)(kb + row) * 32 + c * 8, 16);
+        }
+        if (!waited) {
+            pdl_wait();
+            waited = true;
+        }
+        const int xc = klen / 8;  // 16-byte chunks per token row
+        for (int idx = tid; idx < kTok * xc; idx += blockDim.x) {
+            const int row = idx / xc, c = idx - row * xc;
+            const bool ok = row < ntok;
+            cp_async16(smem_u32(&Xs[row * kPitchX + c * 8]), ok ? X + (size_t)(tokb + row) * K + kb + c * 8 : X,
+                       ok ? 16u : 0u);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        const int mat = lane >> 3, row8 = lane & 7;
+        for (int kk = 0; kk < klen; kk += 16) {
+            // A operand: X rows warp*16 .. +15, K columns kk .. kk+15 (row-major 16x16)
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(smem_u32(&Xs[(warp * 16 + (mat & 1) * 8 + row8) * kPitchX + kk + (mat >> 1) * 8]), a0, a1, a2, a3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(smem_u32(&As[(kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8]), b0, b1, b2,
+                          b3);
+                mma_16816(acc[2 * h], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[2 * h + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        __syncthreads();
+    }
+    if (!waited) pdl_wait();
+
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+        const int r = nt * 8 + 2 * t;
+        part[(warp * 16 + g) * 32 + r] = acc[nt][0];
+        part[(warp * 16 + g) * 32 + r + 1] = acc[nt][1];
+        part[(warp * 16 + g + 8) * 32 + r] = acc[nt][2];
+        part[(warp * 16 + g + 8) * 32 + r + 1] = acc[nt][3];
+    }
+    cluster_sync_all();
+    // Every CTA of the cluster finishes an interleaved share of the valid
+    // outputs; each output adds the partials in rank order 0..nsplit-1.
+    const int valid = ntok * 32;
+    for (int idx = (int)rank * blockDim.x + tid; idx < valid; idx += nsplit * blockDim.x) {
+        const uint32_t la = smem_u32(&part[idx]);
+        float v[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) v[q] = q < nsplit ? ld_peer_f32(la, (uint32_t)q) : 0.f;
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+            if (q < nsplit) s += v[q];
+        T[(size_t)(tokb + idx / 32) * 32 + (idx & 31)] = __float2half_rn(s);
+    }
+    cluster_sync_all();  // keep every CTA's shared memory alive until all peers have read it
+}
+
+}  // namespace
+
+cudaError_t lora_down_prepare() {
+    return cudaFuncSetAttribute(lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
+}
+
+cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, cudaStream_t st) {
+    const int nch = K / 16;
+    int nsplit = nch < kMaxCluster ? nch : kMaxCluster;
+    if (nsplit < 1) nsplit = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nsplit, (Mt + kTok - 1) / kTok);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kLoraSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = nsplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, lora_down_kernel, X, A, T, Mt, K, nsplit);
+}
+
+}  // namespace mnb

@@ -1,0 +1,164 @@
+/*
+ * mnb.h -- C ABI of libmnb.so: block-quantized MatMulNBits with a fused
+ * rank-32 FP16 LoRA term, for NVIDIA GB300 (sm_103a).
+ *
+ *     Y[m, n] = sum_k X[m, k] * w[n, k]  +  sum_r T[m, r] * B[n, r],   T = X * A
+ *     w[n, k] = (q[n, k] - zp[n, k / 32]) * scale[n, k / 32]
+ *
+ * The operation is the one defined by "[WebGPU] Fuse rank-32 quantized LoRA
+ * with MatMulNBits" (onnxruntime pull request 33370), commit message adding
+ * the MatMulNBitsLoRA operator: INT4 / block-32 base weights, replaceable FP16
+ * rank-32 adapters, B read in its transposed [N, r] layout, an empty adapter
+ * runs only the base projection, and the GEMV-style (decode) or GEMM-style
+ * (prefill) implementation is chosen per call from the per-matrix row count
+ * of X, independent of the batch size.  The dequantization map is the one of
+ * DequantizeLinear followed by MatMul in "Fuse DQ->MatMulNBits for shared
+ * initializers and skip outer-scope weights" (onnxruntime pull request 33800),
+ * Description and repro.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *    and contiguous, 16-byte aligned.  The library keeps no pointer after a
+ *    call returns, copies nothing and never allocates device memory.
+ *  - "fp16" is IEEE binary16.  Codes are unsigned.  INT4 codes are packed two
+ *    per byte along K, code k = 2j in the low nibble of byte j.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    only enqueue work; they never synchronize the host, except
+ *    mnb_sync_status.
+ *  - Return value: MNB_OK (0) or a negative MNB_ERR_* code; on error nothing
+ *    has been enqueued unless the code is MNB_ERR_CUDA.
+ */
+#ifndef MNB_H
+#define MNB_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MNB_OK                   0
+#define MNB_ERR_ARG             -1  /* NULL required pointer, negative size, bad handle */
+#define MNB_ERR_UNSUPPORTED     -2  /* bits not 4/8, block_size not 32, K % 32 != 0, rank not 0/32 */
+#define MNB_ERR_ALIGN           -3  /* a tensor pointer is not 16-byte aligned */
+#define MNB_ERR_CUDA            -4  /* a CUDA runtime call or kernel launch failed */
+#define MNB_ERR_DEVICE_TIMEOUT  -5  /* a bounded device-side wait gave up (see mnb_sync_status) */
+#define MNB_ERR_NO_DEVICE       -6  /* no usable sm_100-family GPU is current */
+
+/* ---- routes (which kernel family ran the last call) -------------------- */
+#define MNB_ROUTE_NONE  0   /* nothing launched: M, N or batch is 0 */
+#define MNB_ROUTE_GEMV  1   /* decode kernel: weight-streaming, mma.sync fragments */
+#define MNB_ROUTE_GEMM  2   /* prefill kernel: TMA + tcgen05 MMA with TMEM accumulators */
+#define MNB_ROUTE_FILL  3   /* K == 0: the output is filled with zeros */
+
+/* ---- mode (mnb_desc.mode) ---------------------------------------------- */
+#define MNB_MODE_AUTO        0  /* GEMV when the per-matrix M <= gemv_max_m, else GEMM */
+#define MNB_MODE_FORCE_GEMV  1  /* always the decode kernel (any M) */
+#define MNB_MODE_FORCE_GEMM  2  /* always the prefill kernel (any M) */
+
+typedef struct mnb_handle_s* mnb_handle;
+
+/* Fixed properties of one quantized projection.
+ *   N, K        output features and input features (K % 32 == 0, both >= 0)
+ *   bits        4 or 8
+ *   block_size  32 (the only supported block)
+ *   max_rank    0 or 32: the largest adapter rank mnb_run will be given
+ *   mode        MNB_MODE_*
+ *   gemv_max_m  largest per-matrix M routed to the decode kernel in AUTO
+ *               mode; <= 0 selects the default 16 */
+typedef struct {
+    int64_t N;
+    int64_t K;
+    int32_t bits;
+    int32_t block_size;
+    int32_t max_rank;
+    int32_t mode;
+    int32_t gemv_max_m;
+} mnb_desc;
+
+/* Launch plan of one call, as computed by the dispatcher (host only). */
+typedef struct {
+    int32_t route;          /* MNB_ROUTE_* */
+    int32_t lora_kernel;    /* 1 if the LoRA down projection kernel runs first */
+    int32_t grid_x, grid_y; /* grid of the main kernel */
+    int32_t block_threads;  /* threads per CTA of the main kernel */
+    int32_t rows_per_cta;   /* GEMV: output rows per CTA; GEMM: output rows per tile */
+    int32_t k_splits;       /* GEMV: warps sharing one 16-row tile along K */
+    int32_t tokens_per_cta; /* GEMV: token rows per CTA (8 or 16); GEMM: token tile */
+} mnb_plan_info;
+
+/* Validate `desc` and create a handle.  Host memory only: no device call is
+ * made, so this works without a GPU.  Errors: MNB_ERR_ARG (NULL pointers,
+ * negative N/K), MNB_ERR_UNSUPPORTED (bits, block_size, K % 32, max_rank). */
+int mnb_create(const mnb_desc* desc, mnb_handle* out);
+
+/* Release a handle (NULL is ignored).  Enqueued work is not waited for. */
+void mnb_destroy(mnb_handle h);
+
+/* Y = X * dequant(Wq)^T (+ (X * A) * B^T), enqueued on `stream`.
+ *   X       fp16 [batch, M, K]
+ *   Wq      uint8 [N, K/32, 16] (INT4) or [N, K/32, 32] (INT8)
+ *   scales  fp16 [N, K/32]
+ *   zp      uint8 [N, K/32], or NULL for the default 2^(bits-1)
+ *   A, B    fp16 [K, rank] and [N, rank] (B is the transposed up weight);
+ *           both NULL or rank == 0 selects the empty adapter (base only)
+ *   rank    0 or 32, at most desc.max_rank
+ *   Y       fp16 [batch, M, N], written entirely
+ *   T_ws    fp16 [batch*M, rank] scratch for T = X * A (rounded to fp16, the
+ *           FP16 intermediate of the fused operator); may be NULL when the
+ *           adapter is empty.  Its contents on return are T.
+ * The kernel family is chosen from the per-matrix row count M (not batch*M).
+ * M, N or batch == 0 launches nothing; K == 0 writes zeros.
+ * Every row of X is independent: [batch, M] gives the same bits as one matrix
+ * of batch*M rows routed the same way.  Results are deterministic run to run.
+ * Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_ALIGN, MNB_ERR_NO_DEVICE,
+ * MNB_ERR_CUDA.  No allocation and no host synchronization happen here. */
+int mnb_run(mnb_handle h,
+            const void* X, const void* Wq, const void* scales, const void* zp,
+            const void* A, const void* B, int32_t rank,
+            void* Y, void* T_ws,
+            int64_t batch, int64_t M, void* stream);
+
+/* The plan mnb_run would use for (batch, M, rank) on a GPU with `sm_count`
+ * SMs (sm_count <= 0: query the current device).  Host only.  Follows the
+ * auto mode selection of the MatMulNBitsLoRA commit message (per-matrix row
+ * count, independent of batch). */
+int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_count,
+             mnb_plan_info* out);
+
+/* MNB_ROUTE_* of the last successful mnb_run on this handle. */
+int mnb_last_route(mnb_handle h);
+
+/* Synchronize `stream`, then read and clear the library's device status word.
+ * Returns MNB_OK, MNB_ERR_DEVICE_TIMEOUT when a bounded device-side wait of a
+ * kernel gave up since the last call (that kernel's output is then
+ * incomplete), or MNB_ERR_CUDA. */
+int mnb_sync_status(mnb_handle h, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* mnb_status_str(int code);
+
+/* The dequantization step on its own: W16[n, k] = fp16_rne((q - zp) * scale),
+ * the weight map of DequantizeLinear in "Fuse DQ->MatMulNBits for shared
+ * initializers and skip outer-scope weights" (Description), computed with the
+ * same device arithmetic as the matmul kernels.  Exact: one rounding.
+ *   W16      fp16 [N, K] output
+ *   variant  0 = the natural-order unpacking the prefill kernel uses,
+ *            1 = the pair-interleaved unpacking the decode kernel uses
+ *            (both must give identical bits)
+ * Errors as for mnb_run. */
+int mnb_dequant(const void* Wq, const void* scales, const void* zp,
+                int64_t N, int64_t K, int32_t bits, int32_t block_size,
+                void* W16, int32_t variant, void* stream);
+
+/* The LoRA down projection on its own: T[m, r] = fp16_rne(sum_k X[m, k] A[k, r]),
+ * "T" of the fuse_up / fuse_down steps in the MatMulNBitsLoRA commit message.
+ *   X fp16 [Mt, K], A fp16 [K, rank], T fp16 [Mt, rank]; rank == 32. */
+int mnb_lora_down(const void* X, const void* A, void* T, int64_t Mt, int64_t K, int32_t rank,
+                  void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MNB_H */

@@ -1,0 +1,156 @@
+"""Host-side checks of libmnb.so that need no GPU: the library loads, exports
+every entry point include/mnb.h declares, validates its arguments and makes
+the dispatch decision from the per-matrix row count.  No compute call here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+from block_quantized_matmul_matmulnbits_gb300 import build as mnb_build
+from block_quantized_matmul_matmulnbits_gb300 import mnb
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    mnb_build.build()
+    yield
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "mnb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mnb_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_what_the_binding_wraps():
+    assert declared_symbols() == sorted(mnb.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(mnb.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = mnb.status_str(code)
+        assert s.startswith("MNB_")
+    assert "UNKNOWN" in mnb.status_str(-99)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=-1, K=64), mnb.MNB_ERR_ARG),
+    (dict(N=64, K=-32), mnb.MNB_ERR_ARG),
+    (dict(N=64, K=48), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(N=64, K=64, bits=2), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(N=64, K=64, block_size=64), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(N=64, K=64, max_rank=16), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(N=64, K=64, mode=7), mnb.MNB_ERR_ARG),
+])
+def test_create_rejects_bad_descriptors(kw, code):
+    with pytest.raises(mnb.MnbError) as e:
+        mnb.mnb_create(**kw)
+    assert e.value.code == code
+
+
+def test_create_accepts_valid_descriptors_and_empty_shapes():
+    for kw in (dict(N=4096, K=4096), dict(N=49152, K=576, bits=8, max_rank=0), dict(N=0, K=0), dict(N=5, K=0)):
+        h = mnb.mnb_create(**kw)
+        mnb.mnb_destroy(h)
+    mnb.mnb_destroy(None)
+
+
+def test_route_follows_per_matrix_rows_not_batch():
+    h = mnb.mnb_create(4096, 4096, 4)
+    try:
+        for M, route in ((1, mnb.ROUTE_GEMV), (16, mnb.ROUTE_GEMV), (17, mnb.ROUTE_GEMM), (1024, mnb.ROUTE_GEMM)):
+            assert mnb.mnb_plan(h, 1, M, 0, 152)["route"] == route
+        # batch never changes the route: 64 one-row matrices stay on the decode path,
+        # 2 x 512 stays on the prefill path
+        assert mnb.mnb_plan(h, 64, 1, 0, 152)["route"] == mnb.ROUTE_GEMV
+        assert mnb.mnb_plan(h, 2, 512, 0, 152)["route"] == mnb.ROUTE_GEMM
+        assert mnb.mnb_plan(h, 0, 5, 0, 152)["route"] == mnb.ROUTE_NONE
+        assert mnb.mnb_plan(h, 3, 0, 0, 152)["route"] == mnb.ROUTE_NONE
+        assert mnb.mnb_plan(h, 1, 1, 32, 152)["lora_kernel"] == 1
+        assert mnb.mnb_plan(h, 1, 1, 0, 152)["lora_kernel"] == 0
+    finally:
+        mnb.mnb_destroy(h)
+
+
+def test_forced_modes_and_threshold():
+    g = mnb.mnb_create(4096, 4096, 4, mode=mnb.MODE_FORCE_GEMV)
+    m = mnb.mnb_create(4096, 4096, 4, mode=mnb.MODE_FORCE_GEMM)
+    t = mnb.mnb_create(4096, 4096, 4, gemv_max_m=64)
+    try:
+        assert mnb.mnb_plan(g, 1, 1024, 0, 152)["route"] == mnb.ROUTE_GEMV
+        assert mnb.mnb_plan(m, 1, 1, 0, 152)["route"] == mnb.ROUTE_GEMM
+        assert mnb.mnb_plan(t, 1, 64, 0, 152)["route"] == mnb.ROUTE_GEMV
+        assert mnb.mnb_plan(t, 1, 65, 0, 152)["route"] == mnb.ROUTE_GEMM
+    finally:
+        for h in (g, m, t):
+            mnb.mnb_destroy(h)
+
+
+def test_k_zero_is_a_fill():
+    h = mnb.mnb_create(100, 0, 4)
+    try:
+        assert mnb.mnb_plan(h, 1, 3, 0, 152)["route"] == mnb.ROUTE_FILL
+    finally:
+        mnb.mnb_destroy(h)
+
+
+def test_gemv_plan_balances_rows_over_sms():
+    for N, K, bits in ((4096, 4096, 4), (14336, 4096, 4), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4)):
+        h = mnb.mnb_create(N, K, bits)
+        try:
+            p = mnb.mnb_plan(h, 1, 1, 0, 152)
+            R = p["rows_per_cta"]
+            assert p["grid_x"] * R >= N and (p["grid_x"] - 1) * R < N
+            assert p["grid_x"] <= 152 or R <= 16
+            assert 32 <= p["block_threads"] <= 512 and p["block_threads"] % 32 == 0
+            assert p["tokens_per_cta"] == 8
+        finally:
+            mnb.mnb_destroy(h)
+
+
+def test_run_validation_needs_no_device():
+    h = mnb.mnb_create(64, 64, 4)
+    try:
+        def rc(**kw):
+            args = dict(X=0x1000, Wq=0x2000, scales=0x3000, zp=None, A=None, B=None, rank=0, Y=0x4000,
+                        T_ws=None, batch=1, M=1)
+            args.update(kw)
+            return mnb.lib().mnb_run(h, args["X"], args["Wq"], args["scales"], args["zp"], args["A"], args["B"],
+                                     args["rank"], args["Y"], args["T_ws"], args["batch"], args["M"], None)
+        assert rc(X=None) == mnb.MNB_ERR_ARG
+        assert rc(Y=None) == mnb.MNB_ERR_ARG
+        assert rc(batch=-1) == mnb.MNB_ERR_ARG
+        assert rc(rank=16) == mnb.MNB_ERR_UNSUPPORTED
+        assert rc(rank=32, A=0x5000, B=None) == mnb.MNB_ERR_ARG
+        assert rc(rank=32, A=0x5000, B=0x6000, T_ws=None) == mnb.MNB_ERR_ARG
+        assert rc(X=0x1008) == mnb.MNB_ERR_ALIGN
+        assert rc(zp=0x7001) == mnb.MNB_ERR_ALIGN
+        assert rc(M=0) == mnb.MNB_OK and mnb.mnb_last_route(h) == mnb.ROUTE_NONE
+        assert rc(batch=0) == mnb.MNB_OK
+    finally:
+        mnb.mnb_destroy(h)
+    h0 = mnb.mnb_create(64, 64, 4, max_rank=0)
+    try:
+        assert mnb.lib().mnb_run(h0, 0x1000, 0x2000, 0x3000, None, 0x5000, 0x6000, 32, 0x4000, 0x7000, 1, 1,
+                                 None) == mnb.MNB_ERR_ARG
+    finally:
+        mnb.mnb_destroy(h0)
+
+
+def test_dequant_and_lora_down_validation_needs_no_device():
+    L = mnb.lib()
+    assert L.mnb_dequant(0x1000, 0x2000, None, 4, 48, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
+    assert L.mnb_dequant(0x1000, 0x2000, None, 4, 64, 4, 32, 0x3000, 2, None) == mnb.MNB_ERR_ARG
+    assert L.mnb_dequant(0x1000, 0x2000, None, 0, 64, 4, 32, 0x3000, 0, None) == mnb.MNB_OK
+    assert L.mnb_dequant(0x1004, 0x2000, None, 4, 64, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_ALIGN
+    assert L.mnb_lora_down(0x1000, 0x2000, 0x3000, 4, 64, 16, None) == mnb.MNB_ERR_UNSUPPORTED
+    assert L.mnb_lora_down(0x1000, 0x2000, 0x3000, 0, 64, 32, None) == mnb.MNB_OK
