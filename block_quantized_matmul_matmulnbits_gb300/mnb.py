@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
 EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_plan", "mnb_last_route", "mnb_sync_status",
-           "mnb_status_str", "mnb_dequant", "mnb_lora_down")
+           "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
 class MnbDesc(ctypes.Structure):
@@ -85,6 +85,10 @@ def lib() -> ctypes.CDLL:
             L.mnb_dequant.restype = ctypes.c_int
             L.mnb_lora_down.argtypes = [P, P, P, I64, I64, I32, P]
             L.mnb_lora_down.restype = ctypes.c_int
+            L.mnb_run_noalloc.argtypes = [P, P, P, P, P, P, P, I32, P, I64, I64, P]
+            L.mnb_run_noalloc.restype = ctypes.c_int
+            L.mnb_noalloc_max_rows.argtypes = []
+            L.mnb_noalloc_max_rows.restype = I64
             _lib = L
     return _lib
 
@@ -134,6 +138,18 @@ def mnb_destroy(h) -> None:
 def mnb_run(h, X, Wq, scales, zp, A, B, rank: int, Y, T_ws, batch: int, M: int, stream=None) -> None:
     _check(lib().mnb_run(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank,
                          _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run")
+
+
+def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:
+    """mnb_run for callers that cannot allocate device memory: T lives in the
+    library's own fixed device array (at most mnb_noalloc_max_rows() token
+    rows with an adapter; concurrent calls on the GPU race on it)."""
+    _check(lib().mnb_run_noalloc(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank,
+                                 _ptr(Y), batch, M, _stream(stream)), "mnb_run_noalloc")
+
+
+def mnb_noalloc_max_rows() -> int:
+    return int(lib().mnb_noalloc_max_rows())
 
 
 def mnb_plan(h, batch: int, M: int, rank: int = 0, sm_count: int = 0) -> dict:

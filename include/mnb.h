@@ -158,6 +158,32 @@ int mnb_dequant(const void* Wq, const void* scales, const void* zp,
 int mnb_lora_down(const void* X, const void* A, void* T, int64_t Mt, int64_t K, int32_t rank,
                   void* stream);
 
+/* mnb_run without the T_ws argument, for callers that cannot allocate device
+ * memory: code running inside a host runtime that owns every device
+ * allocation and gives plugins no allocator, or latency-critical loops where
+ * cudaMalloc / cudaFree are not allowed because they can synchronize the
+ * device.  The pages have no counterpart to this entry point; it exists only
+ * for such callers.
+ *   Arguments and results are those of mnb_run, minus T_ws.  T lives in a
+ *   fixed array inside the library's device memory (512 KiB on every GPU that
+ *   loads the library, held until the process exits), so at most
+ *   mnb_noalloc_max_rows() = 8192 token rows (batch * M) are accepted when an
+ *   adapter is given; larger calls return MNB_ERR_UNSUPPORTED and launch
+ *   nothing.  Without an adapter there is no limit.
+ *   No cudaMalloc, cudaFree or other allocating call is made.  The first call
+ *   with an adapter on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) for that device; make that first call before any
+ *   stream capture.
+ *   Every call shares the one array: calls whose kernels may overlap on the
+ *   GPU (other streams, or other host threads without ordering) race on it. */
+int mnb_run_noalloc(mnb_handle h,
+                    const void* X, const void* Wq, const void* scales, const void* zp,
+                    const void* A, const void* B, int32_t rank,
+                    void* Y, int64_t batch, int64_t M, void* stream);
+
+/* Largest batch * M mnb_run_noalloc accepts with an adapter. */
+int64_t mnb_noalloc_max_rows(void);
+
 #ifdef __cplusplus
 }
 #endif
