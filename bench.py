@@ -179,7 +179,8 @@ class Workload:
             c["Y"] = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
             c["T"] = torch.empty((M, rank), dtype=torch.float16, device="cuda") if rank else None
             self.copies.append(c)
-        self.h = mnb.mnb_create(N, K, bits, 32, 32, 0, 0)
+        # decode loops keep the weights constant: let each call stream them early
+        self.h = mnb.mnb_create(N, K, bits, 32, 32, 0, 0, mnb.FLAG_EARLY_WEIGHTS)
 
     def step(self, i, rank=None):
         c = self.copies[i % len(self.copies)]
@@ -347,7 +348,7 @@ def run_gpu_arm(args, dist_ctx):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded)",
         "config": {"workload": "decode GEMV M=1 K=4096 N=4096 INT4 block-32, explicit uint8 zero points, "
                                "rank-32 FP16 LoRA (A,B ~ N(0,0.02))", "M": 1, "K": 4096, "N": 4096, "bits": 4,
-                   "rank": 32, "bytes_per_step": step_bytes,
+                   "rank": 32, "bytes_per_step": step_bytes, "flags": "MNB_FLAG_EARLY_WEIGHTS",
                    "l2": f"inputs larger than L2: {copies} rotating weight copies "
                          f"({copies * step_bytes / 2 ** 20:.0f} MiB vs {l2 / 2 ** 20:.0f} MiB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

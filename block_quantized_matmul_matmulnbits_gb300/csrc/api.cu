@@ -48,6 +48,7 @@ int validate_desc(const mnb_desc* d) {
     if (d->K % 32 != 0) return MNB_ERR_UNSUPPORTED;
     if (d->max_rank != 0 && d->max_rank != 32) return MNB_ERR_UNSUPPORTED;
     if (d->mode < MNB_MODE_AUTO || d->mode > MNB_MODE_FORCE_GEMM) return MNB_ERR_ARG;
+    if ((d->flags & ~MNB_FLAG_EARLY_WEIGHTS) != 0) return MNB_ERR_ARG;
     return MNB_OK;
 }
 
@@ -86,32 +87,17 @@ int device_setup(int* sm_count, unsigned int** status = nullptr) {
 
 int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// Decode-kernel geometry: balanced row ranges, one CTA per SM, up to 16 warps.
-void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p, int* maxseg_out) {
-    const int64_t N = d.N;
-    const int rowbytes = (int)(d.K * d.bits / 8);
-    const int steps = cdiv(rowbytes, 64);
-    const int tok = Mt <= 8 ? 8 : 16;
-    int ctas = sms > 0 ? sms : 1;
-    int R, warps, maxseg;
-    for (;;) {
-        R = cdiv(N, ctas);
-        const int RT = cdiv(R, 16);
-        const int64_t items = (int64_t)RT * steps;
-        warps = (int)(items < 16 ? (items > 0 ? items : 1) : 16);
-        const int64_t per = (items + warps - 1) / warps;
-        maxseg = (int)((per + steps - 1) / (steps > 0 ? steps : 1)) + 1;
-        if (mnb::gemv_smem_bytes(warps, maxseg, tok) <= (size_t)mnb::kGemvMaxSmem || R <= 16) break;
-        ctas *= 2;  // too many rows per CTA for the reduction buffer: spread over more CTAs
-    }
+// Decode-kernel geometry: balanced row ranges, one CTA per SM and token group.
+void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
+    int R, CH, tok, threads;
+    mnb::gemv_geometry((int)d.N, (int)d.K, d.bits, (int)Mt, sms, &R, &CH, &tok, &threads);
     p->route = MNB_ROUTE_GEMV;
-    p->grid_x = cdiv(N, R);
+    p->grid_x = cdiv(d.N, R);
     p->grid_y = cdiv(Mt, tok);
-    p->block_threads = warps * 32;
+    p->block_threads = threads;
     p->rows_per_cta = R;
-    p->k_splits = 0;
+    p->k_splits = CH;
     p->tokens_per_cta = tok;
-    *maxseg_out = maxseg;
 }
 
 // Prefill-kernel geometry: 128 weight rows x up to 256 token rows per tile,
@@ -128,9 +114,8 @@ void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
     p->tokens_per_cta = tok;
 }
 
-int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p, int* maxseg) {
+int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p) {
     *p = mnb_plan_info{};
-    *maxseg = 0;
     const int64_t Mt = batch * M;
     if (Mt == 0 || d.N == 0) {
         p->route = MNB_ROUTE_NONE;
@@ -145,7 +130,7 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
     if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
     if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
     if (route == MNB_ROUTE_GEMV)
-        plan_gemv(d, Mt, sms, p, maxseg);
+        plan_gemv(d, Mt, sms, p);
     else
         plan_gemm(d, Mt, sms, p);
     p->lora_kernel = rank > 0 ? 1 : 0;
@@ -183,8 +168,7 @@ int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_co
         const int rc = device_setup(&sms);
         if (rc != MNB_OK) return rc;
     }
-    int maxseg;
-    return make_plan(h->d, batch, M, rank, sms, out, &maxseg);
+    return make_plan(h->d, batch, M, rank, sms, out);
 }
 
 int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
@@ -210,14 +194,13 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         return MNB_ERR_ALIGN;
 
     mnb_plan_info p;
-    int maxseg = 0;
     int sms = 0;
     unsigned int* status = nullptr;
     if (Mt > 0 && d.N > 0) {
         const int rc = device_setup(&sms, &status);
         if (rc != MNB_OK) return rc;
     }
-    make_plan(d, batch, M, rank, sms, &p, &maxseg);
+    make_plan(d, batch, M, rank, sms, &p);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
 
@@ -235,10 +218,16 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
 
     const __half* Xh = static_cast<const __half*>(X);
     __half* Th = static_cast<__half*>(T_ws);
+    // Programmatic dependent launch: with early weights every kernel may start
+    // before its predecessor on the stream ends (and only reads X / T after
+    // griddepcontrol.wait); otherwise only the matmul kernel overlaps the
+    // LoRA down kernel of the same call.
+    const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
     if (rank > 0) {
-        e = mnb::lora_down_launch(Xh, static_cast<const __half*>(A), Th, (int)Mt, (int)d.K, st);
+        e = mnb::lora_down_launch(Xh, static_cast<const __half*>(A), Th, (int)Mt, (int)d.K, early, st);
         if (e != cudaSuccess) return MNB_ERR_CUDA;
     }
+    const bool pdl = rank > 0 || early;
     if (p.route == MNB_ROUTE_GEMV) {
         mnb::GemvArgs a;
         a.X = Xh;
@@ -251,10 +240,11 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.Mt = (int)Mt;
         a.N = (int)d.N;
         a.K = (int)d.K;
-        a.rows_per_cta = p.rows_per_cta;
-        a.maxseg = maxseg;
+        a.R = p.rows_per_cta;
+        a.CH = p.k_splits;
         a.rank = rank;
-        e = mnb::gemv_launch(a, p, d.bits, rank > 0, st);
+        a.status = status;
+        e = mnb::gemv_launch(a, p, d.bits, pdl, st);
     } else {
         mnb::GemmArgs a;
         a.X = Xh;
@@ -270,7 +260,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.bits = d.bits;
         a.rank = rank;
         a.status = status;
-        e = mnb::gemm_launch(a, p, rank > 0, st);
+        e = mnb::gemm_launch(a, p, pdl, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return MNB_ERR_CUDA;
@@ -337,7 +327,7 @@ int mnb_lora_down(const void* X, const void* A, void* T, int64_t Mt, int64_t K, 
     }
     if (!X || !A) return MNB_ERR_ARG;
     const cudaError_t e = mnb::lora_down_launch(static_cast<const __half*>(X), static_cast<const __half*>(A),
-                                                static_cast<__half*>(T), (int)Mt, (int)K, st);
+                                                static_cast<__half*>(T), (int)Mt, (int)K, false, st);
     return e == cudaSuccess ? MNB_OK : MNB_ERR_CUDA;
 }
 

@@ -6,25 +6,29 @@
 // adding MatMulNBitsLoRA: base GEMV and LoRA down projection first, then the
 // base plus T * Bt^T), restated for sm_103a:
 //
-//  * Every packed weight byte is read from HBM exactly once per token group:
-//    CTA c owns output rows [c R, (c+1) R) with R = ceil(N / #SMs), so every SM
-//    streams the same number of bytes.
-//  * Inside a CTA the work is a list of items (16-row tile, 64-byte K step);
-//    warp w takes the contiguous item range [w I / W, (w+1) I / W), so all
-//    warps carry the same load whatever the shape.  A thread loads 16 bytes
-//    of two rows (g and g+8 of the tile) per step with 128-bit loads that
-//    bypass L1; 4 steps are in flight per thread before any is consumed.
-//  * Codes are unpacked and dequantized in registers (exact (q - zp), one
-//    rounding by the scale, see common.cuh) straight into the A fragments of
-//    mma.sync m16n8k16 (FP16 in, FP32 accumulate), the 8 or 16 token rows
-//    being the N side.  INT4 uses the pair-interleaved unpacking: the K order
-//    inside each 8-code word is permuted identically for the weight and the X
-//    fragment, which leaves the sum unchanged.
-//  * Partial sums of the warps that share a tile are added in shared memory in
-//    a fixed order (deterministic, no atomics), then the LoRA term is added:
-//    T (written by the LoRA down kernel, which this grid waits for with
-//    griddepcontrol.wait only now, after the weight stream) times the
-//    adapter row B[n, :].  Output is rounded once to FP16.
+//  * Every packed weight byte is read from HBM once per token group.  CTA c
+//    owns output rows [c R, (c+1) R) with R = ceil(N / (2 #SMs)), two CTAs per
+//    SM, so every SM streams the same number of bytes.
+//  * A producer warp streams the CTA's rows through a ring of shared-memory
+//    stages.  A stage is one 16-row group x one K chunk of at most 1 KB per
+//    row, moved with 1-D bulk copies (one copy for the whole group when a
+//    chunk is a full row, since the rows are contiguous), together with the
+//    group's scales, zero points and adapter rows B[n, :].  Large contiguous
+//    copies keep the copy engine near the HBM rate; small 2-D boxes do not.
+//    The producer never waits on the work queued before this kernel: weights
+//    are prefetched while that work (or the LoRA down kernel) still runs.
+//  * Eight consumer warps wait (griddepcontrol.wait) for X and T, then split
+//    each stage along K in 64-byte pieces: 16-byte loads of rows g and g+8
+//    from shared memory, exact (q - zp) and one rounding by the scale in
+//    registers (common.cuh), straight into mma.sync m16n8k16 A fragments with
+//    the 8 or 16 token rows as the N side (FP32 accumulate, independent
+//    accumulator chains, X fragments prefetched one stage ahead).  INT4 uses
+//    the pair-interleaved unpacking; the same K permutation is applied to the
+//    X fragment, which leaves the sum unchanged.
+//  * After a group's last chunk the warps' partial sums are added in shared
+//    memory in warp order (deterministic, no atomics), the LoRA term
+//    T[m, :] . B[n, :] is added, and each output is rounded once to FP16.
+//  * Waits on the ring are bounded and report through the status word.
 #include "common.cuh"
 #include "mnb_internal.h"
 
@@ -32,209 +36,353 @@ namespace mnb {
 
 namespace {
 
-// K steps in flight per thread: 4 with one n8 token tile, 2 with two (registers).
-template <int NT>
-struct Unroll {
-    static constexpr int value = NT == 1 ? 4 : 2;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreadsGemv = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxRing = 4;                                // ring stages (2 or 4)
+constexpr uint32_t kXStageMax = 24 * 1024;                 // largest X tile staged in shared memory
+constexpr int kGroup = 16;                                 // rows per stage / MMA tile
+constexpr int kMaxChunk = 1024;                            // K bytes per row and stage
+
+struct GemvLayout {
+    uint32_t stage;            // bytes of one ring stage
+    uint32_t w, sc, zp, b;     // offsets inside a stage: codes, scales, zero points, B rows
+    uint32_t x, t, red, bars, total;
 };
 
-__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory layout, identical on host and device.  `ch` = K bytes per chunk,
+// `ring` = stages (2 or 4), `xbytes` = staged X (0 when X is read from global).
+__host__ __device__ inline GemvLayout gemv_layout(int ch, int nblk, int tok, int ring, uint32_t xbytes) {
+    GemvLayout L;
+    L.w = 0;
+    L.sc = align_up((uint32_t)kGroup * ch + 128u, 128u);  // + slack: the last 128-byte piece may pass CH
+    L.zp = L.sc + align_up((uint32_t)kGroup * nblk * 2u + 32u, 128u);
+    L.b = L.zp + align_up((uint32_t)kGroup * nblk + 32u, 128u);
+    L.stage = L.b + kGroup * 64u;
+    uint32_t off = (uint32_t)ring * L.stage;
+    L.x = off;
+    off += align_up(xbytes, 128u);
+    L.t = off;
+    off += align_up((uint32_t)tok * 64u, 128u);
+    L.red = off;  // two buffers (alternate groups)
+    off += 2u * kConsumerWarps * kGroup * tok * 4u;
+    L.bars = align_up(off, 16u);
+    L.total = L.bars + 2 * (uint32_t)ring * 8;
+    return L;
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-template <int BITS, bool HAS_ZP, int NT>
-__global__ void __launch_bounds__(512, 1) gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(16) float red[];  // [W][maxseg][16][TOK] then T rows
+// Plain C++ shared-memory loads (byte offsets into the dynamic shared array):
+// ordered after the mbarrier waits by their memory clobber, otherwise free to
+// be scheduled early by the compiler.
+__device__ __forceinline__ uint4 lds128(const unsigned char* sm, uint32_t off) {
+    return *reinterpret_cast<const uint4*>(sm + off);
+}
+__device__ __forceinline__ uint32_t lds_u16(const unsigned char* sm, uint32_t off) {
+    return *reinterpret_cast<const uint16_t*>(sm + off);
+}
+__device__ __forceinline__ uint32_t lds_u8(const unsigned char* sm, uint32_t off) { return sm[off]; }
+
+template <int BITS, bool HAS_ZP, int NT, bool XS>
+__global__ void __launch_bounds__(kThreadsGemv, 2)
+    gemv_kernel(const GemvArgs a) {
+    extern __shared__ __align__(1024) unsigned char sm[];
     constexpr int TOK = 8 * NT;
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
-    constexpr int kBytesPerBlock = 32 * BITS / 8;  // 16 (INT4) or 32 (INT8)
-    constexpr int kUnroll = Unroll<NT>::value;
+    constexpr int kBpb = 32 * BITS / 8;  // packed bytes per quantization block
 
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int warp = threadIdx.x >> 5, W = blockDim.x >> 5;
-    const int rowbytes = a.K * BITS / 8;
     const int nblk = a.K >> 5;
-    const int steps = (rowbytes + 63) >> 6;
-    const int row_begin = blockIdx.x * a.rows_per_cta;
-    const int row_end = min(a.N, row_begin + a.rows_per_cta);
-    const int nrows = row_end - row_begin;
-    const int RT = (nrows + 15) >> 4;
+    const int rowbytes = a.K * BITS / 8;
+    const int CH = a.CH;                                  // K bytes per chunk
+    const int nchunk = (rowbytes + CH - 1) / CH;
+    const int ring = a.ring, rmask = a.ring - 1;
+    const GemvLayout L = gemv_layout(CH, nblk, TOK, ring, XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
+    const uint32_t sb = smem_u32(sm);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = blockIdx.x * a.R;
+    const int r1 = min(a.N, r0 + a.R);
+    const int ngroups = (r1 - r0 + kGroup - 1) / kGroup;
+    const int nstages = ngroups * nchunk;
     const int token0 = blockIdx.y * TOK;
-    const int total = RT * steps;  // items; bounded by the host plan (< 2^31 / 16)
-    const int i0 = (int)((long long)total * warp / W), i1 = (int)((long long)total * (warp + 1) / W);
-    const int tile_first = i0 / steps;
+    unsigned int* status = a.status;
 
-    __shared__ int wrange[2 * 32];  // item range [i0, i1) of every warp, read by the epilogue
-    if (lane == 0) {
-        wrange[2 * warp] = i0;
-        wrange[2 * warp + 1] = i1;
+    auto full = [&](int s) { return sb + L.bars + 8u * s; };
+    auto empty = [&](int s) { return sb + L.bars + 8u * (ring + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ring; ++s) {
+            mbar_init(full(s), 2);  // lane 0: bulk copies (+ bytes); lane 1: tail bytes
+            mbar_init(empty(s), kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    pdl_launch_dependents();
 
-    for (int i = i0; i < i1;) {
-        const int tile = i / steps;
-        const int js = i - tile * steps;
-        const int je = min(steps, js + (i1 - i));
-        i += je - js;
-
-        const int rA = row_begin + tile * 16 + g, rB = rA + 8;
-        const bool vA = rA < row_end, vB = rB < row_end;
-        const uint8_t* wA = a.Wq + (size_t)rA * rowbytes;
-        const uint8_t* wB = a.Wq + (size_t)rB * rowbytes;
-        const uint16_t* sA = reinterpret_cast<const uint16_t*>(a.S) + (size_t)rA * nblk;
-        const uint16_t* sB = reinterpret_cast<const uint16_t*>(a.S) + (size_t)rB * nblk;
-        const uint8_t* zA = a.Z + (size_t)rA * nblk;
-        const uint8_t* zB = a.Z + (size_t)rB * nblk;
-
-        float acc[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-
-        for (int j = js; j < je; j += kUnroll) {
-            uint4 wa[kUnroll], wb[kUnroll];
-            uint32_t sa[kUnroll], sb[kUnroll], za[kUnroll], zb[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int off = (j + u) * 64 + t * 16;
-                const bool kv = (j + u < je) && off < rowbytes;
-                const int blk = off / kBytesPerBlock;
-                const bool la = kv && vA, lb = kv && vB;
-                wa[u] = la ? ldg_stream16(wA + off) : make_uint4(0, 0, 0, 0);
-                wb[u] = lb ? ldg_stream16(wB + off) : make_uint4(0, 0, 0, 0);
-                sa[u] = la ? __ldg(sA + blk) : 0u;
-                sb[u] = lb ? __ldg(sB + blk) : 0u;
-                if (HAS_ZP) {
-                    za[u] = la ? __ldg(zA + blk) : 0u;
-                    zb[u] = lb ? __ldg(zB + blk) : 0u;
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const uint64_t total_s = (uint64_t)a.N * nblk * 2, total_z = (uint64_t)a.N * nblk;
+        if (lane < 2) {
+            bool ok = true;
+            for (int st = 0; ok && st < nstages; ++st) {
+                const int s = st & rmask;
+                const int q = st / nchunk, c = st - q * nchunk;
+                const int ra = r0 + q * kGroup, rows = min(kGroup, r1 - ra);
+                const uint32_t slot = sb + (uint32_t)s * L.stage;
+                if (!(ok = mbar_wait(empty(s), ((uint32_t)(st / ring) & 1u) ^ 1u, status))) break;
+                // scales / zero points of the group's full rows as 16-byte aligned supersets;
+                // bytes past the last 16-byte boundary of an array come from lane 1
+                const uint64_t s0 = (uint64_t)ra * nblk * 2, s1 = (uint64_t)(ra + rows) * nblk * 2;
+                const uint64_t s_lo = s0 & ~15ull, s_hi = min((s1 + 15) & ~15ull, total_s & ~15ull);
+                const uint64_t z0 = (uint64_t)ra * nblk, z1 = (uint64_t)(ra + rows) * nblk;
+                const uint64_t z_lo = z0 & ~15ull, z_hi = min((z1 + 15) & ~15ull, total_z & ~15ull);
+                if (lane == 0) {
+                    const int cb = min(CH, rowbytes - c * CH);  // bytes of this chunk per row
+                    uint32_t bytes = (uint32_t)rows * (uint32_t)cb;
+                    if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
+                    if (HAS_ZP && z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
+                    if (a.rank > 0) bytes += (uint32_t)rows * 64u;
+                    mbar_arrive_tx(full(s), bytes);
+                    const uint8_t* src = a.Wq + (size_t)ra * rowbytes + (size_t)c * CH;
+                    if (nchunk == 1) {
+                        bulk_load(slot + L.w, src, (uint32_t)(rows * rowbytes), full(s));  // rows are contiguous
+                    } else {
+                        for (int i = 0; i < rows; ++i)
+                            bulk_load(slot + L.w + (uint32_t)(i * CH), src + (size_t)i * rowbytes, (uint32_t)cb, full(s));
+                    }
+                    if (s_hi > s_lo)
+                        bulk_load(slot + L.sc, reinterpret_cast<const uint8_t*>(a.S) + s_lo, (uint32_t)(s_hi - s_lo),
+                                  full(s));
+                    if (HAS_ZP && z_hi > z_lo) bulk_load(slot + L.zp, a.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
+                    if (a.rank > 0) bulk_load(slot + L.b, a.B + (size_t)ra * 32, (uint32_t)rows * 64u, full(s));
                 } else {
-                    za[u] = kDefaultZp;
-                    zb[u] = kDefaultZp;
+                    unsigned char* st8 = sm + (uint32_t)s * L.stage;
+                    for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
+                        st8[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(a.S)[i];
+                    if (HAS_ZP)
+                        for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) st8[L.zp + (uint32_t)(i - z_lo)] = a.Z[i];
+                    mbar_arrive(full(s));
                 }
             }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int ctid = threadIdx.x;  // 0..255
+    pdl_wait();                    // X and T are produced by work queued before this kernel
+    if (a.rank > 0) {
+        for (int i = ctid; i < TOK * 32; i += kConsumerWarps * 32) {
+            const int tok = token0 + i / 32;
+            reinterpret_cast<__half*>(sm + L.t)[i] = tok < a.Mt ? a.T[(size_t)tok * 32 + (i & 31)] : __float2half_rn(0.f);
+        }
+    }
+    if (XS) {
+        // X rows of this token group into shared memory, once; for INT4 each group
+        // of 8 codes is stored in the pair-interleaved order (0,4,1,5,2,6,3,7) the
+        // unpacking produces, so the inner loop needs no permutes.
+        const int mv = min(TOK, a.Mt - token0), kc = a.K / 8;
+        for (int i = ctid; i < mv * kc; i += kConsumerWarps * 32) {
+            const int row = i / kc, c8 = i - row * kc;
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(token0 + row) * a.K) + c8);
+            if (BITS == 4)
+                v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
+                               prmt(v.y, v.w, 0x7632u));
+            *reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c8 * 8u) * 2u) = v;
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);
+    }
+    float* red = reinterpret_cast<float*>(sm + L.red);
+    const int npieces = (CH + 127) / 128;  // 128-byte pieces per chunk row: 32 bytes per thread and row
+    // shared-memory row pitch: a single-chunk group is one contiguous copy of full rows
+    const uint32_t pitch = nchunk == 1 ? (uint32_t)rowbytes : (uint32_t)CH;
+
+    // Independent accumulator chains per n8 tile, summed at the end of a group,
+    // so consecutive MMAs of a warp do not wait on each other.
+    constexpr int kChains = NT == 1 ? 4 : 2;
+    float acc[NT][kChains][4];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                if (j + u >= je) break;  // warp-uniform
-                const int off = (j + u) * 64 + t * 16;
-                const bool kv = off < rowbytes;
-                const int k0 = off * 8 / BITS;  // first K index of this thread's 16 bytes
-                const DqConst cA = dq_const(za[u], (uint16_t)sa[u]);
-                const DqConst cB = dq_const(zb[u], (uint16_t)sb[u]);
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int qq = 0; qq < kChains; ++qq)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][qq][e] = 0.f;
+
+    // Loop-invariant per-thread pieces of every address.  Loads are issued
+    // unconditionally at clamped, in-bounds addresses; invalid values are then
+    // replaced by zeros with selects, so the inner loop has no branches.
+    const __half* xrow[NT];
+    bool xok[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int tok = token0 + nt * 8 + g;
+        xok[nt] = tok < a.Mt;
+        xrow[nt] = a.X + (size_t)(xok[nt] ? tok : 0) * a.K;
+    }
+    const int Mt = a.Mt, rank = a.rank;
+    // last X element offset at which one half's X loads (8 halfs per 16-byte load) stay inside the row
+    const int xmax = a.K - 8 * (BITS == 4 ? 4 : 2);
+    const uint32_t w_thr = L.w + (uint32_t)g * pitch + (uint32_t)t * 32u;      // row g, this thread's 32 bytes
+    const uint32_t w_rowB = 8u * pitch;                                         // row g+8 relative to row g
+    const uint32_t s_thr = L.sc + (uint32_t)g * (uint32_t)nblk * 2u;           // scales of row g
+    const uint32_t z_thr = L.zp + (uint32_t)g * (uint32_t)nblk;                // zero points of row g
+    const uint32_t s_rowB = 8u * (uint32_t)nblk * 2u, z_rowB = 8u * (uint32_t)nblk;
+    const int blk_thr = t * 32 / kBpb;  // block of the thread's first byte within a 128-byte piece
+
+    bool ok = true;
+    int q = 0, c = 0;  // group and chunk of stage st (counters: no divisions in the loop)
+    for (int st = 0; st < nstages; ++st) {
+        const int s = st & rmask;
+        const int ra = r0 + q * kGroup, rows = min(kGroup, r1 - ra);
+        if (ok) ok = mbar_wait(full(s), (uint32_t)(st / ring) & 1u, status);
+        const uint32_t soff = (uint32_t)s * L.stage;  // byte offset of the stage in `sm`
+        const uint32_t s_al = ((uint32_t)ra * (uint32_t)nblk * 2u) & 15u;  // scale copy alignment offset
+        const uint32_t z_al = ((uint32_t)ra * (uint32_t)nblk) & 15u;
+        const bool vA = g < rows, vB = g + 8 < rows;
+        const int kchunk = c * CH;
+        for (int p = warp; ok && p < npieces; p += kConsumerWarps) {
+            const int kb = kchunk + p * 128 + t * 32;  // first byte of this thread's 32 in the row
+            const uint32_t wpc = soff + w_thr + (uint32_t)p * 128u;
+            const int blk0 = (kchunk + p * 128) / kBpb + blk_thr;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // two 16-byte halves
+                const int kbh = kb + 16 * h;
+                const bool kv = kbh < rowbytes;
+                const int blk = blk0 + (BITS == 4 ? h : 0);
+                // X of these 16 bytes' codes, for this thread's token rows
+                constexpr int kXv = BITS == 4 ? 4 : 2;
+                const int kx = min(kbh * 8 / BITS, xmax);
+                uint4 xv[NT][kXv];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const bool use = kv && xok[nt];
+#pragma unroll
+                    for (int w = 0; w < kXv; ++w) {
+                        uint4 v = make_uint4(0, 0, 0, 0);
+                        if (XS) {
+                            if (use) v = lds128(sm, L.x + ((uint32_t)(nt * 8 + g) * a.K + (uint32_t)kx) * 2u + 16u * w);
+                        } else {
+                            if (use) v = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + kx) + w);  // predicated
+                        }
+                        xv[nt][w] = v;
+                    }
+                }
+                const uint4 wa = lds128(sm, wpc + 16u * h);
+                const uint4 wb = lds128(sm, wpc + 16u * h + w_rowB);
+                const uint32_t so = soff + s_thr + s_al + (uint32_t)blk * 2u;
+                const uint32_t sa0 = lds_u16(sm, so), sb0 = lds_u16(sm, so + s_rowB);
+                const uint32_t sa = (kv && vA) ? sa0 : 0u;  // a zero scale removes the row / K tail
+                const uint32_t sbv = (kv && vB) ? sb0 : 0u;
+                uint32_t za = kDefaultZp, zb = kDefaultZp;
+                if (HAS_ZP) {
+                    const uint32_t zo = soff + z_thr + z_al + (uint32_t)blk;
+                    za = lds_u8(sm, zo);
+                    zb = lds_u8(sm, zo + z_rowB);
+                }
+                const DqConst cA = dq_const(za, (uint16_t)sa);
+                const DqConst cB = dq_const(zb, (uint16_t)sbv);
                 if constexpr (BITS == 4) {
-                    // 32 codes = 4 words of 8 codes; X in the same interleaved pair order.
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
                         uint32_t dA[4], dB[4];
-                        dq_int4_interleaved(word_of(wa[u], w), cA, dA);
-                        dq_int4_interleaved(word_of(wb[u], w), cB, dB);
+                        dq_int4_interleaved(word_of(wa, w), cA, dA);
+                        dq_int4_interleaved(word_of(wb, w), cB, dB);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const int tok = token0 + nt * 8 + g;
-                            uint4 xv = make_uint4(0, 0, 0, 0);
-                            if (kv && tok < a.Mt)
-                                xv = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)tok * a.K + k0 + 8 * w));
-                            const uint32_t x04 = prmt(xv.x, xv.z, 0x5410u), x15 = prmt(xv.x, xv.z, 0x7632u);
-                            const uint32_t x26 = prmt(xv.y, xv.w, 0x5410u), x37 = prmt(xv.y, xv.w, 0x7632u);
-                            mma_16816(acc[nt], dA[0], dB[0], dA[1], dB[1], x04, x15);
-                            mma_16816(acc[nt], dA[2], dB[2], dA[3], dB[3], x26, x37);
+                            const uint4 x = xv[nt][w];
+                            // staged X is already in pair-interleaved order
+                            const uint32_t x04 = XS ? x.x : prmt(x.x, x.z, 0x5410u);
+                            const uint32_t x15 = XS ? x.y : prmt(x.x, x.z, 0x7632u);
+                            const uint32_t x26 = XS ? x.z : prmt(x.y, x.w, 0x5410u);
+                            const uint32_t x37 = XS ? x.w : prmt(x.y, x.w, 0x7632u);
+                            mma_16816(acc[nt][(2 * w) % kChains], dA[0], dB[0], dA[1], dB[1], x04, x15);
+                            mma_16816(acc[nt][(2 * w + 1) % kChains], dA[2], dB[2], dA[3], dB[3], x26, x37);
                         }
                     }
                 } else {
-                    // 16 codes = 4 words of 4 codes, natural pair order.
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 xv[NT];
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t dA[2], dB[2];
+                        dq_int8_natural(word_of(wa, w), cA, dA);
+                        dq_int8_natural(word_of(wb, w), cB, dB);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const int tok = token0 + nt * 8 + g;
-                            xv[nt] = make_uint4(0, 0, 0, 0);
-                            if (kv && tok < a.Mt)
-                                xv[nt] = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)tok * a.K + k0 + 8 * h));
-                        }
-#pragma unroll
-                        for (int ww = 0; ww < 2; ++ww) {
-                            const int w = 2 * h + ww;
-                            uint32_t dA[2], dB[2];
-                            dq_int8_natural(word_of(wa[u], w), cA, dA);
-                            dq_int8_natural(word_of(wb[u], w), cB, dB);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt) {
-                                const uint32_t b0 = ww == 0 ? xv[nt].x : xv[nt].z;
-                                const uint32_t b1 = ww == 0 ? xv[nt].y : xv[nt].w;
-                                mma_16816(acc[nt], dA[0], dB[0], dA[1], dB[1], b0, b1);
-                            }
+                            const uint4 x = xv[nt][w >> 1];
+                            const uint32_t b0 = (w & 1) == 0 ? x.x : x.z;
+                            const uint32_t b1 = (w & 1) == 0 ? x.y : x.w;
+                            mma_16816(acc[nt][w % kChains], dA[0], dB[0], dA[1], dB[1], b0, b1);
                         }
                     }
                 }
             }
         }
+        const bool last_chunk = c == nchunk - 1;
+        if (++c == nchunk) {
+            c = 0;
+            ++q;
+        }
+        if (!last_chunk) {
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(empty(s));
+            continue;
+        }
 
-        // C fragment: (row g, tokens 2t, 2t+1) and (row g+8, same tokens), per n8 tile.
-        float* r = red + ((size_t)(warp * a.maxseg + (tile - tile_first)) * 16) * TOK;
+        // Last chunk of the group: partial sums (row g, tokens 2t, 2t+1), (row g+8,
+        // same), per n8 tile.  The buffer alternates between groups, so one barrier
+        // per group suffices: a warp writes the partials of group q+2 only after
+        // every warp passed group q+1's barrier, i.e. after all reads of group q.
+        float* redq = red + (size_t)((q - 1) & 1) * kConsumerWarps * kGroup * TOK;
+        float* r = redq + (size_t)warp * kGroup * TOK;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            r[g * TOK + nt * 8 + 2 * t] = acc[nt][0];
-            r[g * TOK + nt * 8 + 2 * t + 1] = acc[nt][1];
-            r[(g + 8) * TOK + nt * 8 + 2 * t] = acc[nt][2];
-            r[(g + 8) * TOK + nt * 8 + 2 * t + 1] = acc[nt][3];
-        }
-    }
-
-    __half* tsm = reinterpret_cast<__half*>(red + (size_t)W * a.maxseg * 16 * TOK);
-    if (a.rank > 0) {
-        pdl_wait();  // T is written by the LoRA down kernel that precedes this grid
-        for (int idx = threadIdx.x; idx < TOK * 32; idx += blockDim.x) {
-            const int tok = token0 + idx / 32;
-            tsm[idx] = tok < a.Mt ? a.T[(size_t)tok * 32 + (idx & 31)] : __float2half_rn(0.f);
-        }
-    }
-    __syncthreads();
-
-    for (int idx = threadIdx.x; idx < nrows * TOK; idx += blockDim.x) {
-        const int tok = idx / nrows, rr = idx - tok * nrows;
-        const int token = token0 + tok;
-        if (token >= a.Mt) continue;
-        const int tile = rr >> 4, rit = rr & 15;
-        float sum = 0.f;
-        const int t_lo = tile * steps, t_hi = t_lo + steps;
-        for (int w = 0; w < W; ++w) {  // fixed order over the warps that covered this tile
-            const int w0 = wrange[2 * w], w1 = wrange[2 * w + 1];
-            if (w0 >= w1 || w1 <= t_lo || w0 >= t_hi) continue;
-            const int tf = w0 / steps;
-            sum += red[((size_t)(w * a.maxseg + (tile - tf)) * 16 + rit) * TOK + tok];
-        }
-        const int n = row_begin + rr;
-        if (a.rank > 0) {
-            const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)n * 32);
-            float l = 0.f;
+            float v[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 bv = __ldg(brow + q);
-                const __half* bh = reinterpret_cast<const __half*>(&bv);
+            for (int e = 0; e < 4; ++e) {
+                v[e] = acc[nt][0][e];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) l = fmaf(__half2float(tsm[tok * 32 + q * 8 + e]), __half2float(bh[e]), l);
+                for (int qq = 1; qq < kChains; ++qq) v[e] += acc[nt][qq][e];
+#pragma unroll
+                for (int qq = 0; qq < kChains; ++qq) acc[nt][qq][e] = 0.f;
             }
-            sum += l;
+            r[g * TOK + nt * 8 + 2 * t] = v[0];
+            r[g * TOK + nt * 8 + 2 * t + 1] = v[1];
+            r[(g + 8) * TOK + nt * 8 + 2 * t] = v[2];
+            r[(g + 8) * TOK + nt * 8 + 2 * t + 1] = v[3];
         }
-        a.Y[(size_t)token * a.N + n] = __float2half_rn(sum);
+        named_barrier_sync(1, kConsumerWarps * 32);
+        // one output per thread: row rr = ctid % 16, token tok = ctid / 16
+        const int rr = ctid & (kGroup - 1), tok = ctid >> 4;
+        const int token = token0 + tok;
+        if (ok && tok < TOK && rr < rows && token < Mt) {
+            const int nw = min(kConsumerWarps, npieces);
+            float sum = 0.f;
+            for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
+            if (rank > 0) {
+                const __half* tsm = reinterpret_cast<const __half*>(sm + L.t) + tok * 32;
+                const __half* bsm = reinterpret_cast<const __half*>(sm + soff + L.b) + rr * 32;
+                float l = 0.f;
+#pragma unroll 8
+                for (int k = 0; k < 32; ++k) l = fmaf(__half2float(tsm[k]), __half2float(bsm[k]), l);
+                sum += l;
+            }
+            a.Y[(size_t)token * a.N + ra + rr] = __float2half_rn(sum);
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(empty(s));  // after this warp's reads of the stage's B rows
     }
 }
 
-template <int BITS, bool HAS_ZP, int NT>
-cudaError_t launch_one(const GemvArgs& a, dim3 grid, int threads, size_t smem, bool pdl, cudaStream_t st) {
+template <int BITS, bool HAS_ZP, int NT, bool XS>
+cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cudaStream_t st) {
     static_assert(NT == 1 || NT == 2, "token tiles");
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(threads);
+    cfg.blockDim = dim3(kThreadsGemv);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -242,42 +390,81 @@ cudaError_t launch_one(const GemvArgs& a, dim3 grid, int threads, size_t smem, b
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT>, a);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS>, a);
 }
+
+template <int BITS, bool HAS_ZP, int NT>
+cudaError_t launch_xs(const GemvArgs& a, dim3 grid, size_t smem, bool xs, bool pdl, cudaStream_t st) {
+    return xs ? launch_one<BITS, HAS_ZP, NT, true>(a, grid, smem, pdl, st)
+              : launch_one<BITS, HAS_ZP, NT, false>(a, grid, smem, pdl, st);
+}
+
+constexpr int kGemvSmemLimit = 112 * 1024;  // two CTAs per SM
 
 }  // namespace
 
-size_t gemv_smem_bytes(int warps, int maxseg, int tok) {
-    return (size_t)warps * maxseg * 16 * tok * sizeof(float) + (size_t)tok * 32 * sizeof(__half);
+size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R_out, int* CH_out, int* tok_out, int* threads) {
+    const int tok = Mt <= 8 ? 8 : 16;
+    // two CTAs per SM (16 consumer warps), but at least one 16-row group per CTA
+    int ctas = 2 * (sms > 0 ? sms : 1);
+    if (ctas > (N + kGroup - 1) / kGroup) ctas = (N + kGroup - 1) / kGroup;
+    if (ctas < 1) ctas = 1;
+    int R = (N + ctas - 1) / ctas;
+    if (R < 1) R = 1;
+    const int nblk = K / 32;
+    const int rowbytes = K * bits / 8;
+    // K chunk: a full row when it fits (one contiguous copy per group), else 1 KB
+    int CH = rowbytes <= kMaxChunk ? rowbytes : kMaxChunk;
+    CH = (CH + 63) / 64 * 64;
+    if (CH < 64) CH = 64;
+    *R_out = R;
+    *CH_out = CH;
+    *tok_out = tok;
+    *threads = kThreadsGemv;
+    const uint32_t xrows = (uint32_t)(Mt < tok ? Mt : tok);  // X rows one CTA stages
+    const bool xs = xrows * K * 2u <= kXStageMax;
+    const int nstages = (R + kGroup - 1) / kGroup * ((rowbytes + CH - 1) / CH);
+    return gemv_layout(CH, nblk, tok, nstages <= 2 ? 2 : kMaxRing, xs ? xrows * K * 2u : 0u).total;
 }
 
 cudaError_t gemv_prepare() {
-    const int bytes = kGemvMaxSmem;
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = tensor_map_prepare();
 #define MNB_SET(B, Z, T)                                                                                       \
     if (e == cudaSuccess)                                                                                      \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+                                 227 * 1024);                                                                  \
+    if (e == cudaSuccess)                                                                                      \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     MNB_SET(4, false, 1) MNB_SET(4, false, 2) MNB_SET(4, true, 1) MNB_SET(4, true, 2)
     MNB_SET(8, false, 1) MNB_SET(8, false, 2) MNB_SET(8, true, 1) MNB_SET(8, true, 2)
 #undef MNB_SET
     return e;
 }
 
-cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st) {
+cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st) {
+    GemvArgs a = a_in;
+    const int tok = p.tokens_per_cta;
+    const int rowbytes = a.K * bits / 8;
+    const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
+    a.ring = nstages <= 2 ? 2 : kMaxRing;
+    const uint32_t xrows = (uint32_t)(a.Mt < tok ? a.Mt : tok);
+    const bool xs = xrows * a.K * 2u <= kXStageMax;
+    a.xrows = xs ? (int)xrows : 0;
+    const size_t smem = gemv_layout(a.CH, a.K / 32, tok, a.ring, xs ? xrows * a.K * 2u : 0u).total;
+    if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const dim3 grid(p.grid_x, p.grid_y);
-    const int nt = p.tokens_per_cta / 8;
-    const size_t smem = gemv_smem_bytes(p.block_threads / 32, a.maxseg, p.tokens_per_cta);
     const bool zp = a.Z != nullptr;
+    const int nt = tok / 8;
     if (bits == 4) {
-        if (zp) return nt == 1 ? launch_one<4, true, 1>(a, grid, p.block_threads, smem, pdl, st)
-                               : launch_one<4, true, 2>(a, grid, p.block_threads, smem, pdl, st);
-        return nt == 1 ? launch_one<4, false, 1>(a, grid, p.block_threads, smem, pdl, st)
-                       : launch_one<4, false, 2>(a, grid, p.block_threads, smem, pdl, st);
+        if (zp) return nt == 1 ? launch_xs<4, true, 1>(a, grid, smem, xs, pdl, st)
+                               : launch_xs<4, true, 2>(a, grid, smem, xs, pdl, st);
+        return nt == 1 ? launch_xs<4, false, 1>(a, grid, smem, xs, pdl, st)
+                       : launch_xs<4, false, 2>(a, grid, smem, xs, pdl, st);
     }
-    if (zp) return nt == 1 ? launch_one<8, true, 1>(a, grid, p.block_threads, smem, pdl, st)
-                           : launch_one<8, true, 2>(a, grid, p.block_threads, smem, pdl, st);
-    return nt == 1 ? launch_one<8, false, 1>(a, grid, p.block_threads, smem, pdl, st)
-                   : launch_one<8, false, 2>(a, grid, p.block_threads, smem, pdl, st);
+    if (zp) return nt == 1 ? launch_xs<8, true, 1>(a, grid, smem, xs, pdl, st)
+                           : launch_xs<8, true, 2>(a, grid, smem, xs, pdl, st);
+    return nt == 1 ? launch_xs<8, false, 1>(a, grid, smem, xs, pdl, st)
+                   : launch_xs<8, false, 2>(a, grid, smem, xs, pdl, st);
 }
 
 }  // namespace mnb

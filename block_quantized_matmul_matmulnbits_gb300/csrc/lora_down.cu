@@ -83,8 +83,13 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_rank();
-    const int tokb = blockIdx.y * kTok;  // first token row of this CTA
-    const int ntok = min(kTok, Mt - tokb);
+    // Few token rows (decode): one 16-row tile per CTA and the four warps split
+    // the K slice; otherwise 64 token rows per CTA, one 16-row tile per warp.
+    const bool few = Mt <= 16;
+    const int tokc = few ? 16 : kTok;
+    const int tokb = blockIdx.y * tokc;  // first token row of this CTA
+    const int ntok = min(tokc, Mt - tokb);
+    const int wrow = few ? 0 : warp * 16;
     const int nch = K / 16;
     const int c0 = (int)((long long)rank * nch / nsplit), c1 = (int)((long long)(rank + 1) * nch / nsplit);
 
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
             waited = true;
         }
         const int xc = klen / 8;  // 16-byte chunks per token row
-        for (int idx = tid; idx < kTok * xc; idx += blockDim.x) {
+        for (int idx = tid; idx < tokc * xc; idx += blockDim.x) {
             const int row = idx / xc, c = idx - row * xc;
             const bool ok = row < ntok;
             cp_async16(smem_u32(&Xs[row * kPitchX + c * 8]), ok ? X + (size_t)(tokb + row) * K + kb + c * 8 : X,
@@ -116,10 +121,10 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         cp_async_wait_all();
         __syncthreads();
         const int mat = lane >> 3, row8 = lane & 7;
-        for (int kk = 0; kk < klen; kk += 16) {
-            // A operand: X rows warp*16 .. +15, K columns kk .. kk+15 (row-major 16x16)
+        for (int kk = few ? 16 * warp : 0; kk < klen; kk += few ? 64 : 16) {
+            // A operand: X rows wrow .. +15, K columns kk .. kk+15 (row-major 16x16)
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(smem_u32(&Xs[(warp * 16 + (mat & 1) * 8 + row8) * kPitchX + kk + (mat >> 1) * 8]), a0, a1, a2, a3);
+            ldsm_x4(smem_u32(&Xs[(wrow + (mat & 1) * 8 + row8) * kPitchX + kk + (mat >> 1) * 8]), a0, a1, a2, a3);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t b0, b1, b2, b3;
@@ -141,6 +146,11 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         part[(warp * 16 + g) * 32 + r + 1] = acc[nt][1];
         part[(warp * 16 + g + 8) * 32 + r] = acc[nt][2];
         part[(warp * 16 + g + 8) * 32 + r + 1] = acc[nt][3];
+    }
+    if (few) {  // add the four warps' K quarters in warp order into rows 0..15
+        __syncthreads();
+        for (int idx = tid; idx < 16 * 32; idx += blockDim.x)
+            part[idx] = ((part[idx] + part[512 + idx]) + part[1024 + idx]) + part[1536 + idx];
     }
     cluster_sync_all();
     // Every CTA of the cluster finishes an interleaved share of the valid
@@ -166,22 +176,25 @@ cudaError_t lora_down_prepare() {
     return cudaFuncSetAttribute(lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
 }
 
-cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, cudaStream_t st) {
+cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st) {
     const int nch = K / 16;
     int nsplit = nch < kMaxCluster ? nch : kMaxCluster;
     if (nsplit < 1) nsplit = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nsplit, (Mt + kTok - 1) / kTok);
+    const int tokc = Mt <= 16 ? 16 : kTok;
+    cfg.gridDim = dim3(nsplit, (Mt + tokc - 1) / tokc);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = kLoraSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = nsplit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, lora_down_kernel, X, A, T, Mt, K, nsplit);
 }
 

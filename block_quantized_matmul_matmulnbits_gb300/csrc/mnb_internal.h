@@ -2,6 +2,7 @@
 // translation units of libmnb.  Not installed; not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -14,8 +15,10 @@ namespace mnb {
 // kernel as a pointer) when one of its bounded waits gives up.
 constexpr unsigned int kStatusTimeout = 1u;
 
-// Largest dynamic shared memory the decode kernel is allowed to request.
-constexpr int kGemvMaxSmem = 160 * 1024;
+// Host-side TMA descriptors (tensor_map.cu).
+cudaError_t tensor_map_prepare();
+cudaError_t encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
+                      uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 struct GemvArgs {
     const __half* X;     // [Mt, K]
@@ -26,18 +29,23 @@ struct GemvArgs {
     const __half* B;     // [N, 32] or nullptr
     __half* Y;           // [Mt, N]
     int Mt, N, K;
-    int rows_per_cta;    // output rows owned by one CTA
-    int maxseg;          // tile segments one warp can touch (sizes the reduction buffer)
+    int R;               // output rows owned by one CTA
+    int CH;              // K bytes per row and pipeline stage (multiple of 64)
+    int ring;            // shared-memory ring stages (2 or 4), set by the launcher
+    int xrows;           // X rows staged in shared memory per CTA (0: X read from global)
     int rank;            // 0 or 32
+    unsigned int* status;
 };
 
-size_t gemv_smem_bytes(int warps, int maxseg, int tok);
+// Decode-kernel geometry for (N, K, token rows) on `sms` SMs: rows per CTA
+// and K bytes per stage; returns the dynamic shared memory it needs.
+size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R, int* CH, int* tok, int* threads);
 cudaError_t gemv_prepare();
 cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st);
 
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.
 cudaError_t lora_down_prepare();
-cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, cudaStream_t st);
+cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st);
 
 struct GemmArgs {
     const __half* X;

@@ -26,6 +26,7 @@ MNB_ERR_NO_DEVICE = -6
 
 ROUTE_NONE, ROUTE_GEMV, ROUTE_GEMM, ROUTE_FILL = 0, 1, 2, 3
 MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
+FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
 EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_plan", "mnb_last_route", "mnb_sync_status",
@@ -35,7 +36,7 @@ EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_plan", "mnb_last_route",
 class MnbDesc(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int64), ("K", ctypes.c_int64), ("bits", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("max_rank", ctypes.c_int32), ("mode", ctypes.c_int32),
-                ("gemv_max_m", ctypes.c_int32)]
+                ("gemv_max_m", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class MnbPlanInfo(ctypes.Structure):
@@ -124,8 +125,8 @@ def mnb_status_str(code: int) -> str:
 
 
 def mnb_create(N: int, K: int, bits: int = 4, block_size: int = 32, max_rank: int = 32,
-               mode: int = MODE_AUTO, gemv_max_m: int = 0) -> ctypes.c_void_p:
-    d = MnbDesc(N, K, bits, block_size, max_rank, mode, gemv_max_m)
+               mode: int = MODE_AUTO, gemv_max_m: int = 0, flags: int = 0) -> ctypes.c_void_p:
+    d = MnbDesc(N, K, bits, block_size, max_rank, mode, gemv_max_m, flags)
     h = ctypes.c_void_p()
     _check(lib().mnb_create(ctypes.byref(d), ctypes.byref(h)), "mnb_create")
     return h
@@ -185,9 +186,9 @@ class Projection:
     """
 
     def __init__(self, N: int, K: int, bits: int = 4, max_rank: int = 32, mode: int = MODE_AUTO,
-                 gemv_max_m: int = 0):
+                 gemv_max_m: int = 0, flags: int = 0):
         self.N, self.K, self.bits = N, K, bits
-        self.h = mnb_create(N, K, bits, 32, max_rank, mode, gemv_max_m)
+        self.h = mnb_create(N, K, bits, 32, max_rank, mode, gemv_max_m, flags)
 
     def __call__(self, X, Wq, scales, zp=None, A=None, B=None, out=None, T_ws=None, stream=None):
         import torch

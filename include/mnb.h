@@ -52,6 +52,14 @@ extern "C" {
 #define MNB_ROUTE_GEMM  2   /* prefill kernel: TMA + tcgen05 MMA with TMEM accumulators */
 #define MNB_ROUTE_FILL  3   /* K == 0: the output is filled with zeros */
 
+/* ---- flags (mnb_desc.flags) -------------------------------------------- */
+/* The weight-side inputs (Wq, scales, zp, A, B) stay constant while calls are
+ * in flight, so mnb_run may start streaming them before the work queued ahead
+ * of it on the stream has finished (programmatic dependent launch): X and T
+ * are still read only after that work completes.  Without this flag every
+ * call starts after the preceding work on the stream, as usual. */
+#define MNB_FLAG_EARLY_WEIGHTS  1
+
 /* ---- mode (mnb_desc.mode) ---------------------------------------------- */
 #define MNB_MODE_AUTO        0  /* GEMV when the per-matrix M <= gemv_max_m, else GEMM */
 #define MNB_MODE_FORCE_GEMV  1  /* always the decode kernel (any M) */
@@ -66,7 +74,8 @@ typedef struct mnb_handle_s* mnb_handle;
  *   max_rank    0 or 32: the largest adapter rank mnb_run will be given
  *   mode        MNB_MODE_*
  *   gemv_max_m  largest per-matrix M routed to the decode kernel in AUTO
- *               mode; <= 0 selects the default 16 */
+ *               mode; <= 0 selects the default 16
+ *   flags       0 or MNB_FLAG_EARLY_WEIGHTS */
 typedef struct {
     int64_t N;
     int64_t K;
@@ -75,6 +84,7 @@ typedef struct {
     int32_t max_rank;
     int32_t mode;
     int32_t gemv_max_m;
+    int32_t flags;
 } mnb_desc;
 
 /* Launch plan of one call, as computed by the dispatcher (host only). */
@@ -84,7 +94,7 @@ typedef struct {
     int32_t grid_x, grid_y; /* grid of the main kernel */
     int32_t block_threads;  /* threads per CTA of the main kernel */
     int32_t rows_per_cta;   /* GEMV: output rows per CTA; GEMM: output rows per tile */
-    int32_t k_splits;       /* GEMV: warps sharing one 16-row tile along K */
+    int32_t k_splits;       /* GEMV: K bytes per row and pipeline stage; GEMM: 0 */
     int32_t tokens_per_cta; /* GEMV: token rows per CTA (8 or 16); GEMM: token tile */
 } mnb_plan_info;
 

@@ -245,3 +245,34 @@ def test_exact_arithmetic_bitwise(env):
     Y, _, _ = run_gpu(mnb, torch, inp)
     Y16, _, _ = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, N, K, 4)
     assert np.array_equal(bits_of(Y).reshape(M, N), Y16)
+
+
+@pytest.mark.parametrize("M,N,K,rank", [(1, 4096, 4096, 32), (1, 4096, 4096, 0), (3, 1000, 576, 32),
+                                        (300, 640, 512, 32)])
+def test_early_weights_back_to_back_calls(env, M, N, K, rank):
+    """With MNB_FLAG_EARLY_WEIGHTS consecutive calls overlap (each streams its
+    weights before the previous call ends); every output must still match."""
+    torch, mnb = env
+    inps = [synth.make_inputs(M=M, K=K, N=N, bits=4, seed=700 + i, zp_range=(0, 15), rank=rank) for i in range(3)]
+    devs = [upload(i, torch) for i in inps]
+    h = mnb.mnb_create(N, K, 4, 32, 32, 0, 0, mnb.FLAG_EARLY_WEIGHTS)
+    outs = []
+    try:
+        for rep in range(4):
+            for i, d in enumerate(devs):
+                Y = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+                T = torch.empty((M, 32), dtype=torch.float16, device="cuda") if rank else None
+                mnb.mnb_run(h, d["X"], d["Wq"], d["scales"], d["zp"], d["A"] if rank else None,
+                            d["B"] if rank else None, rank, Y, T, 1, M)
+                outs.append((i, Y))
+        torch.cuda.synchronize()
+        assert mnb.mnb_sync_status(h) == 0
+    finally:
+        mnb.mnb_destroy(h)
+    refs = [oracle_ref(i) for i in inps]
+    for i, Y in outs:
+        assert_within_tolerance(bits_of(Y), refs[i][0], refs[i][1], f"back-to-back call {i}")
+    # bitwise equal across repetitions of the same inputs
+    for i in range(3):
+        same = [Y for j, Y in outs if j == i]
+        assert all(torch.equal(same[0], y) for y in same[1:])
