@@ -105,12 +105,16 @@ void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
 void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
     const int tok = mnb::gemm_token_tile((int)Mt);
     const int ntiles = cdiv(d.N, 128) * cdiv(Mt, tok);
+    const int split = mnb::gemm_split((int)d.N, (int)Mt, (int)d.K, sms);
     p->route = MNB_ROUTE_GEMM;
-    p->grid_x = ntiles < sms ? ntiles : (sms > 0 ? sms : 1);
+    if (split > 1)
+        p->grid_x = ntiles * split;  // one cluster of `split` CTAs per tile
+    else
+        p->grid_x = ntiles < sms ? ntiles : (sms > 0 ? sms : 1);
     p->grid_y = 1;
     p->block_threads = mnb::gemm_threads();
     p->rows_per_cta = 128;
-    p->k_splits = 0;
+    p->k_splits = split;
     p->tokens_per_cta = tok;
 }
 
@@ -260,7 +264,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.bits = d.bits;
         a.rank = rank;
         a.status = status;
-        e = mnb::gemm_launch(a, p, pdl, st);
+        e = mnb::gemm_launch(a, p, pdl, early, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return MNB_ERR_CUDA;

@@ -1,4 +1,5 @@
-// gemm.cu -- prefill kernel (many token rows): a tcgen05 tensor-core contraction.
+// gemm.cu -- tensor-core kernel: the prefill contraction, and decode shapes
+// split along K.
 //
 // Computes Y[m, n] = sum_k X[m, k] w[n, k] + sum_r T[m, r] B[n, r], the
 // "fuse_up" prefill path of "[WebGPU] Fuse rank-32 quantized LoRA with
@@ -6,30 +7,36 @@
 // T first, then the base GEMM "with an integrated T * Bt^T epilogue"),
 // restated for sm_103a:
 //
-//  * One CTA per SM, persistent over output tiles of 128 weight rows x BN
-//    token rows (BN <= 256, token tiles fastest so that CTAs running together
-//    share a weight tile in L2).
-//  * Warp 0 (one lane) is the TMA producer: per 64-wide K step it loads the X
-//    tile [BN x 64] FP16 with the 128-byte swizzle and the packed weight tile
-//    [128 rows x 64 codes] into a 4-deep shared-memory ring (mbarrier
-//    complete_tx).
-//  * Warps 6..13 dequantize the packed tile -- exact (q - zp), one rounding by
-//    the FP16 scale, the DequantizeLinear map of "Fuse DQ->MatMulNBits for
-//    shared initializers and skip outer-scope weights" (PR 33800) -- into the
-//    canonical K-major 128B-swizzled FP16 operand layout, then fence the
-//    generic->async proxy and arrive on the stage's barrier.
-//  * Warp 1 allocates tensor memory (two 128 x BN FP32 accumulators, so the
-//    epilogue of one tile overlaps the main loop of the next) and one lane
-//    issues tcgen05.mma.kind::f16 (A = dequantized weights, B = X, both from
-//    shared memory descriptors), committing each stage back to the producer.
-//  * The LoRA term is one more K step with A = B_lora[n, 0:32] and B =
-//    T[m, 0:32] (written into the same ring by the dequant warps after
-//    griddepcontrol.wait on the LoRA down kernel), so it accumulates into the
-//    same tensor-memory tile: the integrated T * Bt^T epilogue.
+//  * Output tiles of 128 weight rows x BN token rows (BN <= 256).  With enough
+//    tiles one CTA per SM runs persistently over them (token tiles fastest, so
+//    CTAs running together share a weight tile in L2).  With few tiles (decode
+//    shapes) the K range of a tile is split over the S CTAs of a thread-block
+//    cluster; their partial tiles are added in rank order through distributed
+//    shared memory (deterministic, no atomics).
+//  * Two producer warps, so that the weight stream runs ahead of X: warp 0
+//    copies the packed weights of 128 rows in super-stages of 256 bytes per
+//    row (two TMA boxes of 128 rows x 128 bytes, 128-byte swizzle), warp 14
+//    the X tile [BN x 64] FP16 of each 64-wide K step (TMA, 128-byte swizzle).
+//    Few large boxes: one TMA copy costs about as much to issue as a small
+//    one, so per-row copies of a few hundred bytes cannot feed an SM.
+//  * Warps 6..13 dequantize: exact (q - zp), one rounding by the FP16 scale --
+//    the DequantizeLinear map of "Fuse DQ->MatMulNBits for shared initializers
+//    and skip outer-scope weights" (PR 33800) -- into the canonical K-major
+//    128B-swizzled FP16 operand layout, fence the generic->async proxy and
+//    arrive on the stage's barrier.
+//  * Warp 1 allocates tensor memory (two 128 x BN FP32 accumulators) and one
+//    lane issues tcgen05.mma.kind::f16 (A = dequantized weights, B = X, both
+//    from shared memory descriptors), committing each stage back to the
+//    producer.
+//  * The LoRA term is one more K step (in the last K split of a tile) with A =
+//    B_lora[n, 0:32] and B = T[m, 0:32], written into the ring by the dequant
+//    warps after griddepcontrol.wait on the LoRA down kernel: the integrated
+//    T * Bt^T epilogue, accumulated into the same tensor-memory tile.
 //  * Warps 2..5 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
 //    32 (w % 4) .. +31 = weight rows), round once to FP16 and store Y.
 //  * Every mbarrier wait is bounded: after ~2 s the kernel records a timeout
-//    in the status word, stops, lets its copies land and frees its TMEM.
+//    in the status word, stops, lets its copies and MMAs land and frees its
+//    tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -42,20 +49,16 @@ namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // K per pipeline step: one 128-byte swizzle atom of FP16
-constexpr int kStages = 4;
 constexpr int kMaxBN = 256;
-constexpr int kThreads = 448;    // 14 warps
+constexpr int kThreads = 480;    // 15 warps
 constexpr int kDqWarp0 = 6;      // first dequant warp
+constexpr int kXWarp = 14;       // X producer
 constexpr int kDqThreads = 256;
 constexpr int kEpiThreads = 128;
-constexpr int kXSlot = kMaxBN * 128;    // bytes
-constexpr int kWSlot = BM * 128;        // dequantized FP16 A tile
-constexpr int kPSlot = BM * 64;         // packed codes (INT8 needs 64 B per row)
-constexpr int kStageBytes = kXSlot + kWSlot + kPSlot;
-constexpr int kBarOffset = kStages * kStageBytes;
-constexpr int kNumBars = 3 * kStages + 4 + 1;
-constexpr int kSmemBytes = kBarOffset + kNumBars * 8 + 16 + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kWSlot = BM * 128; // dequantized FP16 A tile of one K step
+constexpr int kPBox = BM * 128;  // one packed-weight TMA box: 128 rows x 128 bytes
+constexpr int kMaxSplit = 8;
+constexpr uint32_t kSmemBudget = 232448;
 
 // ------------------------------------------------------------------ tcgen05 wrappers
 
@@ -108,14 +111,101 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {  // byte offset
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+__host__ __device__ inline uint32_t g_align(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory plan, identical on host and device.
+// The split-K partial tile (128 x BN FP32) reuses the ring from offset 0: a
+// CTA of a split runs one unit, and once its accumulator is complete every
+// copy into the ring has landed and every read of it has finished.
+// Three rings: X tiles (nx slots), dequantized A tiles (nw slots of 16 KB),
+// packed-weight super-stages (np slots).  X has its own ring so that its
+// loads run ahead of the MMA instead of waiting for a slot of the A ring.
+struct GemmLayout {
+    uint32_t xslot;    // bytes of one X slot (BN rows x 128 B, 1024-aligned)
+    int nx, nw, np;    // slots of the X, A and packed rings
+    int pboxes;        // TMA boxes per packed super-stage (128 packed bytes of each row per box)
+    uint32_t pstage;   // bytes of one packed super-stage
+    uint32_t w_off, p_off, red_bytes, bar_off, total;
+};
+
+__host__ __device__ inline GemmLayout gemm_layout(int BN) {
+    GemmLayout L;
+    L.xslot = g_align((uint32_t)BN * 128u, 1024u);
+    // Small token tiles (decode shapes) are bound by the weight stream: deep
+    // packed ring, large super-stages.  Large tiles keep four X slots.
+    L.pboxes = BN <= 64 ? 2 : 1;
+    L.pstage = (uint32_t)(L.pboxes * kPBox);
+    L.np = BN <= 64 ? 4 : 3;
+    L.nw = BN <= 64 ? 4 : 3;
+    L.red_bytes = (uint32_t)BM * BN * 4u;
+    const uint32_t fixed = L.np * L.pstage + L.nw * (uint32_t)kWSlot + 512u + 1024u;
+    int nx = fixed < kSmemBudget ? (int)((kSmemBudget - fixed) / L.xslot) : 0;
+    if (nx > 12) nx = 12;
+    L.nx = nx;
+    L.w_off = (uint32_t)nx * L.xslot;
+    L.p_off = L.w_off + (uint32_t)L.nw * kWSlot;
+    L.bar_off = L.p_off + (uint32_t)L.np * L.pstage;
+    L.total = L.bar_off + 512u + 1024u;
+    return L;
+}
+
 struct GemmParams {
     GemmArgs a;
-    int BN;          // token rows per tile (multiple of 16, <= 256)
-    int tiles_m;     // token tiles
-    int tiles;       // total tiles
-    int ksteps;      // 64-wide K steps
-    int tmem_cols;   // allocated tensor-memory columns (power of two >= 2 BN)
+    int BN;         // token rows per tile (multiple of 16, <= 256)
+    int tiles_m;    // token tiles
+    int tiles;      // total tiles
+    int ksteps;     // 64-wide K steps of a full row
+    int split;      // CTAs (one cluster) sharing a tile along K; 1 = persistent over tiles
+    int tmem_cols;  // allocated tensor-memory columns (power of two >= 2 BN)
+    int x_wait;     // X may be written by the work queued before this grid: wait for it
 };
+
+// One unit of work of a CTA: a tile and a K-step range.
+struct Unit {
+    int n0, m0, i0, i1;
+    bool lora;  // this unit adds the LoRA K step
+};
+
+__device__ __forceinline__ bool next_unit(const GemmParams& P, int& cursor, Unit& u) {
+    const int split = P.split;
+    int tile;
+    int cr = 0;
+    if (split == 1) {
+        tile = cursor;
+        cursor += gridDim.x;
+    } else {
+        if (cursor != (int)blockIdx.x) return false;  // one unit per CTA
+        tile = (int)blockIdx.x / split;
+        cr = (int)blockIdx.x % split;
+        cursor = -1;
+    }
+    if (tile < 0 || tile >= P.tiles) return false;
+    u.m0 = (tile % P.tiles_m) * P.BN;
+    u.n0 = (tile / P.tiles_m) * BM;
+    u.i0 = (int)((long long)cr * P.ksteps / split);
+    u.i1 = (int)((long long)(cr + 1) * P.ksteps / split);
+    u.lora = P.a.rank > 0 && cr == split - 1;
+    return true;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote));
+    return v;
+}
 
 template <int BITS, bool HAS_ZP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -124,31 +214,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base_raw = smem_u32(smem_raw);
     const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
     unsigned char* sptr = smem_raw + (sbase - base_raw);
+    const GemmLayout L = gemm_layout(P.BN);
+    const int nx = L.nx, nw = L.nw, np = L.np;
 
-    const uint32_t bars = sbase + kBarOffset;
-    auto full_tma = [&](int s) { return bars + 8u * s; };
-    auto full_w = [&](int s) { return bars + 8u * (kStages + s); };
-    auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
-    auto acc_full = [&](int a) { return bars + 8u * (3 * kStages + a); };
-    auto acc_empty = [&](int a) { return bars + 8u * (3 * kStages + 2 + a); };
-    const uint32_t drain = bars + 8u * (3 * kStages + 4);  // teardown: all MMAs of this CTA done
-    const uint32_t tmem_slot = bars + 8u * kNumBars;
-    auto xslot = [&](int s) { return sbase + (uint32_t)(s * kStageBytes); };
-    auto wslot = [&](int s) { return sbase + (uint32_t)(s * kStageBytes + kXSlot); };
-    auto pslot = [&](int s) { return (uint32_t)(s * kStageBytes + kXSlot + kWSlot); };  // offset from sptr
+    const uint32_t bars = sbase + L.bar_off;
+    auto full_x = [&](int s) { return bars + 8u * s; };
+    auto empty_x = [&](int s) { return bars + 8u * (nx + s); };
+    auto full_w = [&](int s) { return bars + 8u * (2 * nx + s); };
+    auto empty_w = [&](int s) { return bars + 8u * (2 * nx + nw + s); };
+    const int b0 = 2 * nx + 2 * nw;
+    auto full_p = [&](int j) { return bars + 8u * (b0 + j); };
+    auto empty_p = [&](int j) { return bars + 8u * (b0 + np + j); };
+    auto acc_full = [&](int a) { return bars + 8u * (b0 + 2 * np + a); };
+    auto acc_empty = [&](int a) { return bars + 8u * (b0 + 2 * np + 2 + a); };
+    const uint32_t drain = bars + 8u * (b0 + 2 * np + 4);
+    const uint32_t tmem_slot = drain + 8u;
+    auto xslot = [&](int s) { return sbase + (uint32_t)s * L.xslot; };
+    auto wslot = [&](int s) { return sbase + L.w_off + (uint32_t)s * kWSlot; };
 
     const GemmArgs& a = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool lora = a.rank > 0;
-    const int steps_per_tile = P.ksteps + (lora ? 1 : 0);
     const int BN = P.BN;
+    constexpr int kStepBytes = BK * BITS / 8;  // packed bytes of one K step per row
+    const int kps = L.pboxes * 128 / kStepBytes;  // K steps per packed super-stage (a power of two)
     unsigned int* status = a.status;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_tma(s), 1);
+        for (int s = 0; s < nx; ++s) {
+            mbar_init(full_x(s), 1);
+            mbar_init(empty_x(s), 1);
+        }
+        for (int s = 0; s < nw; ++s) {
             mbar_init(full_w(s), kDqThreads);
-            mbar_init(empty(s), 1);
+            mbar_init(empty_w(s), 1);
+        }
+        for (int j = 0; j < np; ++j) {
+            mbar_init(full_p(j), 1);
+            mbar_init(empty_p(j), kDqThreads);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full(i), 1);
@@ -166,65 +268,99 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(sptr + kBarOffset + 8 * kNumBars);
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(sptr + (tmem_slot - sbase));
     pdl_launch_dependents();
 
     const int nblk = a.K / 32;
     const uint32_t x_bytes = (uint32_t)BN * 128u;
-    const uint32_t w_bytes = (uint32_t)BM * (uint32_t)(BK * BITS / 8);
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------------- packed-weight producer
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
-            int step = 0;
+            int pstep = 0, cursor = blockIdx.x;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < P.tiles; tile += gridDim.x) {
-                const int m0 = (tile % P.tiles_m) * BN, n0 = (tile / P.tiles_m) * BM;
-                for (int i = 0; ok && i < steps_per_tile; ++i, ++step) {
-                    const int s = step % kStages;
-                    const uint32_t ph = (uint32_t)(step / kStages) & 1u;
-                    if (!(ok = mbar_wait(empty(s), ph ^ 1u, status))) break;
-                    if (i < P.ksteps) {
-                        mbar_arrive_tx(full_tma(s), x_bytes + w_bytes);
-                        tma_load_2d(xslot(s), &tmX, i * BK, m0, full_tma(s));
-                        tma_load_2d(sbase + pslot(s), &tmW, i * (BK * BITS / 8), n0, full_tma(s));
-                    } else {
-                        mbar_arrive(full_tma(s));  // LoRA step: the slot is free, nothing to load
-                    }
+            Unit u;
+            while (ok && next_unit(P, cursor, u)) {
+                for (int i = u.i0; i < u.i1; i += kps, ++pstep) {
+                    const int j = pstep % np;
+                    const uint32_t ph = (uint32_t)(pstep / np) & 1u;
+                    if (!(ok = mbar_wait(empty_p(j), ph ^ 1u, status))) break;
+                    // boxes holding this unit's K steps; rows past N and bytes past K read as zero
+                    const int bytes = min(kps, u.i1 - i) * kStepBytes;
+                    const int nbox = (bytes + 127) / 128;
+                    mbar_arrive_tx(full_p(j), (uint32_t)(nbox * kPBox));
+                    const uint32_t dst = sbase + L.p_off + (uint32_t)j * L.pstage;
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d(dst + (uint32_t)b * kPBox, &tmW, i * kStepBytes + 128 * b, u.n0, full_p(j));
                 }
             }
             // let every copy issued into the ring land before the CTA can exit
-            for (int j = 1; j <= kStages && step - j >= 0; ++j) {
-                const int st = step - j;
-                if (!mbar_wait(full_tma(st % kStages), (uint32_t)(st / kStages) & 1u, status, false)) break;
+            for (int j = 1; j <= np && pstep - j >= 0; ++j) {
+                const int st = pstep - j;
+                if (!mbar_wait(full_p(st % np), (uint32_t)(st / np) & 1u, status, false)) break;
             }
         }
+        __syncwarp();
+    } else if (warp == kXWarp) {
+        // ---------------------------------------------------------------- X producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+            int step = 0, cursor = blockIdx.x;
+            bool ok = true, x_ready = P.x_wait == 0;
+            Unit u;
+            while (ok && next_unit(P, cursor, u)) {
+                const int nsteps = (u.i1 - u.i0) + (u.lora ? 1 : 0);
+                for (int i = 0; i < nsteps; ++i, ++step) {
+                    const int s = step % nx;
+                    const uint32_t ph = (uint32_t)(step / nx) & 1u;
+                    if (!(ok = mbar_wait(empty_x(s), ph ^ 1u, status))) break;
+                    if (i >= u.i1 - u.i0) {  // LoRA step: the dequant warps fill the slot
+                        mbar_arrive(full_x(s));
+                        continue;
+                    }
+                    if (!x_ready) {
+                        pdl_wait();  // weights went ahead; X only after the preceding work
+                        x_ready = true;
+                    }
+                    mbar_arrive_tx(full_x(s), x_bytes);
+                    tma_load_2d(xslot(s), &tmX, (u.i0 + i) * BK, u.m0, full_x(s));
+                }
+            }
+            for (int j = 1; j <= nx && step - j >= 0; ++j) {
+                const int st = step - j;
+                if (!mbar_wait(full_x(st % nx), (uint32_t)(st / nx) & 1u, status, false)) break;
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(BM, BN);
-            int step = 0, tl = 0;
+            int step = 0, tl = 0, cursor = blockIdx.x;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < P.tiles; tile += gridDim.x, ++tl) {
+            Unit u;
+            while (ok && next_unit(P, cursor, u)) {
                 const int acc = tl & 1;
                 if (!(ok = mbar_wait(acc_empty(acc), ((uint32_t)(tl >> 1) & 1u) ^ 1u, status))) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int i = 0; i < steps_per_tile; ++i, ++step) {
-                    const int s = step % kStages;
-                    const uint32_t ph = (uint32_t)(step / kStages) & 1u;
-                    if (!(ok = mbar_wait(full_tma(s), ph, status))) break;
-                    if (!(ok = mbar_wait(full_w(s), ph, status))) break;
+                const int nsteps = (u.i1 - u.i0) + (u.lora ? 1 : 0);
+                for (int i = 0; i < nsteps; ++i, ++step) {
+                    const int sx = step % nx, sw = step % nw;
+                    if (!(ok = mbar_wait(full_x(sx), (uint32_t)(step / nx) & 1u, status))) break;
+                    if (!(ok = mbar_wait(full_w(sw), (uint32_t)(step / nw) & 1u, status))) break;
                     tc_fence_after();
-                    const int kk = i < P.ksteps ? BK / 16 : 2;  // the LoRA step covers K = 32
+                    const bool lora_step = i >= u.i1 - u.i0;
+                    const int kk = lora_step ? 2 : BK / 16;  // the LoRA step covers K = 32
                     for (int j = 0; j < kk; ++j)
-                        tc_mma(d_tmem, sw128_desc(wslot(s) + 32u * j), sw128_desc(xslot(s) + 32u * j), idesc,
+                        tc_mma(d_tmem, sw128_desc(wslot(sw) + 32u * j), sw128_desc(xslot(sx) + 32u * j), idesc,
                                (i > 0 || j > 0) ? 1u : 0u);
-                    tc_commit(empty(s));
+                    tc_commit(empty_x(sx));
+                    tc_commit(empty_w(sw));
                 }
                 if (ok) tc_commit(acc_full(acc));
+                ++tl;
             }
             tc_commit(drain);  // tensor memory is freed only after every issued MMA has finished
             mbar_wait(drain, 0, status, false);
@@ -234,78 +370,112 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter of this warp
         const int row = q * 32 + lane;
-        int tl = 0;
-        for (int tile = blockIdx.x; tile < P.tiles; tile += gridDim.x, ++tl) {
-            const int m0 = (tile % P.tiles_m) * BN, n0 = (tile / P.tiles_m) * BM;
+        int tl = 0, cursor = blockIdx.x;
+        Unit u;
+        while (next_unit(P, cursor, u)) {
             const int acc = tl & 1;
             if (!mbar_wait(acc_full(acc), (uint32_t)(tl >> 1) & 1u, status)) break;
             tc_fence_after();
-            const int n = n0 + row;
+            const int n = u.n0 + row;
             for (int c = 0; c < BN; c += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
-                if (n < a.N) {
+                if (P.split > 1) {  // partial tile for the cluster reduction
+                    float4* dst = reinterpret_cast<float4*>(sptr + ((uint32_t)row * BN + c) * 4u);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                } else if (n < a.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int m = m0 + c + j;
+                        const int m = u.m0 + c + j;
                         if (m < a.Mt) a.Y[(size_t)m * a.N + n] = __float2half_rn(__uint_as_float(v[j]));
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(acc_empty(acc));
+            ++tl;
         }
     } else {
         // ---------------------------------------------------------------- dequant
+        // thread -> (row r, block h of the step): a quarter warp takes 8
+        // consecutive rows with one h, so its swizzled 16-byte reads of the
+        // packed box and writes of the A tile hit 8 distinct bank groups
         const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
-        const int r = d & (BM - 1), h = d >> 7;     // row of the tile, which block of the step
-        constexpr int kPrefetch = 4;                // scale / zero-point loads in flight
+        const int dl = d & 31;
+        const int r = (d >> 5) * 16 + (dl & 7) + ((dl >> 4) << 3);
+        const int h = (dl >> 3) & 1;
+        constexpr int kPrefetch = 6;                // scale / zero-point loads in flight
         constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
-        int step = 0;
+        int step = 0, pstep = 0, cursor = blockIdx.x;
         bool ok = true, waited = false;
-        for (int tile = blockIdx.x; ok && tile < P.tiles; tile += gridDim.x) {
-            const int m0 = (tile % P.tiles_m) * BN, n0 = (tile / P.tiles_m) * BM;
-            const int n = n0 + r;
+        Unit u;
+        while (ok && next_unit(P, cursor, u)) {
+            const int n = u.n0 + r;
             const bool row_ok = n < a.N;
-            const uint16_t* srow = reinterpret_cast<const uint16_t*>(a.S) + (size_t)n * nblk;
-            const uint8_t* zrow = a.Z + (size_t)n * nblk;
+            const uint16_t* srow = reinterpret_cast<const uint16_t*>(a.S) + (size_t)(row_ok ? n : 0) * nblk;
+            const uint8_t* zrow = a.Z + (size_t)(row_ok ? n : 0) * nblk;
+            // The loads are unconditional (clamped to a valid address) and the
+            // validity is kept as a bit: a select on a load's result right
+            // after it would wait for the load and defeat the prefetch.
             uint32_t sc[kPrefetch], zz[kPrefetch];
+            uint32_t vmask = 0;
 #pragma unroll
-            for (int u = 0; u < kPrefetch; ++u) {
-                const int blk = 2 * u + h;
-                const bool v = row_ok && blk < nblk && u < P.ksteps;
-                sc[u] = v ? (uint32_t)__ldg(srow + blk) : 0u;
-                zz[u] = HAS_ZP ? (v ? (uint32_t)__ldg(zrow + blk) : 0u) : kDefaultZp;
+            for (int v = 0; v < kPrefetch; ++v) {
+                const int blk = 2 * (u.i0 + v) + h;
+                const bool ld = row_ok && blk < nblk && u.i0 + v < u.i1;
+                const int bc = ld ? blk : 0;
+                sc[v] = (uint32_t)__ldg(srow + bc);
+                zz[v] = HAS_ZP ? (uint32_t)__ldg(zrow + bc) : kDefaultZp;
+                vmask |= ld ? (1u << v) : 0u;
             }
-            for (int i0 = 0; ok && i0 < P.ksteps; i0 += kPrefetch) {
+            int cur_p = 0;
+            for (int i0 = u.i0; ok && i0 < u.i1; i0 += kPrefetch) {
 #pragma unroll
-                for (int u = 0; u < kPrefetch; ++u) {
-                    const int i = i0 + u;
-                    if (i >= P.ksteps) break;
-                    const int s = step % kStages;
-                    const uint32_t ph = (uint32_t)(step / kStages) & 1u;
-                    if (!(ok = mbar_wait(full_tma(s), ph, status))) break;
-                    const DqConst dc = dq_const(zz[u], (uint16_t)sc[u]);
+                for (int v = 0; v < kPrefetch; ++v) {
+                    const int i = i0 + v;
+                    if (i >= u.i1) break;
+                    const int local = i - u.i0;
+                    if ((local & (kps - 1)) == 0) {
+                        cur_p = pstep % np;
+                        if (!(ok = mbar_wait(full_p(cur_p), (uint32_t)(pstep / np) & 1u, status))) break;
+                        ++pstep;
+                    }
+                    const int s = step % nw;
+                    const uint32_t ph = (uint32_t)(step / nw) & 1u;
+                    if (!(ok = mbar_wait(empty_w(s), ph ^ 1u, status))) break;  // the MMA is done with the slot
+                    // invalid block (row past N, K tail): scale 0 makes its products 0
+                    const DqConst dc = dq_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
                     {  // refill this prefetch slot with step i + kPrefetch
                         const int blk = 2 * (i + kPrefetch) + h;
-                        const bool v = row_ok && blk < nblk;
-                        sc[u] = v ? (uint32_t)__ldg(srow + blk) : 0u;
-                        if (HAS_ZP) zz[u] = v ? (uint32_t)__ldg(zrow + blk) : 0u;
+                        const bool ld = row_ok && blk < nblk && i + kPrefetch < u.i1;
+                        const int bc = ld ? blk : 0;
+                        sc[v] = (uint32_t)__ldg(srow + bc);
+                        if (HAS_ZP) zz[v] = (uint32_t)__ldg(zrow + bc);
+                        vmask = ld ? (vmask | (1u << v)) : (vmask & ~(1u << v));
                     }
-                    const uint32_t wrow = wslot(s);
+                    // this step's bytes of row r: box li*kStepBytes/128, 16-byte chunk c0 (+1)
+                    const int li = (local & (kps - 1));
+                    const int pb = li * kStepBytes;
+                    const int c0 = ((pb & 127) >> 4) + h * (kStepBytes / 32);
+                    const unsigned char* prow =
+                        sptr + L.p_off + (uint32_t)cur_p * L.pstage + (uint32_t)(pb >> 7) * kPBox + (uint32_t)r * 128u;
                     uint32_t out[16];
                     if constexpr (BITS == 4) {
-                        const uint4 pk = *reinterpret_cast<const uint4*>(sptr + pslot(s) + r * 32 + h * 16);
+                        const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
                         const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
                         for (int w = 0; w < 4; ++w) dq_int4_natural(wv[w], dc, &out[4 * w]);
                     } else {
-                        const uint4 p0 = *reinterpret_cast<const uint4*>(sptr + pslot(s) + r * 64 + h * 32);
-                        const uint4 p1 = *reinterpret_cast<const uint4*>(sptr + pslot(s) + r * 64 + h * 32 + 16);
+                        const uint4 p0 = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
+                        const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((c0 + 1) ^ (r & 7)) << 4));
                         const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
                         for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], dc, &out[2 * w]);
                     }
+                    const uint32_t wrow = wslot(s);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint32_t dst = wrow + swz128(r, 4 * h + c);
@@ -315,19 +485,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fence_proxy_async();
                     mbar_arrive(full_w(s));
+                    if ((local & (kps - 1)) == kps - 1 || i == u.i1 - 1) mbar_arrive(empty_p(cur_p));
                     ++step;
                 }
             }
-            if (ok && lora) {
-                const int s = step % kStages;
-                const uint32_t ph = (uint32_t)(step / kStages) & 1u;
-                if (!(ok = mbar_wait(full_tma(s), ph, status))) break;
+            if (ok && u.lora) {
+                const int s = step % nw, sx = step % nx;
+                if (!(ok = mbar_wait(empty_w(s), ((uint32_t)(step / nw) & 1u) ^ 1u, status))) break;
+                if (!(ok = mbar_wait(empty_x(sx), ((uint32_t)(step / nx) & 1u) ^ 1u, status))) break;
                 if (!waited) {
                     pdl_wait();  // T is written by the LoRA down kernel queued before this grid
                     waited = true;
                 }
                 if (h == 0) {  // A operand: B_lora[n, 0:32] in chunks 0..3 of row r
-                    const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)n * 32);
+                    const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)(row_ok ? n : 0) * 32);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const uint4 v = row_ok ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
@@ -338,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int idx = d; idx < BN * 4; idx += kDqThreads) {  // B operand: T[m, 0:32]
                     const int tr = idx >> 2, c = idx & 3;
-                    const int m = m0 + tr;
+                    const int m = u.m0 + tr;
                     const uint4 v = m < a.Mt ? *reinterpret_cast<const uint4*>(a.T + (size_t)m * 32 + c * 8)
                                              : make_uint4(0, 0, 0, 0);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xslot(s) + swz128(tr, c)), "r"(v.x),
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(xslot(sx) + swz128(tr, c)), "r"(v.x),
                                  "r"(v.y), "r"(v.z), "r"(v.w)
                                  : "memory");
                 }
@@ -355,6 +526,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    if (P.split > 1) {
+        // Split-K: every CTA of the cluster holds a partial 128 x BN tile; rank q
+        // finishes a contiguous slice of the token columns, adding the partials
+        // of ranks 0..S-1 in order.
+        cluster_barrier();
+        if (warp >= 2 && warp < kDqWarp0 && (*reinterpret_cast<volatile unsigned int*>(status) & kStatusTimeout) == 0) {
+            const int q = warp & 3, row = q * 32 + lane;
+            const uint32_t rank = cluster_ctarank();
+            const int S = P.split;
+            const int tile = (int)blockIdx.x / S;
+            const int m0 = (tile % P.tiles_m) * BN, n0 = (tile / P.tiles_m) * BM;
+            const int ncol4 = (min(BN, a.Mt - m0) + 3) / 4;  // token columns holding valid rows
+            const int c0 = (int)((long long)rank * ncol4 / S), c1 = (int)((long long)(rank + 1) * ncol4 / S);
+            const int n = n0 + row;
+            for (int c4 = c0; c4 < c1; ++c4) {
+                const uint32_t la = sbase + ((uint32_t)row * BN + (uint32_t)c4 * 4u) * 4u;
+                float4 sum = ld_peer_f32x4(la, 0);
+                for (int qq = 1; qq < S; ++qq) {
+                    const float4 v = ld_peer_f32x4(la, (uint32_t)qq);
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
+                }
+                if (n < a.N) {
+                    const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int m = m0 + c4 * 4 + j;
+                        if (m < a.Mt) a.Y[(size_t)m * a.N + n] = __float2half_rn(vals[j]);
+                    }
+                }
+            }
+        }
+        cluster_barrier();  // keep every CTA's partial alive until all peers have read it
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(P.tmem_cols)
@@ -364,36 +571,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-cudaError_t load_encoder() {
-    if (g_encode) return cudaSuccess;
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return cudaSuccess;
-}
-
 template <int BITS, bool HAS_ZP>
 cudaError_t set_attr() {
-    return cudaFuncSetAttribute(gemm_kernel<BITS, HAS_ZP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    return cudaFuncSetAttribute(gemm_kernel<BITS, HAS_ZP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kSmemBudget);
 }
 
 template <int BITS, bool HAS_ZP>
-cudaError_t launch(const CUtensorMap& tx, const CUtensorMap& tw, const GemmParams& P, int grid, bool pdl,
+cudaError_t launch(const CUtensorMap& tx, const CUtensorMap& tw, const GemmParams& P, int grid, size_t smem, bool pdl,
                    cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (P.split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = P.split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<BITS, HAS_ZP>, tx, tw, P);
 }
 
@@ -407,8 +614,20 @@ int gemm_token_tile(int Mt) {
 
 int gemm_threads() { return kThreads; }
 
+// K splits per tile: enough CTAs for the SMs when the tiles alone are too few.
+int gemm_split(int N, int Mt, int K, int sms) {
+    const int BN = gemm_token_tile(Mt);
+    const int tiles = ((N + BM - 1) / BM) * ((Mt + BN - 1) / BN);
+    const int ksteps = (K + BK - 1) / BK;
+    if (sms <= 0 || tiles * 2 > sms) return 1;
+    int s = sms / tiles;
+    if (s > kMaxSplit) s = kMaxSplit;
+    if (s > ksteps) s = ksteps;
+    return s < 2 ? 1 : s;
+}
+
 cudaError_t gemm_prepare() {
-    cudaError_t e = load_encoder();
+    cudaError_t e = tensor_map_prepare();
     if (e == cudaSuccess) e = set_attr<4, false>();
     if (e == cudaSuccess) e = set_attr<4, true>();
     if (e == cudaSuccess) e = set_attr<8, false>();
@@ -416,44 +635,36 @@ cudaError_t gemm_prepare() {
     return e;
 }
 
-cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, cudaStream_t st) {
-    if (!g_encode) return cudaErrorNotSupported;
+cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, bool x_wait, cudaStream_t st) {
     GemmParams P;
     P.a = a;
     P.BN = p.tokens_per_cta;
     P.tiles_m = (a.Mt + P.BN - 1) / P.BN;
     P.tiles = P.tiles_m * ((a.N + BM - 1) / BM);
     P.ksteps = (a.K + BK - 1) / BK;
+    P.split = p.k_splits > 1 ? p.k_splits : 1;
     int cols = 32;
     while (cols < 2 * P.BN) cols *= 2;
     P.tmem_cols = cols;
+    P.x_wait = x_wait ? 1 : 0;
+    const GemmLayout L = gemm_layout(P.BN);
+    if (L.nx < 2 || L.total > kSmemBudget || (P.split > 1 && L.red_bytes > L.bar_off))
+        return cudaErrorInvalidConfiguration;
 
-    CUtensorMap tx, tw;
-    {
-        const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.Mt};
-        const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-        const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)P.BN};
-        const cuuint32_t es[2] = {1, 1};
-        if (g_encode(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(a.X), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    {
-        const int rowbytes = a.K * a.bits / 8;
-        const cuuint64_t dims[2] = {(cuuint64_t)rowbytes, (cuuint64_t)a.N};
-        const cuuint64_t strides[1] = {(cuuint64_t)rowbytes};
-        const cuuint32_t box[2] = {(cuuint32_t)(BK * a.bits / 8), (cuuint32_t)BM};
-        const cuuint32_t es[2] = {1, 1};
-        if (g_encode(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.Wq), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    CUtensorMap tx;
+    cudaError_t e = encode_2d(&tx, a.X, 2, (uint64_t)a.K, (uint64_t)a.Mt, (uint64_t)a.K * 2, (uint32_t)BK,
+                              (uint32_t)P.BN, true);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tw;  // packed weights [N rows x K*bits/8 bytes], boxes of 128 rows x 128 bytes
+    e = encode_2d(&tw, a.Wq, 1, (uint64_t)a.K * a.bits / 8, (uint64_t)a.N, (uint64_t)a.K * a.bits / 8, 128u, (uint32_t)BM,
+                  true);
+    if (e != cudaSuccess) return e;
     const int grid = p.grid_x;
     const bool zp = a.Z != nullptr;
-    if (a.bits == 4) return zp ? launch<4, true>(tx, tw, P, grid, pdl, st) : launch<4, false>(tx, tw, P, grid, pdl, st);
-    return zp ? launch<8, true>(tx, tw, P, grid, pdl, st) : launch<8, false>(tx, tw, P, grid, pdl, st);
+    if (a.bits == 4)
+        return zp ? launch<4, true>(tx, tw, P, grid, L.total, pdl, st)
+                  : launch<4, false>(tx, tw, P, grid, L.total, pdl, st);
+    return zp ? launch<8, true>(tx, tw, P, grid, L.total, pdl, st) : launch<8, false>(tx, tw, P, grid, L.total, pdl, st);
 }
 
 }  // namespace mnb

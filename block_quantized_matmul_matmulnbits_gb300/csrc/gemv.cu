@@ -11,10 +11,11 @@
 //    SM, so every SM streams the same number of bytes.
 //  * A producer warp streams the CTA's rows through a ring of shared-memory
 //    stages.  A stage is one 16-row group x one K chunk of at most 1 KB per
-//    row, moved with 1-D bulk copies (one copy for the whole group when a
-//    chunk is a full row, since the rows are contiguous), together with the
-//    group's scales, zero points and adapter rows B[n, :].  Large contiguous
-//    copies keep the copy engine near the HBM rate; small 2-D boxes do not.
+//    row: one 1-D bulk copy when a chunk is a full row (the rows are
+//    contiguous), else one 3-D TMA box of 16 rows x 4 pieces of 256 bytes,
+//    together with the group's scales, zero points and adapter rows B[n, :].
+//    A copy costs about the same to issue whatever its size, so the copies
+//    are few and large: per-row copies of 1 KB cannot feed an SM.
 //    The producer never waits on the work queued before this kernel: weights
 //    are prefetched while that work (or the LoRA down kernel) still runs.
 //  * Eight consumer warps wait (griddepcontrol.wait) for X and T, then split
@@ -29,6 +30,8 @@
 //    memory in warp order (deterministic, no atomics), the LoRA term
 //    T[m, :] . B[n, :] is added, and each output is rounded once to FP16.
 //  * Waits on the ring are bounded and report through the status word.
+#include <cstring>
+
 #include "common.cuh"
 #include "mnb_internal.h"
 
@@ -89,7 +92,7 @@ __device__ __forceinline__ uint32_t lds_u8(const unsigned char* sm, uint32_t off
 
 template <int BITS, bool HAS_ZP, int NT, bool XS>
 __global__ void __launch_bounds__(kThreadsGemv, 2)
-    gemv_kernel(const GemvArgs a) {
+    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     constexpr int TOK = 8 * NT;
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
@@ -142,7 +145,8 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
                 const uint64_t z_lo = z0 & ~15ull, z_hi = min((z1 + 15) & ~15ull, total_z & ~15ull);
                 if (lane == 0) {
                     const int cb = min(CH, rowbytes - c * CH);  // bytes of this chunk per row
-                    uint32_t bytes = (uint32_t)rows * (uint32_t)cb;
+                    // a 3-D box always lands whole (rows past N, pieces past K read as zero)
+                    uint32_t bytes = nchunk > 1 && a.w3d ? (uint32_t)kGroup * (uint32_t)CH : (uint32_t)rows * (uint32_t)cb;
                     if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
                     if (HAS_ZP && z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
                     if (a.rank > 0) bytes += (uint32_t)rows * 64u;
@@ -150,6 +154,8 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
                     const uint8_t* src = a.Wq + (size_t)ra * rowbytes + (size_t)c * CH;
                     if (nchunk == 1) {
                         bulk_load(slot + L.w, src, (uint32_t)(rows * rowbytes), full(s));  // rows are contiguous
+                    } else if (a.w3d) {
+                        tma_load_3d(slot + L.w, &tmW, 0, c * CH / 256, ra, full(s));
                     } else {
                         for (int i = 0; i < rows; ++i)
                             bulk_load(slot + L.w + (uint32_t)(i * CH), src + (size_t)i * rowbytes, (uint32_t)cb, full(s));
@@ -390,7 +396,18 @@ cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS>, a);
+    // weights of multi-chunk stages as 3-D boxes when the row length allows it
+    CUtensorMap tw;
+    memset(&tw, 0, sizeof(tw));
+    GemvArgs b = a;
+    b.w3d = 0;
+    const uint64_t rowbytes = (uint64_t)a.K * BITS / 8;
+    if (rowbytes > (uint64_t)a.CH && rowbytes % 256 == 0 && a.CH % 256 == 0) {
+        const cudaError_t e = encode_rows_3d(&tw, a.Wq, rowbytes, (uint64_t)a.N, (uint32_t)(a.CH / 256), kGroup);
+        if (e != cudaSuccess) return e;
+        b.w3d = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS>, tw, b);
 }
 
 template <int BITS, bool HAS_ZP, int NT>
@@ -398,8 +415,6 @@ cudaError_t launch_xs(const GemvArgs& a, dim3 grid, size_t smem, bool xs, bool p
     return xs ? launch_one<BITS, HAS_ZP, NT, true>(a, grid, smem, pdl, st)
               : launch_one<BITS, HAS_ZP, NT, false>(a, grid, smem, pdl, st);
 }
-
-constexpr int kGemvSmemLimit = 112 * 1024;  // two CTAs per SM
 
 }  // namespace
 

@@ -17,6 +17,11 @@ constexpr unsigned int kStatusTimeout = 1u;
 
 // Host-side TMA descriptors (tensor_map.cu).
 cudaError_t tensor_map_prepare();
+// Byte matrix [rows, rowbytes] (rowbytes % 256 == 0) seen as [rows][rowbytes/256][256]:
+// one box copies `box_rows` rows x `box_chunks` 256-byte pieces, rows `box_chunks*256`
+// bytes apart in shared memory.
+cudaError_t encode_rows_3d(CUtensorMap* map, const void* base, uint64_t rowbytes, uint64_t rows, uint32_t box_chunks,
+                           uint32_t box_rows);
 cudaError_t encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
                       uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
@@ -34,6 +39,7 @@ struct GemvArgs {
     int ring;            // shared-memory ring stages (2 or 4), set by the launcher
     int xrows;           // X rows staged in shared memory per CTA (0: X read from global)
     int rank;            // 0 or 32
+    int w3d;             // weights of a multi-chunk stage come as one 3-D TMA box (set by the launcher)
     unsigned int* status;
 };
 
@@ -60,8 +66,10 @@ struct GemmArgs {
 };
 int gemm_token_tile(int Mt);  // token rows per prefill tile (multiple of 16, <= 256)
 int gemm_threads();
+int gemm_split(int N, int Mt, int K, int sms);  // CTAs sharing one tile along K
 cudaError_t gemm_prepare();
-cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, cudaStream_t st);
+// x_wait: X may be written by the work queued before this grid (early weights)
+cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, bool x_wait, cudaStream_t st);
 
 // Y = 0 over `count` halfs (K == 0 case).
 cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st);

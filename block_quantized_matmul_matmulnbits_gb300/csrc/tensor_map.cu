@@ -45,4 +45,18 @@ cudaError_t encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_rows_3d(CUtensorMap* map, const void* base, uint64_t rowbytes, uint64_t rows, uint32_t box_chunks,
+                           uint32_t box_rows) {
+    if (!g_encode) return cudaErrorNotSupported;
+    if (rowbytes % 256 != 0) return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {256, (cuuint64_t)(rowbytes / 256), (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {256, (cuuint64_t)rowbytes};
+    const cuuint32_t box[3] = {256, box_chunks, box_rows};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace mnb

@@ -154,3 +154,32 @@ def test_dequant_and_lora_down_validation_needs_no_device():
     assert L.mnb_dequant(0x1004, 0x2000, None, 4, 64, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_ALIGN
     assert L.mnb_lora_down(0x1000, 0x2000, 0x3000, 4, 64, 16, None) == mnb.MNB_ERR_UNSUPPORTED
     assert L.mnb_lora_down(0x1000, 0x2000, 0x3000, 0, 64, 32, None) == mnb.MNB_OK
+
+
+def test_gemm_plan_splits_k_only_when_tiles_are_few():
+    # 4096 x 4096 at M = 1: 32 tiles of 128 weight rows -> 4 CTAs (one cluster) per tile
+    h = mnb.mnb_create(4096, 4096, 4, mode=mnb.MODE_FORCE_GEMM)
+    try:
+        p = mnb.mnb_plan(h, 1, 1, 0, 152)
+        assert p["route"] == mnb.ROUTE_GEMM and p["k_splits"] == 4 and p["grid_x"] == 128
+        assert p["tokens_per_cta"] == 16
+        # prefill M = 1024: 128 tiles, persistent CTAs, no split
+        p = mnb.mnb_plan(h, 1, 1024, 0, 152)
+        assert p["k_splits"] == 1 and p["grid_x"] == 128 and p["tokens_per_cta"] == 256
+        # many tiles: one CTA per SM walks over them
+        p = mnb.mnb_plan(h, 1, 4096, 0, 152)
+        assert p["k_splits"] == 1 and p["grid_x"] == 152
+    finally:
+        mnb.mnb_destroy(h)
+    # never more CTAs per tile than K steps, never more than a portable cluster
+    h = mnb.mnb_create(256, 128, 4, mode=mnb.MODE_FORCE_GEMM)
+    try:
+        p = mnb.mnb_plan(h, 1, 1, 0, 152)
+        assert p["k_splits"] == 2 and p["grid_x"] == 4
+    finally:
+        mnb.mnb_destroy(h)
+    h = mnb.mnb_create(128, 4096, 4, mode=mnb.MODE_FORCE_GEMM)
+    try:
+        assert mnb.mnb_plan(h, 1, 1, 0, 152)["k_splits"] == 8
+    finally:
+        mnb.mnb_destroy(h)
