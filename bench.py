@@ -338,8 +338,8 @@ def run_gpu_arm(args, dist_ctx):
     def rnd(x, n=2):
         return None if x is None else round(x, n)
 
-    gbs = step_bytes * args.steps / t_decode / 1e9 * world
-    per_gbs = step_bytes * args.steps / t_decode / 1e9
+    gbs = job_rate(step_bytes, args.steps, t_decode, world) / 1e9
+    per_gbs = job_rate(step_bytes, args.steps, t_decode, 1) / 1e9
     base_gbs = base_bytes * args.steps / t_base / 1e9
     e2e_gbs = step_bytes * e2e_steps / t_e2e / 1e9 * world
     line = {
@@ -406,6 +406,12 @@ def run_reference_arm(args):
 
 
 # ----------------------------------------------------------------------------- distribution
+
+def job_rate(units_per_step, steps, t_max, world):
+    """Whole-job throughput: every rank processes `steps` steps of its own
+    replica (weak scaling), and the job takes the slowest rank's time."""
+    return units_per_step * steps * world / t_max
+
 
 def make_dist_ctx():
     world = int(os.environ.get("WORLD_SIZE", "1"))

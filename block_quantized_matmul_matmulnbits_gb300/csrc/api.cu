@@ -247,6 +247,8 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.R = p.rows_per_cta;
         a.CH = p.k_splits;
         a.rank = rank;
+        a.x_wait = early ? 1 : 0;
+        a.w3d = 0;
         a.status = status;
         e = mnb::gemv_launch(a, p, d.bits, pdl, st);
     } else {

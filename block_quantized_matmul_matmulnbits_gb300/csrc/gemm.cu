@@ -132,11 +132,12 @@ __host__ __device__ inline GemmLayout gemm_layout(int BN) {
     GemmLayout L;
     L.xslot = g_align((uint32_t)BN * 128u, 1024u);
     // Small token tiles (decode shapes) are bound by the weight stream: deep
-    // packed ring, large super-stages.  Large tiles keep four X slots.
+    // packed ring, large super-stages.  Large tiles keep four X slots and four
+    // A slots (the dequant runs up to four steps ahead of the MMA).
     L.pboxes = BN <= 64 ? 2 : 1;
     L.pstage = (uint32_t)(L.pboxes * kPBox);
-    L.np = BN <= 64 ? 4 : 3;
-    L.nw = BN <= 64 ? 4 : 3;
+    L.np = BN <= 64 ? 4 : 2;
+    L.nw = 4;
     L.red_bytes = (uint32_t)BM * BN * 4u;
     const uint32_t fixed = L.np * L.pstage + L.nw * (uint32_t)kWSlot + 512u + 1024u;
     int nx = fixed < kSmemBudget ? (int)((kSmemBudget - fixed) / L.xslot) : 0;

@@ -18,7 +18,10 @@
 //    are few and large: per-row copies of 1 KB cannot feed an SM.
 //    The producer never waits on the work queued before this kernel: weights
 //    are prefetched while that work (or the LoRA down kernel) still runs.
-//  * Eight consumer warps wait (griddepcontrol.wait) for X and T, then split
+//  * Eight consumer warps wait (griddepcontrol.wait) for X when it may come
+//    from the work queued before the kernel, and for T (the LoRA down kernel
+//    of the same call) only at the first group's epilogue, so that kernel can
+//    overlap the main loop.  They split
 //    each stage along K in 64-byte pieces: 16-byte loads of rows g and g+8
 //    from shared memory, exact (q - zp) and one rounding by the scale in
 //    registers (common.cuh), straight into mma.sync m16n8k16 A fragments with
@@ -181,13 +184,8 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
     const int ctid = threadIdx.x;  // 0..255
-    pdl_wait();                    // X and T are produced by work queued before this kernel
-    if (a.rank > 0) {
-        for (int i = ctid; i < TOK * 32; i += kConsumerWarps * 32) {
-            const int tok = token0 + i / 32;
-            reinterpret_cast<__half*>(sm + L.t)[i] = tok < a.Mt ? a.T[(size_t)tok * 32 + (i & 31)] : __float2half_rn(0.f);
-        }
-    }
+    if (a.x_wait) pdl_wait();  // X is produced by work queued before this kernel
+    bool t_ready = a.rank == 0;
     if (XS) {
         // X rows of this token group into shared memory, once; for INT4 each group
         // of 8 codes is stored in the pair-interleaved order (0,4,1,5,2,6,3,7) the
@@ -359,6 +357,15 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
             r[g * TOK + nt * 8 + 2 * t + 1] = v[1];
             r[(g + 8) * TOK + nt * 8 + 2 * t] = v[2];
             r[(g + 8) * TOK + nt * 8 + 2 * t + 1] = v[3];
+        }
+        if (!t_ready) {  // first epilogue: T of the LoRA down kernel queued just before
+            pdl_wait();
+            for (int i = ctid; i < TOK * 32; i += kConsumerWarps * 32) {
+                const int tok = token0 + i / 32;
+                reinterpret_cast<__half*>(sm + L.t)[i] =
+                    tok < a.Mt ? a.T[(size_t)tok * 32 + (i & 31)] : __float2half_rn(0.f);
+            }
+            t_ready = true;
         }
         named_barrier_sync(1, kConsumerWarps * 32);
         // one output per thread: row rr = ctid % 16, token tok = ctid / 16

@@ -32,25 +32,8 @@ constexpr int kPitchX = kPiece + 8;  // halfs per staged X row (pad: conflict-fr
 constexpr int kMaxCluster = 8;
 constexpr int kLoraSmem = kPiece * kPitchA * 2 + kTok * kPitchX * 2 + kTok * 32 * 4;
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Load from the shared memory of CTA `rank` of this cluster.  Volatile keeps
-// it after the cluster barrier (also volatile); having no memory clobber lets
-// the loads of one output be issued back to back.
-__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-    return v;
 }
 
 // 16-byte global -> shared copy; src_bytes == 0 writes zeros and reads nothing.

@@ -39,6 +39,7 @@ struct GemvArgs {
     int ring;            // shared-memory ring stages (2 or 4), set by the launcher
     int xrows;           // X rows staged in shared memory per CTA (0: X read from global)
     int rank;            // 0 or 32
+    int x_wait;          // X may be written by the work queued before this kernel (early weights)
     int w3d;             // weights of a multi-chunk stage come as one 3-D TMA box (set by the launcher)
     unsigned int* status;
 };
