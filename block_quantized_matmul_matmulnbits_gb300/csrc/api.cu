@@ -248,6 +248,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.CH = p.k_splits;
         a.rank = rank;
         a.x_wait = early ? 1 : 0;
+        a.sms = sms;
         a.w3d = 0;
         a.status = status;
         e = mnb::gemv_launch(a, p, d.bits, pdl, st);

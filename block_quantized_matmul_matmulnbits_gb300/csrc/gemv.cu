@@ -29,9 +29,11 @@
 //    accumulator chains, X fragments prefetched one stage ahead).  INT4 uses
 //    the pair-interleaved unpacking; the same K permutation is applied to the
 //    X fragment, which leaves the sum unchanged.
-//  * After a group's last chunk the warps' partial sums are added in shared
-//    memory in warp order (deterministic, no atomics), the LoRA term
-//    T[m, :] . B[n, :] is added, and each output is rounded once to FP16.
+//  * After a group's last chunk warp 0 adds the LoRA term sum_r B[n, r] T[m, r]
+//    to its accumulators (two m16n8k16 per token tile from the stage's B rows
+//    and T in shared memory), the warps' partial sums are added in shared
+//    memory in warp order (deterministic, no atomics), and each output is
+//    rounded once to FP16.
 //  * Waits on the ring are bounded and report through the status word.
 #include <cstring>
 
@@ -78,6 +80,18 @@ __host__ __device__ inline GemvLayout gemv_layout(int ch, int nblk, int tok, int
     return L;
 }
 
+// CTAs per SM: three when there are rows enough for them and the kernel is a
+// single-token-tile one with X staged (it then fits 72 registers without
+// spilling and a two-stage ring in a third of the shared memory), two
+// otherwise (96 registers: more independent work per thread).
+inline int gemv_ctas_per_sm(int N, int nt, bool xs, int sms) {
+    return nt == 1 && xs && (N + kGroup - 1) / kGroup > 2 * sms ? 3 : 2;
+}
+
+// Ring stages: two when three CTAs share an SM (they still keep 96 KB of
+// weights in flight per SM) or when a CTA has at most two stages, else four.
+inline int gemv_ring(int nstages, int occ) { return nstages <= 2 || occ == 3 ? 2 : kMaxRing; }
+
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -93,8 +107,8 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* sm, uint32_t of
 }
 __device__ __forceinline__ uint32_t lds_u8(const unsigned char* sm, uint32_t off) { return sm[off]; }
 
-template <int BITS, bool HAS_ZP, int NT, bool XS>
-__global__ void __launch_bounds__(kThreadsGemv, 2)
+template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC>
+__global__ void __launch_bounds__(kThreadsGemv, OCC)
     gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     constexpr int TOK = 8 * NT;
@@ -340,6 +354,37 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
         // same), per n8 tile.  The buffer alternates between groups, so one barrier
         // per group suffices: a warp writes the partials of group q+2 only after
         // every warp passed group q+1's barrier, i.e. after all reads of group q.
+        if (!t_ready) {  // first epilogue: T of the LoRA down kernel queued just before
+            pdl_wait();
+            for (int i = ctid; i < TOK * 32; i += kConsumerWarps * 32) {
+                const int tok = token0 + i / 32;
+                reinterpret_cast<__half*>(sm + L.t)[i] =
+                    tok < a.Mt ? a.T[(size_t)tok * 32 + (i & 31)] : __float2half_rn(0.f);
+            }
+            named_barrier_sync(1, kConsumerWarps * 32);
+            t_ready = true;
+        }
+        if (rank > 0 && warp == 0) {
+            // LoRA term of the group's 16 rows, sum_r B[n, r] T[m, r], on the tensor
+            // cores: two m16n8k16 per token tile (A = the stage's B rows, B = T),
+            // into this warp's accumulators, so the warp-order sum below adds it.
+            const unsigned char* bs = sm + soff + L.b;  // 16 rows x 32 halves
+            const unsigned char* ts = sm + L.t;         // TOK rows x 32 halves
+#pragma unroll
+            for (int kc = 0; kc < 2; ++kc) {
+                const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
+                const uint32_t b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
+                const uint32_t b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
+                const uint32_t b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
+                const uint32_t b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const unsigned char* trow = ts + (nt * 8 + g) * 64 + o;
+                    mma_16816(acc[nt][0], b0r0, b0r8, b8r0, b8r8, *reinterpret_cast<const uint32_t*>(trow),
+                              *reinterpret_cast<const uint32_t*>(trow + 16));
+                }
+            }
+        }
         float* redq = red + (size_t)((q - 1) & 1) * kConsumerWarps * kGroup * TOK;
         float* r = redq + (size_t)warp * kGroup * TOK;
 #pragma unroll
@@ -358,15 +403,6 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
             r[(g + 8) * TOK + nt * 8 + 2 * t] = v[2];
             r[(g + 8) * TOK + nt * 8 + 2 * t + 1] = v[3];
         }
-        if (!t_ready) {  // first epilogue: T of the LoRA down kernel queued just before
-            pdl_wait();
-            for (int i = ctid; i < TOK * 32; i += kConsumerWarps * 32) {
-                const int tok = token0 + i / 32;
-                reinterpret_cast<__half*>(sm + L.t)[i] =
-                    tok < a.Mt ? a.T[(size_t)tok * 32 + (i & 31)] : __float2half_rn(0.f);
-            }
-            t_ready = true;
-        }
         named_barrier_sync(1, kConsumerWarps * 32);
         // one output per thread: row rr = ctid % 16, token tok = ctid / 16
         const int rr = ctid & (kGroup - 1), tok = ctid >> 4;
@@ -375,22 +411,14 @@ __global__ void __launch_bounds__(kThreadsGemv, 2)
             const int nw = min(kConsumerWarps, npieces);
             float sum = 0.f;
             for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
-            if (rank > 0) {
-                const __half* tsm = reinterpret_cast<const __half*>(sm + L.t) + tok * 32;
-                const __half* bsm = reinterpret_cast<const __half*>(sm + soff + L.b) + rr * 32;
-                float l = 0.f;
-#pragma unroll 8
-                for (int k = 0; k < 32; ++k) l = fmaf(__half2float(tsm[k]), __half2float(bsm[k]), l);
-                sum += l;
-            }
             a.Y[(size_t)token * a.N + ra + rr] = __float2half_rn(sum);
         }
         __syncwarp();
-        if (ok && lane == 0) mbar_arrive(empty(s));  // after this warp's reads of the stage's B rows
+        if (ok && lane == 0) mbar_arrive(empty(s));
     }
 }
 
-template <int BITS, bool HAS_ZP, int NT, bool XS>
+template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC>
 cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cudaStream_t st) {
     static_assert(NT == 1 || NT == 2, "token tiles");
     cudaLaunchConfig_t cfg = {};
@@ -414,21 +442,27 @@ cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cuda
         if (e != cudaSuccess) return e;
         b.w3d = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS>, tw, b);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS, OCC>, tw, b);
 }
 
 template <int BITS, bool HAS_ZP, int NT>
-cudaError_t launch_xs(const GemvArgs& a, dim3 grid, size_t smem, bool xs, bool pdl, cudaStream_t st) {
-    return xs ? launch_one<BITS, HAS_ZP, NT, true>(a, grid, smem, pdl, st)
-              : launch_one<BITS, HAS_ZP, NT, false>(a, grid, smem, pdl, st);
+cudaError_t launch_xs(const GemvArgs& a, dim3 grid, size_t smem, bool xs, int occ, bool pdl, cudaStream_t st) {
+    if constexpr (NT == 1) {
+        if (xs && occ == 3) return launch_one<BITS, HAS_ZP, 1, true, 3>(a, grid, smem, pdl, st);
+    }
+    return xs ? launch_one<BITS, HAS_ZP, NT, true, 2>(a, grid, smem, pdl, st)
+              : launch_one<BITS, HAS_ZP, NT, false, 2>(a, grid, smem, pdl, st);
 }
 
 }  // namespace
 
 size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R_out, int* CH_out, int* tok_out, int* threads) {
     const int tok = Mt <= 8 ? 8 : 16;
-    // two CTAs per SM (16 consumer warps), but at least one 16-row group per CTA
-    int ctas = 2 * (sms > 0 ? sms : 1);
+    const uint32_t xrows = (uint32_t)(Mt < tok ? Mt : tok);  // X rows one CTA stages
+    const bool xs = xrows * K * 2u <= kXStageMax;
+    // two or three CTAs per SM, but at least one 16-row group per CTA
+    const int occ = gemv_ctas_per_sm(N, tok / 8, xs, sms > 0 ? sms : 1);
+    int ctas = occ * (sms > 0 ? sms : 1);
     if (ctas > (N + kGroup - 1) / kGroup) ctas = (N + kGroup - 1) / kGroup;
     if (ctas < 1) ctas = 1;
     int R = (N + ctas - 1) / ctas;
@@ -443,20 +477,22 @@ size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R_out, int* C
     *CH_out = CH;
     *tok_out = tok;
     *threads = kThreadsGemv;
-    const uint32_t xrows = (uint32_t)(Mt < tok ? Mt : tok);  // X rows one CTA stages
-    const bool xs = xrows * K * 2u <= kXStageMax;
     const int nstages = (R + kGroup - 1) / kGroup * ((rowbytes + CH - 1) / CH);
-    return gemv_layout(CH, nblk, tok, nstages <= 2 ? 2 : kMaxRing, xs ? xrows * K * 2u : 0u).total;
+    return gemv_layout(CH, nblk, tok, gemv_ring(nstages, occ), xs ? xrows * K * 2u : 0u).total;
 }
 
 cudaError_t gemv_prepare() {
     cudaError_t e = tensor_map_prepare();
 #define MNB_SET(B, Z, T)                                                                                       \
     if (e == cudaSuccess)                                                                                      \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,     \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
                                  227 * 1024);                                                                  \
     if (e == cudaSuccess)                                                                                      \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                 227 * 1024);                                                                  \
+    if (e == cudaSuccess && T == 1)                                                                            \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, 1, true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                                 227 * 1024);
     MNB_SET(4, false, 1) MNB_SET(4, false, 2) MNB_SET(4, true, 1) MNB_SET(4, true, 2)
     MNB_SET(8, false, 1) MNB_SET(8, false, 2) MNB_SET(8, true, 1) MNB_SET(8, true, 2)
 #undef MNB_SET
@@ -468,9 +504,10 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
     const int tok = p.tokens_per_cta;
     const int rowbytes = a.K * bits / 8;
     const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
-    a.ring = nstages <= 2 ? 2 : kMaxRing;
     const uint32_t xrows = (uint32_t)(a.Mt < tok ? a.Mt : tok);
     const bool xs = xrows * a.K * 2u <= kXStageMax;
+    const int occ = gemv_ctas_per_sm(a.N, tok / 8, xs, a.sms > 0 ? a.sms : 1);
+    a.ring = gemv_ring(nstages, occ);
     a.xrows = xs ? (int)xrows : 0;
     const size_t smem = gemv_layout(a.CH, a.K / 32, tok, a.ring, xs ? xrows * a.K * 2u : 0u).total;
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
@@ -478,15 +515,15 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
     const bool zp = a.Z != nullptr;
     const int nt = tok / 8;
     if (bits == 4) {
-        if (zp) return nt == 1 ? launch_xs<4, true, 1>(a, grid, smem, xs, pdl, st)
-                               : launch_xs<4, true, 2>(a, grid, smem, xs, pdl, st);
-        return nt == 1 ? launch_xs<4, false, 1>(a, grid, smem, xs, pdl, st)
-                       : launch_xs<4, false, 2>(a, grid, smem, xs, pdl, st);
+        if (zp) return nt == 1 ? launch_xs<4, true, 1>(a, grid, smem, xs, occ, pdl, st)
+                               : launch_xs<4, true, 2>(a, grid, smem, xs, occ, pdl, st);
+        return nt == 1 ? launch_xs<4, false, 1>(a, grid, smem, xs, occ, pdl, st)
+                       : launch_xs<4, false, 2>(a, grid, smem, xs, occ, pdl, st);
     }
-    if (zp) return nt == 1 ? launch_xs<8, true, 1>(a, grid, smem, xs, pdl, st)
-                           : launch_xs<8, true, 2>(a, grid, smem, xs, pdl, st);
-    return nt == 1 ? launch_xs<8, false, 1>(a, grid, smem, xs, pdl, st)
-                   : launch_xs<8, false, 2>(a, grid, smem, xs, pdl, st);
+    if (zp) return nt == 1 ? launch_xs<8, true, 1>(a, grid, smem, xs, occ, pdl, st)
+                           : launch_xs<8, true, 2>(a, grid, smem, xs, occ, pdl, st);
+    return nt == 1 ? launch_xs<8, false, 1>(a, grid, smem, xs, occ, pdl, st)
+                   : launch_xs<8, false, 2>(a, grid, smem, xs, occ, pdl, st);
 }
 
 }  // namespace mnb

@@ -40,6 +40,7 @@ struct GemvArgs {
     int xrows;           // X rows staged in shared memory per CTA (0: X read from global)
     int rank;            // 0 or 32
     int x_wait;          // X may be written by the work queued before this kernel (early weights)
+    int sms;             // SMs of the device (the launcher picks the CTAs per SM from it)
     int w3d;             // weights of a multi-chunk stage come as one 3-D TMA box (set by the launcher)
     unsigned int* status;
 };

@@ -110,7 +110,8 @@ def test_gemv_plan_balances_rows_over_sms():
             p = mnb.mnb_plan(h, 1, 1, 0, 152)
             R = p["rows_per_cta"]
             assert p["grid_x"] * R >= N and (p["grid_x"] - 1) * R < N
-            assert p["grid_x"] <= 2 * 152 and (R >= 16 or N < 16 * 2 * 152)
+            # two or three CTAs per SM (three for one token tile with X staged), >= 16 rows each
+            assert p["grid_x"] <= 3 * 152 and (R >= 16 or N < 16 * 3 * 152)
             assert p["block_threads"] == 288 and p["k_splits"] % 64 == 0 and 64 <= p["k_splits"] <= 1024
             assert p["tokens_per_cta"] == 8
         finally:
