@@ -89,10 +89,10 @@ int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // Decode-kernel geometry: balanced row ranges, one CTA per SM and token group.
 void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
-    int R, CH, tok, threads;
-    mnb::gemv_geometry((int)d.N, (int)d.K, d.bits, (int)Mt, sms, &R, &CH, &tok, &threads);
+    int ctas, R, CH, tok, threads;
+    mnb::gemv_geometry((int)d.N, (int)d.K, d.bits, (int)Mt, sms, &ctas, &R, &CH, &tok, &threads);
     p->route = MNB_ROUTE_GEMV;
-    p->grid_x = cdiv(d.N, R);
+    p->grid_x = ctas;
     p->grid_y = cdiv(Mt, tok);
     p->block_threads = threads;
     p->rows_per_cta = R;

@@ -6,9 +6,10 @@
 // adding MatMulNBitsLoRA: base GEMV and LoRA down projection first, then the
 // base plus T * Bt^T), restated for sm_103a:
 //
-//  * Every packed weight byte is read from HBM once per token group.  CTA c
-//    owns output rows [c R, (c+1) R) with R = ceil(N / (2 #SMs)), two CTAs per
-//    SM, so every SM streams the same number of bytes.
+//  * Every packed weight byte is read from HBM once per token group.  Rows are
+//    dealt out in whole 16-row groups: CTA c of C owns groups
+//    [c G / C, (c+1) G / C) of the G = ceil(N / 16), and C is chosen so that
+//    the most groups any SM has to run (CTAs per SM x groups per CTA) is least.
 //  * A producer warp streams the CTA's rows through a ring of shared-memory
 //    stages.  A stage is one 16-row group x one K chunk of at most 1 KB per
 //    row: one 1-D bulk copy when a chunk is a full row (the rows are
@@ -123,8 +124,9 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     const GemvLayout L = gemv_layout(CH, nblk, TOK, ring, XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r0 = blockIdx.x * a.R;
-    const int r1 = min(a.N, r0 + a.R);
+    const int G = (a.N + kGroup - 1) / kGroup;
+    const int r0 = kGroup * (int)((long long)blockIdx.x * G / gridDim.x);
+    const int r1 = min(a.N, kGroup * (int)((long long)(blockIdx.x + 1) * G / gridDim.x));
     const int ngroups = (r1 - r0 + kGroup - 1) / kGroup;
     const int nstages = ngroups * nchunk;
     const int token0 = blockIdx.y * TOK;
@@ -456,7 +458,8 @@ cudaError_t launch_xs(const GemvArgs& a, dim3 grid, size_t smem, bool xs, int oc
 
 }  // namespace
 
-size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R_out, int* CH_out, int* tok_out, int* threads) {
+size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* ctas_out, int* R_out, int* CH_out, int* tok_out,
+                     int* threads) {
     const int tok = Mt <= 8 ? 8 : 16;
     const uint32_t xrows = (uint32_t)(Mt < tok ? Mt : tok);  // X rows one CTA stages
     const bool xs = xrows * K * 2u <= kXStageMax;
@@ -465,14 +468,25 @@ size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R_out, int* C
     int ctas = occ * (sms > 0 ? sms : 1);
     if (ctas > (N + kGroup - 1) / kGroup) ctas = (N + kGroup - 1) / kGroup;
     if (ctas < 1) ctas = 1;
-    int R = (N + ctas - 1) / ctas;
-    if (R < 1) R = 1;
+    // fewest groups on the busiest SM; among equals, more CTAs (more warps)
+    const int G = (N + kGroup - 1) / kGroup, s = sms > 0 ? sms : 1;
+    int best = ctas, best_cost = 1 << 30;
+    for (int cc = ctas; cc >= 1; --cc) {
+        const int cost = ((cc + s - 1) / s) * ((G + cc - 1) / cc);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = cc;
+        }
+    }
+    ctas = best;
+    const int R = kGroup * ((G + ctas - 1) / ctas);  // rows of the largest share
     const int nblk = K / 32;
     const int rowbytes = K * bits / 8;
     // K chunk: a full row when it fits (one contiguous copy per group), else 1 KB
     int CH = rowbytes <= kMaxChunk ? rowbytes : kMaxChunk;
     CH = (CH + 63) / 64 * 64;
     if (CH < 64) CH = 64;
+    *ctas_out = ctas;
     *R_out = R;
     *CH_out = CH;
     *tok_out = tok;

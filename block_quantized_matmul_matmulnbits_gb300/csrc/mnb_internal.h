@@ -45,9 +45,9 @@ struct GemvArgs {
     unsigned int* status;
 };
 
-// Decode-kernel geometry for (N, K, token rows) on `sms` SMs: rows per CTA
-// and K bytes per stage; returns the dynamic shared memory it needs.
-size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* R, int* CH, int* tok, int* threads);
+// Decode-kernel geometry for (N, K, token rows) on `sms` SMs: `ctas` CTAs, each owning
+// whole 16-row groups (at most R rows), K bytes per stage; returns the shared memory it needs.
+size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* ctas, int* R, int* CH, int* tok, int* threads);
 cudaError_t gemv_prepare();
 cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st);
 

@@ -93,7 +93,8 @@ typedef struct {
     int32_t lora_kernel;    /* 1 if the LoRA down projection kernel runs first */
     int32_t grid_x, grid_y; /* grid of the main kernel */
     int32_t block_threads;  /* threads per CTA of the main kernel */
-    int32_t rows_per_cta;   /* GEMV: output rows per CTA; GEMM: output rows per tile */
+    int32_t rows_per_cta;   /* GEMV: most output rows a CTA owns (whole 16-row groups, dealt out
+                               evenly); GEMM: output rows per tile */
     int32_t k_splits;       /* GEMV: K bytes per row and pipeline stage; GEMM: CTAs (one cluster)
                                sharing a tile along K, 1 = persistent CTAs over tiles */
     int32_t tokens_per_cta; /* GEMV: token rows per CTA (8 or 16); GEMM: token tile */

@@ -108,10 +108,14 @@ def test_gemv_plan_balances_rows_over_sms():
         h = mnb.mnb_create(N, K, bits)
         try:
             p = mnb.mnb_plan(h, 1, 1, 0, 152)
-            R = p["rows_per_cta"]
-            assert p["grid_x"] * R >= N and (p["grid_x"] - 1) * R < N
-            # two or three CTAs per SM (three for one token tile with X staged), >= 16 rows each
-            assert p["grid_x"] <= 3 * 152 and (R >= 16 or N < 16 * 3 * 152)
+            R, C, G = p["rows_per_cta"], p["grid_x"], -(-N // 16)
+            # whole 16-row groups dealt out evenly: the largest share is ceil(G / C) groups
+            assert C <= G and R == 16 * -(-G // C)
+            # two or three CTAs per SM (three for one token tile with X staged)
+            assert C <= 3 * 152
+            # no other CTA count gives the busiest SM fewer groups
+            cost = lambda c: -(-c // 152) * -(-G // c)
+            assert all(cost(C) <= cost(c) for c in range(1, min(G, 3 * 152) + 1))
             assert p["block_threads"] == 288 and p["k_splits"] % 64 == 0 and 64 <= p["k_splits"] <= 1024
             assert p["tokens_per_cta"] == 8
         finally:
