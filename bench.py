@@ -368,6 +368,105 @@ def run_gpu_arm(args, dist_ctx):
     return line
 
 
+# ----------------------------------------------------------------------------- sweep
+
+SWEEP_M = (1, 2, 4, 8, 16, 64, 256, 1024, 4096)
+
+
+def run_sweep(args):
+    """The lm_head shapes and the M sweep at K=4096, N=14336 (INT4, default
+    zero point, adapter on and off), every route, per-call time = median of 10
+    replays of a graph of back-to-back calls over weight copies larger than 4x
+    L2.  Reports the decode/prefill crossover."""
+    import torch
+
+    from block_quantized_matmul_matmulnbits_gb300 import mnb, synth
+
+    torch.cuda.set_device(0)
+    mnb.lib()
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    hbm_peak, bf16_peak, _, peak_src = load_peaks()
+
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def measure(M, K, N, bits, rank, zp_range, scale_range, mode, seed):
+        inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=seed, zp_range=zp_range,
+                                scale_range=scale_range or (0.005, 0.02), rank=rank)
+        nbytes = decode_bytes(M, K, N, bits, rank, zp=zp_range is not None)
+        copies = max(2, min(64, math.ceil(4 * l2 / nbytes)))
+        base = dict(X=dev(inp.X), Wq=dev(inp.Wq), S=dev(inp.scales), Z=dev(inp.zp), A=dev(inp.A), B=dev(inp.B))
+        cps = [{k: (None if v is None else v.clone()) for k, v in base.items()} for _ in range(copies)]
+        Y = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+        T = torch.empty((M, 32), dtype=torch.float16, device="cuda") if rank else None
+        h = mnb.mnb_create(N, K, bits, 32, 32, mode, 0, mnb.FLAG_EARLY_WEIGHTS)
+        try:
+            def call(i):
+                c = cps[i % copies]
+                mnb.mnb_run(h, c["X"], c["Wq"], c["S"], c["Z"], c["A"], c["B"], rank, Y, T, 1, M)
+            n = max(4, min(200, int(2e-3 / max(1e-6, 2 * M * N * K / 1e15))))  # about 2 ms of calls per graph
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                call(0)
+            torch.cuda.current_stream().wait_stream(st)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    call(i)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            times = []
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3 / n)
+            if mnb.mnb_sync_status(h) != mnb.MNB_OK:
+                raise RuntimeError("device timeout")
+            route = mnb.mnb_last_route(h)
+        finally:
+            mnb.mnb_destroy(h)
+        us = float(np.median(times))
+        fl = prefill_flops(M, K, N, rank)
+        return {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1), "TFps": round(fl / us / 1e6, 2),
+                "hbm_frac": round(nbytes / us / 1e3 / hbm_peak, 4), "tensor_frac": round(fl / us / 1e6 / bf16_peak, 4),
+                "route": {1: "gemv", 2: "gemm"}.get(route, str(route))}
+
+    rows = []
+    for name, (K, N, zpr, scr) in {"lm_head K=576 N=49152 INT8": (576, 49152, (120, 136), (0.001, 0.01)),
+                                   "lm_head K=896 N=151936 INT8": (896, 151936, (120, 136), (0.001, 0.01))}.items():
+        r = measure(1, K, N, 8, 0, zpr, scr, mnb.MODE_AUTO, synth.SEED_BASE + 4)
+        rows.append({"workload": name, "M": 1, "rank": 0, "mode": "auto", **r})
+        print(json.dumps(rows[-1]), flush=True)
+    cross = {}
+    for rank in (0, 32):
+        for M in SWEEP_M:
+            res = {}
+            for mname, mode in (("gemv", mnb.MODE_FORCE_GEMV), ("gemm", mnb.MODE_FORCE_GEMM)):
+                if mname == "gemv" and M > 64:
+                    continue  # the decode kernel re-reads the weights per 16 tokens
+                res[mname] = measure(M, 4096, 14336, 4, rank, None, None, mode, synth.SEED_BASE + 5)
+                rows.append({"workload": "K=4096 N=14336 INT4", "M": M, "rank": rank, "mode": mname, **res[mname]})
+                print(json.dumps(rows[-1]), flush=True)
+            if "gemv" in res and res["gemm"]["us"] < res["gemv"]["us"] and rank not in cross:
+                cross[rank] = M
+    summary = {"sweep": "lm_head + K=4096 N=14336 M sweep", "peaks": {"hbm_GBps": hbm_peak, "tensor_TFps": bf16_peak,
+                                                                     "source": peak_src},
+               "crossover_M_gemm_faster": cross, "rows": len(rows)}
+    print(json.dumps(summary), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 def oracle_decode_sample(target_s):
@@ -446,7 +545,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", choices=["all", "decode", "decode_base", "prefill"], default="all",
                     help="run one leg only (for profiling); the printed line then lacks the other legs")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: the lm_head shapes and the M sweep at K=4096, N=14336 "
+                         "(both routes), one JSON line per point")
     args = ap.parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
