@@ -222,16 +222,18 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
 
     const __half* Xh = static_cast<const __half*>(X);
     __half* Th = static_cast<__half*>(T_ws);
-    // Programmatic dependent launch: with early weights every kernel may start
-    // before its predecessor on the stream ends (and only reads X / T after
-    // griddepcontrol.wait); otherwise only the matmul kernel overlaps the
-    // LoRA down kernel of the same call.
+    // Programmatic dependent launch.  With early weights the first kernel of a
+    // call may start before the work queued ahead of it has completed: it
+    // streams weights at once and reads X only after griddepcontrol.wait.  The
+    // LoRA down kernel lets the matmul kernel start only after its own wait,
+    // so behind it the matmul kernel reads X at once and waits only for T.
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
-    if (rank > 0) {
+    const bool lora_kernel = rank > 0;
+    if (lora_kernel) {
         e = mnb::lora_down_launch(Xh, static_cast<const __half*>(A), Th, (int)Mt, (int)d.K, early, st);
         if (e != cudaSuccess) return MNB_ERR_CUDA;
     }
-    const bool pdl = rank > 0 || early;
+    const bool pdl = lora_kernel || early;
     if (p.route == MNB_ROUTE_GEMV) {
         mnb::GemvArgs a;
         a.X = Xh;
@@ -247,7 +249,9 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.R = p.rows_per_cta;
         a.CH = p.k_splits;
         a.rank = rank;
-        a.x_wait = early ? 1 : 0;
+        // after the LoRA down kernel the preceding work is complete when this
+        // kernel starts (see lora_down.cu): only T needs the wait
+        a.x_wait = early && !lora_kernel ? 1 : 0;
         a.sms = sms;
         a.w3d = 0;
         a.status = status;
@@ -267,7 +271,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.bits = d.bits;
         a.rank = rank;
         a.status = status;
-        e = mnb::gemm_launch(a, p, pdl, early, st);
+        e = mnb::gemm_launch(a, p, pdl, early && !lora_kernel, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return MNB_ERR_CUDA;

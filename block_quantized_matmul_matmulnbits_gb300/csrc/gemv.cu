@@ -19,10 +19,12 @@
 //    are few and large: per-row copies of 1 KB cannot feed an SM.
 //    The producer never waits on the work queued before this kernel: weights
 //    are prefetched while that work (or the LoRA down kernel) still runs.
-//  * Eight consumer warps wait (griddepcontrol.wait) for X when it may come
-//    from the work queued before the kernel, and for T (the LoRA down kernel
-//    of the same call) only at the first group's epilogue, so that kernel can
-//    overlap the main loop.  They split
+//  * Eight consumer warps wait (griddepcontrol.wait) for X only when the
+//    kernel may start before the work queued ahead of it has completed (early
+//    weights, no adapter); after the LoRA down kernel of the same call -- which
+//    lets this kernel start only once that work is complete -- they read X at
+//    once and wait for T at the first group's epilogue, so the two kernels
+//    overlap.  They split
 //    each stage along K in 64-byte pieces: 16-byte loads of rows g and g+8
 //    from shared memory, exact (q - zp) and one rounding by the scale in
 //    registers (common.cuh), straight into mma.sync m16n8k16 A fragments with

@@ -15,9 +15,10 @@
 // cluster barrier every CTA finishes an interleaved share of the outputs,
 // adding the partials of all CTAs in rank order through distributed shared
 // memory, rounds once to FP16 and stores T.  No atomics, so T is bitwise
-// reproducible.  The kernel
-// signals programmatic launch completion on entry so that the matmul kernel
-// queued after it can start streaming weights at once.
+// reproducible.  The kernel signals programmatic launch completion right
+// after its own griddepcontrol.wait: the matmul kernel queued after it then
+// starts only once the work before this kernel has completed, so it may read
+// X at once and waits (griddepcontrol.wait) only for T.
 #include "common.cuh"
 #include "mnb_internal.h"
 
@@ -62,8 +63,6 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
     __half* Xs = As + kPiece * kPitchA;                                       // [kTok][kPitchX]
     float* part = reinterpret_cast<float*>(Xs + kTok * kPitchX);              // [kTok][32]
 
-    pdl_launch_dependents();
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_rank();
     // Few token rows (decode): one 16-row tile per CTA and the four warps split
@@ -92,6 +91,7 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         }
         if (!waited) {
             pdl_wait();
+            pdl_launch_dependents();  // the work before this kernel is complete: X is readable
             waited = true;
         }
         const int xc = klen / 8;  // 16-byte chunks per token row
@@ -119,7 +119,10 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         }
         __syncthreads();
     }
-    if (!waited) pdl_wait();
+    if (!waited) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
 
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
