@@ -177,6 +177,12 @@ int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_co
 
 int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
             const void* B, int32_t rank, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
+    return mnb_run_bias(h, X, Wq, scales, zp, A, B, rank, nullptr, Y, T_ws, batch, M, stream);
+}
+
+int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+                 const void* B, int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M,
+                 void* stream) {
     if (!h || batch < 0 || M < 0) return MNB_ERR_ARG;
     const mnb_desc& d = h->d;
     if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
@@ -194,8 +200,9 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         if (d.K > 0 && (!X || !Wq || !scales)) return MNB_ERR_ARG;
     }
     if (!aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zp) || !aligned16(Y) ||
-        (rank > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(T_ws))))
+        !aligned16(bias) || (rank > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(T_ws))))
         return MNB_ERR_ALIGN;
+    const __half* biash = static_cast<const __half*>(bias);
 
     mnb_plan_info p;
     int sms = 0;
@@ -213,7 +220,8 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         return MNB_OK;
     }
     if (p.route == MNB_ROUTE_FILL) {
-        e = mnb::fill_zero_launch(static_cast<__half*>(Y), (size_t)Mt * (size_t)d.N, st);
+        e = biash ? mnb::fill_bias_launch(static_cast<__half*>(Y), biash, (size_t)Mt, (size_t)d.N, st)
+                  : mnb::fill_zero_launch(static_cast<__half*>(Y), (size_t)Mt * (size_t)d.N, st);
         if (e == cudaSuccess && rank > 0) e = mnb::fill_zero_launch(static_cast<__half*>(T_ws), (size_t)Mt * 32, st);
         if (e != cudaSuccess) return MNB_ERR_CUDA;
         h->last_route = MNB_ROUTE_FILL;
@@ -242,6 +250,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.Z = static_cast<const uint8_t*>(zp);
         a.T = Th;
         a.B = static_cast<const __half*>(B);
+        a.bias = biash;
         a.Y = static_cast<__half*>(Y);
         a.Mt = (int)Mt;
         a.N = (int)d.N;
@@ -264,6 +273,7 @@ int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, con
         a.Z = static_cast<const uint8_t*>(zp);
         a.T = Th;
         a.B = static_cast<const __half*>(B);
+        a.bias = biash;
         a.Y = static_cast<__half*>(Y);
         a.Mt = (int)Mt;
         a.N = (int)d.N;

@@ -81,6 +81,24 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ Wq, const __half* __r
 
 }  // namespace
 
+namespace {
+// K == 0 with a bias: every output row is the bias (the output keeps its
+// logical shape and holds zeros or the broadcast bias).
+__global__ void fill_bias_kernel(__half* __restrict__ Y, const __half* __restrict__ bias, size_t rows, size_t N) {
+    const size_t total = rows * N, stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) Y[i] = bias[i % N];
+}
+}  // namespace
+
+cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st) {
+    const size_t total = rows * N;
+    if (total == 0) return cudaSuccess;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    fill_bias_kernel<<<(unsigned)blocks, 256, 0, st>>>(Y, bias, rows, N);
+    return cudaGetLastError();
+}
+
 cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st) {
     const size_t n16 = count / 8, ntail = count % 8;
     size_t blocks = (n16 + 255) / 256;

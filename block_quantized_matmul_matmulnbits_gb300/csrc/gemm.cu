@@ -388,10 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                 } else if (n < a.N) {
+                    const float bn = a.bias ? __half2float(a.bias[n]) : 0.f;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = u.m0 + c + j;
-                        if (m < a.Mt) a.Y[(size_t)m * a.N + n] = __float2half_rn(__uint_as_float(v[j]));
+                        if (m < a.Mt) a.Y[(size_t)m * a.N + n] = __float2half_rn(__uint_as_float(v[j]) + bn);
                     }
                 }
             }
@@ -552,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sum.w += v.w;
                 }
                 if (n < a.N) {
-                    const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+                    const float bn = a.bias ? __half2float(a.bias[n]) : 0.f;
+                    const float vals[4] = {sum.x + bn, sum.y + bn, sum.z + bn, sum.w + bn};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int m = m0 + c4 * 4 + j;

@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
             const int nw = min(kConsumerWarps, npieces);
             float sum = 0.f;
             for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
+            if (a.bias) sum += __half2float(a.bias[ra + rr]);
             a.Y[(size_t)token * a.N + ra + rr] = __float2half_rn(sum);
         }
         __syncwarp();

@@ -32,6 +32,7 @@ struct GemvArgs {
     const uint8_t* Z;    // [N, K/32] or nullptr (default zero point)
     const __half* T;     // [Mt, 32] or nullptr
     const __half* B;     // [N, 32] or nullptr
+    const __half* bias;  // [N] or nullptr: added to every output row before the rounding
     __half* Y;           // [Mt, N]
     int Mt, N, K;
     int R;               // output rows owned by one CTA
@@ -62,6 +63,7 @@ struct GemmArgs {
     const uint8_t* Z;
     const __half* T;
     const __half* B;
+    const __half* bias;  // [N] or nullptr
     __half* Y;
     int Mt, N, K, bits, rank;
     unsigned int* status;  // device status word (bounded waits report here)
@@ -75,6 +77,8 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
 
 // Y = 0 over `count` halfs (K == 0 case).
 cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st);
+// Y[m, n] = bias[n] for m < rows (K == 0 with a bias)
+cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st);
 
 // W16[n, k] = fp16((q - zp) * scale) with the kernels' own dequant arithmetic.
 cudaError_t dequant_launch(const uint8_t* Wq, const __half* S, const uint8_t* Z, int N, int K, int bits,

@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -74,6 +74,8 @@ def lib() -> ctypes.CDLL:
             L.mnb_destroy.restype = None
             L.mnb_run.argtypes = [P, P, P, P, P, P, P, I32, P, P, I64, I64, P]
             L.mnb_run.restype = ctypes.c_int
+            L.mnb_run_bias.argtypes = [P, P, P, P, P, P, P, I32, P, P, P, I64, I64, P]
+            L.mnb_run_bias.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -141,6 +143,11 @@ def mnb_run(h, X, Wq, scales, zp, A, B, rank: int, Y, T_ws, batch: int, M: int, 
                          _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run")
 
 
+def mnb_run_bias(h, X, Wq, scales, zp, A, B, rank: int, bias, Y, T_ws, batch: int, M: int, stream=None) -> None:
+    _check(lib().mnb_run_bias(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
+                              _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run_bias")
+
+
 def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:
     """mnb_run for callers that cannot allocate device memory: T lives in the
     library's own fixed device array (at most mnb_noalloc_max_rows() token
@@ -190,7 +197,7 @@ class Projection:
         self.N, self.K, self.bits = N, K, bits
         self.h = mnb_create(N, K, bits, 32, max_rank, mode, gemv_max_m, flags)
 
-    def __call__(self, X, Wq, scales, zp=None, A=None, B=None, out=None, T_ws=None, stream=None):
+    def __call__(self, X, Wq, scales, zp=None, A=None, B=None, out=None, T_ws=None, stream=None, bias=None):
         import torch
         batch, M = (X.shape[0], X.shape[1]) if X.dim() == 3 else (1, X.shape[0])
         rank = 0 if A is None else int(A.shape[1])
@@ -199,7 +206,7 @@ class Projection:
             out = torch.empty(shape, dtype=torch.float16, device=X.device)
         if rank and T_ws is None:
             T_ws = torch.empty((batch * M, rank), dtype=torch.float16, device=X.device)
-        mnb_run(self.h, X, Wq, scales, zp, A, B, rank, out, T_ws, batch, M, stream)
+        mnb_run_bias(self.h, X, Wq, scales, zp, A, B, rank, bias, out, T_ws, batch, M, stream)
         return out
 
     @property

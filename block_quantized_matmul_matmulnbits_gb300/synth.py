@@ -90,6 +90,13 @@ def make_inputs(*, M: int, K: int, N: int, bits: int = 4, seed: int,
     return Inputs(X=X, Wq=Wq, scales=scales, zp=zp, A=A, B=B, batch=batch, M=M, N=N, K=K, bits=bits)
 
 
+def make_bias(N: int, seed: int, std: float = 0.5) -> np.ndarray:
+    """A seeded FP16 bias [N] (bit patterns), drawn from its own stream so the
+    other inputs of the same seed are unchanged."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0xB1A5]))
+    return _f16_bits(rng.standard_normal(size=N) * std)
+
+
 # Named workloads (shapes and value ranges of the five configurations).
 
 def tiny(M: int, rank: int, seed_offset: int = 0) -> Inputs:

@@ -132,6 +132,20 @@ int mnb_run(mnb_handle h,
             void* Y, void* T_ws,
             int64_t batch, int64_t M, void* stream);
 
+/* mnb_run with an optional bias: Y[m, n] = fp16_rne(sum + bias[n]), the bias
+ * added to every row before the one rounding.  With K == 0 every row of Y is
+ * the bias.  Follows the operator's optional bias input: "[WebGPU] Fuse rank-32
+ * quantized LoRA with MatMulNBits", referenced commit "Support empty packed
+ * weights in CPU and WebGPU MatMulNBits", Description (the output holds zeros
+ * or the broadcast bias).
+ *   bias    fp16 [N], 16-byte aligned, or NULL (then exactly mnb_run)
+ * All other arguments, results and errors are those of mnb_run. */
+int mnb_run_bias(mnb_handle h,
+                 const void* X, const void* Wq, const void* scales, const void* zp,
+                 const void* A, const void* B, int32_t rank, const void* bias,
+                 void* Y, void* T_ws,
+                 int64_t batch, int64_t M, void* stream);
+
 /* The plan mnb_run would use for (batch, M, rank) on a GPU with `sm_count`
  * SMs (sm_count <= 0: query the current device).  Host only.  Follows the
  * auto mode selection of the MatMulNBitsLoRA commit message (per-matrix row

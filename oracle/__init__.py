@@ -70,6 +70,8 @@ def _load():
             lib.mnb_ref_lora_down.argtypes = [P, P, I64, I64, I, P]
             lib.mnb_ref_lora_down.restype = I
             lib.mnb_ref_run.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, I, I, P, P, P]
+            lib.mnb_ref_run_bias.argtypes = [P, P, P, P, P, P, I, P, I64, I64, I64, I, I, I, P, P, P]
+            lib.mnb_ref_run_bias.restype = I
             lib.mnb_ref_run.restype = I
             lib.mnb_ref_threads.argtypes = []
             lib.mnb_ref_threads.restype = I
@@ -153,10 +155,11 @@ def lora_down(X, A) -> np.ndarray:
     return T
 
 
-def run(X, Wq, scales, zp, A, B, N, K, bits, block=32, round_t=False):
-    """Y = X * dequant(Wq)^T (+ (X*A) * B^T).
+def run(X, Wq, scales, zp, A, B, N, K, bits, block=32, round_t=False, bias=None):
+    """Y = X * dequant(Wq)^T (+ (X*A) * B^T) (+ bias broadcast over rows).
 
-    X: [Mt, K] FP16 bit patterns (uint16); A [K, r], B [N, r] FP16 bits or None.
+    X: [Mt, K] FP16 bit patterns (uint16); A [K, r], B [N, r] FP16 bits or None;
+    bias: [N] FP16 bits or None.
     Returns (Y16 bits [Mt, N], Y64 [Mt, N], bound [Mt, N]) where bound is the
     sum of absolute products that scales the FP16 tolerance.
     """
@@ -169,8 +172,9 @@ def run(X, Wq, scales, zp, A, B, N, K, bits, block=32, round_t=False):
     Y16 = np.empty((Mt, N), dtype=np.uint16)
     Y64 = np.empty((Mt, N), dtype=np.float64)
     bound = np.empty((Mt, N), dtype=np.float64)
-    rc = _load().mnb_ref_run(_ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank,
-                             Mt, N, K, bits, block, 1 if round_t else 0,
-                             _ptr(Y16), _ptr(Y64), _ptr(bound))
+    bias = _c(bias, np.uint16) if bias is not None else None
+    rc = _load().mnb_ref_run_bias(_ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
+                                  Mt, N, K, bits, block, 1 if round_t else 0,
+                                  _ptr(Y16), _ptr(Y64), _ptr(bound))
     _check(rc, "run")
     return Y16, Y64, bound

@@ -14,6 +14,7 @@
  *   w[n,k] = (q[n,k] - zp[n, k/bs]) * scale[n, k/bs]                  (dequant)
  *   t[m,r] = sum_k x[m,k] * A[k,r]                                     (LoRA down)
  *   y[m,n] = sum_k x[m,k] * w[n,k]  +  sum_r t[m,r] * B[n,r]           (base + LoRA up)
+ *            (+ bias[n] when a bias is given)
  *   Y[m,n] = fp16_round_to_nearest_even(y[m,n])
  *
  * Sources, cited by page title and section:
@@ -38,6 +39,11 @@
  *    array is passed the default is 2^(bits-1) (8 for INT4, 128 for INT8).
  *  - T is kept exact (fp64) here; the fused GPU path rounds T to FP16 as the
  *    pages do.  mnb_ref_run can also round T first (round_t = 1).
+ *  - Bias: "[WebGPU] Fuse rank-32 quantized LoRA with MatMulNBits", the
+ *    referenced commit "Support empty packed weights in CPU and WebGPU
+ *    MatMulNBits", Description: with empty weights the output holds zeros or
+ *    the broadcast bias.  Read as: an optional FP16 vector over N added to
+ *    every output row before the one rounding (mnb_ref_run_bias).
  *
  * Everything is plain loops; OpenMP only splits independent output rows.
  */
@@ -220,10 +226,10 @@ int mnb_ref_lora_down(const uint16_t* X, const uint16_t* A, int64_t Mt, int64_t 
  * pages' FP16 intermediate); 0 keeps it exact.
  * ------------------------------------------------------------------------- */
 
-int mnb_ref_run(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
-                const uint16_t* A, const uint16_t* B, int rank,
-                int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
-                uint16_t* Y16, double* Y64, double* bound)
+int mnb_ref_run_bias(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                     const uint16_t* A, const uint16_t* B, int rank, const uint16_t* bias,
+                     int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                     uint16_t* Y16, double* Y64, double* bound)
 {
     int rc = check_shape(N, K, bits, bs);
     if (rc) return rc;
@@ -254,12 +260,26 @@ int mnb_ref_run(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, co
             acc += p;
             mag += fabs(p);
         }
+        if (bias) {
+            double b = mnb_ref_f16_to_f64(bias[n]);
+            acc += b;
+            mag += fabs(b);
+        }
         if (Y64) Y64[i] = acc;
         if (bound) bound[i] = mag;
         if (Y16) Y16[i] = mnb_ref_f64_to_f16(acc);
     }
     free(T);
     return 0;
+}
+
+/* mnb_ref_run_bias without a bias. */
+int mnb_ref_run(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                const uint16_t* A, const uint16_t* B, int rank,
+                int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                uint16_t* Y16, double* Y64, double* bound)
+{
+    return mnb_ref_run_bias(X, Wq, scales, zp, A, B, rank, NULL, Mt, N, K, bits, bs, round_t, Y16, Y64, bound);
 }
 
 /* Threads the parallel loop above will use. */

@@ -26,7 +26,9 @@ def upload(inp, torch):
                 A=dev(inp.A, torch), B=dev(inp.B, torch))
 
 
-def run_gpu(mnb, torch, inp, mode=0, gemv_max_m=0, d=None, Y=None, T=None, rank=None):
+def run_gpu(mnb, torch, inp, mode=0, gemv_max_m=0, d=None, Y=None, T=None, rank=None, bias=None):
+    """Run one problem through the C ABI; ``bias`` (a CUDA FP16 [N] tensor) goes
+    through mnb_run_bias, None through mnb_run."""
     d = d or upload(inp, torch)
     rank = inp.rank if rank is None else rank
     h = mnb.mnb_create(inp.N, inp.K, inp.bits, 32, 32, mode, gemv_max_m)
@@ -36,8 +38,11 @@ def run_gpu(mnb, torch, inp, mode=0, gemv_max_m=0, d=None, Y=None, T=None, rank=
             Y = torch.empty((inp.batch, inp.M, inp.N), dtype=torch.float16, device="cuda")
         if T is None and rank:
             T = torch.empty((Mt, rank), dtype=torch.float16, device="cuda")
-        mnb.mnb_run(h, d["X"], d["Wq"], d["scales"], d["zp"], d["A"] if rank else None, d["B"] if rank else None,
-                    rank, Y, T, inp.batch, inp.M)
+        AB = (d["A"], d["B"]) if rank else (None, None)
+        if bias is None:
+            mnb.mnb_run(h, d["X"], d["Wq"], d["scales"], d["zp"], *AB, rank, Y, T, inp.batch, inp.M)
+        else:
+            mnb.mnb_run_bias(h, d["X"], d["Wq"], d["scales"], d["zp"], *AB, rank, bias, Y, T, inp.batch, inp.M)
         torch.cuda.synchronize()
         assert mnb.mnb_sync_status(h) == 0
         route = mnb.mnb_last_route(h)
@@ -46,16 +51,18 @@ def run_gpu(mnb, torch, inp, mode=0, gemv_max_m=0, d=None, Y=None, T=None, rank=
     return Y, T, route
 
 
-def oracle_ref(inp, rows=None, tokens=None):
-    """Oracle Y64 and bound, optionally on a subset of output rows / token rows."""
+def oracle_ref(inp, rows=None, tokens=None, bias=None):
+    """Oracle Y64 and bound, optionally on a subset of output rows / token rows;
+    ``bias`` is FP16 bits [N] or None."""
     X = inp.X2d if tokens is None else inp.X2d[tokens]
     Wq, S, Z, B = inp.Wq, inp.scales, inp.zp, inp.B
     if rows is not None:
         Wq, S = Wq[rows], S[rows]
         Z = None if Z is None else Z[rows]
         B = None if B is None else B[rows]
+        bias = None if bias is None else bias[rows]
     N = Wq.shape[0]
-    _, Y64, bound = oracle.run(X, Wq, S, Z, inp.A, B, N, inp.K, inp.bits)
+    _, Y64, bound = oracle.run(X, Wq, S, Z, inp.A, B, N, inp.K, inp.bits, bias=bias)
     return Y64, bound
 
 

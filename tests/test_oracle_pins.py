@@ -362,3 +362,44 @@ def test_negative_control_untransposed_weight_fails_equivalence():
     ref = f16val(X) @ ((q_kn.astype(np.float64) - 8) * f16val(s)[0, 0])          # DQ of W[K, N]
     _, Y64, bound = oracle.run(X, oracle.pack(q_kn, 4), s, None, None, None, N, K, 4)  # forgot .T
     assert not np.all(np.abs(Y64 - ref) <= 1e-13 * bound)
+
+
+# ---------------------------------------------------------------- bias ("[WebGPU] Fuse rank-32 quantized LoRA
+# with MatMulNBits", the referenced commit "Support empty packed weights in CPU and WebGPU MatMulNBits",
+# Description: the output holds zeros or the broadcast bias)
+
+def _bias_bits(N, seed):
+    rng = np.random.default_rng(seed)
+    return oracle.f64_to_f16_bits(rng.normal(0.0, 1.0, size=N))
+
+
+def test_bias_alone_when_every_weight_is_zero():
+    # q == zp everywhere: every w is exactly 0, so y[m, n] is exactly bias[n] for every row m
+    M, K, N = 3, 64, 40
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=11, zp_range=(0, 15), rank=0)
+    q = np.broadcast_to(inp.zp.reshape(N, K // 32, 1), (N, K // 32, 32))
+    Wq = oracle.pack(np.ascontiguousarray(q.reshape(N, K)), 4)
+    bias = _bias_bits(N, 5)
+    Y16, Y64, _ = oracle.run(inp.X2d, Wq, inp.scales, inp.zp, None, None, N, K, 4, bias=bias)
+    want = oracle.f16_bits_to_f64(bias)
+    assert np.array_equal(Y64, np.broadcast_to(want, (M, N)))
+    assert np.array_equal(Y16, np.broadcast_to(bias, (M, N)))
+
+
+def test_bias_adds_once_after_base_and_adapter():
+    inp = synth.make_inputs(M=4, K=128, N=48, bits=4, seed=12, zp_range=(0, 15), rank=32)
+    bias = _bias_bits(48, 6)
+    _, y0, b0 = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 48, 128, 4)
+    y16, y1, b1 = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 48, 128, 4, bias=bias)
+    bv = oracle.f16_bits_to_f64(bias)
+    assert np.allclose(y1 - y0, np.broadcast_to(bv, y0.shape), rtol=0, atol=1e-12 * (1 + np.abs(y0).max()))
+    assert np.allclose(b1 - b0, np.broadcast_to(np.abs(bv), y0.shape), rtol=0, atol=1e-9)
+    assert np.array_equal(y16, oracle.f64_to_f16_bits(y1))  # one rounding of the whole sum
+
+
+def test_no_bias_is_bitwise_the_plain_run():
+    inp = synth.make_inputs(M=2, K=64, N=24, bits=8, seed=13, zp_range=(120, 136), rank=32)
+    a = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 24, 64, 8)
+    b = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 24, 64, 8, bias=None)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
