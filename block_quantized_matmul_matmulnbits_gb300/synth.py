@@ -66,8 +66,8 @@ def make_inputs(*, M: int, K: int, N: int, bits: int = 4, seed: int,
                 rank: int = 0, lora_std: float = 0.02, partial: bool = False,
                 x_std: float = 1.0) -> Inputs:
     """Draw one seeded problem.  ``zp_range`` is inclusive; None = default zp."""
-    if bits not in (4, 8):
-        raise ValueError("bits must be 4 or 8")
+    if bits not in (2, 4, 8):
+        raise ValueError("bits must be 2, 4 or 8")
     if K % BLOCK:
         raise ValueError("K must be a multiple of 32")
     rng = np.random.Generator(np.random.PCG64(seed))

@@ -34,9 +34,12 @@
  * Readings where the pages leave a step open (each is listed in the design doc):
  *  - INT4 packing: two 4-bit codes per byte along K; element k = 2j sits in
  *    the low nibble (bits 0..3) of byte j of the block, k = 2j + 1 in the
- *    high nibble.  INT8: one code per byte.
+ *    high nibble.  INT8: one code per byte.  INT2 (the 2-bit weights of the
+ *    empty-packed-weights commit's tests): four codes per byte, the same
+ *    low-bits-first order, element k = 4j + i in bits 2i..2i+1 of byte j.
  *  - Zero points: one unsigned byte per (row, block), used as given; when no
- *    array is passed the default is 2^(bits-1) (8 for INT4, 128 for INT8).
+ *    array is passed the default is 2^(bits-1) (2 for INT2, 8 for INT4, 128
+ *    for INT8).
  *  - T is kept exact (fp64) here; the fused GPU path rounds T to FP16 as the
  *    pages do.  mnb_ref_run can also round T first (round_t = 1).
  *  - Bias: "[WebGPU] Fuse rank-32 quantized LoRA with MatMulNBits", the
@@ -118,18 +121,19 @@ uint16_t mnb_ref_f64_to_f16(double v)
 static int check_shape(int64_t N, int64_t K, int bits, int bs)
 {
     if (N < 0 || K < 0) return -1;
-    if (bits != 4 && bits != 8) return -2;
+    if (bits != 2 && bits != 4 && bits != 8) return -2;
     if (bs <= 0 || (bs * bits) % 8 != 0) return -2;
     if (K % bs != 0) return -2;
     return 0;
 }
 
-/* code q[n,k] read from the packed weight bytes */
+/* code q[n,k] read from the packed weight bytes: row n is K * bits / 8 bytes,
+ * code k is in byte k / per_byte at bit bits * (k % per_byte) */
 static int code_at(const uint8_t* Wq, int64_t K, int bits, int64_t n, int64_t k)
 {
-    if (bits == 8) return Wq[n * K + k];
-    uint8_t byte = Wq[n * (K / 2) + k / 2];
-    return (k % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+    int per_byte = 8 / bits;
+    uint8_t byte = Wq[n * (K / per_byte) + k / per_byte];
+    return (byte >> (bits * (int)(k % per_byte))) & ((1 << bits) - 1);
 }
 
 int mnb_ref_unpack(const uint8_t* Wq, int64_t N, int64_t K, int bits, int bs, uint8_t* q)
@@ -145,14 +149,12 @@ int mnb_ref_pack(const uint8_t* q, int64_t N, int64_t K, int bits, int bs, uint8
 {
     int rc = check_shape(N, K, bits, bs);
     if (rc) return rc;
-    if (bits == 8) {
-        memcpy(Wq, q, (size_t)(N * K));
-        return 0;
-    }
+    int per_byte = 8 / bits, mask = (1 << bits) - 1;
     for (int64_t n = 0; n < N; ++n)
-        for (int64_t j = 0; j < K / 2; ++j) {
-            uint8_t lo = q[n * K + 2 * j] & 0x0f, hi = q[n * K + 2 * j + 1] & 0x0f;
-            Wq[n * (K / 2) + j] = (uint8_t)(lo | (hi << 4));
+        for (int64_t j = 0; j < K / per_byte; ++j) {
+            int byte = 0;
+            for (int i = 0; i < per_byte; ++i) byte |= (q[n * K + j * per_byte + i] & mask) << (bits * i);
+            Wq[n * (K / per_byte) + j] = (uint8_t)byte;
         }
     return 0;
 }

@@ -82,7 +82,43 @@ def test_int8_unpack_is_byte_order():
     assert np.array_equal(q, Wq.reshape(2, 32))
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+def _read_int2_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "int2_code_order.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                parts = line.split()
+                rows.append((int(parts[0], 16), [int(v) for v in parts[1:5]], [float(v) for v in parts[5:9]]))
+    return rows
+
+
+def test_int2_unpack_golden():
+    rows = _read_int2_fixture()
+    Wq = np.array([b for b, _, _ in rows], dtype=np.uint8).reshape(1, 1, 8)
+    expect = np.array([c for _, codes, _ in rows for c in codes], dtype=np.uint8)
+    assert np.array_equal(oracle.unpack(Wq, 1, 32, 2)[0], expect)
+
+
+def test_int2_dequant_golden_default_zero_point():
+    rows = _read_int2_fixture()
+    Wq = np.array([b for b, _, _ in rows], dtype=np.uint8).reshape(1, 1, 8)
+    expect = np.array([v for _, _, vals in rows for v in vals]).reshape(1, 32)
+    W = oracle.dequant(Wq, f16([[0.25]]), None, 1, 32, 2)
+    assert np.array_equal(W, expect)
+
+
+def test_negative_control_reversed_int2_order_fails_the_golden():
+    """Codes read highest bits first would be a plausible mistake: it must not
+    pass the golden block."""
+    rows = _read_int2_fixture()
+    raw = np.array([b for b, _, _ in rows], dtype=np.uint8)
+    wrong = np.stack([(raw >> (6 - 2 * i)) & 3 for i in range(4)], axis=1).reshape(-1)
+    expect = np.array([c for _, codes, _ in rows for c in codes], dtype=np.uint8)
+    assert not np.array_equal(wrong, expect)
+    assert np.array_equal(oracle.unpack(raw.reshape(1, 1, 8), 1, 32, 2)[0], expect)
+
+
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_pack_unpack_roundtrip(bits):
     rng = np.random.default_rng(bits)
     q = rng.integers(0, 1 << bits, size=(5, 96), dtype=np.uint8)
@@ -104,19 +140,24 @@ def test_int4_dequant_golden():
     assert np.array_equal(f16val(W16), expect)
 
 
-@pytest.mark.parametrize("bits,zp_range", [(4, None), (4, (0, 15)), (8, None), (8, (120, 136)), (8, (0, 255))])
+def _codes_numpy(Wq, N, K, bits):
+    """Codes decoded with numpy bit operations, independently of the oracle:
+    per byte, lowest bits first."""
+    raw = Wq.reshape(N, -1).astype(np.int64)
+    per = 8 // bits
+    codes = np.empty((N, K), dtype=np.int64)
+    for i in range(per):
+        codes[:, i::per] = (raw >> (bits * i)) & ((1 << bits) - 1)
+    return codes
+
+
+@pytest.mark.parametrize("bits,zp_range", [(2, None), (2, (0, 3)), (4, None), (4, (0, 15)), (8, None),
+                                           (8, (120, 136)), (8, (0, 255))])
 def test_dequant_exact_vs_rationals(bits, zp_range):
     inp = synth.make_inputs(M=1, K=64, N=6, bits=bits, seed=11, zp_range=zp_range,
                             scale_range=(1e-4, 3.0))
     W = oracle.dequant(inp.Wq, inp.scales, inp.zp, 6, 64, bits)
-    # codes read independently of the oracle: numpy bit operations on the bytes
-    raw = inp.Wq.reshape(6, -1)
-    if bits == 4:
-        codes = np.empty((6, 64), dtype=np.int64)
-        codes[:, 0::2] = raw & 0x0F
-        codes[:, 1::2] = raw >> 4
-    else:
-        codes = raw.astype(np.int64)
+    codes = _codes_numpy(inp.Wq, 6, 64, bits)
     s = f16val(inp.scales)
     for n in range(6):
         for k in range(64):
@@ -125,7 +166,7 @@ def test_dequant_exact_vs_rationals(bits, zp_range):
             assert Fraction(float(W[n, k])) == exact
 
 
-@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_dequant_f16_is_single_rounding(bits):
     inp = synth.make_inputs(M=1, K=256, N=64, bits=bits, seed=12, zp_range=(0, (1 << bits) - 1),
                             scale_range=(1e-6, 40.0))
@@ -163,13 +204,7 @@ def test_one_hot_rows_recover_dequant_columns():
 def _exact_y(inp, round_t=False):
     """Exact rational y for a tiny problem, from numpy-decoded codes."""
     Mt, K, N, bits = inp.batch * inp.M, inp.K, inp.N, inp.bits
-    raw = inp.Wq.reshape(N, -1)
-    codes = np.empty((N, K), dtype=np.int64)
-    if bits == 4:
-        codes[:, 0::2] = raw & 0x0F
-        codes[:, 1::2] = raw >> 4
-    else:
-        codes[:] = raw
+    codes = _codes_numpy(inp.Wq, N, K, bits)
     x = [[Fraction(float(v)) for v in row] for row in f16val(inp.X2d)]
     s = f16val(inp.scales)
     w = [[Fraction(int(codes[n, k]) - ((1 << (bits - 1)) if inp.zp is None else int(inp.zp[n, k // 32])))
@@ -185,7 +220,8 @@ def _exact_y(inp, round_t=False):
     return y
 
 
-@pytest.mark.parametrize("bits,rank,zp", [(4, 0, None), (4, 32, (0, 15)), (8, 32, (120, 136))])
+@pytest.mark.parametrize("bits,rank,zp", [(4, 0, None), (4, 32, (0, 15)), (8, 32, (120, 136)), (2, 0, None),
+                                         (2, 32, (0, 3))])
 def test_brute_force_exact_rationals(bits, rank, zp):
     inp = synth.make_inputs(M=2, K=64, N=5, bits=bits, seed=14, zp_range=zp, rank=rank)
     Y16, Y64, bound = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 5, 64, bits)
