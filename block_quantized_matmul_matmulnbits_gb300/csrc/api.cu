@@ -43,9 +43,9 @@ int validate_desc(const mnb_desc* d) {
     if (!d) return MNB_ERR_ARG;
     if (d->N < 0 || d->K < 0) return MNB_ERR_ARG;
     if (d->N > (int64_t)INT32_MAX || d->K > (int64_t)INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
-    if (d->bits != 4 && d->bits != 8) return MNB_ERR_UNSUPPORTED;
+    if (d->bits != 2 && d->bits != 4 && d->bits != 8) return MNB_ERR_UNSUPPORTED;
     if (d->block_size != 32) return MNB_ERR_UNSUPPORTED;
-    if (d->K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (d->K % (d->bits == 2 ? 64 : 32) != 0) return MNB_ERR_UNSUPPORTED;  // packed rows of whole 16-byte units
     if (d->max_rank != 0 && d->max_rank != 32) return MNB_ERR_UNSUPPORTED;
     if (d->mode < MNB_MODE_AUTO || d->mode > MNB_MODE_FORCE_GEMM) return MNB_ERR_ARG;
     if ((d->flags & ~MNB_FLAG_EARLY_WEIGHTS) != 0) return MNB_ERR_ARG;
@@ -315,8 +315,8 @@ const char* mnb_status_str(int code) {
 int mnb_dequant(const void* Wq, const void* scales, const void* zp, int64_t N, int64_t K, int32_t bits,
                 int32_t block_size, void* W16, int32_t variant, void* stream) {
     if (N < 0 || K < 0 || variant < 0 || variant > 1) return MNB_ERR_ARG;
-    if (bits != 4 && bits != 8) return MNB_ERR_UNSUPPORTED;
-    if (block_size != 32 || K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (bits != 2 && bits != 4 && bits != 8) return MNB_ERR_UNSUPPORTED;
+    if (block_size != 32 || K % (bits == 2 ? 64 : 32) != 0) return MNB_ERR_UNSUPPORTED;
     if (N > INT32_MAX || K > INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
     if (N == 0 || K == 0) return MNB_OK;
     if (!Wq || !scales || !W16) return MNB_ERR_ARG;

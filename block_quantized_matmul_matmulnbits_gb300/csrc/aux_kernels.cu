@@ -10,7 +10,8 @@
 //    initializers and skip outer-scope weights" (onnxruntime PR 33800,
 //    Description).  It runs the exact device helpers of the matmul kernels
 //    (variant 0: natural order, variant 1: the decode kernel's pair-interleaved
-//    INT4 order, un-permuted on store) so their bits can be checked one by one.
+//    INT4 / INT2 order, un-permuted on store) so their bits can be checked one
+//    by one.
 #include "common.cuh"
 #include "mnb_internal.h"
 
@@ -44,7 +45,32 @@ __global__ void dequant_kernel(const uint8_t* __restrict__ Wq, const __half* __r
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
     const int k0 = c * 16 * 8 / BITS;
     uint32_t out[16];  // up to 32 halfs as half2 words
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {  // 64 codes: words 0, 1 are block blk, words 2, 3 block blk + 1
+        uint32_t o2[32];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int b = blk + (w >> 1);
+            const uint16_t sb2 = reinterpret_cast<const uint16_t*>(S)[(size_t)n * nblk + b];
+            const uint32_t z2 = Z ? Z[(size_t)n * nblk + b] : 2u;
+            const Dq2Const c2 = dq2_const(z2, sb2);
+            uint32_t d[8];
+            if (variant == 0) {
+                dq_int2_natural(words[w], c2, d);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o2[8 * w + j] = d[j];
+            } else {
+                dq_int2_interleaved(words[w], c2, d);  // d[j] = (k_j, k_{j+8})
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    o2[8 * w + i] = prmt(d[2 * i], d[2 * i + 1], 0x5410u);      // (k_{2i}, k_{2i+1})
+                    o2[8 * w + 4 + i] = prmt(d[2 * i], d[2 * i + 1], 0x7632u);  // (k_{2i+8}, k_{2i+9})
+                }
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(W16 + (size_t)n * K + k0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_uint4(o2[4 * q], o2[4 * q + 1], o2[4 * q + 2], o2[4 * q + 3]);
+    } else if constexpr (BITS == 4) {
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             uint32_t d[4];
@@ -113,7 +139,9 @@ cudaError_t dequant_launch(const uint8_t* Wq, const __half* S, const uint8_t* Z,
     const long long total = (long long)N * (K * bits / 8 / 16);
     if (total == 0) return cudaSuccess;
     const unsigned blocks = (unsigned)((total + 255) / 256);
-    if (bits == 4)
+    if (bits == 2)
+        dequant_kernel<2><<<blocks, 256, 0, st>>>(Wq, S, Z, N, K, W16, variant);
+    else if (bits == 4)
         dequant_kernel<4><<<blocks, 256, 0, st>>>(Wq, S, Z, N, K, W16, variant);
     else
         dequant_kernel<8><<<blocks, 256, 0, st>>>(Wq, S, Z, N, K, W16, variant);

@@ -113,6 +113,64 @@ __device__ __forceinline__ void dq_int8_natural(uint32_t w, const DqConst& c, ui
     d[1] = hmul2_rn(hsub2_rn(h23, c.c0), c.s2);
 }
 
+// INT2: four codes per byte, code 4b + i in bits 2i..2i+1 of byte b.  A code
+// masked in place at bit 2i of a half's fraction reads as 1024 + 4^i q; one
+// fused multiply by 4^-i (exact: a power of two) and add of -(1024 4^-i + zp)
+// leaves q - zp exactly (every value an integer below 2048 in magnitude), and
+// the multiply by the scale rounds once.
+__host__ __device__ constexpr uint32_t int2_mul(int i) {  // half2(4^-i): 1, 1/4, 1/16, 1/64
+    return i == 0 ? 0x3C003C00u : i == 1 ? 0x34003400u : i == 2 ? 0x2C002C00u : 0x24002400u;
+}
+__host__ __device__ constexpr uint32_t int2_base(int i) {  // half2(1024 - 1024 4^-i): 0, 768, 960, 1008
+    return i == 0 ? 0x00000000u : i == 1 ? 0x62006200u : i == 2 ? 0x63806380u : 0x63E063E0u;
+}
+
+struct Dq2Const {
+    uint32_t off[4];  // half2(-(1024 4^-i + zp)), i = 0..3
+    uint32_t s2;
+};
+
+__device__ __forceinline__ Dq2Const dq2_const(uint32_t zp, uint16_t scale_bits) {
+    Dq2Const c;
+    const uint32_t z = kMagic1024x2 | (zp * 0x00010001u);  // half2(1024 + zp)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c.off[i] = hsub2_rn(int2_base(i), z);
+    c.s2 = (uint32_t)scale_bits * 0x00010001u;
+    return c;
+}
+
+// Pair-interleaved order (decode kernel).  Word w holds codes k0..k15.  Output
+// half2s d[j] = (w_kj, w_k{j+8}), j = 0..7: code j sits at bit 2j and code
+// j + 8 at bit 16 + 2j, so one mask serves both halves.
+__device__ __forceinline__ void dq_int2_interleaved(uint32_t w, const Dq2Const& c, uint32_t d[8]) {
+    const uint32_t w8 = w >> 8;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int i = j & 3;
+        const uint32_t h = lop3_and_or(j < 4 ? w : w8, 0x00030003u << (2 * i), kMagic1024x2);
+        d[j] = hmul2_rn(hfma2_rn(h, int2_mul(i), c.off[i]), c.s2);
+    }
+}
+
+// Natural order (prefill kernel, K-major FP16 operand).  d[j] = (w_k{2j},
+// w_k{2j+1}), j = 0..7.  Byte b is copied to both halves; the low half keeps
+// code 4b (bit 0) or 4b + 2 (bit 4), the high half code 4b + 1 (bit 2) or
+// 4b + 3 (bit 6), each removed with its own power of two.
+__device__ __forceinline__ void dq_int2_natural(uint32_t w, const Dq2Const& c, uint32_t d[8]) {
+    const uint32_t m01 = prmt(int2_mul(0), int2_mul(1), 0x7610u);  // (lo 1, hi 1/4)
+    const uint32_t m23 = prmt(int2_mul(2), int2_mul(3), 0x7610u);  // (lo 1/16, hi 1/64)
+    const uint32_t o01 = prmt(c.off[0], c.off[1], 0x7610u);
+    const uint32_t o23 = prmt(c.off[2], c.off[3], 0x7610u);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t t = prmt(w, 0u, 0x4040u | (uint32_t)b | ((uint32_t)b << 8));
+        const uint32_t h01 = lop3_and_or(t, 0x000C0003u, kMagic1024x2);
+        const uint32_t h23 = lop3_and_or(t, 0x00C00030u, kMagic1024x2);
+        d[2 * b] = hmul2_rn(hfma2_rn(h01, m01, o01), c.s2);
+        d[2 * b + 1] = hmul2_rn(hfma2_rn(h23, m23, o23), c.s2);
+    }
+}
+
 // ---------------------------------------------------------------- tensor ops
 
 // D = A(16x16, row) * B(16x8, col) + C, FP16 inputs, FP32 accumulate.  Not

@@ -450,6 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(empty_w(s), ph ^ 1u, status))) break;  // the MMA is done with the slot
                     // invalid block (row past N, K tail): scale 0 makes its products 0
                     const DqConst dc = dq_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
+                    Dq2Const d2 = {};
+                    if constexpr (BITS == 2) d2 = dq2_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
                     {  // refill this prefetch slot with step i + kPrefetch
                         const int blk = 2 * (i + kPrefetch) + h;
                         const bool ld = row_ok && blk < nblk && i + kPrefetch < u.i1;
@@ -461,11 +463,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // this step's bytes of row r: box li*kStepBytes/128, 16-byte chunk c0 (+1)
                     const int li = (local & (kps - 1));
                     const int pb = li * kStepBytes;
-                    const int c0 = ((pb & 127) >> 4) + h * (kStepBytes / 32);
+                    const int c0 = ((pb & 127) >> 4) + (BITS == 2 ? 0 : h * (kStepBytes / 32));
                     const unsigned char* prow =
                         sptr + L.p_off + (uint32_t)cur_p * L.pstage + (uint32_t)(pb >> 7) * kPBox + (uint32_t)r * 128u;
                     uint32_t out[16];
-                    if constexpr (BITS == 4) {
+                    if constexpr (BITS == 2) {  // the step's 16 bytes are one chunk; block h is its half h
+                        const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
+                        dq_int2_natural(h ? pk.z : pk.x, d2, &out[0]);
+                        dq_int2_natural(h ? pk.w : pk.y, d2, &out[8]);
+                    } else if constexpr (BITS == 4) {
                         const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
                         const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
 #pragma unroll
@@ -631,6 +637,8 @@ int gemm_split(int N, int Mt, int K, int sms) {
 
 cudaError_t gemm_prepare() {
     cudaError_t e = tensor_map_prepare();
+    if (e == cudaSuccess) e = set_attr<2, false>();
+    if (e == cudaSuccess) e = set_attr<2, true>();
     if (e == cudaSuccess) e = set_attr<4, false>();
     if (e == cudaSuccess) e = set_attr<4, true>();
     if (e == cudaSuccess) e = set_attr<8, false>();
@@ -664,6 +672,9 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
     if (e != cudaSuccess) return e;
     const int grid = p.grid_x;
     const bool zp = a.Z != nullptr;
+    if (a.bits == 2)
+        return zp ? launch<2, true>(tx, tw, P, grid, L.total, pdl, st)
+                  : launch<2, false>(tx, tw, P, grid, L.total, pdl, st);
     if (a.bits == 4)
         return zp ? launch<4, true>(tx, tw, P, grid, L.total, pdl, st)
                   : launch<4, false>(tx, tw, P, grid, L.total, pdl, st);

@@ -30,8 +30,9 @@
 //    registers (common.cuh), straight into mma.sync m16n8k16 A fragments with
 //    the 8 or 16 token rows as the N side (FP32 accumulate, independent
 //    accumulator chains, X fragments prefetched one stage ahead).  INT4 uses
-//    the pair-interleaved unpacking; the same K permutation is applied to the
-//    X fragment, which leaves the sum unchanged.
+//    the pair-interleaved unpacking (codes j and j + 4 of a word in one
+//    half2), INT2 pairs codes j and j + 8; the same K permutation is applied
+//    to the X fragment, which leaves the sum unchanged.
 //  * After a group's last chunk warp 0 adds the LoRA term sum_r B[n, r] T[m, r]
 //    to its accumulators (two m16n8k16 per token tile from the stage's B rows
 //    and T in shared memory), the warps' partial sums are added in shared
@@ -208,14 +209,31 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
         // X rows of this token group into shared memory, once; for INT4 each group
         // of 8 codes is stored in the pair-interleaved order (0,4,1,5,2,6,3,7) the
         // unpacking produces, so the inner loop needs no permutes.
-        const int mv = min(TOK, a.Mt - token0), kc = a.K / 8;
-        for (int i = ctid; i < mv * kc; i += kConsumerWarps * 32) {
-            const int row = i / kc, c8 = i - row * kc;
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(token0 + row) * a.K) + c8);
-            if (BITS == 4)
-                v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
-                               prmt(v.y, v.w, 0x7632u));
-            *reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c8 * 8u) * 2u) = v;
+        const int mv = min(TOK, a.Mt - token0);
+        if constexpr (BITS == 2) {
+            // INT2: each group of 16 codes as the pairs (x_j, x_{j+8}), j = 0..7
+            const int kc = a.K / 16;
+            for (int i = ctid; i < mv * kc; i += kConsumerWarps * 32) {
+                const int row = i / kc, c16 = i - row * kc;
+                const uint4* src = reinterpret_cast<const uint4*>(a.X + (size_t)(token0 + row) * a.K) + 2 * c16;
+                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                uint32_t xw[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xw[j] = prmt(word_of(v0, j >> 1), word_of(v1, j >> 1), (j & 1) ? 0x7632u : 0x5410u);
+                uint4* dst = reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c16 * 16u) * 2u);
+                dst[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+                dst[1] = make_uint4(xw[4], xw[5], xw[6], xw[7]);
+            }
+        } else {
+            const int kc = a.K / 8;
+            for (int i = ctid; i < mv * kc; i += kConsumerWarps * 32) {
+                const int row = i / kc, c8 = i - row * kc;
+                uint4 v = __ldg(reinterpret_cast<const uint4*>(a.X + (size_t)(token0 + row) * a.K) + c8);
+                if (BITS == 4)
+                    v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
+                                   prmt(v.y, v.w, 0x7632u));
+                *reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c8 * 8u) * 2u) = v;
+            }
         }
         named_barrier_sync(1, kConsumerWarps * 32);
     }
@@ -275,6 +293,69 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
             for (int h = 0; h < 2; ++h) {  // two 16-byte halves
                 const int kbh = kb + 16 * h;
                 const bool kv = kbh < rowbytes;
+                if constexpr (BITS == 2) {
+                    // 16 bytes = 64 codes = two blocks: words 2 bb and 2 bb + 1 are block
+                    // blk0 + 2 h + bb.  K % 64 == 0, so a half is whole or wholly past K.
+                    const int kx = kbh * 4;  // first code of the half
+                    const uint4 wa = lds128(sm, wpc + 16u * h);
+                    const uint4 wb = lds128(sm, wpc + 16u * h + w_rowB);
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) {
+                        const int blk = blk0 + 2 * h + bb;
+                        const uint32_t so = soff + s_thr + s_al + (uint32_t)blk * 2u;
+                        const uint32_t sa0 = lds_u16(sm, so), sb0 = lds_u16(sm, so + s_rowB);
+                        const uint32_t sa = (kv && vA) ? sa0 : 0u;
+                        const uint32_t sbv = (kv && vB) ? sb0 : 0u;
+                        uint32_t za = kDefaultZp, zb = kDefaultZp;
+                        if (HAS_ZP) {
+                            const uint32_t zo = soff + z_thr + z_al + (uint32_t)blk;
+                            za = lds_u8(sm, zo);
+                            zb = lds_u8(sm, zo + z_rowB);
+                        }
+                        const Dq2Const cA = dq2_const(za, (uint16_t)sa);
+                        const Dq2Const cB = dq2_const(zb, (uint16_t)sbv);
+#pragma unroll
+                        for (int ww = 0; ww < 2; ++ww) {
+                            const int w = 2 * bb + ww;
+                            uint32_t dA[8], dB[8];
+                            dq_int2_interleaved(word_of(wa, w), cA, dA);
+                            dq_int2_interleaved(word_of(wb, w), cB, dB);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt) {
+                                // X pairs (x_j, x_{j+8}) of the word's 16 codes
+                                const bool use = kv && xok[nt];
+                                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+                                uint32_t xw[8];
+                                if (XS) {
+                                    if (use) {
+                                        const uint32_t xo = L.x + ((uint32_t)(nt * 8 + g) * a.K + (uint32_t)(kx + 16 * w)) * 2u;
+                                        v0 = lds128(sm, xo);
+                                        v1 = lds128(sm, xo + 16u);
+                                    }
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        xw[j] = word_of(v0, j);
+                                        xw[4 + j] = word_of(v1, j);
+                                    }
+                                } else {
+                                    if (use) {
+                                        const uint4* xp = reinterpret_cast<const uint4*>(xrow[nt] + kx + 16 * w);
+                                        v0 = __ldg(xp);
+                                        v1 = __ldg(xp + 1);
+                                    }
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j)
+                                        xw[j] = prmt(word_of(v0, j >> 1), word_of(v1, j >> 1), (j & 1) ? 0x7632u : 0x5410u);
+                                }
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    mma_16816(acc[nt][(4 * w + i) % kChains], dA[2 * i], dB[2 * i], dA[2 * i + 1],
+                                              dB[2 * i + 1], xw[2 * i], xw[2 * i + 1]);
+                            }
+                        }
+                    }
+                    continue;
+                }
                 const int blk = blk0 + (BITS == 4 ? h : 0);
                 // X of these 16 bytes' codes, for this thread's token rows
                 constexpr int kXv = BITS == 4 ? 4 : 2;
@@ -510,6 +591,7 @@ cudaError_t gemv_prepare() {
     if (e == cudaSuccess && T == 1)                                                                            \
         e = cudaFuncSetAttribute(gemv_kernel<B, Z, 1, true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
                                  227 * 1024);
+    MNB_SET(2, false, 1) MNB_SET(2, false, 2) MNB_SET(2, true, 1) MNB_SET(2, true, 2)
     MNB_SET(4, false, 1) MNB_SET(4, false, 2) MNB_SET(4, true, 1) MNB_SET(4, true, 2)
     MNB_SET(8, false, 1) MNB_SET(8, false, 2) MNB_SET(8, true, 1) MNB_SET(8, true, 2)
 #undef MNB_SET
@@ -531,6 +613,12 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
     const dim3 grid(p.grid_x, p.grid_y);
     const bool zp = a.Z != nullptr;
     const int nt = tok / 8;
+    if (bits == 2) {
+        if (zp) return nt == 1 ? launch_xs<2, true, 1>(a, grid, smem, xs, occ, pdl, st)
+                               : launch_xs<2, true, 2>(a, grid, smem, xs, occ, pdl, st);
+        return nt == 1 ? launch_xs<2, false, 1>(a, grid, smem, xs, occ, pdl, st)
+                       : launch_xs<2, false, 2>(a, grid, smem, xs, occ, pdl, st);
+    }
     if (bits == 4) {
         if (zp) return nt == 1 ? launch_xs<4, true, 1>(a, grid, smem, xs, occ, pdl, st)
                                : launch_xs<4, true, 2>(a, grid, smem, xs, occ, pdl, st);

@@ -21,7 +21,11 @@
  *    and contiguous, 16-byte aligned.  The library keeps no pointer after a
  *    call returns, copies nothing and never allocates device memory.
  *  - "fp16" is IEEE binary16.  Codes are unsigned.  INT4 codes are packed two
- *    per byte along K, code k = 2j in the low nibble of byte j.
+ *    per byte along K, code k = 2j in the low nibble of byte j; INT2 codes
+ *    four per byte, code k = 4j + i in bits 2i..2i+1 of byte j (the 2-bit
+ *    weights of the commit "Support empty packed weights in CPU and WebGPU
+ *    MatMulNBits", referenced by "[WebGPU] Fuse rank-32 quantized LoRA with
+ *    MatMulNBits", Description).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *    only enqueue work; they never synchronize the host, except
  *    mnb_sync_status.
@@ -40,7 +44,8 @@ extern "C" {
 /* ---- status codes ------------------------------------------------------ */
 #define MNB_OK                   0
 #define MNB_ERR_ARG             -1  /* NULL required pointer, negative size, bad handle */
-#define MNB_ERR_UNSUPPORTED     -2  /* bits not 4/8, block_size not 32, K % 32 != 0, rank not 0/32 */
+#define MNB_ERR_UNSUPPORTED     -2  /* bits not 2/4/8, block_size not 32, K % 32 != 0 (K % 64 for 2 bits),
+                                       rank not 0/32 */
 #define MNB_ERR_ALIGN           -3  /* a tensor pointer is not 16-byte aligned */
 #define MNB_ERR_CUDA            -4  /* a CUDA runtime call or kernel launch failed */
 #define MNB_ERR_DEVICE_TIMEOUT  -5  /* a bounded device-side wait gave up (see mnb_sync_status) */
@@ -68,8 +73,9 @@ extern "C" {
 typedef struct mnb_handle_s* mnb_handle;
 
 /* Fixed properties of one quantized projection.
- *   N, K        output features and input features (K % 32 == 0, both >= 0)
- *   bits        4 or 8
+ *   N, K        output features and input features (K % 32 == 0, both >= 0;
+ *               K % 64 == 0 for 2-bit weights: rows of whole 16-byte units)
+ *   bits        2, 4 or 8
  *   block_size  32 (the only supported block)
  *   max_rank    0 or 32: the largest adapter rank mnb_run will be given
  *   mode        MNB_MODE_*
@@ -110,9 +116,9 @@ void mnb_destroy(mnb_handle h);
 
 /* Y = X * dequant(Wq)^T (+ (X * A) * B^T), enqueued on `stream`.
  *   X       fp16 [batch, M, K]
- *   Wq      uint8 [N, K/32, 16] (INT4) or [N, K/32, 32] (INT8)
+ *   Wq      uint8 [N, K/32, 32*bits/8]: 8 (INT2), 16 (INT4) or 32 (INT8) bytes a block
  *   scales  fp16 [N, K/32]
- *   zp      uint8 [N, K/32], or NULL for the default 2^(bits-1)
+ *   zp      uint8 [N, K/32], or NULL for the default 2^(bits-1) (2, 8, 128)
  *   A, B    fp16 [K, rank] and [N, rank] (B is the transposed up weight);
  *           both NULL or rank == 0 selects the empty adapter (base only)
  *   rank    0 or 32, at most desc.max_rank
@@ -172,7 +178,7 @@ const char* mnb_status_str(int code);
  *   W16      fp16 [N, K] output
  *   variant  0 = the natural-order unpacking the prefill kernel uses,
  *            1 = the pair-interleaved unpacking the decode kernel uses
- *            (both must give identical bits)
+ *            (both must give identical bits; INT8 has only the natural one)
  * Errors as for mnb_run. */
 int mnb_dequant(const void* Wq, const void* scales, const void* zp,
                 int64_t N, int64_t K, int32_t bits, int32_t block_size,

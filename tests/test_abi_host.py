@@ -46,7 +46,8 @@ def test_status_strings():
     (dict(N=-1, K=64), mnb.MNB_ERR_ARG),
     (dict(N=64, K=-32), mnb.MNB_ERR_ARG),
     (dict(N=64, K=48), mnb.MNB_ERR_UNSUPPORTED),
-    (dict(N=64, K=64, bits=2), mnb.MNB_ERR_UNSUPPORTED),
+    (dict(N=64, K=96, bits=2), mnb.MNB_ERR_UNSUPPORTED),   # 2-bit rows must be whole 16-byte units
+    (dict(N=64, K=64, bits=3), mnb.MNB_ERR_UNSUPPORTED),
     (dict(N=64, K=64, block_size=64), mnb.MNB_ERR_UNSUPPORTED),
     (dict(N=64, K=64, max_rank=16), mnb.MNB_ERR_UNSUPPORTED),
     (dict(N=64, K=64, mode=7), mnb.MNB_ERR_ARG),
@@ -58,7 +59,8 @@ def test_create_rejects_bad_descriptors(kw, code):
 
 
 def test_create_accepts_valid_descriptors_and_empty_shapes():
-    for kw in (dict(N=4096, K=4096), dict(N=49152, K=576, bits=8, max_rank=0), dict(N=0, K=0), dict(N=5, K=0)):
+    for kw in (dict(N=4096, K=4096), dict(N=49152, K=576, bits=8, max_rank=0), dict(N=0, K=0), dict(N=5, K=0),
+               dict(N=4096, K=4096, bits=2), dict(N=64, K=0, bits=2)):
         h = mnb.mnb_create(**kw)
         mnb.mnb_destroy(h)
     mnb.mnb_destroy(None)
@@ -154,6 +156,8 @@ def test_run_validation_needs_no_device():
 def test_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 48, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
+    assert L.mnb_dequant(0x1000, 0x2000, None, 4, 96, 2, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
+    assert L.mnb_dequant(0x1000, 0x2000, None, 0, 128, 2, 32, 0x3000, 1, None) == mnb.MNB_OK
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 64, 4, 32, 0x3000, 2, None) == mnb.MNB_ERR_ARG
     assert L.mnb_dequant(0x1000, 0x2000, None, 0, 64, 4, 32, 0x3000, 0, None) == mnb.MNB_OK
     assert L.mnb_dequant(0x1004, 0x2000, None, 4, 64, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_ALIGN
