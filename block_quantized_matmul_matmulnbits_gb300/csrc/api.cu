@@ -197,7 +197,9 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
     }
     if (Mt > 0 && d.N > 0) {
         if (!Y) return MNB_ERR_ARG;
-        if (d.K > 0 && (!X || !Wq || !scales)) return MNB_ERR_ARG;
+        // Wq == NULL with K > 0: an empty packed weight (scales, zp unused)
+        if (d.K > 0 && Wq && (!X || !scales)) return MNB_ERR_ARG;
+        if (d.K > 0 && !Wq && rank > 0 && !X) return MNB_ERR_ARG;
     }
     if (!aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zp) || !aligned16(Y) ||
         !aligned16(bias) || (rank > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(T_ws))))
@@ -218,6 +220,21 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
     if (p.route == MNB_ROUTE_NONE) {
         h->last_route = MNB_ROUTE_NONE;
         return MNB_OK;
+    }
+    if (p.route != MNB_ROUTE_FILL && !Wq) {
+        // empty packed weight: zeros or the broadcast bias, plus the adapter term
+        if (rank == 0) {
+            p.route = MNB_ROUTE_FILL;
+        } else {
+            e = mnb::lora_down_launch(static_cast<const __half*>(X), static_cast<const __half*>(A),
+                                      static_cast<__half*>(T_ws), (int)Mt, (int)d.K, false, st);
+            if (e == cudaSuccess)
+                e = mnb::lora_up_launch(static_cast<const __half*>(T_ws), static_cast<const __half*>(B), biash,
+                                        static_cast<__half*>(Y), (int)Mt, (int)d.N, st);
+            if (e != cudaSuccess) return MNB_ERR_CUDA;
+            h->last_route = MNB_ROUTE_FILL;
+            return MNB_OK;
+        }
     }
     if (p.route == MNB_ROUTE_FILL) {
         e = biash ? mnb::fill_bias_launch(static_cast<__half*>(Y), biash, (size_t)Mt, (size_t)d.N, st)

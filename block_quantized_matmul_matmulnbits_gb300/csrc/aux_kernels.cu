@@ -5,6 +5,8 @@
 //    rank-32 quantized LoRA with MatMulNBits" (onnxruntime PR 33370, commit
 //    message on empty packed weights: the WebGPU side records a fill dispatch
 //    so that graph replay rewrites the output).
+//  * lora_up: an empty packed weight with an adapter leaves only the adapter
+//    term, Y = T * Bt^T (+ bias), on the CUDA cores.
 //  * dequant: the dequantization step on its own, W16 = fp16((q - zp) * scale),
 //    the DequantizeLinear weight map of "Fuse DQ->MatMulNBits for shared
 //    initializers and skip outer-scope weights" (onnxruntime PR 33800,
@@ -114,6 +116,29 @@ __global__ void fill_bias_kernel(__half* __restrict__ Y, const __half* __restric
     const size_t total = rows * N, stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) Y[i] = bias[i % N];
 }
+
+// An empty packed weight with an adapter: Y[m, n] = fp16(sum_r T[m, r] B[n, r]
+// (+ bias[n])), the adapter term alone, summed in FP32 in r order (each
+// FP16 x FP16 product is exact in FP32).
+__global__ void lora_up_kernel(const __half* __restrict__ T, const __half* __restrict__ B,
+                               const __half* __restrict__ bias, __half* __restrict__ Y, int Mt, int N) {
+    const size_t total = (size_t)Mt * (size_t)N;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const size_t m = i / (size_t)N, n = i % (size_t)N;
+        const __half2* t = reinterpret_cast<const __half2*>(T + m * 32);
+        const __half2* b = reinterpret_cast<const __half2*>(B + n * 32);
+        float s = 0.f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float2 tv = __half22float2(t[r]), bv = __half22float2(b[r]);
+            s += tv.x * bv.x;
+            s += tv.y * bv.y;
+        }
+        if (bias) s += __half2float(bias[n]);
+        Y[i] = __float2half_rn(s);
+    }
+}
 }  // namespace
 
 cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st) {
@@ -122,6 +147,16 @@ cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t 
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     fill_bias_kernel<<<(unsigned)blocks, 256, 0, st>>>(Y, bias, rows, N);
+    return cudaGetLastError();
+}
+
+cudaError_t lora_up_launch(const __half* T, const __half* B, const __half* bias, __half* Y, int Mt, int N,
+                           cudaStream_t st) {
+    const size_t total = (size_t)Mt * (size_t)N;
+    if (total == 0) return cudaSuccess;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    lora_up_kernel<<<(unsigned)blocks, 256, 0, st>>>(T, B, bias, Y, Mt, N);
     return cudaGetLastError();
 }
 

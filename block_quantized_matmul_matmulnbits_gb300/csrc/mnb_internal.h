@@ -78,6 +78,8 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
 // Y = 0 over `count` halfs (K == 0 case).
 cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st);
 // Y[m, n] = bias[n] for m < rows (K == 0 with a bias)
+cudaError_t lora_up_launch(const __half* T, const __half* B, const __half* bias, __half* Y, int Mt, int N,
+                           cudaStream_t st);
 cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st);
 
 // W16[n, k] = fp16((q - zp) * scale) with the kernels' own dequant arithmetic.

@@ -128,6 +128,13 @@ void mnb_destroy(mnb_handle h);
  *           adapter is empty.  Its contents on return are T.
  * The kernel family is chosen from the per-matrix row count M (not batch*M).
  * M, N or batch == 0 launches nothing; K == 0 writes zeros.
+ * Wq == NULL with K > 0 is an empty packed weight (the rule of "Support empty
+ * packed weights in CPU and WebGPU MatMulNBits", referenced by "[WebGPU] Fuse
+ * rank-32 quantized LoRA with MatMulNBits", Description): the base term is
+ * zero, scales and zp are not read (may be NULL), Y keeps its logical shape
+ * and holds zeros -- or, with an adapter, T * B^T alone (route FILL, one LoRA
+ * down and one small up-projection kernel).  mnb_plan describes the call with
+ * a nonempty weight.
  * Every row of X is independent: [batch, M] gives the same bits as one matrix
  * of batch*M rows routed the same way.  Results are deterministic run to run.
  * Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_ALIGN, MNB_ERR_NO_DEVICE,

@@ -135,6 +135,10 @@ def test_run_validation_needs_no_device():
                                      args["rank"], args["Y"], args["T_ws"], args["batch"], args["M"], None)
         assert rc(X=None) == mnb.MNB_ERR_ARG
         assert rc(Y=None) == mnb.MNB_ERR_ARG
+        assert rc(scales=None) == mnb.MNB_ERR_ARG
+        # an empty packed weight (Wq NULL) needs X only for the adapter term
+        assert rc(Wq=None, scales=None, X=None, rank=32, A=0x5000, B=0x6000, T_ws=0x7000) == mnb.MNB_ERR_ARG
+        assert rc(Wq=None, scales=None, X=0x1004) == mnb.MNB_ERR_ALIGN
         assert rc(batch=-1) == mnb.MNB_ERR_ARG
         assert rc(rank=16) == mnb.MNB_ERR_UNSUPPORTED
         assert rc(rank=32, A=0x5000, B=None) == mnb.MNB_ERR_ARG

@@ -161,3 +161,51 @@ def test_misaligned_bias_is_rejected_before_launch(env):
         mnb.mnb_destroy(h)
     torch.cuda.synchronize()
     assert torch.all(Y == 3.0)
+
+
+# ------------------------------------------------------------------ empty packed weights
+
+@pytest.mark.parametrize("M", [1, 300])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_empty_weight_is_zeros_or_bias_bitwise(env, M, with_bias):
+    """Wq NULL with K > 0: the output keeps its logical shape and holds zeros
+    or the broadcast bias, on what would be either route."""
+    torch, mnb = env
+    N, K = 333, 256
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=760 + M)
+    bias = synth.make_bias(N, seed=761)
+    h = mnb.mnb_create(N, K, 4)
+    try:
+        Y = torch.full((1, M, N), 5.0, dtype=torch.float16, device="cuda")
+        X = dev(inp.X, torch)
+        mnb.mnb_run_bias(h, X, None, None, None, None, None, 0, dev(bias, torch) if with_bias else None, Y, None,
+                         1, M)
+        torch.cuda.synchronize()
+        assert mnb.mnb_last_route(h) == mnb.ROUTE_FILL
+    finally:
+        mnb.mnb_destroy(h)
+    expect = np.broadcast_to(bias, (M, N)) if with_bias else np.zeros((M, N), np.uint16)
+    assert np.array_equal(bits_of(Y).reshape(M, N), expect)
+
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_empty_weight_with_adapter_is_adapter_term(env, M):
+    """Wq NULL with an adapter: Y = T * B^T + bias, against the oracle with a
+    zero base (every code equal to its zero point gives an exactly zero base)."""
+    torch, mnb = env
+    N, K = 500, 1024
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=770 + M, rank=32)
+    bias = synth.make_bias(N, seed=771)
+    d = upload(inp, torch)
+    h = mnb.mnb_create(N, K, 4)
+    try:
+        Y = torch.full((1, M, N), 5.0, dtype=torch.float16, device="cuda")
+        T = torch.empty((M, 32), dtype=torch.float16, device="cuda")
+        mnb.mnb_run_bias(h, d["X"], None, None, None, d["A"], d["B"], 32, dev(bias, torch), Y, T, 1, M)
+        torch.cuda.synchronize()
+        assert mnb.mnb_sync_status(h) == 0 and mnb.mnb_last_route(h) == mnb.ROUTE_FILL
+    finally:
+        mnb.mnb_destroy(h)
+    zero_codes = oracle.pack(np.full((N, K), 8, dtype=np.uint8), 4)
+    _, Y64, bound = oracle.run(inp.X2d, zero_codes, inp.scales, None, inp.A, inp.B, N, K, 4, bias=bias)
+    assert_within_tolerance(bits_of(Y), Y64, bound, f"empty weight + adapter M={M}")
