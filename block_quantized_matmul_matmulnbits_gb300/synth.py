@@ -90,6 +90,37 @@ def make_inputs(*, M: int, K: int, N: int, bits: int = 4, seed: int,
     return Inputs(X=X, Wq=Wq, scales=scales, zp=zp, A=A, B=B, batch=batch, M=M, N=N, K=K, bits=bits)
 
 
+@dataclass
+class QLoRA:
+    """INT8 block-32 adapters as 8-bit MatMulNBits weights."""
+    Aq: np.ndarray                # uint8 [r, K/32, 32]   down projection, rank rows along K
+    A_scales: np.ndarray          # uint16 [r, K/32] (FP16 bits)
+    A_zp: Optional[np.ndarray]    # uint8 [r, K/32] or None (default 128)
+    Bq: np.ndarray                # uint8 [N, r/32, 32]   up projection, N rows along the rank
+    B_scales: np.ndarray          # uint16 [N, r/32]
+    B_zp: Optional[np.ndarray]    # uint8 [N, r/32] or None
+
+    @property
+    def rank(self) -> int:
+        return int(self.Aq.shape[0])
+
+
+def make_qlora(*, K: int, N: int, seed: int, rank: int = LORA_RANK, zp: bool = True,
+               scale_range: Tuple[float, float] = (1e-4, 3e-4)) -> QLoRA:
+    """Seeded INT8 adapters: uniform codes over [0, 256), FP16 scales uniform in
+    ``scale_range`` (dequantized values of the size of the FP16 adapters'
+    N(0, 0.02^2)), zero points uniform over [120, 136] or absent.  Drawn from
+    their own stream."""
+    rng = np.random.Generator(np.random.PCG64([seed, 0x51A]))
+    Aq = rng.integers(0, 256, size=(rank, K // BLOCK, BLOCK), dtype=np.uint8)
+    A_scales = _f16_bits(rng.uniform(scale_range[0], scale_range[1], size=(rank, K // BLOCK)))
+    A_zp = rng.integers(120, 137, size=(rank, K // BLOCK), dtype=np.uint8) if zp else None
+    Bq = rng.integers(0, 256, size=(N, rank // BLOCK, BLOCK), dtype=np.uint8)
+    B_scales = _f16_bits(rng.uniform(scale_range[0], scale_range[1], size=(N, rank // BLOCK)))
+    B_zp = rng.integers(120, 137, size=(N, rank // BLOCK), dtype=np.uint8) if zp else None
+    return QLoRA(Aq=Aq, A_scales=A_scales, A_zp=A_zp, Bq=Bq, B_scales=B_scales, B_zp=B_zp)
+
+
 def make_bias(N: int, seed: int, std: float = 0.5) -> np.ndarray:
     """A seeded FP16 bias [N] (bit patterns), drawn from its own stream so the
     other inputs of the same seed are unchanged."""

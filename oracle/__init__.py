@@ -72,6 +72,8 @@ def _load():
             lib.mnb_ref_run.argtypes = [P, P, P, P, P, P, I, I64, I64, I64, I, I, I, P, P, P]
             lib.mnb_ref_run_bias.argtypes = [P, P, P, P, P, P, I, P, I64, I64, I64, I, I, I, P, P, P]
             lib.mnb_ref_run_bias.restype = I
+            lib.mnb_ref_run_qlora.argtypes = [P, P, P, P, P, P, P, P, P, P, I, P, I64, I64, I64, I, I, I, P, P, P]
+            lib.mnb_ref_run_qlora.restype = I
             lib.mnb_ref_run.restype = I
             lib.mnb_ref_threads.argtypes = []
             lib.mnb_ref_threads.restype = I
@@ -177,4 +179,28 @@ def run(X, Wq, scales, zp, A, B, N, K, bits, block=32, round_t=False, bias=None)
                                   Mt, N, K, bits, block, 1 if round_t else 0,
                                   _ptr(Y16), _ptr(Y64), _ptr(bound))
     _check(rc, "run")
+    return Y16, Y64, bound
+
+
+def run_qlora(X, Wq, scales, zp, Aq, A_scales, A_zp, Bq, B_scales, B_zp, N, K, bits, block=32, round_t=False,
+              bias=None):
+    """Y with INT8 block-32 adapters given as 8-bit MatMulNBits weights:
+    Aq [r, K/block, block] u8 (+ A_scales, A_zp [r, K/block]) for the down
+    projection, Bq [N, r/block, block] u8 (+ B_scales, B_zp [N, r/block]) for
+    the up projection; zero points None = 128.  Aq None = no adapter.
+    Returns (Y16 bits, Y64, bound) as ``run``."""
+    X = _c(X, np.uint16)
+    Wq, scales, zp = _c(Wq, np.uint8), _c(scales, np.uint16), _c(zp, np.uint8)
+    rank = 0 if Aq is None else int(np.shape(Aq)[0])
+    Aq, A_scales, A_zp = _c(Aq, np.uint8), _c(A_scales, np.uint16), _c(A_zp, np.uint8)
+    Bq, B_scales, B_zp = _c(Bq, np.uint8), _c(B_scales, np.uint16), _c(B_zp, np.uint8)
+    Mt = X.shape[0]
+    Y16 = np.empty((Mt, N), dtype=np.uint16)
+    Y64 = np.empty((Mt, N), dtype=np.float64)
+    bound = np.empty((Mt, N), dtype=np.float64)
+    bias = _c(bias, np.uint16) if bias is not None else None
+    rc = _load().mnb_ref_run_qlora(_ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(Aq), _ptr(A_scales), _ptr(A_zp),
+                                   _ptr(Bq), _ptr(B_scales), _ptr(B_zp), rank, _ptr(bias), Mt, N, K, bits, block,
+                                   1 if round_t else 0, _ptr(Y16), _ptr(Y64), _ptr(bound))
+    _check(rc, "run_qlora")
     return Y16, Y64, bound

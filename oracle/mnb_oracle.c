@@ -48,6 +48,10 @@
  *    the broadcast bias.  Read as: an optional FP16 vector over N added to
  *    every output row before the one rounding (mnb_ref_run_bias).
  *
+ *  - INT8 adapters (mnb_ref_run_qlora): each adapter projection is an 8-bit
+ *    block-32 MatMulNBits weight, the down one [rank rows x K], the up one
+ *    [N rows x rank]; dequantized exactly, then the same product.
+ *
  * Everything is plain loops; OpenMP only splits independent output rows.
  */
 #include <math.h>
@@ -228,23 +232,23 @@ int mnb_ref_lora_down(const uint16_t* X, const uint16_t* A, int64_t Mt, int64_t 
  * pages' FP16 intermediate); 0 keeps it exact.
  * ------------------------------------------------------------------------- */
 
-int mnb_ref_run_bias(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
-                     const uint16_t* A, const uint16_t* B, int rank, const uint16_t* bias,
-                     int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
-                     uint16_t* Y16, double* Y64, double* bound)
+/* The product with the adapter given as exact values: A64 [K, rank],
+ * B64 [N, rank] (either adapter format is turned into these first). */
+static int run_core(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                    const double* A64, const double* B64, int rank, const uint16_t* bias,
+                    int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                    uint16_t* Y16, double* Y64, double* bound)
 {
-    int rc = check_shape(N, K, bits, bs);
-    if (rc) return rc;
-    if (Mt < 0 || rank < 0) return -1;
-    if (rank > 0 && (!A || !B)) return -1;
-
     double* T = NULL;
     if (rank > 0) {
         T = (double*)malloc(sizeof(double) * (size_t)(Mt > 0 ? Mt : 1) * (size_t)rank);
         if (!T) return -3;
-        mnb_ref_lora_down(X, A, Mt, K, rank, T);
-        if (round_t)
-            for (int64_t i = 0; i < Mt * rank; ++i) T[i] = mnb_ref_f16_to_f64(mnb_ref_f64_to_f16(T[i]));
+        for (int64_t m = 0; m < Mt; ++m)
+            for (int j = 0; j < rank; ++j) {
+                double t = 0.0;
+                for (int64_t k = 0; k < K; ++k) t += mnb_ref_f16_to_f64(X[m * K + k]) * A64[k * rank + j];
+                T[m * rank + j] = round_t ? mnb_ref_f16_to_f64(mnb_ref_f64_to_f16(t)) : t;
+            }
     }
 
     int64_t total = Mt * N;
@@ -258,7 +262,7 @@ int mnb_ref_run_bias(const uint16_t* X, const uint8_t* Wq, const uint16_t* scale
             mag += fabs(p);
         }
         for (int j = 0; j < rank; ++j) {
-            double p = T[m * rank + j] * mnb_ref_f16_to_f64(B[n * rank + j]);
+            double p = T[m * rank + j] * B64[n * rank + j];
             acc += p;
             mag += fabs(p);
         }
@@ -273,6 +277,78 @@ int mnb_ref_run_bias(const uint16_t* X, const uint8_t* Wq, const uint16_t* scale
     }
     free(T);
     return 0;
+}
+
+int mnb_ref_run_bias(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                     const uint16_t* A, const uint16_t* B, int rank, const uint16_t* bias,
+                     int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                     uint16_t* Y16, double* Y64, double* bound)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    if (Mt < 0 || rank < 0) return -1;
+    if (rank > 0 && (!A || !B)) return -1;
+    double *A64 = NULL, *B64 = NULL;
+    if (rank > 0) {
+        A64 = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)rank);
+        B64 = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * (size_t)rank);
+        if (!A64 || !B64) {
+            free(A64);
+            free(B64);
+            return -3;
+        }
+        for (int64_t i = 0; i < K * rank; ++i) A64[i] = mnb_ref_f16_to_f64(A[i]);
+        for (int64_t i = 0; i < N * rank; ++i) B64[i] = mnb_ref_f16_to_f64(B[i]);
+    }
+    rc = run_core(X, Wq, scales, zp, A64, B64, rank, bias, Mt, N, K, bits, bs, round_t, Y16, Y64, bound);
+    free(A64);
+    free(B64);
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * INT8 block-32 adapters ("[WebGPU] Fuse rank-32 quantized LoRA with
+ * MatMulNBits", commit message adding the INT8-adapter kernels and the later
+ * MatMulNBitsQLoRA commit: INT4 base weights with block-32 INT8 rank-32
+ * adapters, the adapters' original INT8 arithmetic kept).  Reading: each
+ * adapter projection is itself an 8-bit MatMulNBits weight --
+ *   down: Aq [rank, K/bs, bs] with A_scales / A_zp [rank, K/bs]
+ *         (rank output rows along K), a[k, r] = dequant of row r, column k;
+ *   up:   Bq [N, rank/bs, bs] with B_scales / B_zp [N, rank/bs]
+ *         (N output rows along the rank), b[n, r] = dequant of row n, column r;
+ * zero points NULL = the 8-bit default 128.  The dequantized values are exact
+ * here; the rest is the product above.
+ * ------------------------------------------------------------------------- */
+
+int mnb_ref_run_qlora(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                      const uint8_t* Aq, const uint16_t* A_scales, const uint8_t* A_zp,
+                      const uint8_t* Bq, const uint16_t* B_scales, const uint8_t* B_zp, int rank,
+                      const uint16_t* bias, int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                      uint16_t* Y16, double* Y64, double* bound)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    if (Mt < 0 || rank < 0) return -1;
+    if (rank > 0 && (!Aq || !A_scales || !Bq || !B_scales)) return -1;
+    if (rank > 0 && (check_shape(rank, K, 8, bs) || check_shape(N, rank, 8, bs))) return -2;
+    double *A64 = NULL, *B64 = NULL;
+    if (rank > 0) {
+        A64 = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * (size_t)rank);
+        B64 = (double*)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1) * (size_t)rank);
+        if (!A64 || !B64) {
+            free(A64);
+            free(B64);
+            return -3;
+        }
+        for (int r = 0; r < rank; ++r)
+            for (int64_t k = 0; k < K; ++k) A64[k * rank + r] = dequant_at(Aq, A_scales, A_zp, K, 8, bs, r, k);
+        for (int64_t n = 0; n < N; ++n)
+            for (int r = 0; r < rank; ++r) B64[n * rank + r] = dequant_at(Bq, B_scales, B_zp, rank, 8, bs, n, r);
+    }
+    rc = run_core(X, Wq, scales, zp, A64, B64, rank, bias, Mt, N, K, bits, bs, round_t, Y16, Y64, bound);
+    free(A64);
+    free(B64);
+    return rc;
 }
 
 /* mnb_ref_run_bias without a bias. */

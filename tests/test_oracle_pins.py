@@ -439,3 +439,88 @@ def test_no_bias_is_bitwise_the_plain_run():
     b = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, 24, 64, 8, bias=None)
     for u, v in zip(a, b):
         assert np.array_equal(u, v)
+
+
+# ---------------------------------------------------------------- INT8 adapters
+
+def _qlora_dequant_numpy(q, scales, zp):
+    """[rows, nblk, 32] u8 codes -> exact float64 [rows, nblk*32], from numpy
+    alone: (q - zp) * scale, zero point 128 when absent."""
+    rows, nblk, _ = q.shape
+    z = np.full((rows, nblk), 128, np.int64) if zp is None else zp.astype(np.int64)
+    s = f16val(scales)
+    return ((q.astype(np.int64) - z[:, :, None]) * s[:, :, None]).reshape(rows, nblk * 32)
+
+
+def _pow2_qlora(K, N, seed, zp=True):
+    """INT8 adapters whose dequantized values are exact in FP16: power-of-two
+    scales, |q - zp| <= 255 (8 significant bits)."""
+    ql = synth.make_qlora(K=K, N=N, seed=seed, zp=zp)
+    rng = np.random.default_rng(seed)
+    ql.A_scales = f16(np.ldexp(1.0, rng.integers(-14, -10, size=ql.A_scales.shape)))
+    ql.B_scales = f16(np.ldexp(1.0, rng.integers(-14, -10, size=ql.B_scales.shape)))
+    return ql
+
+
+@pytest.mark.parametrize("zp", [True, False])
+def test_qlora_equals_fp16_adapter_when_dequant_is_exact(zp):
+    """With FP16-exact dequantized adapters, the INT8-adapter product equals the
+    FP16-adapter product with A = dequant(Aq)^T and B = dequant(Bq), bit for
+    bit: the down weight's rows are ranks along K, the up weight's rows are N."""
+    K, N, M = 128, 40, 3
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=61, zp_range=(0, 15))
+    ql = _pow2_qlora(K, N, 62, zp)
+    A = _qlora_dequant_numpy(ql.Aq, ql.A_scales, ql.A_zp)          # [r, K]
+    B = _qlora_dequant_numpy(ql.Bq, ql.B_scales, ql.B_zp)          # [N, r]
+    A16, B16 = f16(A.T), f16(B)
+    assert np.array_equal(f16val(A16), A.T) and np.array_equal(f16val(B16), B)  # exact in FP16
+    got = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq, ql.B_scales,
+                           ql.B_zp, N, K, 4)
+    ref = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, A16, B16, N, K, 4)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
+
+
+def test_negative_control_untransposed_int8_down_weight_fails():
+    """Reading the down weight as [K, r] instead of [r, K] is a plausible
+    mistake; it must not reproduce the INT8-adapter product."""
+    K, N, M = 32, 24, 2   # K == r, so the wrong reading has the right shape
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=63)
+    ql = _pow2_qlora(K, N, 64)
+    A = _qlora_dequant_numpy(ql.Aq, ql.A_scales, ql.A_zp)
+    B = _qlora_dequant_numpy(ql.Bq, ql.B_scales, ql.B_zp)
+    _, got, _ = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq,
+                                 ql.B_scales, ql.B_zp, N, K, 4)
+    _, wrong, _ = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, f16(A), f16(B), N, K, 4)
+    _, right, _ = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, f16(A.T), f16(B), N, K, 4)
+    assert np.array_equal(got, right) and not np.allclose(got, wrong)
+
+
+def test_qlora_brute_force_exact_rationals():
+    K, N, M = 64, 5, 2
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=65, zp_range=(0, 15))
+    ql = synth.make_qlora(K=K, N=N, seed=66)
+    Y16, Y64, bound = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq,
+                                       ql.B_scales, ql.B_zp, N, K, 4)
+    base = _exact_y(inp)
+    x = [[Fraction(float(v)) for v in row] for row in f16val(inp.X2d)]
+    A = [[Fraction(float(v)) for v in row] for row in _qlora_dequant_numpy(ql.Aq, ql.A_scales, ql.A_zp)]
+    B = [[Fraction(float(v)) for v in row] for row in _qlora_dequant_numpy(ql.Bq, ql.B_scales, ql.B_zp)]
+    for m in range(M):
+        t = [sum(x[m][k] * A[r][k] for k in range(K)) for r in range(32)]
+        for n in range(N):
+            ex = base[m][n] + sum(t[r] * B[n][r] for r in range(32))
+            assert abs(Fraction(float(Y64[m, n])) - ex) <= Fraction(1, 10 ** 12) * Fraction(float(bound[m, n]))
+            assert Y16[m, n] == np.float64(float(ex)).astype(np.float16).view(np.uint16)
+
+
+def test_qlora_codes_at_zero_point_is_base_bitwise():
+    K, N, M = 96, 33, 3
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=8, seed=67, zp_range=(120, 136))
+    ql = synth.make_qlora(K=K, N=N, seed=68)
+    ql.Aq = np.repeat(ql.A_zp[:, :, None], 32, axis=2)
+    ql.Bq = np.repeat(ql.B_zp[:, :, None], 32, axis=2)
+    got = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq, ql.B_scales,
+                           ql.B_zp, N, K, 8)
+    ref = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, None, None, N, K, 8)
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
