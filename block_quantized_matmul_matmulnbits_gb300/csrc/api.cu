@@ -175,25 +175,34 @@ int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_co
     return make_plan(h->d, batch, M, rank, sms, out);
 }
 
-int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
-            const void* B, int32_t rank, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
-    return mnb_run_bias(h, X, Wq, scales, zp, A, B, rank, nullptr, Y, T_ws, batch, M, stream);
-}
+}  // extern "C"
 
-int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
-                 const void* B, int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M,
-                 void* stream) {
+namespace {
+
+// The adapter of one call: FP16 A [K, 32] and B [N, 32], or INT8 block-32
+// weights Aq [32, K] / Bq [N, 32] with their scales and zero points.
+struct Adapter {
+    const void *A, *B;
+    const void *Aq, *As, *Az, *Bq, *Bs, *Bz;
+    bool q8;
+};
+
+int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const Adapter& ad,
+             int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
     if (!h || batch < 0 || M < 0) return MNB_ERR_ARG;
     const mnb_desc& d = h->d;
     if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
     const int64_t Mt = batch * M;
     if (Mt > 0 && d.N > 0 && Mt * d.N > ((int64_t)1 << 40)) return MNB_ERR_UNSUPPORTED;
-    // empty adapter: rank 0, or both adapter pointers NULL
+    // empty adapter: rank 0, or both adapter weights NULL
     if (rank != 0 && rank != 32) return MNB_ERR_UNSUPPORTED;
-    if (A == nullptr && B == nullptr) rank = 0;
+    const void* down = ad.q8 ? ad.Aq : ad.A;
+    const void* up = ad.q8 ? ad.Bq : ad.B;
+    if (down == nullptr && up == nullptr) rank = 0;
     if (rank > 0) {
         if (rank > d.max_rank) return MNB_ERR_ARG;
-        if (!A || !B || !T_ws) return MNB_ERR_ARG;
+        if (!down || !up || !T_ws) return MNB_ERR_ARG;
+        if (ad.q8 && (!ad.As || !ad.Bs)) return MNB_ERR_ARG;
     }
     if (Mt > 0 && d.N > 0) {
         if (!Y) return MNB_ERR_ARG;
@@ -202,9 +211,19 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
         if (d.K > 0 && !Wq && rank > 0 && !X) return MNB_ERR_ARG;
     }
     if (!aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zp) || !aligned16(Y) ||
-        !aligned16(bias) || (rank > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(T_ws))))
+        !aligned16(bias) || (rank > 0 && (!aligned16(down) || !aligned16(up) || !aligned16(T_ws))) ||
+        (rank > 0 && ad.q8 && (!aligned16(ad.As) || !aligned16(ad.Az) || !aligned16(ad.Bs) || !aligned16(ad.Bz))))
         return MNB_ERR_ALIGN;
     const __half* biash = static_cast<const __half*>(bias);
+    const uint8_t* Bq8 = rank > 0 && ad.q8 ? static_cast<const uint8_t*>(ad.Bq) : nullptr;
+    const __half* Bs8 = Bq8 ? static_cast<const __half*>(ad.Bs) : nullptr;
+    const uint8_t* Bz8 = Bq8 ? static_cast<const uint8_t*>(ad.Bz) : nullptr;
+    auto launch_down = [&](const __half* Xh, __half* Th, bool early, cudaStream_t st) {
+        return ad.q8 ? mnb::lora_down_q8_launch(Xh, static_cast<const uint8_t*>(ad.Aq),
+                                                static_cast<const __half*>(ad.As),
+                                                static_cast<const uint8_t*>(ad.Az), Th, (int)Mt, (int)d.K, early, st)
+                     : mnb::lora_down_launch(Xh, static_cast<const __half*>(ad.A), Th, (int)Mt, (int)d.K, early, st);
+    };
 
     mnb_plan_info p;
     int sms = 0;
@@ -226,11 +245,10 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
         if (rank == 0) {
             p.route = MNB_ROUTE_FILL;
         } else {
-            e = mnb::lora_down_launch(static_cast<const __half*>(X), static_cast<const __half*>(A),
-                                      static_cast<__half*>(T_ws), (int)Mt, (int)d.K, false, st);
+            e = launch_down(static_cast<const __half*>(X), static_cast<__half*>(T_ws), false, st);
             if (e == cudaSuccess)
-                e = mnb::lora_up_launch(static_cast<const __half*>(T_ws), static_cast<const __half*>(B), biash,
-                                        static_cast<__half*>(Y), (int)Mt, (int)d.N, st);
+                e = mnb::lora_up_launch(static_cast<const __half*>(T_ws), static_cast<const __half*>(ad.B), Bq8, Bs8,
+                                        Bz8, biash, static_cast<__half*>(Y), (int)Mt, (int)d.N, st);
             if (e != cudaSuccess) return MNB_ERR_CUDA;
             h->last_route = MNB_ROUTE_FILL;
             return MNB_OK;
@@ -255,7 +273,7 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
     const bool lora_kernel = rank > 0;
     if (lora_kernel) {
-        e = mnb::lora_down_launch(Xh, static_cast<const __half*>(A), Th, (int)Mt, (int)d.K, early, st);
+        e = launch_down(Xh, Th, early, st);
         if (e != cudaSuccess) return MNB_ERR_CUDA;
     }
     const bool pdl = lora_kernel || early;
@@ -266,7 +284,10 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
         a.S = static_cast<const __half*>(scales);
         a.Z = static_cast<const uint8_t*>(zp);
         a.T = Th;
-        a.B = static_cast<const __half*>(B);
+        a.B = static_cast<const __half*>(ad.B);
+        a.Bq = Bq8;
+        a.Bs = Bs8;
+        a.Bz = Bz8;
         a.bias = biash;
         a.Y = static_cast<__half*>(Y);
         a.Mt = (int)Mt;
@@ -289,7 +310,10 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
         a.S = static_cast<const __half*>(scales);
         a.Z = static_cast<const uint8_t*>(zp);
         a.T = Th;
-        a.B = static_cast<const __half*>(B);
+        a.B = static_cast<const __half*>(ad.B);
+        a.Bq = Bq8;
+        a.Bs = Bs8;
+        a.Bz = Bz8;
         a.bias = biash;
         a.Y = static_cast<__half*>(Y);
         a.Mt = (int)Mt;
@@ -304,6 +328,30 @@ int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales
     if (e != cudaSuccess) return MNB_ERR_CUDA;
     h->last_route = p.route;
     return MNB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mnb_run(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+            const void* B, int32_t rank, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
+    return run_impl(h, X, Wq, scales, zp, Adapter{A, B, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, false},
+                    rank, nullptr, Y, T_ws, batch, M, stream);
+}
+
+int mnb_run_bias(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+                 const void* B, int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M,
+                 void* stream) {
+    return run_impl(h, X, Wq, scales, zp, Adapter{A, B, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, false},
+                    rank, bias, Y, T_ws, batch, M, stream);
+}
+
+int mnb_run_qlora(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* Aq,
+                  const void* A_scales, const void* A_zp, const void* Bq, const void* B_scales, const void* B_zp,
+                  int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
+    return run_impl(h, X, Wq, scales, zp, Adapter{nullptr, nullptr, Aq, A_scales, A_zp, Bq, B_scales, B_zp, true},
+                    rank, bias, Y, T_ws, batch, M, stream);
 }
 
 int mnb_sync_status(mnb_handle h, void* stream) {

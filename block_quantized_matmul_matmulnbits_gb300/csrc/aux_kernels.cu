@@ -121,19 +121,34 @@ __global__ void fill_bias_kernel(__half* __restrict__ Y, const __half* __restric
 // (+ bias[n])), the adapter term alone, summed in FP32 in r order (each
 // FP16 x FP16 product is exact in FP32).
 __global__ void lora_up_kernel(const __half* __restrict__ T, const __half* __restrict__ B,
-                               const __half* __restrict__ bias, __half* __restrict__ Y, int Mt, int N) {
+                               const uint8_t* __restrict__ Bq, const __half* __restrict__ Bs,
+                               const uint8_t* __restrict__ Bz, const __half* __restrict__ bias,
+                               __half* __restrict__ Y, int Mt, int N) {
     const size_t total = (size_t)Mt * (size_t)N;
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
         const size_t m = i / (size_t)N, n = i % (size_t)N;
         const __half2* t = reinterpret_cast<const __half2*>(T + m * 32);
-        const __half2* b = reinterpret_cast<const __half2*>(B + n * 32);
         float s = 0.f;
+        if (Bq) {  // INT8 row: b = fp16((q - zp) * scale), the product exact in FP32 and rounded once
+            const float sc = __half2float(Bs[n]);
+            const int z = Bz ? Bz[n] : 128;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const float2 tv = __half22float2(t[r]), bv = __half22float2(b[r]);
-            s += tv.x * bv.x;
-            s += tv.y * bv.y;
+            for (int r = 0; r < 16; ++r) {
+                const float2 tv = __half22float2(t[r]);
+                const float b0 = __half2float(__float2half_rn((float)((int)Bq[n * 32 + 2 * r] - z) * sc));
+                const float b1 = __half2float(__float2half_rn((float)((int)Bq[n * 32 + 2 * r + 1] - z) * sc));
+                s += tv.x * b0;
+                s += tv.y * b1;
+            }
+        } else {
+            const __half2* b = reinterpret_cast<const __half2*>(B + n * 32);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float2 tv = __half22float2(t[r]), bv = __half22float2(b[r]);
+                s += tv.x * bv.x;
+                s += tv.y * bv.y;
+            }
         }
         if (bias) s += __half2float(bias[n]);
         Y[i] = __float2half_rn(s);
@@ -150,13 +165,13 @@ cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t 
     return cudaGetLastError();
 }
 
-cudaError_t lora_up_launch(const __half* T, const __half* B, const __half* bias, __half* Y, int Mt, int N,
-                           cudaStream_t st) {
+cudaError_t lora_up_launch(const __half* T, const __half* B, const uint8_t* Bq, const __half* Bs, const uint8_t* Bz,
+                           const __half* bias, __half* Y, int Mt, int N, cudaStream_t st) {
     const size_t total = (size_t)Mt * (size_t)N;
     if (total == 0) return cudaSuccess;
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    lora_up_kernel<<<(unsigned)blocks, 256, 0, st>>>(T, B, bias, Y, Mt, N);
+    lora_up_kernel<<<(unsigned)blocks, 256, 0, st>>>(T, B, Bq, Bs, Bz, bias, Y, Mt, N);
     return cudaGetLastError();
 }
 

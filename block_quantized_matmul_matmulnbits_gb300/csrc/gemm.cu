@@ -29,7 +29,8 @@
 //    from shared memory descriptors), committing each stage back to the
 //    producer.
 //  * The LoRA term is one more K step (in the last K split of a tile) with A =
-//    B_lora[n, 0:32] and B = T[m, 0:32], written into the ring by the dequant
+//    B_lora[n, 0:32] (FP16, or dequantized from an INT8 block-32 up weight)
+//    and B = T[m, 0:32], written into the ring by the dequant
 //    warps after griddepcontrol.wait on the LoRA down kernel: the integrated
 //    T * Bt^T epilogue, accumulated into the same tensor-memory tile.
 //  * Warps 2..5 read the accumulator with tcgen05.ld (warp w owns TMEM lanes
@@ -505,7 +506,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pdl_wait();  // T is written by the LoRA down kernel queued before this grid
                     waited = true;
                 }
-                if (h == 0) {  // A operand: B_lora[n, 0:32] in chunks 0..3 of row r
+                if (h == 0 && a.Bq) {  // A operand from the INT8 up weight: one block per row
+                    const size_t nn = (size_t)(row_ok ? n : 0);
+                    const uint4* brow = reinterpret_cast<const uint4*>(a.Bq + nn * 32);
+                    const uint4 p0 = __ldg(brow), p1 = __ldg(brow + 1);
+                    const uint16_t sbits = row_ok ? reinterpret_cast<const uint16_t*>(a.Bs)[nn] : (uint16_t)0;
+                    const DqConst bc = dq_const(a.Bz ? (uint32_t)a.Bz[nn] : 128u, sbits);  // scale 0: row past N
+                    const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                    uint32_t o[16];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], bc, &o[2 * w]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(wslot(s) + swz128(r, c)),
+                                     "r"(o[4 * c]), "r"(o[4 * c + 1]), "r"(o[4 * c + 2]), "r"(o[4 * c + 3])
+                                     : "memory");
+                } else if (h == 0) {  // A operand: B_lora[n, 0:32] in chunks 0..3 of row r
                     const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)(row_ok ? n : 0) * 32);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {

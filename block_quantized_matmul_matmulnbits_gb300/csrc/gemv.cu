@@ -54,6 +54,10 @@ constexpr int kMaxRing = 4;                                // ring stages (2 or 
 constexpr uint32_t kXStageMax = 24 * 1024;                 // largest X tile staged in shared memory
 constexpr int kGroup = 16;                                 // rows per stage / MMA tile
 constexpr int kMaxChunk = 1024;                            // K bytes per row and stage
+// Inside a stage's adapter region (1 KB: 16 FP16 rows of B, or 16 INT8 rows of
+// 32 bytes followed by their scales and zero points)
+constexpr uint32_t kBqScale = 512;                         // 16 x 2 bytes (+ 16 bytes slack)
+constexpr uint32_t kBqZero = 576;                          // 16 bytes (+ 16 bytes slack)
 
 struct GemvLayout {
     uint32_t stage;            // bytes of one ring stage
@@ -165,13 +169,23 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 const uint64_t s_lo = s0 & ~15ull, s_hi = min((s1 + 15) & ~15ull, total_s & ~15ull);
                 const uint64_t z0 = (uint64_t)ra * nblk, z1 = (uint64_t)(ra + rows) * nblk;
                 const uint64_t z_lo = z0 & ~15ull, z_hi = min((z1 + 15) & ~15ull, total_z & ~15ull);
+                // INT8 adapter rows: their scales (2 bytes) and zero points (1 byte) the same way;
+                // ra is a multiple of 16, so both start on a 16-byte boundary
+                const uint64_t qs0 = (uint64_t)ra * 2, qs1 = (uint64_t)(ra + rows) * 2;
+                const uint64_t qs_lo = qs0, qs_hi = min((qs1 + 15) & ~15ull, ((uint64_t)a.N * 2) & ~15ull);
+                const uint64_t qz_lo = (uint64_t)ra, qz1 = (uint64_t)(ra + rows);
+                const uint64_t qz_hi = min((qz1 + 15) & ~15ull, (uint64_t)a.N & ~15ull);
                 if (lane == 0) {
                     const int cb = min(CH, rowbytes - c * CH);  // bytes of this chunk per row
                     // a 3-D box always lands whole (rows past N, pieces past K read as zero)
                     uint32_t bytes = nchunk > 1 && a.w3d ? (uint32_t)kGroup * (uint32_t)CH : (uint32_t)rows * (uint32_t)cb;
                     if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
                     if (HAS_ZP && z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
-                    if (a.rank > 0) bytes += (uint32_t)rows * 64u;
+                    if (a.rank > 0) bytes += (uint32_t)rows * (a.Bq ? 32u : 64u);
+                    if (a.rank > 0 && a.Bq) {
+                        if (qs_hi > qs_lo) bytes += (uint32_t)(qs_hi - qs_lo);
+                        if (a.Bz && qz_hi > qz_lo) bytes += (uint32_t)(qz_hi - qz_lo);
+                    }
                     mbar_arrive_tx(full(s), bytes);
                     const uint8_t* src = a.Wq + (size_t)ra * rowbytes + (size_t)c * CH;
                     if (nchunk == 1) {
@@ -186,13 +200,28 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                         bulk_load(slot + L.sc, reinterpret_cast<const uint8_t*>(a.S) + s_lo, (uint32_t)(s_hi - s_lo),
                                   full(s));
                     if (HAS_ZP && z_hi > z_lo) bulk_load(slot + L.zp, a.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
-                    if (a.rank > 0) bulk_load(slot + L.b, a.B + (size_t)ra * 32, (uint32_t)rows * 64u, full(s));
+                    if (a.rank > 0 && !a.Bq) bulk_load(slot + L.b, a.B + (size_t)ra * 32, (uint32_t)rows * 64u, full(s));
+                    if (a.rank > 0 && a.Bq) {
+                        bulk_load(slot + L.b, a.Bq + (size_t)ra * 32, (uint32_t)rows * 32u, full(s));
+                        if (qs_hi > qs_lo)
+                            bulk_load(slot + L.b + kBqScale, reinterpret_cast<const uint8_t*>(a.Bs) + qs_lo,
+                                      (uint32_t)(qs_hi - qs_lo), full(s));
+                        if (a.Bz && qz_hi > qz_lo)
+                            bulk_load(slot + L.b + kBqZero, a.Bz + qz_lo, (uint32_t)(qz_hi - qz_lo), full(s));
+                    }
                 } else {
                     unsigned char* st8 = sm + (uint32_t)s * L.stage;
                     for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
                         st8[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(a.S)[i];
                     if (HAS_ZP)
                         for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) st8[L.zp + (uint32_t)(i - z_lo)] = a.Z[i];
+                    if (a.rank > 0 && a.Bq) {
+                        for (uint64_t i = max(qs_hi, qs_lo); i < qs1; ++i)
+                            st8[L.b + kBqScale + (uint32_t)(i - qs_lo)] = reinterpret_cast<const uint8_t*>(a.Bs)[i];
+                        if (a.Bz)
+                            for (uint64_t i = max(qz_hi, qz_lo); i < qz1; ++i)
+                                st8[L.b + kBqZero + (uint32_t)(i - qz_lo)] = a.Bz[i];
+                    }
                     mbar_arrive(full(s));
                 }
             }
@@ -453,18 +482,37 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
             // LoRA term of the group's 16 rows, sum_r B[n, r] T[m, r], on the tensor
             // cores: two m16n8k16 per token tile (A = the stage's B rows, B = T),
             // into this warp's accumulators, so the warp-order sum below adds it.
-            const unsigned char* bs = sm + soff + L.b;  // 16 rows x 32 halves
+            const unsigned char* bs = sm + soff + L.b;  // 16 rows x 32 halves (INT8: 16 rows x 32 bytes)
             const unsigned char* ts = sm + L.t;         // TOK rows x 32 halves
+            DqConst q0 = {}, q8 = {};
+            if (a.Bq) {  // INT8 adapter rows g and g + 8: one block per row
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(bs + kBqScale);
+                q0 = dq_const(a.Bz ? (uint32_t)bs[kBqZero + g] : 128u, sc[g]);
+                q8 = dq_const(a.Bz ? (uint32_t)bs[kBqZero + g + 8] : 128u, sc[g + 8]);
+            }
 #pragma unroll
             for (int kc = 0; kc < 2; ++kc) {
-                const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
-                const uint32_t b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
-                const uint32_t b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
-                const uint32_t b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
-                const uint32_t b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
+                uint32_t b0r0, b0r8, b8r0, b8r8;
+                if (a.Bq) {  // the two codes of a pair as 1024 + q in each half, then exact q - zp, one rounding
+                    const uint32_t o = (uint32_t)(16 * kc + 2 * t);
+                    auto pair = [&](int row, uint32_t off, const DqConst& c) {
+                        const uint32_t v = *reinterpret_cast<const uint16_t*>(bs + row * 32 + off);
+                        return hmul2_rn(hsub2_rn(prmt(v, 0x64646464u, 0x4140u), c.c0), c.s2);
+                    };
+                    b0r0 = pair(g, o, q0);
+                    b0r8 = pair(g + 8, o, q8);
+                    b8r0 = pair(g, o + 8, q0);
+                    b8r8 = pair(g + 8, o + 8, q8);
+                } else {
+                    const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
+                    b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
+                    b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
+                    b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
+                    b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const unsigned char* trow = ts + (nt * 8 + g) * 64 + o;
+                    const unsigned char* trow = ts + (nt * 8 + g) * 64 + (16 * kc + 2 * t) * 2;  // T[m, 16kc + 2t]
                     mma_16816(acc[nt][0], b0r0, b0r8, b8r0, b8r8, *reinterpret_cast<const uint32_t*>(trow),
                               *reinterpret_cast<const uint32_t*>(trow + 16));
                 }

@@ -6,6 +6,10 @@
 // fuse_down pairs T with the decode GEMV.  T is kept as an FP16 intermediate
 // ("preserving FP16 rounding").
 //
+// The down weight is FP16 A [K, 32], or an INT8 block-32 weight Aq [32, K]
+// (the INT8 adapters of the same page's later commits), dequantized while it is
+// staged with the base kernels' arithmetic (exact q - zp, one rounding).
+//
 // Design (sm_103a): K is split across the CTAs of one thread-block cluster
 // (up to 8).  Each CTA stages its slices of A and X in padded shared memory
 // with every 16-byte copy in flight at once (A, a weight, before the
@@ -56,10 +60,25 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
-__global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict__ X, const __half* __restrict__ A,
+constexpr int kPitchR = kPiece + 8;  // halfs per staged rank row of a dequantized INT8 A slice
+static_assert(32 * kPitchR <= kPiece * kPitchA, "the INT8 A slice reuses the FP16 A slice's space");
+
+// The down weight in one of two formats: FP16 A [K, 32], or INT8 Aq [32, K]
+// (block-32 rows along K) with FP16 scales As and zero points Az [32, K/32].
+struct DownWeight {
+    const __half* A;
+    const uint8_t* Aq;
+    const __half* As;
+    const uint8_t* Az;
+};
+
+template <bool Q8>
+__global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict__ X, const DownWeight W,
                                                          __half* __restrict__ T, int Mt, int K, int nsplit) {
     extern __shared__ __align__(16) unsigned char lds_raw[];
-    __half* As = reinterpret_cast<__half*>(lds_raw);                          // [kPiece][kPitchA]
+    // FP16 A: [kPiece][kPitchA] (k-major, read transposed); INT8 A: dequantized
+    // into [32][kPitchR] (rank-major, read as is)
+    __half* As = reinterpret_cast<__half*>(lds_raw);
     __half* Xs = As + kPiece * kPitchA;                                       // [kTok][kPitchX]
     float* part = reinterpret_cast<float*>(Xs + kTok * kPitchX);              // [kTok][32]
 
@@ -85,9 +104,30 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
     for (int kb = 16 * c0; kb < 16 * c1; kb += kPiece) {
         const int klen = min(kPiece, 16 * c1 - kb);
         // A (a weight) first, then X once the producer of X has finished.
-        for (int idx = tid; idx < klen * 4; idx += blockDim.x) {
-            const int row = idx >> 2, c = idx & 3;
-            cp_async16(smem_u32(&As[row * kPitchA + c * 8]), A + (size_t)(kb + row) * 32 + c * 8, 16);
+        if constexpr (Q8) {
+            // 16 codes of one rank row per item (a 16-code piece never straddles a block):
+            // exact (q - zp), one rounding by the scale, the base kernels' arithmetic
+            const int pc = klen / 16, nblk = K / 32;
+            for (int idx = tid; idx < 32 * pc; idx += blockDim.x) {
+                const int r = idx / pc, c = idx - r * pc;
+                const int k = kb + c * 16;
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(W.Aq + (size_t)r * K + k));
+                const int b = r * nblk + k / 32;
+                const DqConst dc = dq_const(W.Az ? (uint32_t)W.Az[b] : 128u, reinterpret_cast<const uint16_t*>(W.As)[b]);
+                uint32_t d[8];
+                dq_int8_natural(v.x, dc, &d[0]);
+                dq_int8_natural(v.y, dc, &d[2]);
+                dq_int8_natural(v.z, dc, &d[4]);
+                dq_int8_natural(v.w, dc, &d[6]);
+                uint4* dst = reinterpret_cast<uint4*>(&As[r * kPitchR + c * 16]);
+                dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+                dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+            }
+        } else {
+            for (int idx = tid; idx < klen * 4; idx += blockDim.x) {
+                const int row = idx >> 2, c = idx & 3;
+                cp_async16(smem_u32(&As[row * kPitchA + c * 8]), W.A + (size_t)(kb + row) * 32 + c * 8, 16);
+            }
         }
         if (!waited) {
             pdl_wait();
@@ -111,8 +151,12 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(smem_u32(&As[(kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8]), b0, b1, b2,
-                          b3);
+                if constexpr (Q8)  // rank rows h*16 .. +15, K columns kk .. kk+15
+                    ldsm_x4(smem_u32(&As[(h * 16 + (mat >> 1) * 8 + row8) * kPitchR + kk + (mat & 1) * 8]), b0, b1,
+                            b2, b3);
+                else
+                    ldsm_x4_t(smem_u32(&As[(kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8]), b0, b1,
+                              b2, b3);
                 mma_16816(acc[2 * h], a0, a1, a2, a3, b0, b1);
                 mma_16816(acc[2 * h + 1], a0, a1, a2, a3, b2, b3);
             }
@@ -159,10 +203,16 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
 }  // namespace
 
 cudaError_t lora_down_prepare() {
-    return cudaFuncSetAttribute(lora_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
+    cudaError_t e = cudaFuncSetAttribute(lora_down_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lora_down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
+    return e;
 }
 
-cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st) {
+namespace {
+
+cudaError_t launch_down(const __half* X, const DownWeight& W, bool q8, __half* T, int Mt, int K, bool pdl,
+                        cudaStream_t st) {
     const int nch = K / 16;
     int nsplit = nch < kMaxCluster ? nch : kMaxCluster;
     if (nsplit < 1) nsplit = 1;
@@ -181,7 +231,19 @@ cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, lora_down_kernel, X, A, T, Mt, K, nsplit);
+    return q8 ? cudaLaunchKernelEx(&cfg, lora_down_kernel<true>, X, W, T, Mt, K, nsplit)
+              : cudaLaunchKernelEx(&cfg, lora_down_kernel<false>, X, W, T, Mt, K, nsplit);
+}
+
+}  // namespace
+
+cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st) {
+    return launch_down(X, DownWeight{A, nullptr, nullptr, nullptr}, false, T, Mt, K, pdl, st);
+}
+
+cudaError_t lora_down_q8_launch(const __half* X, const uint8_t* Aq, const __half* As, const uint8_t* Az, __half* T,
+                                int Mt, int K, bool pdl, cudaStream_t st) {
+    return launch_down(X, DownWeight{nullptr, Aq, As, Az}, true, T, Mt, K, pdl, st);
 }
 
 }  // namespace mnb

@@ -32,6 +32,9 @@ struct GemvArgs {
     const uint8_t* Z;    // [N, K/32] or nullptr (default zero point)
     const __half* T;     // [Mt, 32] or nullptr
     const __half* B;     // [N, 32] or nullptr
+    const uint8_t* Bq;   // INT8 up weight [N, 32] (one block a row), used instead of B, or nullptr
+    const __half* Bs;    // [N] scales of Bq
+    const uint8_t* Bz;   // [N] zero points of Bq, or nullptr (128)
     const __half* bias;  // [N] or nullptr: added to every output row before the rounding
     __half* Y;           // [Mt, N]
     int Mt, N, K;
@@ -55,6 +58,10 @@ cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, boo
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.
 cudaError_t lora_down_prepare();
 cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st);
+// The same with an INT8 down weight: Aq [32, K] (block-32 rows along K), As / Az [32, K/32]
+// (Az nullptr: 128); A[k, r] = fp16((Aq[r, k] - zp) * scale).
+cudaError_t lora_down_q8_launch(const __half* X, const uint8_t* Aq, const __half* As, const uint8_t* Az, __half* T,
+                                int Mt, int K, bool pdl, cudaStream_t st);
 
 struct GemmArgs {
     const __half* X;
@@ -63,6 +70,9 @@ struct GemmArgs {
     const uint8_t* Z;
     const __half* T;
     const __half* B;
+    const uint8_t* Bq;   // INT8 up weight [N, 32] instead of B, or nullptr
+    const __half* Bs;    // [N]
+    const uint8_t* Bz;   // [N] or nullptr (128)
     const __half* bias;  // [N] or nullptr
     __half* Y;
     int Mt, N, K, bits, rank;
@@ -77,9 +87,11 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
 
 // Y = 0 over `count` halfs (K == 0 case).
 cudaError_t fill_zero_launch(__half* Y, size_t count, cudaStream_t st);
-// Y[m, n] = bias[n] for m < rows (K == 0 with a bias)
-cudaError_t lora_up_launch(const __half* T, const __half* B, const __half* bias, __half* Y, int Mt, int N,
-                           cudaStream_t st);
+// Y[m, n] = fp16(sum_r T[m, r] B[n, r] (+ bias[n])), the adapter term alone (empty packed
+// weight); B is FP16 [N, 32], or INT8 Bq [N, 32] with Bs / Bz [N] when Bq is not null.
+cudaError_t lora_up_launch(const __half* T, const __half* B, const uint8_t* Bq, const __half* Bs, const uint8_t* Bz,
+                           const __half* bias, __half* Y, int Mt, int N, cudaStream_t st);
+// Y[m, n] = bias[n] for m < rows (K == 0 or an empty weight, with a bias)
 cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st);
 
 // W16[n, k] = fp16((q - zp) * scale) with the kernels' own dequant arithmetic.

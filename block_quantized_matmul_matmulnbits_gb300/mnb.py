@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.mnb_run.restype = ctypes.c_int
             L.mnb_run_bias.argtypes = [P, P, P, P, P, P, P, I32, P, P, P, I64, I64, P]
             L.mnb_run_bias.restype = ctypes.c_int
+            L.mnb_run_qlora.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, P, P, P, I64, I64, P]
+            L.mnb_run_qlora.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -146,6 +148,13 @@ def mnb_run(h, X, Wq, scales, zp, A, B, rank: int, Y, T_ws, batch: int, M: int, 
 def mnb_run_bias(h, X, Wq, scales, zp, A, B, rank: int, bias, Y, T_ws, batch: int, M: int, stream=None) -> None:
     _check(lib().mnb_run_bias(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
                               _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run_bias")
+
+
+def mnb_run_qlora(h, X, Wq, scales, zp, Aq, A_scales, A_zp, Bq, B_scales, B_zp, rank: int, bias, Y, T_ws,
+                  batch: int, M: int, stream=None) -> None:
+    _check(lib().mnb_run_qlora(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(Aq), _ptr(A_scales), _ptr(A_zp),
+                               _ptr(Bq), _ptr(B_scales), _ptr(B_zp), rank, _ptr(bias), _ptr(Y), _ptr(T_ws), batch, M,
+                               _stream(stream)), "mnb_run_qlora")
 
 
 def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:

@@ -159,6 +159,27 @@ int mnb_run_bias(mnb_handle h,
                  void* Y, void* T_ws,
                  int64_t batch, int64_t M, void* stream);
 
+/* mnb_run_bias with INT8 block-32 rank-32 adapters instead of FP16 ones: the
+ * INT4 base with "block-32 INT8 adapters" and their "original INT8
+ * arithmetic" of "[WebGPU] Fuse rank-32 quantized LoRA with MatMulNBits"
+ * (commit message adding the INT8-adapter graph fusion and kernels, and the
+ * later MatMulNBitsQLoRA commit).  Each adapter projection is an 8-bit
+ * MatMulNBits weight:
+ *   Aq        uint8 [32, K/32, 32]  down projection: rank rows along K
+ *   A_scales  fp16 [32, K/32];  A_zp uint8 [32, K/32] or NULL (128)
+ *   Bq        uint8 [N, 1, 32]     up projection: N rows along the rank
+ *   B_scales  fp16 [N];  B_zp uint8 [N] or NULL (128)
+ * a[k, r] = fp16((Aq[r, k] - zp) * scale), b[n, r] likewise (exact q - zp,
+ * one rounding, as the base weights), T = fp16(X * a), Y = fp16(base + T * b^T
+ * (+ bias)).  Aq and Bq both NULL, or rank == 0, is the empty adapter.  All
+ * pointers 16-byte aligned.  Other arguments, results and errors as mnb_run_bias. */
+int mnb_run_qlora(mnb_handle h,
+                  const void* X, const void* Wq, const void* scales, const void* zp,
+                  const void* Aq, const void* A_scales, const void* A_zp,
+                  const void* Bq, const void* B_scales, const void* B_zp, int32_t rank,
+                  const void* bias, void* Y, void* T_ws,
+                  int64_t batch, int64_t M, void* stream);
+
 /* The plan mnb_run would use for (batch, M, rank) on a GPU with `sm_count`
  * SMs (sm_count <= 0: query the current device).  Host only.  Follows the
  * auto mode selection of the MatMulNBitsLoRA commit message (per-matrix row

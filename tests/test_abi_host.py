@@ -157,6 +157,28 @@ def test_run_validation_needs_no_device():
         mnb.mnb_destroy(h0)
 
 
+def test_qlora_validation_needs_no_device():
+    h = mnb.mnb_create(64, 64, 4)
+    try:
+        def rc(**kw):
+            args = dict(X=0x1000, Wq=0x2000, scales=0x3000, zp=None, Aq=0x5000, As=0x6000, Az=None, Bq=0x7000,
+                        Bs=0x8000, Bz=None, rank=32, bias=None, Y=0x4000, T_ws=0x9000, batch=1, M=1)
+            args.update(kw)
+            return mnb.lib().mnb_run_qlora(h, args["X"], args["Wq"], args["scales"], args["zp"], args["Aq"],
+                                           args["As"], args["Az"], args["Bq"], args["Bs"], args["Bz"], args["rank"],
+                                           args["bias"], args["Y"], args["T_ws"], args["batch"], args["M"], None)
+        assert rc(As=None) == mnb.MNB_ERR_ARG          # an INT8 weight needs its scales
+        assert rc(Bs=None) == mnb.MNB_ERR_ARG
+        assert rc(Bq=None) == mnb.MNB_ERR_ARG          # half an adapter
+        assert rc(T_ws=None) == mnb.MNB_ERR_ARG
+        assert rc(rank=16) == mnb.MNB_ERR_UNSUPPORTED
+        assert rc(Az=0x6008) == mnb.MNB_ERR_ALIGN
+        assert rc(Bs=0x8002) == mnb.MNB_ERR_ALIGN
+        assert rc(M=0) == mnb.MNB_OK and mnb.mnb_last_route(h) == mnb.ROUTE_NONE
+    finally:
+        mnb.mnb_destroy(h)
+
+
 def test_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 48, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
