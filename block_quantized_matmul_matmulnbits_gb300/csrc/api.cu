@@ -278,20 +278,18 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     }
     const bool pdl = lora_kernel || early;
     if (p.route == MNB_ROUTE_GEMV) {
-        mnb::GemvArgs a;
+        mnb::GemvArgs a = {};
+        a.nseg = 1;
+        a.G = cdiv(d.N, 16);
+        a.seg[0] = mnb::GemvSeg{0, (int)d.N, static_cast<const uint8_t*>(Wq), static_cast<const __half*>(scales),
+                                static_cast<const uint8_t*>(zp), biash, static_cast<__half*>(Y)};
         a.X = Xh;
-        a.Wq = static_cast<const uint8_t*>(Wq);
-        a.S = static_cast<const __half*>(scales);
-        a.Z = static_cast<const uint8_t*>(zp);
         a.T = Th;
         a.B = static_cast<const __half*>(ad.B);
         a.Bq = Bq8;
         a.Bs = Bs8;
         a.Bz = Bz8;
-        a.bias = biash;
-        a.Y = static_cast<__half*>(Y);
         a.Mt = (int)Mt;
-        a.N = (int)d.N;
         a.K = (int)d.K;
         a.R = p.rows_per_cta;
         a.CH = p.k_splits;
@@ -352,6 +350,118 @@ int mnb_run_qlora(mnb_handle h, const void* X, const void* Wq, const void* scale
                   int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
     return run_impl(h, X, Wq, scales, zp, Adapter{nullptr, nullptr, Aq, A_scales, A_zp, Bq, B_scales, B_zp, true},
                     rank, bias, Y, T_ws, batch, M, stream);
+}
+
+int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32_t nproj, int64_t batch, int64_t M,
+                  void* stream) {
+    if (!h || !proj || batch < 0 || M < 0) return MNB_ERR_ARG;
+    if (nproj < 1 || nproj > mnb::kMaxSeg) return MNB_ERR_UNSUPPORTED;
+    const mnb_desc& d = h->d;
+    if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
+    const int64_t Mt = batch * M;
+    int64_t total = 0;
+    int nonempty = 0, with_zp = 0;
+    for (int i = 0; i < nproj; ++i) {
+        const mnb_projection& q = proj[i];
+        if (q.N < 0 || q.N > (int64_t)INT32_MAX) return MNB_ERR_ARG;
+        total += q.N;
+        if (!aligned16(q.Wq) || !aligned16(q.scales) || !aligned16(q.zp) || !aligned16(q.bias) || !aligned16(q.Y))
+            return MNB_ERR_ALIGN;
+        if (Mt > 0 && q.N > 0) {
+            if (!q.Y) return MNB_ERR_ARG;
+            if (d.K > 0 && q.Wq) {
+                if (!q.scales || !X) return MNB_ERR_ARG;
+                ++nonempty;
+                with_zp += q.zp ? 1 : 0;
+            }
+        }
+    }
+    if (total != d.N) return MNB_ERR_ARG;  // the handle describes the fused weight: N = sum of the projections
+    if (with_zp != 0 && with_zp != nonempty) return MNB_ERR_UNSUPPORTED;  // zero points for all or none
+    if (!aligned16(X)) return MNB_ERR_ALIGN;
+    if (Mt > 0 && Mt * d.N > ((int64_t)1 << 40)) return MNB_ERR_UNSUPPORTED;
+    if (Mt == 0 || d.N == 0) {
+        h->last_route = MNB_ROUTE_NONE;
+        return MNB_OK;
+    }
+    int sms = 0;
+    unsigned int* status = nullptr;
+    int rc = device_setup(&sms, &status);
+    if (rc != MNB_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    // empty members (or K == 0): zeros or the broadcast bias, the shared fallback
+    for (int i = 0; i < nproj && e == cudaSuccess; ++i) {
+        const mnb_projection& q = proj[i];
+        if (q.N == 0 || (d.K > 0 && q.Wq)) continue;
+        __half* Yq = static_cast<__half*>(q.Y);
+        e = q.bias ? mnb::fill_bias_launch(Yq, static_cast<const __half*>(q.bias), (size_t)Mt, (size_t)q.N, st)
+                   : mnb::fill_zero_launch(Yq, (size_t)Mt * (size_t)q.N, st);
+    }
+    if (e != cudaSuccess) return MNB_ERR_CUDA;
+    if (nonempty == 0) {
+        h->last_route = MNB_ROUTE_FILL;
+        return MNB_OK;
+    }
+    const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
+    mnb_plan_info p;
+    make_plan(d, batch, M, 0, sms, &p);
+    if (p.route == MNB_ROUTE_GEMV) {
+        // one launch over the nonempty members, each starting on a 16-row group
+        mnb::GemvArgs a = {};
+        int G = 0;
+        for (int i = 0; i < nproj; ++i) {
+            const mnb_projection& q = proj[i];
+            if (q.N == 0 || !q.Wq) continue;
+            a.seg[a.nseg++] = mnb::GemvSeg{G, (int)q.N, static_cast<const uint8_t*>(q.Wq),
+                                           static_cast<const __half*>(q.scales), static_cast<const uint8_t*>(q.zp),
+                                           static_cast<const __half*>(q.bias), static_cast<__half*>(q.Y)};
+            G += cdiv(q.N, 16);
+        }
+        a.G = G;
+        mnb_desc dv = d;
+        dv.N = (int64_t)G * 16;  // the launch geometry of the members' row space
+        make_plan(dv, batch, M, 0, sms, &p);
+        a.X = static_cast<const __half*>(X);
+        a.Mt = (int)Mt;
+        a.K = (int)d.K;
+        a.R = p.rows_per_cta;
+        a.CH = p.k_splits;
+        a.rank = 0;
+        a.x_wait = early ? 1 : 0;
+        a.sms = sms;
+        a.status = status;
+        e = mnb::gemv_launch(a, p, d.bits, early, st);
+    } else {
+        // prefill: one tensor-core launch per nonempty member (each long enough
+        // that a launch costs nothing in comparison)
+        for (int i = 0; i < nproj && e == cudaSuccess; ++i) {
+            const mnb_projection& q = proj[i];
+            if (q.N == 0 || !q.Wq) continue;
+            mnb_desc dq = d;
+            dq.N = q.N;
+            mnb_plan_info pq;
+            make_plan(dq, batch, M, 0, sms, &pq);
+            mnb::GemmArgs a = {};
+            a.X = static_cast<const __half*>(X);
+            a.Wq = static_cast<const uint8_t*>(q.Wq);
+            a.S = static_cast<const __half*>(q.scales);
+            a.Z = static_cast<const uint8_t*>(q.zp);
+            a.bias = static_cast<const __half*>(q.bias);
+            a.Y = static_cast<__half*>(q.Y);
+            a.Mt = (int)Mt;
+            a.N = (int)q.N;
+            a.K = (int)d.K;
+            a.bits = d.bits;
+            a.rank = 0;
+            a.status = status;
+            e = mnb::gemm_launch(a, pq, early, early, st);
+            if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
+        }
+    }
+    if (e != cudaSuccess) return MNB_ERR_CUDA;
+    h->last_route = p.route;
+    return MNB_OK;
 }
 
 int mnb_sync_status(mnb_handle h, void* stream) {

@@ -6,6 +6,10 @@
 // adding MatMulNBitsLoRA: base GEMV and LoRA down projection first, then the
 // base plus T * Bt^T), restated for sm_103a:
 //
+//  * One launch may compute up to four projections of the same X (the fused
+//    QKV / MLP projections of the empty-packed-weights commit referenced by
+//    the same page): their 16-row groups are laid end to end and a small table
+//    in parameter space gives each group its projection's pointers.
 //  * Every packed weight byte is read from HBM once per token group.  Rows are
 //    dealt out in whole 16-row groups: CTA c of C owns groups
 //    [c G / C, (c+1) G / C) of the G = ceil(N / 16), and C is chosen so that
@@ -115,9 +119,14 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* sm, uint32_t of
 }
 __device__ __forceinline__ uint32_t lds_u8(const unsigned char* sm, uint32_t off) { return sm[off]; }
 
+// 3-D TMA descriptors of the projections' packed weights (multi-chunk stages).
+struct GemvMaps {
+    CUtensorMap m[kMaxSeg];
+};
+
 template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC>
 __global__ void __launch_bounds__(kThreadsGemv, OCC)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
     extern __shared__ __align__(1024) unsigned char sm[];
     constexpr int TOK = 8 * NT;
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
@@ -131,10 +140,17 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     const GemvLayout L = gemv_layout(CH, nblk, TOK, ring, XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = (a.N + kGroup - 1) / kGroup;
-    const int r0 = kGroup * (int)((long long)blockIdx.x * G / gridDim.x);
-    const int r1 = min(a.N, kGroup * (int)((long long)(blockIdx.x + 1) * G / gridDim.x));
-    const int ngroups = (r1 - r0 + kGroup - 1) / kGroup;
+    // groups [g_begin, g_end) of the row space of all projections
+    const int G = a.G;
+    const int g_begin = (int)((long long)blockIdx.x * G / gridDim.x);
+    const int ngroups = (int)((long long)(blockIdx.x + 1) * G / gridDim.x) - g_begin;
+    // projection owning group gq (the table lives in parameter space: no local copy)
+    auto seg_of = [&](int gq) {
+        int sg = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxSeg; ++i) sg += (i < a.nseg && gq >= a.seg[i].g0) ? 1 : 0;
+        return sg;
+    };
     const int nstages = ngroups * nchunk;
     const int token0 = blockIdx.y * TOK;
     unsigned int* status = a.status;
@@ -154,13 +170,15 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------------ producer
-        const uint64_t total_s = (uint64_t)a.N * nblk * 2, total_z = (uint64_t)a.N * nblk;
         if (lane < 2) {
             bool ok = true;
             for (int st = 0; ok && st < nstages; ++st) {
                 const int s = st & rmask;
                 const int q = st / nchunk, c = st - q * nchunk;
-                const int ra = r0 + q * kGroup, rows = min(kGroup, r1 - ra);
+                const int sg = seg_of(g_begin + q);
+                const GemvSeg& pj = a.seg[sg];
+                const int ra = (g_begin + q - pj.g0) * kGroup, rows = min(kGroup, pj.N - ra);  // rows of projection sg
+                const uint64_t total_s = (uint64_t)pj.N * nblk * 2, total_z = (uint64_t)pj.N * nblk;
                 const uint32_t slot = sb + (uint32_t)s * L.stage;
                 if (!(ok = mbar_wait(empty(s), ((uint32_t)(st / ring) & 1u) ^ 1u, status))) break;
                 // scales / zero points of the group's full rows as 16-byte aligned supersets;
@@ -172,9 +190,9 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 // INT8 adapter rows: their scales (2 bytes) and zero points (1 byte) the same way;
                 // ra is a multiple of 16, so both start on a 16-byte boundary
                 const uint64_t qs0 = (uint64_t)ra * 2, qs1 = (uint64_t)(ra + rows) * 2;
-                const uint64_t qs_lo = qs0, qs_hi = min((qs1 + 15) & ~15ull, ((uint64_t)a.N * 2) & ~15ull);
+                const uint64_t qs_lo = qs0, qs_hi = min((qs1 + 15) & ~15ull, ((uint64_t)pj.N * 2) & ~15ull);
                 const uint64_t qz_lo = (uint64_t)ra, qz1 = (uint64_t)(ra + rows);
-                const uint64_t qz_hi = min((qz1 + 15) & ~15ull, (uint64_t)a.N & ~15ull);
+                const uint64_t qz_hi = min((qz1 + 15) & ~15ull, (uint64_t)pj.N & ~15ull);
                 if (lane == 0) {
                     const int cb = min(CH, rowbytes - c * CH);  // bytes of this chunk per row
                     // a 3-D box always lands whole (rows past N, pieces past K read as zero)
@@ -187,19 +205,19 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                         if (a.Bz && qz_hi > qz_lo) bytes += (uint32_t)(qz_hi - qz_lo);
                     }
                     mbar_arrive_tx(full(s), bytes);
-                    const uint8_t* src = a.Wq + (size_t)ra * rowbytes + (size_t)c * CH;
+                    const uint8_t* src = pj.Wq + (size_t)ra * rowbytes + (size_t)c * CH;
                     if (nchunk == 1) {
                         bulk_load(slot + L.w, src, (uint32_t)(rows * rowbytes), full(s));  // rows are contiguous
                     } else if (a.w3d) {
-                        tma_load_3d(slot + L.w, &tmW, 0, c * CH / 256, ra, full(s));
+                        tma_load_3d(slot + L.w, &maps.m[sg], 0, c * CH / 256, ra, full(s));
                     } else {
                         for (int i = 0; i < rows; ++i)
                             bulk_load(slot + L.w + (uint32_t)(i * CH), src + (size_t)i * rowbytes, (uint32_t)cb, full(s));
                     }
                     if (s_hi > s_lo)
-                        bulk_load(slot + L.sc, reinterpret_cast<const uint8_t*>(a.S) + s_lo, (uint32_t)(s_hi - s_lo),
+                        bulk_load(slot + L.sc, reinterpret_cast<const uint8_t*>(pj.S) + s_lo, (uint32_t)(s_hi - s_lo),
                                   full(s));
-                    if (HAS_ZP && z_hi > z_lo) bulk_load(slot + L.zp, a.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
+                    if (HAS_ZP && z_hi > z_lo) bulk_load(slot + L.zp, pj.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
                     if (a.rank > 0 && !a.Bq) bulk_load(slot + L.b, a.B + (size_t)ra * 32, (uint32_t)rows * 64u, full(s));
                     if (a.rank > 0 && a.Bq) {
                         bulk_load(slot + L.b, a.Bq + (size_t)ra * 32, (uint32_t)rows * 32u, full(s));
@@ -212,9 +230,9 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 } else {
                     unsigned char* st8 = sm + (uint32_t)s * L.stage;
                     for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
-                        st8[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(a.S)[i];
+                        st8[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(pj.S)[i];
                     if (HAS_ZP)
-                        for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) st8[L.zp + (uint32_t)(i - z_lo)] = a.Z[i];
+                        for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) st8[L.zp + (uint32_t)(i - z_lo)] = pj.Z[i];
                     if (a.rank > 0 && a.Bq) {
                         for (uint64_t i = max(qs_hi, qs_lo); i < qs1; ++i)
                             st8[L.b + kBqScale + (uint32_t)(i - qs_lo)] = reinterpret_cast<const uint8_t*>(a.Bs)[i];
@@ -307,7 +325,8 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     int q = 0, c = 0;  // group and chunk of stage st (counters: no divisions in the loop)
     for (int st = 0; st < nstages; ++st) {
         const int s = st & rmask;
-        const int ra = r0 + q * kGroup, rows = min(kGroup, r1 - ra);
+        const GemvSeg& pj = a.seg[seg_of(g_begin + q)];
+        const int ra = (g_begin + q - pj.g0) * kGroup, rows = min(kGroup, pj.N - ra);  // rows of this projection
         if (ok) ok = mbar_wait(full(s), (uint32_t)(st / ring) & 1u, status);
         const uint32_t soff = (uint32_t)s * L.stage;  // byte offset of the stage in `sm`
         const uint32_t s_al = ((uint32_t)ra * (uint32_t)nblk * 2u) & 15u;  // scale copy alignment offset
@@ -544,8 +563,8 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
             const int nw = min(kConsumerWarps, npieces);
             float sum = 0.f;
             for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
-            if (a.bias) sum += __half2float(a.bias[ra + rr]);
-            a.Y[(size_t)token * a.N + ra + rr] = __float2half_rn(sum);
+            if (pj.bias) sum += __half2float(pj.bias[ra + rr]);
+            pj.Y[(size_t)token * pj.N + ra + rr] = __float2half_rn(sum);
         }
         __syncwarp();
         if (ok && lane == 0) mbar_arrive(empty(s));
@@ -566,17 +585,20 @@ cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cuda
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     // weights of multi-chunk stages as 3-D boxes when the row length allows it
-    CUtensorMap tw;
-    memset(&tw, 0, sizeof(tw));
+    GemvMaps maps;
+    memset(&maps, 0, sizeof(maps));
     GemvArgs b = a;
     b.w3d = 0;
     const uint64_t rowbytes = (uint64_t)a.K * BITS / 8;
     if (rowbytes > (uint64_t)a.CH && rowbytes % 256 == 0 && a.CH % 256 == 0) {
-        const cudaError_t e = encode_rows_3d(&tw, a.Wq, rowbytes, (uint64_t)a.N, (uint32_t)(a.CH / 256), kGroup);
-        if (e != cudaSuccess) return e;
+        for (int i = 0; i < a.nseg; ++i) {
+            const cudaError_t e = encode_rows_3d(&maps.m[i], a.seg[i].Wq, rowbytes, (uint64_t)a.seg[i].N,
+                                                 (uint32_t)(a.CH / 256), kGroup);
+            if (e != cudaSuccess) return e;
+        }
         b.w3d = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS, OCC>, tw, b);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS, OCC>, maps, b);
 }
 
 template <int BITS, bool HAS_ZP, int NT>
@@ -653,13 +675,13 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
     const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
     const uint32_t xrows = (uint32_t)(a.Mt < tok ? a.Mt : tok);
     const bool xs = xrows * a.K * 2u <= kXStageMax;
-    const int occ = gemv_ctas_per_sm(a.N, tok / 8, xs, a.sms > 0 ? a.sms : 1);
+    const int occ = gemv_ctas_per_sm(a.G * kGroup, tok / 8, xs, a.sms > 0 ? a.sms : 1);
     a.ring = gemv_ring(nstages, occ);
     a.xrows = xs ? (int)xrows : 0;
     const size_t smem = gemv_layout(a.CH, a.K / 32, tok, a.ring, xs ? xrows * a.K * 2u : 0u).total;
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const dim3 grid(p.grid_x, p.grid_y);
-    const bool zp = a.Z != nullptr;
+    const bool zp = a.seg[0].Z != nullptr;
     const int nt = tok / 8;
     if (bits == 2) {
         if (zp) return nt == 1 ? launch_xs<2, true, 1>(a, grid, smem, xs, occ, pdl, st)

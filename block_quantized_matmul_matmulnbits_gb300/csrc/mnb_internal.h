@@ -25,19 +25,31 @@ cudaError_t encode_rows_3d(CUtensorMap* map, const void* base, uint64_t rowbytes
 cudaError_t encode_2d(CUtensorMap* map, const void* base, int elem_bytes, uint64_t cols, uint64_t rows,
                       uint64_t pitch_bytes, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
-struct GemvArgs {
-    const __half* X;     // [Mt, K]
+// One projection of a decode launch.  A launch computes up to kMaxSeg
+// projections of the same X; projection s owns the 16-row groups
+// [g0, g0 + ceil(N / 16)) of the kernel's row space.
+constexpr int kMaxSeg = 4;
+struct GemvSeg {
+    int g0;              // first 16-row group of this projection
+    int N;               // output rows of this projection
     const uint8_t* Wq;   // [N, K*bits/8]
     const __half* S;     // [N, K/32]
-    const uint8_t* Z;    // [N, K/32] or nullptr (default zero point)
+    const uint8_t* Z;    // [N, K/32] or nullptr (every projection of a launch alike)
+    const __half* bias;  // [N] or nullptr
+    __half* Y;           // [Mt, N]
+};
+
+struct GemvArgs {
+    int nseg;                 // projections (>= 1); rank > 0 only with one
+    int G;                    // 16-row groups of all projections
+    GemvSeg seg[kMaxSeg];
+    const __half* X;     // [Mt, K]
     const __half* T;     // [Mt, 32] or nullptr
     const __half* B;     // [N, 32] or nullptr
     const uint8_t* Bq;   // INT8 up weight [N, 32] (one block a row), used instead of B, or nullptr
     const __half* Bs;    // [N] scales of Bq
     const uint8_t* Bz;   // [N] zero points of Bq, or nullptr (128)
-    const __half* bias;  // [N] or nullptr: added to every output row before the rounding
-    __half* Y;           // [Mt, N]
-    int Mt, N, K;
+    int Mt, K;
     int R;               // output rows owned by one CTA
     int CH;              // K bytes per row and pipeline stage (multiple of 64)
     int ring;            // shared-memory ring stages (2 or 4), set by the launcher

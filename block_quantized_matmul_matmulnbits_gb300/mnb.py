@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -46,6 +46,11 @@ class MnbPlanInfo(ctypes.Structure):
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class MnbProjection(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("zp", ctypes.c_void_p), ("bias", ctypes.c_void_p), ("Y", ctypes.c_void_p)]
 
 
 class MnbError(RuntimeError):
@@ -78,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.mnb_run_bias.restype = ctypes.c_int
             L.mnb_run_qlora.argtypes = [P, P, P, P, P, P, P, P, P, P, P, I32, P, P, P, I64, I64, P]
             L.mnb_run_qlora.restype = ctypes.c_int
+            L.mnb_run_multi.argtypes = [P, P, ctypes.POINTER(MnbProjection), ctypes.c_int32, I64, I64, P]
+            L.mnb_run_multi.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -155,6 +162,14 @@ def mnb_run_qlora(h, X, Wq, scales, zp, Aq, A_scales, A_zp, Bq, B_scales, B_zp, 
     _check(lib().mnb_run_qlora(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(Aq), _ptr(A_scales), _ptr(A_zp),
                                _ptr(Bq), _ptr(B_scales), _ptr(B_zp), rank, _ptr(bias), _ptr(Y), _ptr(T_ws), batch, M,
                                _stream(stream)), "mnb_run_qlora")
+
+
+def mnb_run_multi(h, X, projections, batch: int, M: int, stream=None) -> None:
+    """projections: sequence of (N, Wq, scales, zp, bias, Y); Wq None = empty weight."""
+    arr = (MnbProjection * len(projections))()
+    for i, (N, Wq, scales, zp, bias, Y) in enumerate(projections):
+        arr[i] = MnbProjection(N, _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(bias), _ptr(Y))
+    _check(lib().mnb_run_multi(h, _ptr(X), arr, len(projections), batch, M, _stream(stream)), "mnb_run_multi")
 
 
 def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:

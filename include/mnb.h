@@ -180,6 +180,34 @@ int mnb_run_qlora(mnb_handle h,
                   const void* bias, void* Y, void* T_ws,
                   int64_t batch, int64_t M, void* stream);
 
+/* One projection of mnb_run_multi (all pointers device, 16-byte aligned). */
+typedef struct {
+    int64_t N;            /* output features of this projection (>= 0) */
+    const void* Wq;       /* uint8 [N, K/32, 32*bits/8], or NULL: an empty packed weight */
+    const void* scales;   /* fp16 [N, K/32] (unused when Wq is NULL) */
+    const void* zp;       /* uint8 [N, K/32] or NULL (default); all nonempty members alike */
+    const void* bias;     /* fp16 [N] or NULL */
+    void* Y;              /* fp16 [batch, M, N] */
+} mnb_projection;
+
+/* Several projections of the same X in one call -- the fused QKV / MLP
+ * projections that "Support empty packed weights in CPU and WebGPU
+ * MatMulNBits" (referenced by "[WebGPU] Fuse rank-32 quantized LoRA with
+ * MatMulNBits", Description) keeps: the nonempty members are computed, an
+ * empty member (Wq NULL) gets the shared zero / bias fallback.
+ *   h        handle of the fused weight: K, bits, mode and flags as for
+ *            mnb_run; desc.N must equal the sum of the members' N
+ *   proj     1 to 4 members; each Y_i[m, n] = fp16(sum_k X[m, k] w_i[n, k] (+ bias_i[n]))
+ * Decode route: ONE decode-kernel launch over all nonempty members (their
+ * 16-row groups laid end to end), plus one fill launch per empty member.
+ * Prefill route: one tensor-core launch per nonempty member.  Each member's
+ * result is bitwise the result of mnb_run_bias on that member alone.  No
+ * adapter.  Errors: MNB_ERR_ARG (N mismatch, NULL required pointer),
+ * MNB_ERR_UNSUPPORTED (more than 4 members, mixed zero-point presence),
+ * MNB_ERR_ALIGN, MNB_ERR_NO_DEVICE, MNB_ERR_CUDA. */
+int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32_t nproj,
+                  int64_t batch, int64_t M, void* stream);
+
 /* The plan mnb_run would use for (batch, M, rank) on a GPU with `sm_count`
  * SMs (sm_count <= 0: query the current device).  Host only.  Follows the
  * auto mode selection of the MatMulNBitsLoRA commit message (per-matrix row

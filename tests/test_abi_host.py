@@ -179,6 +179,30 @@ def test_qlora_validation_needs_no_device():
         mnb.mnb_destroy(h)
 
 
+def test_multi_projection_validation_needs_no_device():
+    h = mnb.mnb_create(96, 64, 4)
+    try:
+        def rc(projs, M=1, X=0x1000):
+            arr = (mnb.MnbProjection * len(projs))(*[mnb.MnbProjection(*p) for p in projs])
+            return mnb.lib().mnb_run_multi(h, X, arr, len(projs), 1, M, None)
+        ok = (64, 0x2000, 0x3000, None, None, 0x4000)
+        ok2 = (32, 0x5000, 0x6000, None, None, 0x7000)
+        assert rc([ok]) == mnb.MNB_ERR_ARG                          # 64 != desc N 96
+        assert rc([ok, ok2, ok2]) == mnb.MNB_ERR_ARG                # 128 != 96
+        assert rc([ok] * 5) == mnb.MNB_ERR_UNSUPPORTED              # at most four members
+        assert mnb.lib().mnb_run_multi(h, 0x1000, (mnb.MnbProjection * 1)(), 0, 1, 1, None) == mnb.MNB_ERR_UNSUPPORTED
+        assert rc([ok, (32, 0x5000, 0x6000, 0x8000, None, 0x7000)]) == mnb.MNB_ERR_UNSUPPORTED  # zp for some only
+        assert rc([ok, (32, 0x5000, None, None, None, 0x7000)]) == mnb.MNB_ERR_ARG  # weight without scales
+        assert rc([ok, (32, 0x5000, 0x6000, None, None, None)]) == mnb.MNB_ERR_ARG  # no output
+        assert rc([ok, (32, 0x5008, 0x6000, None, None, 0x7000)]) == mnb.MNB_ERR_ALIGN
+        assert rc([ok, ok2], X=0x1002) == mnb.MNB_ERR_ALIGN
+        assert rc([ok, ok2], M=0) == mnb.MNB_OK and mnb.mnb_last_route(h) == mnb.ROUTE_NONE
+        # an empty member needs neither weight nor scales
+        assert rc([ok, (32, None, None, None, None, 0x7000)], M=0) == mnb.MNB_OK
+    finally:
+        mnb.mnb_destroy(h)
+
+
 def test_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 48, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
