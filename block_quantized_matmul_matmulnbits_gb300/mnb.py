@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_transpose_dq_weight", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.mnb_run_qlora.restype = ctypes.c_int
             L.mnb_run_multi.argtypes = [P, P, ctypes.POINTER(MnbProjection), ctypes.c_int32, I64, I64, P]
             L.mnb_run_multi.restype = ctypes.c_int
+            L.mnb_transpose_dq_weight.argtypes = [P, P, P, I64, I64, I32, I32, I32, P, P, P]
+            L.mnb_transpose_dq_weight.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -170,6 +172,25 @@ def mnb_run_multi(h, X, projections, batch: int, M: int, stream=None) -> None:
     for i, (N, Wq, scales, zp, bias, Y) in enumerate(projections):
         arr[i] = MnbProjection(N, _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(bias), _ptr(Y))
     _check(lib().mnb_run_multi(h, _ptr(X), arr, len(projections), batch, M, _stream(stream)), "mnb_run_multi")
+
+
+def mnb_transpose_dq_weight(w_q, w_scale, w_zp, bits: int, blocked: bool = True, block_size: int = 32):
+    """numpy in, numpy out (host): DequantizeLinear weight w_q [K, N] (uint8 codes), w_scale
+    (FP16 bits, [K/32, N] or one value), w_zp (uint8 like w_scale, or None) -> (Wq, scales, zp)
+    in the MatMulNBits layout."""
+    import numpy as np
+    w_q = np.ascontiguousarray(w_q, dtype=np.uint8)
+    K, N = w_q.shape
+    w_scale = np.ascontiguousarray(w_scale, dtype=np.uint16)
+    w_zp = None if w_zp is None else np.ascontiguousarray(w_zp, dtype=np.uint8)
+    Wq = np.empty((N, K // block_size, block_size * bits // 8), dtype=np.uint8)
+    scales = np.empty((N, K // block_size), dtype=np.uint16)
+    zp = np.empty((N, K // block_size), dtype=np.uint8)
+    addr = lambda a: None if a is None else a.ctypes.data
+    _check(lib().mnb_transpose_dq_weight(addr(w_q), addr(w_scale), addr(w_zp), K, N, bits, block_size,
+                                         1 if blocked else 0, addr(Wq), addr(scales), addr(zp)),
+           "mnb_transpose_dq_weight")
+    return Wq, scales, zp
 
 
 def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:

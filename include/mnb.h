@@ -208,6 +208,24 @@ typedef struct {
 int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32_t nproj,
                   int64_t batch, int64_t M, void* stream);
 
+/* Rewrite a DequantizeLinear weight into this layout (HOST pointers, host
+ * code, no device call): the transposed initializers that "Fuse
+ * DQ->MatMulNBits for shared initializers and skip outer-scope weights"
+ * (Description) writes when it turns DequantizeLinear -> MatMul into
+ * MatMulNBits.
+ *   w_q      uint8 [K, N], one code per byte, each < 2^bits (else MNB_ERR_ARG)
+ *   w_scale  fp16 [K/32, N] when `blocked`, else one per-tensor value
+ *   w_zp     uint8, shaped like w_scale, or NULL (DequantizeLinear's default 0)
+ *   Wq       out uint8 [N, K/32, 32*bits/8];  scales out fp16 [N, K/32];
+ *   zp       out uint8 [N, K/32], always written (explicit, since 0 is not
+ *            this library's default)
+ * Then mnb_run on (X, Wq, scales, zp) equals X * DequantizeLinear(w_q)
+ * within the usual tolerance.  Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED
+ * (bits, block size, K % 32). */
+int mnb_transpose_dq_weight(const uint8_t* w_q, const uint16_t* w_scale, const uint8_t* w_zp,
+                            int64_t K, int64_t N, int32_t bits, int32_t block_size, int32_t blocked,
+                            uint8_t* Wq, uint16_t* scales, uint8_t* zp);
+
 /* The plan mnb_run would use for (batch, M, rank) on a GPU with `sm_count`
  * SMs (sm_count <= 0: query the current device).  Host only.  Follows the
  * auto mode selection of the MatMulNBitsLoRA commit message (per-matrix row

@@ -129,3 +129,36 @@ def test_multi_matches_oracle_early_weights(env):
     for (inp, bias, _), Y in zip(mem, Ys):
         Y64, bound = oracle_ref(inp, bias=bias)
         assert_within_tolerance(bits_of(Y).reshape(M, inp.N), Y64, bound, f"member N={inp.N}")
+
+
+# ------------------------------------------------------------------ DQ -> MatMulNBits rewrite
+
+@pytest.mark.parametrize("M", [1, 200])
+def test_dq_rewritten_weight_runs_on_both_routes(env, M):
+    """A DequantizeLinear weight [K, N] (the tied lm_head shape of the DQ
+    fusion page, 576 x 49152, INT8, per-block scales along K) rewritten on the
+    host, then run on the GPU, against X * DequantizeLinear(w) in fp64."""
+    torch, mnb = env
+    K, N = 576, 49152
+    rng = np.random.default_rng(1400 + M)
+    w_q = rng.integers(0, 256, size=(K, N), dtype=np.uint8)
+    w_scale = np.ascontiguousarray(rng.uniform(0.001, 0.01, size=(K // 32, N)).astype(np.float16)).view(np.uint16)
+    w_zp = rng.integers(120, 137, size=(K // 32, N), dtype=np.uint8)
+    Wq, scales, zp = mnb.mnb_transpose_dq_weight(w_q, w_scale, w_zp, 8)
+    X = np.ascontiguousarray(rng.standard_normal((M, K)).astype(np.float16)).view(np.uint16)
+    h = mnb.mnb_create(N, K, 8, max_rank=0)
+    try:
+        Y = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+        mnb.mnb_run(h, dev(X, torch), dev(Wq, torch), dev(scales, torch), dev(zp, torch), None, None, 0, Y, None, 1, M)
+        torch.cuda.synchronize()
+        assert mnb.mnb_last_route(h) == (mnb.ROUTE_GEMV if M == 1 else mnb.ROUTE_GEMM)
+    finally:
+        mnb.mnb_destroy(h)
+    cols = np.sort(rng.choice(N, 512, replace=False))
+    s = np.repeat(w_scale.view(np.float16).astype(np.float64), 32, axis=0)[:, cols]
+    z = np.repeat(w_zp.astype(np.float64), 32, axis=0)[:, cols]
+    W = (w_q[:, cols].astype(np.float64) - z) * s
+    x = X.view(np.float16).astype(np.float64)
+    ref, bound = x @ W, np.abs(x) @ np.abs(W)
+    got = bits_of(Y).reshape(M, N)[:, cols].view(np.float16).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-3 * bound + 1e-3)
