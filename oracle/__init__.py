@@ -74,6 +74,10 @@ def _load():
             lib.mnb_ref_run_bias.restype = I
             lib.mnb_ref_run_qlora.argtypes = [P, P, P, P, P, P, P, P, P, P, I, P, I64, I64, I64, I, I, I, P, P, P]
             lib.mnb_ref_run_qlora.restype = I
+            lib.mnb_ref_quantize_x.argtypes = [P, I64, I64, I, P, P]
+            lib.mnb_ref_quantize_x.restype = I
+            lib.mnb_ref_run_q8x.argtypes = [P, P, P, P, P, P, I, P, I64, I64, I64, I, I, I, P, P, P]
+            lib.mnb_ref_run_q8x.restype = I
             lib.mnb_ref_run.restype = I
             lib.mnb_ref_threads.argtypes = []
             lib.mnb_ref_threads.restype = I
@@ -203,4 +207,34 @@ def run_qlora(X, Wq, scales, zp, Aq, A_scales, A_zp, Bq, B_scales, B_zp, N, K, b
                                    _ptr(Bq), _ptr(B_scales), _ptr(B_zp), rank, _ptr(bias), Mt, N, K, bits, block,
                                    1 if round_t else 0, _ptr(Y16), _ptr(Y64), _ptr(bound))
     _check(rc, "run_qlora")
+    return Y16, Y64, bound
+
+
+def quantize_x(X, block=32):
+    """Per-block int8 activation codes and binary32 scales of X [Mt, K] (FP16
+    bits): (Xq int8 [Mt, K], Xs float32 [Mt, K/block])."""
+    X = _c(X, np.uint16)
+    Mt, K = X.shape
+    Xq = np.empty((Mt, K), dtype=np.int8)
+    Xs = np.empty((Mt, K // block), dtype=np.float32)
+    _check(_load().mnb_ref_quantize_x(_ptr(X), Mt, K, block, _ptr(Xq), _ptr(Xs)), "quantize_x")
+    return Xq, Xs
+
+
+def run_q8x(X, Wq, scales, zp, A, B, N, K, bits, block=32, round_t=False, bias=None):
+    """The int8-activation product (per-block int8 X, integer block dots);
+    arguments and returns as ``run``."""
+    X = _c(X, np.uint16)
+    Wq, scales, zp = _c(Wq, np.uint8), _c(scales, np.uint16), _c(zp, np.uint8)
+    rank = 0 if (A is None or B is None) else int(np.shape(A)[1])
+    A = _c(A, np.uint16) if rank else None
+    B = _c(B, np.uint16) if rank else None
+    Mt = X.shape[0]
+    Y16 = np.empty((Mt, N), dtype=np.uint16)
+    Y64 = np.empty((Mt, N), dtype=np.float64)
+    bound = np.empty((Mt, N), dtype=np.float64)
+    bias = _c(bias, np.uint16) if bias is not None else None
+    rc = _load().mnb_ref_run_q8x(_ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
+                                 Mt, N, K, bits, block, 1 if round_t else 0, _ptr(Y16), _ptr(Y64), _ptr(bound))
+    _check(rc, "run_q8x")
     return Y16, Y64, bound

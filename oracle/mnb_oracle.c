@@ -351,6 +351,115 @@ int mnb_ref_run_qlora(const uint16_t* X, const uint8_t* Wq, const uint16_t* scal
     return rc;
 }
 
+/* ---------------------------------------------------------------------------
+ * The int8-activation base ("accuracy level 4" in "[WebGPU] Fuse rank-32
+ * quantized LoRA with MatMulNBits", Performance, and in "Fuse DQ->MatMulNBits
+ * for shared initializers and skip outer-scope weights", Motivation and
+ * Context; the MatMulNBitsLoRA commit keeps "DP4A activation quantization for
+ * the base, with original FP16 X for T").  The pages name the method, not its
+ * steps; the reading written out here:
+ *   per row m and block b of 32 along K, in binary32:
+ *     amax = max_k |x[m,k]|                      (exact)
+ *     amax == 0:  xq = 0, xs = 0
+ *     else:       inv = 127 / amax,  xq = clamp(rint(x * inv), -127, 127),
+ *                 xs = amax / 127                 (each op rounded to nearest)
+ *   base[m,n] = sum_b xs[m,b] * s[n,b] * sum_{k in b} xq[m,k] (q[n,k] - zp[n,b])
+ * the inner sum an exact integer (the DP4A / integer-MMA product).  T, the
+ * adapter term and the bias as in the plain product (T from the FP16 X).
+ * ------------------------------------------------------------------------- */
+
+int mnb_ref_quantize_x(const uint16_t* X, int64_t Mt, int64_t K, int bs, int8_t* Xq, float* Xs)
+{
+    if (Mt < 0 || K < 0 || bs <= 0 || K % bs != 0) return -2;
+    int64_t nb = K / bs;
+    for (int64_t m = 0; m < Mt; ++m)
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint16_t* x = X + m * K + b * bs;
+            float amax = 0.0f;
+            for (int k = 0; k < bs; ++k) {
+                float a = fabsf((float)mnb_ref_f16_to_f64(x[k]));
+                if (a > amax) amax = a;
+            }
+            int8_t* q = Xq + m * K + b * bs;
+            if (amax == 0.0f) {
+                for (int k = 0; k < bs; ++k) q[k] = 0;
+                Xs[m * nb + b] = 0.0f;
+                continue;
+            }
+            float inv = 127.0f / amax;
+            for (int k = 0; k < bs; ++k) {
+                float r = rintf((float)mnb_ref_f16_to_f64(x[k]) * inv);
+                if (r > 127.0f) r = 127.0f;
+                if (r < -127.0f) r = -127.0f;
+                q[k] = (int8_t)r;
+            }
+            Xs[m * nb + b] = amax / 127.0f;
+        }
+    return 0;
+}
+
+int mnb_ref_run_q8x(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
+                    const uint16_t* A, const uint16_t* B, int rank, const uint16_t* bias,
+                    int64_t Mt, int64_t N, int64_t K, int bits, int bs, int round_t,
+                    uint16_t* Y16, double* Y64, double* bound)
+{
+    int rc = check_shape(N, K, bits, bs);
+    if (rc) return rc;
+    if (Mt < 0 || rank < 0) return -1;
+    if (rank > 0 && (!A || !B)) return -1;
+    int64_t nb = K / bs;
+    int8_t* Xq = (int8_t*)malloc((size_t)(Mt * K > 0 ? Mt * K : 1));
+    float* Xs = (float*)malloc(sizeof(float) * (size_t)(Mt * nb > 0 ? Mt * nb : 1));
+    double* T = (double*)malloc(sizeof(double) * (size_t)(Mt > 0 ? Mt : 1) * (size_t)(rank > 0 ? rank : 1));
+    if (!Xq || !Xs || !T) {
+        free(Xq);
+        free(Xs);
+        free(T);
+        return -3;
+    }
+    mnb_ref_quantize_x(X, Mt, K, bs, Xq, Xs);
+    if (rank > 0) {
+        mnb_ref_lora_down(X, A, Mt, K, rank, T);
+        if (round_t)
+            for (int64_t i = 0; i < Mt * rank; ++i) T[i] = mnb_ref_f16_to_f64(mnb_ref_f64_to_f16(T[i]));
+    }
+    int64_t total = Mt * N;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < total; ++i) {
+        int64_t m = i / N, n = i % N;
+        double acc = 0.0, mag = 0.0;
+        for (int64_t b = 0; b < nb; ++b) {
+            int64_t dot = 0, adot = 0;
+            int z = zp ? (int)zp[n * nb + b] : (1 << (bits - 1));
+            for (int64_t k = b * bs; k < (b + 1) * bs; ++k) {
+                int64_t p = (int64_t)Xq[m * K + k] * (code_at(Wq, K, bits, n, k) - z);
+                dot += p;
+                adot += p < 0 ? -p : p;
+            }
+            double sc = (double)Xs[m * nb + b] * mnb_ref_f16_to_f64(scales[n * nb + b]);
+            acc += sc * (double)dot;
+            mag += fabs(sc) * (double)adot;
+        }
+        for (int j = 0; j < rank; ++j) {
+            double p = T[m * rank + j] * mnb_ref_f16_to_f64(B[n * rank + j]);
+            acc += p;
+            mag += fabs(p);
+        }
+        if (bias) {
+            double bv = mnb_ref_f16_to_f64(bias[n]);
+            acc += bv;
+            mag += fabs(bv);
+        }
+        if (Y64) Y64[i] = acc;
+        if (bound) bound[i] = mag;
+        if (Y16) Y16[i] = mnb_ref_f64_to_f16(acc);
+    }
+    free(Xq);
+    free(Xs);
+    free(T);
+    return 0;
+}
+
 /* mnb_ref_run_bias without a bias. */
 int mnb_ref_run(const uint16_t* X, const uint8_t* Wq, const uint16_t* scales, const uint8_t* zp,
                 const uint16_t* A, const uint16_t* B, int rank,

@@ -524,3 +524,79 @@ def test_qlora_codes_at_zero_point_is_base_bitwise():
                            ql.B_zp, N, K, 8)
     ref = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, None, None, N, K, 8)
     assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
+
+
+# ---------------------------------------------------------------- int8 activations
+
+def _read_act_fixture():
+    xs, codes = [], []
+    with open(os.path.join(GOLDEN, "int8_activation_blocks.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                _, x, c = line.split()
+                xs.append(float(x))
+                codes.append(int(c))
+    return np.array(xs), np.array(codes, dtype=np.int8)
+
+
+def test_activation_quantization_golden():
+    x, codes = _read_act_fixture()
+    Xq, Xs = oracle.quantize_x(f16(x.reshape(1, 64)))
+    assert np.array_equal(Xq[0], codes)
+    # block scales amax / 127 in binary32, computed here with numpy's float32 division
+    assert Xs[0, 0] == np.float32(2.0) / np.float32(127.0)
+    assert Xs[0, 1] == np.float32(2.0 ** -6)
+
+
+def test_negative_control_other_roundings_fail_the_activation_golden():
+    """Round-half-away-from-zero and truncation are plausible mistakes; both
+    disagree with the hand-worked codes."""
+    x, codes = _read_act_fixture()
+    inv = np.array([63.5] * 32 + [64.0] * 32)
+    v = x * inv
+    away = np.sign(v) * np.floor(np.abs(v) + 0.5)
+    assert not np.array_equal(away.astype(np.int8), codes)
+    assert not np.array_equal(np.trunc(v).astype(np.int8), codes)
+
+
+def test_activation_quantization_error_is_half_a_step():
+    X = f16(np.random.default_rng(80).standard_normal((5, 256)) * 3.0)
+    Xq, Xs = oracle.quantize_x(X)
+    x = f16val(X)
+    step = np.repeat(Xs.astype(np.float64), 32, axis=1)
+    assert np.all(np.abs(Xq.astype(np.int64)) <= 127)
+    assert np.all(np.abs(x - Xq * step) <= 0.5 * step * (1 + 2.0 ** -20))
+    # each block's largest magnitude maps to +-127
+    amax = np.abs(x).reshape(5, 8, 32).max(axis=2)
+    assert np.array_equal(np.abs(Xq).reshape(5, 8, 32).max(axis=2), np.where(amax > 0, 127, 0))
+
+
+def test_activation_quantization_zero_block_and_power_of_two_scaling():
+    rng = np.random.default_rng(81)
+    x = rng.standard_normal((1, 64))
+    x[0, 32:] = 0.0
+    q1, s1 = oracle.quantize_x(f16(x))
+    q2, s2 = oracle.quantize_x(f16(x * 4.0))
+    assert np.all(q1[0, 32:] == 0) and s1[0, 1] == 0
+    assert np.array_equal(q1, q2) and np.array_equal(s2, s1 * 4)
+
+
+@pytest.mark.parametrize("bits,rank,zp", [(4, 0, (0, 15)), (4, 32, None), (8, 0, (120, 136)), (2, 32, (0, 3))])
+def test_q8x_reduces_to_fp16_product_when_x_is_on_the_grid(bits, rank, zp):
+    """X whose blocks are integers m in [-127, 127] (with |m| = 127 present)
+    times a power of two: quantization is exact (codes m, scale the power of
+    two), so the int8-activation product equals the FP16-activation product
+    bit for bit (every term and sum is exact in binary64)."""
+    M, K, N = 3, 128, 20
+    rng = np.random.default_rng(82 + bits + rank)
+    m = rng.integers(-127, 128, size=(M, K))
+    m[:, ::32] = 127 * rng.choice([-1, 1], size=(M, K // 32))
+    c = np.ldexp(1.0, rng.integers(-9, -5, size=(M, K // 32)))
+    X = f16(m * np.repeat(c, 32, axis=1))
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=83, zp_range=zp, rank=rank)
+    got = oracle.run_q8x(X, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, N, K, bits)
+    ref = oracle.run(X, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, N, K, bits)
+    Xq, Xs = oracle.quantize_x(X)
+    assert np.array_equal(Xq, m) and np.array_equal(Xs, c.astype(np.float32))
+    assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
