@@ -187,8 +187,10 @@ struct Adapter {
     bool q8;
 };
 
+// q8x: the int8-activation base (decode kernel for every M).
 int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const Adapter& ad,
-             int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
+             int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream,
+             bool q8x = false) {
     if (!h || batch < 0 || M < 0) return MNB_ERR_ARG;
     const mnb_desc& d = h->d;
     if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
@@ -233,6 +235,12 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
         if (rc != MNB_OK) return rc;
     }
     make_plan(d, batch, M, rank, sms, &p);
+    if (q8x && (p.route == MNB_ROUTE_GEMV || p.route == MNB_ROUTE_GEMM)) {
+        plan_gemv(d, Mt, sms, &p);  // integer dots on the decode kernel, 8-token tiles
+        p.tokens_per_cta = 8;
+        p.grid_y = cdiv(Mt, 8);
+        p.lora_kernel = rank > 0 ? 1 : 0;
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
 
@@ -300,7 +308,8 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
         a.sms = sms;
         a.w3d = 0;
         a.status = status;
-        e = mnb::gemv_launch(a, p, d.bits, pdl, st);
+        e = q8x ? mnb::gemv_q8x_launch(a, p, d.bits, pdl, st) : mnb::gemv_launch(a, p, d.bits, pdl, st);
+        if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
     } else {
         mnb::GemmArgs a;
         a.X = Xh;
@@ -350,6 +359,28 @@ int mnb_run_qlora(mnb_handle h, const void* X, const void* Wq, const void* scale
                   int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream) {
     return run_impl(h, X, Wq, scales, zp, Adapter{nullptr, nullptr, Aq, A_scales, A_zp, Bq, B_scales, B_zp, true},
                     rank, bias, Y, T_ws, batch, M, stream);
+}
+
+int mnb_run_q8x(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+                const void* B, int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M,
+                void* stream) {
+    return run_impl(h, X, Wq, scales, zp, Adapter{A, B, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, false},
+                    rank, bias, Y, T_ws, batch, M, stream, true);
+}
+
+int mnb_quantize_x(const void* X, int64_t Mt, int64_t K, void* Xq, void* Xs, void* stream) {
+    if (Mt < 0 || K < 0) return MNB_ERR_ARG;
+    if (K % 32 != 0) return MNB_ERR_UNSUPPORTED;
+    if (Mt > INT32_MAX || K > INT32_MAX / 2) return MNB_ERR_UNSUPPORTED;
+    if (Mt == 0 || K == 0) return MNB_OK;
+    if (!X || !Xq || !Xs) return MNB_ERR_ARG;
+    if (!aligned16(X) || !aligned16(Xq) || !aligned16(Xs)) return MNB_ERR_ALIGN;
+    int sms;
+    const int rc = device_setup(&sms);
+    if (rc != MNB_OK) return rc;
+    const cudaError_t e = mnb::quantize_x_launch(static_cast<const __half*>(X), (int)Mt, (int)K, static_cast<int8_t*>(Xq),
+                                                 static_cast<float*>(Xs), reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MNB_OK : MNB_ERR_CUDA;
 }
 
 int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32_t nproj, int64_t batch, int64_t M,

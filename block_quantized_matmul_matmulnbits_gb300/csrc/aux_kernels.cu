@@ -7,6 +7,8 @@
 //    so that graph replay rewrites the output).
 //  * lora_up: an empty packed weight with an adapter leaves only the adapter
 //    term, Y = T * Bt^T (+ bias), on the CUDA cores.
+//  * quantize_x: the int8-activation quantization of X on its own (the device
+//    function the int8-activation decode path stages X with), for checks.
 //  * dequant: the dequantization step on its own, W16 = fp16((q - zp) * scale),
 //    the DequantizeLinear weight map of "Fuse DQ->MatMulNBits for shared
 //    initializers and skip outer-scope weights" (onnxruntime PR 33800,
@@ -26,6 +28,25 @@ __global__ void fill_zero_kernel(uint4* __restrict__ y16, size_t n16, __half* __
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) y16[i] = make_uint4(0, 0, 0, 0);
     if (blockIdx.x == 0)
         for (size_t i = threadIdx.x; i < ntail; i += blockDim.x) tail[i] = __float2half_rn(0.f);
+}
+
+// One thread per (row, block of 32): codes in K order and the block scale.
+__global__ void quantize_x_kernel(const __half* __restrict__ X, int Mt, int K, int8_t* __restrict__ Xq,
+                                  float* __restrict__ Xs) {
+    const int nblk = K / 32;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)Mt * nblk) return;
+    const int m = (int)(i / nblk), b = (int)(i % nblk);
+    int q[32], sum;
+    Xs[i] = quantize_block32(X + (size_t)m * K + b * 32, q, sum);
+    uint32_t w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[j] = ((uint32_t)q[4 * j] & 0xFFu) | (((uint32_t)q[4 * j + 1] & 0xFFu) << 8) |
+               (((uint32_t)q[4 * j + 2] & 0xFFu) << 16) | (((uint32_t)q[4 * j + 3] & 0xFFu) << 24);
+    uint4* dst = reinterpret_cast<uint4*>(Xq + (size_t)m * K + b * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
 template <int BITS>
@@ -162,6 +183,13 @@ cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t 
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     fill_bias_kernel<<<(unsigned)blocks, 256, 0, st>>>(Y, bias, rows, N);
+    return cudaGetLastError();
+}
+
+cudaError_t quantize_x_launch(const __half* X, int Mt, int K, int8_t* Xq, float* Xs, cudaStream_t st) {
+    const long long total = (long long)Mt * (K / 32);
+    if (total == 0) return cudaSuccess;
+    quantize_x_kernel<<<(unsigned)((total + 127) / 128), 128, 0, st>>>(X, Mt, K, Xq, Xs);
     return cudaGetLastError();
 }
 

@@ -185,6 +185,55 @@ __device__ __forceinline__ void mma_16816(float d[4], uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D = A(16x32 u8, row) * B(32x8 s8, col), exact int32, C = 0: the integer dot
+// of the int8-activation path (weight codes unsigned, activation codes signed).
+__device__ __forceinline__ void mma_16832_u8s8(int d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
+
+// ---------------------------------------------------------------- int8 activations
+
+// One block of 32 activations to int8, every step in binary32 with one
+// rounding to nearest: amax = max |x|; amax == 0 gives codes 0 and scale 0;
+// else inv = 127 / amax, code = clamp(rint(x * inv), -127, 127) (ties to
+// even), scale = amax / 127.  `x` is 16-byte aligned; `q` receives the codes
+// in K order, the return value is the scale, `sum` the sum of the codes.
+__device__ __forceinline__ float quantize_block32(const __half* x, int q[32], int& sum) {
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(x) + j);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+            v[8 * j + 2 * i] = f.x;
+            v[8 * j + 2 * i + 1] = f.y;
+        }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    sum = 0;
+    if (amax == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) q[j] = 0;
+        return 0.f;
+    }
+    const float inv = __fdiv_rn(127.f, amax);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int c = __float2int_rn(__fmul_rn(v[j], inv));
+        q[j] = c > 127 ? 127 : (c < -127 ? -127 : c);
+        sum += q[j];
+    }
+    return __fdiv_rn(amax, 127.f);
+}
+
 // ---------------------------------------------------------------- launch ordering
 
 // Programmatic dependent launch: allow the next kernel on the stream to start.

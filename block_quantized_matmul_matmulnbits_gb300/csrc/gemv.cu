@@ -119,14 +119,34 @@ __device__ __forceinline__ uint32_t lds_u16(const unsigned char* sm, uint32_t of
 }
 __device__ __forceinline__ uint32_t lds_u8(const unsigned char* sm, uint32_t off) { return sm[off]; }
 
+// Int8-activation path: staged position p of a 32-code block holds the code
+// of K index q8x_perm<BITS>(p) within the block -- the order in which a thread
+// quad's share of the block comes out of the weight unpacking (thread t of a
+// quad owns codes 8t .. 8t+7; k-slots 4t..4t+3 and 16+4t..16+4t+3 of the
+// m16n8k32 fragment).
+template <int BITS>
+__host__ __device__ constexpr int q8x_perm(int p) {
+    return BITS == 8 ? p
+         : BITS == 4 ? 8 * ((p & 15) >> 2) + 2 * (p & 3) + (p >> 4)
+                     : 8 * ((p & 15) >> 2) + 2 * (p >> 4) + 4 * (p & 1) + ((p & 3) >> 1);
+}
+
+// Staged int8 X of one token tile: codes [tok][K + 16] (padded rows: the
+// B-operand loads of 8 token rows hit distinct banks), then per (token, block)
+// the binary32 scale and the code sum.
+__host__ __device__ inline uint32_t q8x_stage_bytes(int tok, int K) {
+    return (uint32_t)tok * ((uint32_t)K + 16u) + (uint32_t)tok * (uint32_t)(K / 32) * 8u;
+}
+
 // 3-D TMA descriptors of the projections' packed weights (multi-chunk stages).
 struct GemvMaps {
     CUtensorMap m[kMaxSeg];
 };
 
-template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC>
+template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC, bool Q8X>
 __global__ void __launch_bounds__(kThreadsGemv, OCC)
     gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
+    static_assert(!Q8X || (NT == 1 && XS), "the int8-activation path stages one 8-token tile");
     extern __shared__ __align__(1024) unsigned char sm[];
     constexpr int TOK = 8 * NT;
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
@@ -137,7 +157,8 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     const int CH = a.CH;                                  // K bytes per chunk
     const int nchunk = (rowbytes + CH - 1) / CH;
     const int ring = a.ring, rmask = a.ring - 1;
-    const GemvLayout L = gemv_layout(CH, nblk, TOK, ring, XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
+    const GemvLayout L =
+        gemv_layout(CH, nblk, TOK, ring, Q8X ? q8x_stage_bytes(TOK, a.K) : XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // groups [g_begin, g_end) of the row space of all projections
@@ -252,7 +273,38 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     const int ctid = threadIdx.x;  // 0..255
     if (a.x_wait) pdl_wait();  // X is produced by work queued before this kernel
     bool t_ready = a.rank == 0;
-    if (XS) {
+    if constexpr (Q8X) {
+        // X rows of this token group quantized to int8 per block of 32 (quantize_block32),
+        // codes stored in q8x_perm order; rows past Mt get scale 0 and sum 0
+        const uint32_t xp = (uint32_t)a.K + 16u;
+        float* xsc = reinterpret_cast<float*>(sm + L.x + TOK * xp);
+        int* xsum = reinterpret_cast<int*>(xsc + TOK * nblk);
+        const int mv = min(TOK, a.Mt - token0);
+        for (int i = ctid; i < TOK * nblk; i += kConsumerWarps * 32) {
+            const int row = i / nblk, b = i - row * nblk;
+            if (row >= mv) {
+                xsc[i] = 0.f;
+                xsum[i] = 0;
+                continue;
+            }
+            int qv[32], sum;
+            const float scale = quantize_block32(a.X + (size_t)(token0 + row) * a.K + b * 32, qv, sum);
+            uint32_t wd[8];
+#pragma unroll
+            for (int p4 = 0; p4 < 8; ++p4) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) w |= ((uint32_t)qv[q8x_perm<BITS>(4 * p4 + j)] & 0xFFu) << (8 * j);
+                wd[p4] = w;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(sm + L.x + (uint32_t)row * xp + (uint32_t)b * 32u);
+            dst[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            dst[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+            xsc[i] = scale;
+            xsum[i] = sum;
+        }
+        named_barrier_sync(1, kConsumerWarps * 32);
+    } else if (XS) {
         // X rows of this token group into shared memory, once; for INT4 each group
         // of 8 codes is stored in the pair-interleaved order (0,4,1,5,2,6,3,7) the
         // unpacking produces, so the inner loop needs no permutes.
@@ -333,6 +385,64 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
         const uint32_t z_al = ((uint32_t)ra * (uint32_t)nblk) & 15u;
         const bool vA = g < rows, vB = g + 8 < rows;
         const int kchunk = c * CH;
+        if constexpr (Q8X) {
+            // One 32-code block per warp step: quad thread t unpacks codes 8t..8t+7 of
+            // rows g and g+8 into u8 fragments, one m16n8k32 gives the exact int32 dot
+            // with the token rows' int8 codes, then y += sw * sx * (dot - zp * sum(xq)).
+            const uint32_t xp = (uint32_t)a.K + 16u;
+            const float* xsc = reinterpret_cast<const float*>(sm + L.x + TOK * xp);
+            const int* xsum = reinterpret_cast<const int*>(xsc + TOK * nblk);
+            const int bpc = CH / kBpb;
+            for (int bl = warp; ok && bl < bpc; bl += kConsumerWarps) {
+                const int kbyte = kchunk + bl * kBpb;
+                if (kbyte >= rowbytes) break;
+                const int blk = kbyte / kBpb;
+                const uint32_t wa = soff + L.w + (uint32_t)g * pitch + (uint32_t)(bl * kBpb);
+                uint32_t a0, a1, a2, a3;
+                if constexpr (BITS == 4) {
+                    const uint32_t u = *reinterpret_cast<const uint32_t*>(sm + wa + 4 * t);
+                    const uint32_t v = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 4 * t);
+                    a0 = u & 0x0F0F0F0Fu;
+                    a2 = (u >> 4) & 0x0F0F0F0Fu;
+                    a1 = v & 0x0F0F0F0Fu;
+                    a3 = (v >> 4) & 0x0F0F0F0Fu;
+                } else if constexpr (BITS == 8) {
+                    a0 = *reinterpret_cast<const uint32_t*>(sm + wa + 4 * t);
+                    a2 = *reinterpret_cast<const uint32_t*>(sm + wa + 16 + 4 * t);
+                    a1 = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 4 * t);
+                    a3 = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 16 + 4 * t);
+                } else {
+                    const uint32_t u = lds_u16(sm, wa + 2 * t), v = lds_u16(sm, wa + w_rowB + 2 * t);
+                    a0 = (u & 0x0303u) | (((u >> 2) & 0x0303u) << 16);
+                    a2 = ((u >> 4) & 0x0303u) | (((u >> 6) & 0x0303u) << 16);
+                    a1 = (v & 0x0303u) | (((v >> 2) & 0x0303u) << 16);
+                    a3 = ((v >> 4) & 0x0303u) | (((v >> 6) & 0x0303u) << 16);
+                }
+                const uint32_t so = soff + s_thr + s_al + (uint32_t)blk * 2u;
+                const uint32_t s0bits = lds_u16(sm, so), s8bits = lds_u16(sm, so + s_rowB);
+                const float swA = vA ? __half2float(__ushort_as_half((unsigned short)s0bits)) : 0.f;
+                const float swB = vB ? __half2float(__ushort_as_half((unsigned short)s8bits)) : 0.f;
+                int zA = (int)kDefaultZp, zB = (int)kDefaultZp;
+                if (HAS_ZP) {
+                    const uint32_t zo = soff + z_thr + z_al + (uint32_t)blk;
+                    zA = (int)lds_u8(sm, zo);
+                    zB = (int)lds_u8(sm, zo + z_rowB);
+                }
+                const uint32_t xo = L.x + (uint32_t)g * xp + (uint32_t)blk * 32u;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(sm + xo + 4 * t);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(sm + xo + 16 + 4 * t);
+                int d[4];
+                mma_16832_u8s8(d, a0, a1, a2, a3, b0, b1);
+                const int t0 = 2 * t;  // token rows of (d0, d2) and (d1, d3): t0, t0 + 1
+                const float sx0 = xsc[t0 * nblk + blk], sx1 = xsc[(t0 + 1) * nblk + blk];
+                const int q0 = xsum[t0 * nblk + blk], q1 = xsum[(t0 + 1) * nblk + blk];
+                float* ac = acc[0][0];
+                ac[0] = fmaf((float)(d[0] - zA * q0), swA * sx0, ac[0]);
+                ac[1] = fmaf((float)(d[1] - zA * q1), swA * sx1, ac[1]);
+                ac[2] = fmaf((float)(d[2] - zB * q0), swB * sx0, ac[2]);
+                ac[3] = fmaf((float)(d[3] - zB * q1), swB * sx1, ac[3]);
+            }
+        } else
         for (int p = warp; ok && p < npieces; p += kConsumerWarps) {
             const int kb = kchunk + p * 128 + t * 32;  // first byte of this thread's 32 in the row
             const uint32_t wpc = soff + w_thr + (uint32_t)p * 128u;
@@ -560,7 +670,8 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
         const int rr = ctid & (kGroup - 1), tok = ctid >> 4;
         const int token = token0 + tok;
         if (ok && tok < TOK && rr < rows && token < Mt) {
-            const int nw = min(kConsumerWarps, npieces);
+            // warps that held work: 128-byte pieces, or (int8 activations) whole blocks
+            const int nw = min(kConsumerWarps, Q8X ? CH / kBpb : npieces);
             float sum = 0.f;
             for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
             if (pj.bias) sum += __half2float(pj.bias[ra + rr]);
@@ -571,7 +682,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     }
 }
 
-template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC>
+template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC, bool Q8X = false>
 cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cudaStream_t st) {
     static_assert(NT == 1 || NT == 2, "token tiles");
     cudaLaunchConfig_t cfg = {};
@@ -598,7 +709,7 @@ cudaError_t launch_one(const GemvArgs& a, dim3 grid, size_t smem, bool pdl, cuda
         }
         b.w3d = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS, OCC>, maps, b);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<BITS, HAS_ZP, NT, XS, OCC, Q8X>, maps, b);
 }
 
 template <int BITS, bool HAS_ZP, int NT>
@@ -653,14 +764,17 @@ cudaError_t gemv_prepare() {
     cudaError_t e = tensor_map_prepare();
 #define MNB_SET(B, Z, T)                                                                                       \
     if (e == cudaSuccess)                                                                                      \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,  \
-                                 227 * 1024);                                                                  \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, false, 2, false>,                                        \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);                     \
     if (e == cudaSuccess)                                                                                      \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                 227 * 1024);                                                                  \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, T, true, 2, false>,                                         \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);                     \
     if (e == cudaSuccess && T == 1)                                                                            \
-        e = cudaFuncSetAttribute(gemv_kernel<B, Z, 1, true, 3>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                 227 * 1024);
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, 1, true, 3, false>,                                         \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);                     \
+    if (e == cudaSuccess && T == 1)                                                                            \
+        e = cudaFuncSetAttribute(gemv_kernel<B, Z, 1, true, 2, true>,                                          \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     MNB_SET(2, false, 1) MNB_SET(2, false, 2) MNB_SET(2, true, 1) MNB_SET(2, true, 2)
     MNB_SET(4, false, 1) MNB_SET(4, false, 2) MNB_SET(4, true, 1) MNB_SET(4, true, 2)
     MNB_SET(8, false, 1) MNB_SET(8, false, 2) MNB_SET(8, true, 1) MNB_SET(8, true, 2)
@@ -699,6 +813,32 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
                            : launch_xs<8, true, 2>(a, grid, smem, xs, occ, pdl, st);
     return nt == 1 ? launch_xs<8, false, 1>(a, grid, smem, xs, occ, pdl, st)
                    : launch_xs<8, false, 2>(a, grid, smem, xs, occ, pdl, st);
+}
+
+// The int8-activation decode path: one 8-token tile per CTA row of the grid,
+// X always staged (quantized) in shared memory.
+cudaError_t gemv_q8x_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st) {
+    GemvArgs a = a_in;
+    const int rowbytes = a.K * bits / 8;
+    const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
+    a.ring = gemv_ring(nstages, 2);
+    a.xrows = a.Mt < 8 ? a.Mt : 8;
+    size_t smem = gemv_layout(a.CH, a.K / 32, 8, a.ring, q8x_stage_bytes(8, a.K)).total;
+    if (smem > 227 * 1024 && a.ring > 2) {  // large K: the staged codes leave room for two stages
+        a.ring = 2;
+        smem = gemv_layout(a.CH, a.K / 32, 8, a.ring, q8x_stage_bytes(8, a.K)).total;
+    }
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    const dim3 grid(p.grid_x, p.grid_y);
+    const bool zp = a.seg[0].Z != nullptr;
+    if (bits == 2)
+        return zp ? launch_one<2, true, 1, true, 2, true>(a, grid, smem, pdl, st)
+                  : launch_one<2, false, 1, true, 2, true>(a, grid, smem, pdl, st);
+    if (bits == 4)
+        return zp ? launch_one<4, true, 1, true, 2, true>(a, grid, smem, pdl, st)
+                  : launch_one<4, false, 1, true, 2, true>(a, grid, smem, pdl, st);
+    return zp ? launch_one<8, true, 1, true, 2, true>(a, grid, smem, pdl, st)
+              : launch_one<8, false, 1, true, 2, true>(a, grid, smem, pdl, st);
 }
 
 }  // namespace mnb

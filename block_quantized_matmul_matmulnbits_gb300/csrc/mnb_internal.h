@@ -66,6 +66,9 @@ struct GemvArgs {
 size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* ctas, int* R, int* CH, int* tok, int* threads);
 cudaError_t gemv_prepare();
 cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st);
+// The int8-activation variant (X quantized per block of 32 while staged, integer block dots);
+// plan with 8 token rows per CTA.  cudaErrorNotSupported when K is too large to stage.
+cudaError_t gemv_q8x_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st);
 
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.
 cudaError_t lora_down_prepare();
@@ -105,6 +108,10 @@ cudaError_t lora_up_launch(const __half* T, const __half* B, const uint8_t* Bq, 
                            const __half* bias, __half* Y, int Mt, int N, cudaStream_t st);
 // Y[m, n] = bias[n] for m < rows (K == 0 or an empty weight, with a bias)
 cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st);
+
+// Xq[m, k] / Xs[m, k/32]: the int8 activation codes and binary32 block scales the
+// int8-activation path computes (same device function), codes in K order.
+cudaError_t quantize_x_launch(const __half* X, int Mt, int K, int8_t* Xq, float* Xs, cudaStream_t st);
 
 // W16[n, k] = fp16((q - zp) * scale) with the kernels' own dequant arithmetic.
 cudaError_t dequant_launch(const uint8_t* Wq, const __half* S, const uint8_t* Z, int N, int K, int bits,

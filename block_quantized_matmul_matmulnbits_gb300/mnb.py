@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_transpose_dq_weight", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_transpose_dq_weight", "mnb_run_q8x", "mnb_quantize_x", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -87,6 +87,10 @@ def lib() -> ctypes.CDLL:
             L.mnb_run_multi.restype = ctypes.c_int
             L.mnb_transpose_dq_weight.argtypes = [P, P, P, I64, I64, I32, I32, I32, P, P, P]
             L.mnb_transpose_dq_weight.restype = ctypes.c_int
+            L.mnb_run_q8x.argtypes = [P, P, P, P, P, P, P, I32, P, P, P, I64, I64, P]
+            L.mnb_run_q8x.restype = ctypes.c_int
+            L.mnb_quantize_x.argtypes = [P, I64, I64, P, P, P]
+            L.mnb_quantize_x.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -191,6 +195,15 @@ def mnb_transpose_dq_weight(w_q, w_scale, w_zp, bits: int, blocked: bool = True,
                                          1 if blocked else 0, addr(Wq), addr(scales), addr(zp)),
            "mnb_transpose_dq_weight")
     return Wq, scales, zp
+
+
+def mnb_run_q8x(h, X, Wq, scales, zp, A, B, rank: int, bias, Y, T_ws, batch: int, M: int, stream=None) -> None:
+    _check(lib().mnb_run_q8x(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
+                             _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run_q8x")
+
+
+def mnb_quantize_x(X, Mt: int, K: int, Xq, Xs, stream=None) -> None:
+    _check(lib().mnb_quantize_x(_ptr(X), Mt, K, _ptr(Xq), _ptr(Xs), _stream(stream)), "mnb_quantize_x")
 
 
 def mnb_run_noalloc(h, X, Wq, scales, zp, A, B, rank: int, Y, batch: int, M: int, stream=None) -> None:

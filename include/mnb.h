@@ -180,6 +180,30 @@ int mnb_run_qlora(mnb_handle h,
                   const void* bias, void* Y, void* T_ws,
                   int64_t batch, int64_t M, void* stream);
 
+/* mnb_run_bias with the int8-activation base ("accuracy level 4" of "[WebGPU]
+ * Fuse rank-32 quantized LoRA with MatMulNBits", Performance; its
+ * MatMulNBitsLoRA commit keeps "DP4A activation quantization for the base,
+ * with original FP16 X for T"):
+ *   per row of X and block of 32 along K, in binary32: amax = max |x|;
+ *   codes xq = clamp(rint(x * (127 / amax)), -127, 127), scale xs = amax / 127
+ *   (amax == 0: codes 0, scale 0);
+ *   Y = fp16(sum_b xs * scale_w * sum_{k in b} xq * (q - zp)  + T * B^T (+ bias))
+ * with the integer sums exact (u8 x s8 tensor-core dots) and T from the FP16
+ * X.  Runs on the decode kernel for every M (8 token rows per CTA); X is
+ * quantized while it is staged, no workspace.  Arguments, results and errors
+ * as mnb_run_bias; MNB_ERR_UNSUPPORTED also when K is too large to stage
+ * in shared memory (K above about 12,000). */
+int mnb_run_q8x(mnb_handle h,
+                const void* X, const void* Wq, const void* scales, const void* zp,
+                const void* A, const void* B, int32_t rank, const void* bias,
+                void* Y, void* T_ws,
+                int64_t batch, int64_t M, void* stream);
+
+/* The activation quantization of mnb_run_q8x on its own (same device
+ * function): X fp16 [Mt, K] -> Xq int8 [Mt, K] (K order), Xs float [Mt, K/32].
+ * Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED (K % 32), MNB_ERR_ALIGN, MNB_ERR_CUDA. */
+int mnb_quantize_x(const void* X, int64_t Mt, int64_t K, void* Xq, void* Xs, void* stream);
+
 /* One projection of mnb_run_multi (all pointers device, 16-byte aligned). */
 typedef struct {
     int64_t N;            /* output features of this projection (>= 0) */

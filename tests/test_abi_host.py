@@ -22,7 +22,7 @@ def built():
 def declared_symbols():
     text = open(os.path.join(ROOT, "include", "mnb.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mnb_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mnb_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_what_the_binding_wraps():
@@ -205,6 +205,10 @@ def test_multi_projection_validation_needs_no_device():
 
 def test_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
+    assert L.mnb_quantize_x(0x1000, 4, 48, 0x2000, 0x3000, None) == mnb.MNB_ERR_UNSUPPORTED
+    assert L.mnb_quantize_x(0x1000, 0, 64, 0x2000, 0x3000, None) == mnb.MNB_OK
+    assert L.mnb_quantize_x(0x1000, 4, 64, None, 0x3000, None) == mnb.MNB_ERR_ARG
+    assert L.mnb_quantize_x(0x1000, 4, 64, 0x2004, 0x3000, None) == mnb.MNB_ERR_ALIGN
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 48, 4, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
     assert L.mnb_dequant(0x1000, 0x2000, None, 4, 96, 2, 32, 0x3000, 0, None) == mnb.MNB_ERR_UNSUPPORTED
     assert L.mnb_dequant(0x1000, 0x2000, None, 0, 128, 2, 32, 0x3000, 1, None) == mnb.MNB_OK
