@@ -502,6 +502,178 @@ def run_sweep(args):
     return 0
 
 
+def run_next_rows(args):
+    """The rows beyond the core path, timed like the sweep (a graph of
+    back-to-back calls over input copies larger than 4x L2, median of 10
+    replays): FP16 vs INT8 adapters, int8 activations, 2-bit weights, a bias,
+    the fused QKV call against three separate calls, prefill with INT8
+    adapters.  GB/s counts every input byte once plus the output."""
+    import torch
+
+    from block_quantized_matmul_matmulnbits_gb300 import mnb, synth
+
+    torch.cuda.set_device(0)
+    mnb.lib()
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", 129 * 2 ** 20) or 129 * 2 ** 20
+    hbm_peak, bf16_peak, _, peak_src = load_peaks()
+
+    def dev(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.float16)).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def nb(*arrays):
+        return sum(int(a.nbytes) for a in arrays if a is not None)
+
+    def timed(tensors, nbytes, enqueue, handles, calls_per_graph):
+        """tensors: dict of device tensors (inputs), cloned into rotating copies;
+        enqueue(copy, i) issues call i."""
+        copies = max(2, min(64, math.ceil(4 * l2 / max(1, nbytes))))
+        cps = [{k: (None if v is None else v.clone()) for k, v in tensors.items()} for _ in range(copies)]
+        n = calls_per_graph
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            enqueue(cps[0], 0)
+        torch.cuda.current_stream().wait_stream(st)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                enqueue(cps[i % copies], i)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / n)
+        for h in handles:
+            if mnb.mnb_sync_status(h) != mnb.MNB_OK:
+                raise RuntimeError("device timeout")
+        return float(np.median(times))
+
+    rows = []
+    flt = getattr(args, "next_filter", None)
+
+    def want(workload):
+        return not flt or flt in workload
+
+    def report(workload, us, nbytes, flops=0.0, **extra):
+        r = {"workload": workload, "us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+             "hbm_frac": round(nbytes / us / 1e3 / hbm_peak, 4)}
+        if flops:
+            r["TFps"] = round(flops / us / 1e6, 2)
+            r["tensor_frac"] = round(flops / us / 1e6 / bf16_peak, 4)
+        r.update(extra)
+        rows.append(r)
+        print(json.dumps(r), flush=True)
+
+    def single(M, K, N, bits, zp, adapter, q8x=False, bias=False, seed=synth.SEED_BASE + 6, calls=200):
+        """adapter: None, 'fp16' or 'int8'."""
+        inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=seed, zp_range=zp, rank=32 if adapter == "fp16" else 0)
+        ql = synth.make_qlora(K=K, N=N, seed=seed) if adapter == "int8" else None
+        bvec = synth.make_bias(N, seed=seed) if bias else None
+        t = dict(X=dev(inp.X), Wq=dev(inp.Wq), S=dev(inp.scales), Z=dev(inp.zp), A=dev(inp.A), B=dev(inp.B),
+                 bias=dev(bvec))
+        if ql is not None:
+            t.update(Aq=dev(ql.Aq), As=dev(ql.A_scales), Az=dev(ql.A_zp), Bq=dev(ql.Bq), Bs=dev(ql.B_scales),
+                     Bz=dev(ql.B_zp))
+        nbytes = nb(inp.X, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, bvec) + M * N * 2
+        if ql is not None:
+            nbytes += nb(ql.Aq, ql.A_scales, ql.A_zp, ql.Bq, ql.B_scales, ql.B_zp)
+        Y = torch.empty((1, M, N), dtype=torch.float16, device="cuda")
+        T = torch.empty((M, 32), dtype=torch.float16, device="cuda") if adapter else None
+        h = mnb.mnb_create(N, K, bits, 32, 32, mnb.MODE_AUTO, 0, mnb.FLAG_EARLY_WEIGHTS)
+        try:
+            def enqueue(c, i):
+                if adapter == "int8":
+                    mnb.mnb_run_qlora(h, c["X"], c["Wq"], c["S"], c["Z"], c["Aq"], c["As"], c["Az"], c["Bq"], c["Bs"],
+                                      c["Bz"], 32, c["bias"], Y, T, 1, M)
+                elif q8x:
+                    mnb.mnb_run_q8x(h, c["X"], c["Wq"], c["S"], c["Z"], c["A"], c["B"], 32 if adapter else 0,
+                                    c["bias"], Y, T, 1, M)
+                else:
+                    mnb.mnb_run_bias(h, c["X"], c["Wq"], c["S"], c["Z"], c["A"], c["B"], 32 if adapter else 0,
+                                     c["bias"], Y, T, 1, M)
+            us = timed(t, nbytes, enqueue, [h], calls)
+            route = {1: "gemv", 2: "gemm"}.get(mnb.mnb_last_route(h), "?")
+        finally:
+            mnb.mnb_destroy(h)
+        return us, nbytes, prefill_flops(M, K, N, 32 if adapter else 0), route
+
+    K = 4096
+    for name, kw in (("INT4 zp, no adapter", dict(adapter=None)),
+                     ("INT4 zp, FP16 rank-32 adapter", dict(adapter="fp16")),
+                     ("INT4 zp, INT8 rank-32 adapter", dict(adapter="int8")),
+                     ("INT4 zp, bias, no adapter", dict(adapter=None, bias=True)),
+                     ("INT4 zp, int8 activations, no adapter", dict(adapter=None, q8x=True)),
+                     ("INT4 zp, int8 activations, FP16 adapter", dict(adapter="fp16", q8x=True))):
+        if want(f"M=1 K=4096 N=4096 {name}"):
+            us, nbytes, _, route = single(1, K, 4096, 4, (0, 15), **kw)
+            report(f"M=1 K=4096 N=4096 {name}", us, nbytes, route=route)
+    if want("M=1 K=4096 N=4096 INT2 zp, no adapter"):
+        us, nbytes, _, route = single(1, K, 4096, 2, (0, 3), None)
+        report("M=1 K=4096 N=4096 INT2 zp, no adapter", us, nbytes, route=route)
+    for bits, q8x in ((4, False), (4, True), (2, False), (8, False)):
+        name = f"M=1 K=4096 N=14336 INT{bits}{' int8 activations' if q8x else ''}"
+        if want(name):
+            us, nbytes, _, route = single(1, K, 14336, bits, None, None, q8x=q8x)
+            report(name, us, nbytes, route=route)
+    for M in (4, 16, 64):
+        name = f"M={M} K=4096 N=14336 INT4 int8 activations"
+        if want(name):
+            us, nbytes, fl, route = single(M, K, 14336, 4, None, None, q8x=True, calls=100)
+            report(name, us, nbytes, fl, route=route)
+    for adapter in ("fp16", "int8"):
+        name = f"M=1024 K=4096 N=4096 INT4, {adapter.upper()} rank-32 adapter"
+        if want(name):
+            us, nbytes, fl, route = single(1024, K, 4096, 4, None, adapter, seed=synth.SEED_BASE + 2, calls=20)
+            report(name, us, nbytes, fl, route=route)
+
+    # fused QKV (grouped-query shapes) against three separate calls
+    for M in (1, 4):
+        if not want(f"QKV M={M}"):
+            continue
+        Ns = (4096, 1024, 1024)
+        inps = [synth.make_inputs(M=M, K=K, N=n, bits=4, seed=synth.SEED_BASE + 7 + i, zp_range=(0, 15))
+                for i, n in enumerate(Ns)]
+        t = {"X": dev(inps[0].X)}
+        for i, inp in enumerate(inps):
+            t.update({f"Wq{i}": dev(inp.Wq), f"S{i}": dev(inp.scales), f"Z{i}": dev(inp.zp)})
+        Ys = [torch.empty((1, M, n), dtype=torch.float16, device="cuda") for n in Ns]
+        nbytes = nb(inps[0].X, *[a for inp in inps for a in (inp.Wq, inp.scales, inp.zp)]) + M * sum(Ns) * 2
+        hf = mnb.mnb_create(sum(Ns), K, 4, 32, 0, mnb.MODE_AUTO, 0, mnb.FLAG_EARLY_WEIGHTS)
+        hs = [mnb.mnb_create(n, K, 4, 32, 0, mnb.MODE_AUTO, 0, mnb.FLAG_EARLY_WEIGHTS) for n in Ns]
+        try:
+            def fused(c, i):
+                mnb.mnb_run_multi(hf, c["X"], [(n, c[f"Wq{j}"], c[f"S{j}"], c[f"Z{j}"], None, Ys[j])
+                                               for j, n in enumerate(Ns)], 1, M)
+
+            def separate(c, i):
+                for j in range(3):
+                    mnb.mnb_run(hs[j], c["X"], c[f"Wq{j}"], c[f"S{j}"], c[f"Z{j}"], None, None, 0, Ys[j], None, 1, M)
+            us_f = timed(t, nbytes, fused, [hf], 200)
+            us_s = timed(t, nbytes, separate, hs, 200)
+        finally:
+            mnb.mnb_destroy(hf)
+            for h in hs:
+                mnb.mnb_destroy(h)
+        report(f"QKV M={M} K=4096 N=4096+1024+1024 INT4 zp, one mnb_run_multi", us_f, nbytes, launches=1)
+        report(f"QKV M={M} K=4096 N=4096+1024+1024 INT4 zp, three mnb_run", us_s, nbytes, launches=3)
+    print(json.dumps({"sweep": "rows beyond the core path", "peaks": {"hbm_GBps": hbm_peak, "tensor_TFps": bf16_peak,
+                                                                     "source": peak_src}, "rows": len(rows)}),
+          flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 
 def oracle_decode_sample(target_s):
@@ -583,9 +755,16 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the lm_head shapes and the M sweep at K=4096, N=14336 "
                          "(both routes), one JSON line per point")
+    ap.add_argument("--sweep-next", action="store_true",
+                    help="instead of the bench line: the rows beyond the core path (adapter formats, int8 "
+                         "activations, 2-bit weights, bias, fused QKV), one JSON line per point")
+    ap.add_argument("--next-filter", default=None,
+                    help="with --sweep-next: only the workloads whose name contains this text")
     args = ap.parse_args(argv)
     if args.sweep:
         return run_sweep(args)
+    if args.sweep_next:
+        return run_next_rows(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

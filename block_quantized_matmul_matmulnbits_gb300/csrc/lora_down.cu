@@ -107,21 +107,36 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         if constexpr (Q8) {
             // 16 codes of one rank row per item (a 16-code piece never straddles a block):
             // exact (q - zp), one rounding by the scale, the base kernels' arithmetic
-            const int pc = klen / 16, nblk = K / 32;
-            for (int idx = tid; idx < 32 * pc; idx += blockDim.x) {
-                const int r = idx / pc, c = idx - r * pc;
-                const int k = kb + c * 16;
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(W.Aq + (size_t)r * K + k));
-                const int b = r * nblk + k / 32;
-                const DqConst dc = dq_const(W.Az ? (uint32_t)W.Az[b] : 128u, reinterpret_cast<const uint16_t*>(W.As)[b]);
-                uint32_t d[8];
-                dq_int8_natural(v.x, dc, &d[0]);
-                dq_int8_natural(v.y, dc, &d[2]);
-                dq_int8_natural(v.z, dc, &d[4]);
-                dq_int8_natural(v.w, dc, &d[6]);
-                uint4* dst = reinterpret_cast<uint4*>(&As[r * kPitchR + c * 16]);
-                dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
-                dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+            // items of 16 codes, kBatch per thread in flight: all loads first, then the dequant
+            constexpr int kBatch = 8;
+            const int pc = klen / 16, nblk = K / 32, items = 32 * pc;
+            for (int base = 0; base < items; base += kBatch * 128) {
+                uint4 v[kBatch];
+                uint32_t sc[kBatch], zz[kBatch];
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = min(base + j * 128 + tid, items - 1);  // clamped: loads stay in bounds
+                    const int r = idx / pc, c = idx - r * pc;
+                    const int k = kb + c * 16, b = r * nblk + k / 32;
+                    v[j] = __ldg(reinterpret_cast<const uint4*>(W.Aq + (size_t)r * K + k));
+                    sc[j] = reinterpret_cast<const uint16_t*>(W.As)[b];
+                    zz[j] = W.Az ? (uint32_t)W.Az[b] : 128u;
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = base + j * 128 + tid;
+                    if (idx >= items) break;
+                    const int r = idx / pc, c = idx - r * pc;
+                    const DqConst dc = dq_const(zz[j], (uint16_t)sc[j]);
+                    uint32_t d[8];
+                    dq_int8_natural(v[j].x, dc, &d[0]);
+                    dq_int8_natural(v[j].y, dc, &d[2]);
+                    dq_int8_natural(v[j].z, dc, &d[4]);
+                    dq_int8_natural(v[j].w, dc, &d[6]);
+                    uint4* dst = reinterpret_cast<uint4*>(&As[r * kPitchR + c * 16]);
+                    dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+                    dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+                }
             }
         } else {
             for (int idx = tid; idx < klen * 4; idx += blockDim.x) {
