@@ -131,6 +131,30 @@ __host__ __device__ constexpr int q8x_perm(int p) {
                      : 8 * ((p & 15) >> 2) + 2 * (p >> 4) + 4 * (p & 1) + ((p & 3) >> 1);
 }
 
+// 4 x 4 transpose of 32-bit words across the lanes of a thread quad (t = lane & 3):
+// on return w[j] holds word t of quad lane j's input.  Four shuffles.
+__device__ __forceinline__ void quad_transpose(uint32_t w[4], int t) {
+    const bool o = (t & 1) != 0, hi = (t & 2) != 0;
+    const uint32_t a = __shfl_xor_sync(0xffffffffu, o ? w[0] : w[1], 1);
+    const uint32_t b = __shfl_xor_sync(0xffffffffu, o ? w[2] : w[3], 1);
+    if (o) {
+        w[0] = a;
+        w[2] = b;
+    } else {
+        w[1] = a;
+        w[3] = b;
+    }
+    const uint32_t c = __shfl_xor_sync(0xffffffffu, hi ? w[0] : w[2], 2);
+    const uint32_t d = __shfl_xor_sync(0xffffffffu, hi ? w[1] : w[3], 2);
+    if (hi) {
+        w[0] = c;
+        w[1] = d;
+    } else {
+        w[2] = c;
+        w[3] = d;
+    }
+}
+
 // Staged int8 X of one token tile: codes [tok][K + 16] (padded rows: the
 // B-operand loads of 8 token rows hit distinct banks), then per (token, block)
 // the binary32 scale and the code sum.
@@ -392,32 +416,8 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
             const uint32_t xp = (uint32_t)a.K + 16u;
             const float* xsc = reinterpret_cast<const float*>(sm + L.x + TOK * xp);
             const int* xsum = reinterpret_cast<const int*>(xsc + TOK * nblk);
-            const int bpc = CH / kBpb;
-            for (int bl = warp; ok && bl < bpc; bl += kConsumerWarps) {
-                const int kbyte = kchunk + bl * kBpb;
-                if (kbyte >= rowbytes) break;
-                const int blk = kbyte / kBpb;
-                const uint32_t wa = soff + L.w + (uint32_t)g * pitch + (uint32_t)(bl * kBpb);
-                uint32_t a0, a1, a2, a3;
-                if constexpr (BITS == 4) {
-                    const uint32_t u = *reinterpret_cast<const uint32_t*>(sm + wa + 4 * t);
-                    const uint32_t v = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 4 * t);
-                    a0 = u & 0x0F0F0F0Fu;
-                    a2 = (u >> 4) & 0x0F0F0F0Fu;
-                    a1 = v & 0x0F0F0F0Fu;
-                    a3 = (v >> 4) & 0x0F0F0F0Fu;
-                } else if constexpr (BITS == 8) {
-                    a0 = *reinterpret_cast<const uint32_t*>(sm + wa + 4 * t);
-                    a2 = *reinterpret_cast<const uint32_t*>(sm + wa + 16 + 4 * t);
-                    a1 = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 4 * t);
-                    a3 = *reinterpret_cast<const uint32_t*>(sm + wa + w_rowB + 16 + 4 * t);
-                } else {
-                    const uint32_t u = lds_u16(sm, wa + 2 * t), v = lds_u16(sm, wa + w_rowB + 2 * t);
-                    a0 = (u & 0x0303u) | (((u >> 2) & 0x0303u) << 16);
-                    a2 = ((u >> 4) & 0x0303u) | (((u >> 6) & 0x0303u) << 16);
-                    a1 = (v & 0x0303u) | (((v >> 2) & 0x0303u) << 16);
-                    a3 = ((v >> 4) & 0x0303u) | (((v >> 6) & 0x0303u) << 16);
-                }
+            // per block: the int32 dot and its scaling into the accumulators
+            auto block_dot = [&](int blk, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
                 const uint32_t so = soff + s_thr + s_al + (uint32_t)blk * 2u;
                 const uint32_t s0bits = lds_u16(sm, so), s8bits = lds_u16(sm, so + s_rowB);
                 const float swA = vA ? __half2float(__ushort_as_half((unsigned short)s0bits)) : 0.f;
@@ -441,6 +441,62 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 ac[1] = fmaf((float)(d[1] - zA * q1), swA * sx1, ac[1]);
                 ac[2] = fmaf((float)(d[2] - zB * q0), swB * sx0, ac[2]);
                 ac[3] = fmaf((float)(d[3] - zB * q1), swB * sx1, ac[3]);
+            };
+            if constexpr (BITS != 2) {
+                // 128 bytes of rows g and g+8 per warp step: each lane loads 16 bytes from
+                // either 64-byte half (even rows the first half first, odd rows the second:
+                // every load instruction covers all 32 banks), then a quad transpose gives
+                // lane t word t of each 16-byte chunk -- its share of the fragment.
+                for (int sp = warp; ok && sp < npieces; sp += kConsumerWarps) {
+                    const int kseg = kchunk + sp * 128;
+                    if (kseg >= rowbytes) break;
+                    const uint32_t odd = (uint32_t)(g & 1);
+                    const uint32_t rA = soff + L.w + (uint32_t)g * pitch + (uint32_t)sp * 128u + 16u * (uint32_t)t;
+                    const uint4 l0 = lds128(sm, rA + 64u * odd), l1 = lds128(sm, rA + 64u * (1u - odd));
+                    const uint4 l2 = lds128(sm, rA + w_rowB + 64u * odd), l3 = lds128(sm, rA + w_rowB + 64u * (1u - odd));
+                    const uint4 pA = odd ? l1 : l0, qA = odd ? l0 : l1, pB = odd ? l3 : l2, qB = odd ? l2 : l3;
+                    uint32_t PA[4] = {pA.x, pA.y, pA.z, pA.w}, QA[4] = {qA.x, qA.y, qA.z, qA.w};
+                    uint32_t PB[4] = {pB.x, pB.y, pB.z, pB.w}, QB[4] = {qB.x, qB.y, qB.z, qB.w};
+                    quad_transpose(PA, t);
+                    quad_transpose(QA, t);
+                    quad_transpose(PB, t);
+                    quad_transpose(QB, t);
+                    if constexpr (BITS == 4) {  // 16-byte blocks: chunk j is block j
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int kbyte = kseg + 16 * j;
+                            if (kbyte >= rowbytes) break;
+                            const uint32_t u = j < 4 ? PA[j & 3] : QA[j & 3], v = j < 4 ? PB[j & 3] : QB[j & 3];
+                            block_dot(kbyte / kBpb, u & 0x0F0F0F0Fu, v & 0x0F0F0F0Fu, (u >> 4) & 0x0F0F0F0Fu,
+                                      (v >> 4) & 0x0F0F0F0Fu);
+                        }
+                    } else {  // 32-byte blocks: chunks 2j, 2j+1 are block j
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int kbyte = kseg + 32 * j;
+                            if (kbyte >= rowbytes) break;
+                            const uint32_t a0 = j < 2 ? PA[(2 * j) & 3] : QA[(2 * j) & 3];
+                            const uint32_t a2 = j < 2 ? PA[(2 * j + 1) & 3] : QA[(2 * j + 1) & 3];
+                            const uint32_t a1 = j < 2 ? PB[(2 * j) & 3] : QB[(2 * j) & 3];
+                            const uint32_t a3 = j < 2 ? PB[(2 * j + 1) & 3] : QB[(2 * j + 1) & 3];
+                            block_dot(kbyte / kBpb, a0, a1, a2, a3);
+                        }
+                    }
+                }
+            } else {
+            // INT2 (8-byte blocks): one block per warp step, each thread's 2 bytes of
+            // rows g and g+8 loaded directly
+            const int bpc = CH / kBpb;
+            for (int bl = warp; ok && bl < bpc; bl += kConsumerWarps) {
+                const int kbyte = kchunk + bl * kBpb;
+                if (kbyte >= rowbytes) break;
+                const uint32_t wa = soff + L.w + (uint32_t)g * pitch + (uint32_t)(bl * kBpb);
+                const uint32_t u = lds_u16(sm, wa + 2 * t), v = lds_u16(sm, wa + w_rowB + 2 * t);
+                block_dot(kbyte / kBpb, (u & 0x0303u) | (((u >> 2) & 0x0303u) << 16),
+                          (v & 0x0303u) | (((v >> 2) & 0x0303u) << 16),
+                          ((u >> 4) & 0x0303u) | (((u >> 6) & 0x0303u) << 16),
+                          ((v >> 4) & 0x0303u) | (((v >> 6) & 0x0303u) << 16));
+            }
             }
         } else
         for (int p = warp; ok && p < npieces; p += kConsumerWarps) {
@@ -671,7 +727,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
         const int token = token0 + tok;
         if (ok && tok < TOK && rr < rows && token < Mt) {
             // warps that held work: 128-byte pieces, or (int8 activations) whole blocks
-            const int nw = min(kConsumerWarps, Q8X ? CH / kBpb : npieces);
+            const int nw = min(kConsumerWarps, Q8X && BITS == 2 ? CH / kBpb : npieces);
             float sum = 0.f;
             for (int w = 0; w < nw; ++w) sum += redq[((size_t)w * kGroup + rr) * TOK + tok];  // fixed warp order
             if (pj.bias) sum += __half2float(pj.bias[ra + rr]);

@@ -62,6 +62,8 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 
 constexpr int kPitchR = kPiece + 8;  // halfs per staged rank row of a dequantized INT8 A slice
 static_assert(32 * kPitchR <= kPiece * kPitchA, "the INT8 A slice reuses the FP16 A slice's space");
+static_assert(16 * kPitchX * 2 + 32 * kPiece <= kTok * kPitchX * 2, "raw INT8 A fits the X tile's unused rows");
+static_assert(32 * (kPiece / 16) <= 8 * 128, "a pass's INT8 A items fit eight per thread");
 
 // The down weight in one of two formats: FP16 A [K, 32], or INT8 Aq [32, K]
 // (block-32 rows along K) with FP16 scales As and zero points Az [32, K/32].
@@ -104,12 +106,30 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
     for (int kb = 16 * c0; kb < 16 * c1; kb += kPiece) {
         const int klen = min(kPiece, 16 * c1 - kb);
         // A (a weight) first, then X once the producer of X has finished.
+        // INT8 A, few token rows: raw codes go through cp.async into the unused rows of
+        // the X tile (in flight together with X), their block scales and zero points into
+        // registers; the dequant runs shared-to-shared once both have landed.
+        constexpr int kBatch = 8;  // 16-code items per thread and pass: 32 ranks x 512 / 16 / 128
+        uint32_t qsc[kBatch], qzz[kBatch];
+        unsigned char* raw = reinterpret_cast<unsigned char*>(Xs + 16 * kPitchX);  // [32][klen] bytes
+        const bool q8_async = Q8 && few;
         if constexpr (Q8) {
-            // 16 codes of one rank row per item (a 16-code piece never straddles a block):
-            // exact (q - zp), one rounding by the scale, the base kernels' arithmetic
-            // items of 16 codes, kBatch per thread in flight: all loads first, then the dequant
-            constexpr int kBatch = 8;
             const int pc = klen / 16, nblk = K / 32, items = 32 * pc;
+            if (few) {
+                for (int idx = tid; idx < items; idx += blockDim.x) {
+                    const int r = idx / pc, c = idx - r * pc;
+                    cp_async16(smem_u32(raw + r * klen + c * 16), W.Aq + (size_t)r * K + kb + c * 16, 16);
+                }
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    const int idx = min(j * 128 + tid, items - 1);  // clamped: loads stay in bounds
+                    const int r = idx / pc, b = r * nblk + (kb + (idx - r * pc) * 16) / 32;
+                    qsc[j] = reinterpret_cast<const uint16_t*>(W.As)[b];
+                    qzz[j] = W.Az ? (uint32_t)W.Az[b] : 128u;
+                }
+            } else {
+            // many token rows: 16 codes of one rank row per item, kBatch per thread in
+            // flight (all loads first, then the dequant)
             for (int base = 0; base < items; base += kBatch * 128) {
                 uint4 v[kBatch];
                 uint32_t sc[kBatch], zz[kBatch];
@@ -138,6 +158,7 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
                     dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
                 }
             }
+            }
         } else {
             for (int idx = tid; idx < klen * 4; idx += blockDim.x) {
                 const int row = idx >> 2, c = idx & 3;
@@ -158,6 +179,26 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
         }
         cp_async_wait_all();
         __syncthreads();
+        if (q8_async) {  // raw INT8 codes -> the rank-major FP16 tile (exact q - zp, one rounding)
+            const int pc = klen / 16, items = 32 * pc;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int idx = j * 128 + tid;
+                if (idx >= items) break;
+                const int r = idx / pc, c = idx - r * pc;
+                const uint4 v = *reinterpret_cast<const uint4*>(raw + r * klen + c * 16);
+                const DqConst dc = dq_const(qzz[j], (uint16_t)qsc[j]);
+                uint32_t d[8];
+                dq_int8_natural(v.x, dc, &d[0]);
+                dq_int8_natural(v.y, dc, &d[2]);
+                dq_int8_natural(v.z, dc, &d[4]);
+                dq_int8_natural(v.w, dc, &d[6]);
+                uint4* dst = reinterpret_cast<uint4*>(&As[r * kPitchR + c * 16]);
+                dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+                dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+            }
+            __syncthreads();
+        }
         const int mat = lane >> 3, row8 = lane & 7;
         for (int kk = few ? 16 * warp : 0; kk < klen; kk += few ? 64 : 16) {
             // A operand: X rows wrow .. +15, K columns kk .. kk+15 (row-major 16x16)
