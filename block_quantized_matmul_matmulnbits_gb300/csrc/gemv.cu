@@ -55,7 +55,9 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreadsGemv = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kMaxRing = 4;                                // ring stages (2 or 4)
-constexpr uint32_t kXStageMax = 24 * 1024;                 // largest X tile staged in shared memory
+constexpr uint32_t kXStageMax = 64 * 1024;                 // largest X tile staged in shared memory
+constexpr uint32_t kXStageSmall = 24 * 1024;               // X tiles this small leave room for 3 CTAs per SM
+constexpr uint32_t kTwoPerSm = 113 * 1024;                 // shared memory of a CTA when two share an SM
 constexpr int kGroup = 16;                                 // rows per stage / MMA tile
 constexpr int kMaxChunk = 1024;                            // K bytes per row and stage
 // Inside a stage's adapter region (1 KB: 16 FP16 rows of B, or 16 INT8 rows of
@@ -70,6 +72,10 @@ struct GemvLayout {
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Bytes per staged FP16 X row: 16 bytes of padding put the eight token rows a
+// thread quad column reads in distinct banks.
+__host__ __device__ inline uint32_t xs_pitch(int K) { return (uint32_t)K * 2u + 16u; }
 
 // Shared-memory layout, identical on host and device.  `ch` = K bytes per chunk,
 // `ring` = stages (2 or 4), `xbytes` = staged X (0 when X is read from global).
@@ -96,13 +102,20 @@ __host__ __device__ inline GemvLayout gemv_layout(int ch, int nblk, int tok, int
 // single-token-tile one with X staged (it then fits 72 registers without
 // spilling and a two-stage ring in a third of the shared memory), two
 // otherwise (96 registers: more independent work per thread).
-inline int gemv_ctas_per_sm(int N, int nt, bool xs, int sms) {
-    return nt == 1 && xs && (N + kGroup - 1) / kGroup > 2 * sms ? 3 : 2;
+inline int gemv_ctas_per_sm(int N, int nt, uint32_t xbytes, int sms) {
+    return nt == 1 && xbytes > 0 && xbytes <= kXStageSmall && (N + kGroup - 1) / kGroup > 2 * sms ? 3 : 2;
 }
 
 // Ring stages: two when three CTAs share an SM (they still keep 96 KB of
 // weights in flight per SM) or when a CTA has at most two stages, else four.
 inline int gemv_ring(int nstages, int occ) { return nstages <= 2 || occ == 3 ? 2 : kMaxRing; }
+
+// The ring for a CTA: two stages as well when four would not leave room for two
+// CTAs per SM next to a large staged X tile.
+inline int gemv_pick_ring(int ch, int nblk, int tok, int nstages, int occ, uint32_t xbytes) {
+    const int ring = gemv_ring(nstages, occ);
+    return ring > 2 && gemv_layout(ch, nblk, tok, ring, xbytes).total > kTwoPerSm ? 2 : ring;
+}
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -182,7 +195,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
     const int nchunk = (rowbytes + CH - 1) / CH;
     const int ring = a.ring, rmask = a.ring - 1;
     const GemvLayout L =
-        gemv_layout(CH, nblk, TOK, ring, Q8X ? q8x_stage_bytes(TOK, a.K) : XS ? (uint32_t)a.xrows * a.K * 2u : 0u);
+        gemv_layout(CH, nblk, TOK, ring, Q8X ? q8x_stage_bytes(TOK, a.K) : XS ? (uint32_t)a.xrows * xs_pitch(a.K) : 0u);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // groups [g_begin, g_end) of the row space of all projections
@@ -343,7 +356,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 uint32_t xw[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) xw[j] = prmt(word_of(v0, j >> 1), word_of(v1, j >> 1), (j & 1) ? 0x7632u : 0x5410u);
-                uint4* dst = reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c16 * 16u) * 2u);
+                uint4* dst = reinterpret_cast<uint4*>(sm + L.x + (uint32_t)row * xs_pitch(a.K) + (uint32_t)c16 * 32u);
                 dst[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
                 dst[1] = make_uint4(xw[4], xw[5], xw[6], xw[7]);
             }
@@ -355,7 +368,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                 if (BITS == 4)
                     v = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
                                    prmt(v.y, v.w, 0x7632u));
-                *reinterpret_cast<uint4*>(sm + L.x + ((uint32_t)row * a.K + (uint32_t)c8 * 8u) * 2u) = v;
+                *reinterpret_cast<uint4*>(sm + L.x + (uint32_t)row * xs_pitch(a.K) + (uint32_t)c8 * 16u) = v;
             }
         }
         named_barrier_sync(1, kConsumerWarps * 32);
@@ -542,7 +555,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                                 uint32_t xw[8];
                                 if (XS) {
                                     if (use) {
-                                        const uint32_t xo = L.x + ((uint32_t)(nt * 8 + g) * a.K + (uint32_t)(kx + 16 * w)) * 2u;
+                                        const uint32_t xo = L.x + (uint32_t)(nt * 8 + g) * xs_pitch(a.K) + (uint32_t)(kx + 16 * w) * 2u;
                                         v0 = lds128(sm, xo);
                                         v1 = lds128(sm, xo + 16u);
                                     }
@@ -582,7 +595,7 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
                     for (int w = 0; w < kXv; ++w) {
                         uint4 v = make_uint4(0, 0, 0, 0);
                         if (XS) {
-                            if (use) v = lds128(sm, L.x + ((uint32_t)(nt * 8 + g) * a.K + (uint32_t)kx) * 2u + 16u * w);
+                            if (use) v = lds128(sm, L.x + (uint32_t)(nt * 8 + g) * xs_pitch(a.K) + (uint32_t)kx * 2u + 16u * w);
                         } else {
                             if (use) v = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + kx) + w);  // predicated
                         }
@@ -783,9 +796,10 @@ size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* ctas_out, int
                      int* threads) {
     const int tok = Mt <= 8 ? 8 : 16;
     const uint32_t xrows = (uint32_t)(Mt < tok ? Mt : tok);  // X rows one CTA stages
-    const bool xs = xrows * K * 2u <= kXStageMax;
+    const bool xs = xrows * xs_pitch(K) <= kXStageMax;
+    const uint32_t xbytes = xs ? xrows * xs_pitch(K) : 0u;
     // two or three CTAs per SM, but at least one 16-row group per CTA
-    const int occ = gemv_ctas_per_sm(N, tok / 8, xs, sms > 0 ? sms : 1);
+    const int occ = gemv_ctas_per_sm(N, tok / 8, xbytes, sms > 0 ? sms : 1);
     int ctas = occ * (sms > 0 ? sms : 1);
     if (ctas > (N + kGroup - 1) / kGroup) ctas = (N + kGroup - 1) / kGroup;
     if (ctas < 1) ctas = 1;
@@ -813,7 +827,7 @@ size_t gemv_geometry(int N, int K, int bits, int Mt, int sms, int* ctas_out, int
     *tok_out = tok;
     *threads = kThreadsGemv;
     const int nstages = (R + kGroup - 1) / kGroup * ((rowbytes + CH - 1) / CH);
-    return gemv_layout(CH, nblk, tok, gemv_ring(nstages, occ), xs ? xrows * K * 2u : 0u).total;
+    return gemv_layout(CH, nblk, tok, gemv_pick_ring(CH, nblk, tok, nstages, occ, xbytes), xbytes).total;
 }
 
 cudaError_t gemv_prepare() {
@@ -844,11 +858,12 @@ cudaError_t gemv_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bits, 
     const int rowbytes = a.K * bits / 8;
     const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
     const uint32_t xrows = (uint32_t)(a.Mt < tok ? a.Mt : tok);
-    const bool xs = xrows * a.K * 2u <= kXStageMax;
-    const int occ = gemv_ctas_per_sm(a.G * kGroup, tok / 8, xs, a.sms > 0 ? a.sms : 1);
-    a.ring = gemv_ring(nstages, occ);
+    const bool xs = xrows * xs_pitch(a.K) <= kXStageMax;
+    const uint32_t xbytes = xs ? xrows * xs_pitch(a.K) : 0u;
+    const int occ = gemv_ctas_per_sm(a.G * kGroup, tok / 8, xbytes, a.sms > 0 ? a.sms : 1);
+    a.ring = gemv_pick_ring(a.CH, a.K / 32, tok, nstages, occ, xbytes);
     a.xrows = xs ? (int)xrows : 0;
-    const size_t smem = gemv_layout(a.CH, a.K / 32, tok, a.ring, xs ? xrows * a.K * 2u : 0u).total;
+    const size_t smem = gemv_layout(a.CH, a.K / 32, tok, a.ring, xbytes).total;
     if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
     const dim3 grid(p.grid_x, p.grid_y);
     const bool zp = a.seg[0].Z != nullptr;
