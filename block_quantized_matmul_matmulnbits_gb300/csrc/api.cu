@@ -368,6 +368,18 @@ int mnb_run_q8x(mnb_handle h, const void* X, const void* Wq, const void* scales,
                     rank, bias, Y, T_ws, batch, M, stream, true);
 }
 
+int mnb_check_wait_timeout(int64_t limit_cycles, void* stream) {
+    if (limit_cycles < 1000 || limit_cycles > 4000000000LL) return MNB_ERR_ARG;
+    int sms;
+    unsigned int* status = nullptr;
+    const int rc = device_setup(&sms, &status);
+    if (rc != MNB_OK) return rc;
+    return mnb::wait_check_launch(status, (long long)limit_cycles, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? MNB_OK
+               : MNB_ERR_CUDA;
+}
+
 int mnb_quantize_x(const void* X, int64_t Mt, int64_t K, void* Xq, void* Xs, void* stream) {
     if (Mt < 0 || K < 0) return MNB_ERR_ARG;
     if (K % 32 != 0) return MNB_ERR_UNSUPPORTED;

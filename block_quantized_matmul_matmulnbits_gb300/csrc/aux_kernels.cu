@@ -7,6 +7,8 @@
 //    so that graph replay rewrites the output).
 //  * lora_up: an empty packed weight with an adapter leaves only the adapter
 //    term, Y = T * Bt^T (+ bias), on the CUDA cores.
+//  * wait_check: the kernels' bounded wait, run out on purpose on a barrier
+//    nothing arrives on, so the timeout path can be checked without a fault.
 //  * quantize_x: the int8-activation quantization of X on its own (the device
 //    function the int8-activation decode path stages X with), for checks.
 //  * dequant: the dequantization step on its own, W16 = fp16((q - zp) * scale),
@@ -28,6 +30,20 @@ __global__ void fill_zero_kernel(uint4* __restrict__ y16, size_t n16, __half* __
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) y16[i] = make_uint4(0, 0, 0, 0);
     if (blockIdx.x == 0)
         for (size_t i = threadIdx.x; i < ntail; i += blockDim.x) tail[i] = __float2half_rn(0.f);
+}
+
+// The kernels' bounded wait on a phase that nothing completes: no thread ever
+// arrives on the barrier, so the wait gives up after `limit` cycles, records
+// the timeout in the status word and the kernel returns normally.
+__global__ void wait_check_kernel(unsigned int* status, long long limit) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(b, 0u, status, false, limit);
 }
 
 // One thread per (row, block of 32): codes in K order and the block scale.
@@ -183,6 +199,11 @@ cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t 
     size_t blocks = (total + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     fill_bias_kernel<<<(unsigned)blocks, 256, 0, st>>>(Y, bias, rows, N);
+    return cudaGetLastError();
+}
+
+cudaError_t wait_check_launch(unsigned int* status, long long limit_cycles, cudaStream_t st) {
+    wait_check_kernel<<<1, 32, 0, st>>>(status, limit_cycles);
     return cudaGetLastError();
 }
 

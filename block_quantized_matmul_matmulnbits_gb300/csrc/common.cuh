@@ -286,14 +286,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // records a timeout) when the limit passes, or -- when `abortable` -- as soon
 // as another role of the kernel has already given up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* status,
-                                          bool abortable = true) {
+                                          bool abortable = true, long long limit = kWaitCycles) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return true;
         if ((it & 7u) == 0) {
             if (abortable && (*reinterpret_cast<volatile unsigned int*>(status) & kStatusTimeout)) return false;
-            if (clock64() - t0 > kWaitCycles) {
+            if (clock64() - t0 > limit) {
                 atomicOr(status, kStatusTimeout);
                 return false;
             }

@@ -109,6 +109,9 @@ cudaError_t lora_up_launch(const __half* T, const __half* B, const uint8_t* Bq, 
 // Y[m, n] = bias[n] for m < rows (K == 0 or an empty weight, with a bias)
 cudaError_t fill_bias_launch(__half* Y, const __half* bias, size_t rows, size_t N, cudaStream_t st);
 
+// One kernel whose bounded wait nothing satisfies: it records a timeout in `status`.
+cudaError_t wait_check_launch(unsigned int* status, long long limit_cycles, cudaStream_t st);
+
 // Xq[m, k] / Xs[m, k/32]: the int8 activation codes and binary32 block scales the
 // int8-activation path computes (same device function), codes in K order.
 cudaError_t quantize_x_launch(const __half* X, int Mt, int K, int8_t* Xq, float* Xs, cudaStream_t st);

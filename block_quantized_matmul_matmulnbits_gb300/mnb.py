@@ -29,7 +29,7 @@ MODE_AUTO, MODE_FORCE_GEMV, MODE_FORCE_GEMM = 0, 1, 2
 FLAG_EARLY_WEIGHTS = 1
 
 # Every symbol include/mnb.h declares (checked against the header by the tests).
-EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_transpose_dq_weight", "mnb_run_q8x", "mnb_quantize_x", "mnb_plan", "mnb_last_route", "mnb_sync_status",
+EXPORTS = ("mnb_create", "mnb_destroy", "mnb_run", "mnb_run_bias", "mnb_run_qlora", "mnb_run_multi", "mnb_transpose_dq_weight", "mnb_run_q8x", "mnb_quantize_x", "mnb_check_wait_timeout", "mnb_plan", "mnb_last_route", "mnb_sync_status",
            "mnb_status_str", "mnb_dequant", "mnb_lora_down", "mnb_run_noalloc", "mnb_noalloc_max_rows")
 
 
@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
             L.mnb_run_q8x.restype = ctypes.c_int
             L.mnb_quantize_x.argtypes = [P, I64, I64, P, P, P]
             L.mnb_quantize_x.restype = ctypes.c_int
+            L.mnb_check_wait_timeout.argtypes = [I64, P]
+            L.mnb_check_wait_timeout.restype = ctypes.c_int
             L.mnb_plan.argtypes = [P, I64, I64, I32, I32, ctypes.POINTER(MnbPlanInfo)]
             L.mnb_plan.restype = ctypes.c_int
             L.mnb_last_route.argtypes = [P]
@@ -200,6 +202,10 @@ def mnb_transpose_dq_weight(w_q, w_scale, w_zp, bits: int, blocked: bool = True,
 def mnb_run_q8x(h, X, Wq, scales, zp, A, B, rank: int, bias, Y, T_ws, batch: int, M: int, stream=None) -> None:
     _check(lib().mnb_run_q8x(h, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zp), _ptr(A), _ptr(B), rank, _ptr(bias),
                              _ptr(Y), _ptr(T_ws), batch, M, _stream(stream)), "mnb_run_q8x")
+
+
+def mnb_check_wait_timeout(limit_cycles: int, stream=None) -> None:
+    _check(lib().mnb_check_wait_timeout(limit_cycles, _stream(stream)), "mnb_check_wait_timeout")
 
 
 def mnb_quantize_x(X, Mt: int, K: int, Xq, Xs, stream=None) -> None:

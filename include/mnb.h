@@ -199,6 +199,15 @@ int mnb_run_q8x(mnb_handle h,
                 void* Y, void* T_ws,
                 int64_t batch, int64_t M, void* stream);
 
+/* Failure-detection check: one kernel runs the library's bounded device wait
+ * (the one every pipeline barrier uses) on a barrier that nothing completes;
+ * after `limit_cycles` SM cycles (1e3 .. 4e9; the kernels use 4e9, about 2 s)
+ * it gives up, sets the timeout bit of the device status word and returns.
+ * A following mnb_sync_status reports MNB_ERR_DEVICE_TIMEOUT once (and clears
+ * the bit); the CUDA context stays usable.  No fault, trap or hang.
+ * Errors: MNB_ERR_ARG (limit out of range), MNB_ERR_NO_DEVICE, MNB_ERR_CUDA. */
+int mnb_check_wait_timeout(int64_t limit_cycles, void* stream);
+
 /* The activation quantization of mnb_run_q8x on its own (same device
  * function): X fp16 [Mt, K] -> Xq int8 [Mt, K] (K order), Xs float [Mt, K/32].
  * Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED (K % 32), MNB_ERR_ALIGN, MNB_ERR_CUDA. */

@@ -205,6 +205,8 @@ def test_multi_projection_validation_needs_no_device():
 
 def test_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
+    assert L.mnb_check_wait_timeout(10, None) == mnb.MNB_ERR_ARG
+    assert L.mnb_check_wait_timeout(5_000_000_000, None) == mnb.MNB_ERR_ARG
     assert L.mnb_quantize_x(0x1000, 4, 48, 0x2000, 0x3000, None) == mnb.MNB_ERR_UNSUPPORTED
     assert L.mnb_quantize_x(0x1000, 0, 64, 0x2000, 0x3000, None) == mnb.MNB_OK
     assert L.mnb_quantize_x(0x1000, 4, 64, None, 0x3000, None) == mnb.MNB_ERR_ARG

@@ -276,3 +276,22 @@ def test_early_weights_back_to_back_calls(env, M, N, K, rank):
     for i in range(3):
         same = [Y for j, Y in outs if j == i]
         assert all(torch.equal(same[0], y) for y in same[1:])
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(env):
+    """Failure detection without a fault: the kernels' bounded wait, run on a
+    barrier nothing completes with a short limit, reports MNB_ERR_DEVICE_TIMEOUT
+    through the status word once; the next call works and reports OK."""
+    torch, mnb = env
+    h = mnb.mnb_create(256, 256, 4)
+    try:
+        assert mnb.mnb_sync_status(h) == mnb.MNB_OK
+        mnb.mnb_check_wait_timeout(2_000_000)          # ~1 ms of waiting
+        assert mnb.mnb_sync_status(h) == mnb.MNB_ERR_DEVICE_TIMEOUT
+        assert mnb.mnb_sync_status(h) == mnb.MNB_OK    # reported once, then cleared
+    finally:
+        mnb.mnb_destroy(h)
+    inp = synth.tiny(M=1, rank=32)
+    Y, _, _ = run_gpu(mnb, torch, inp)                 # run_gpu asserts a clean status
+    Y64, bound = oracle_ref(inp)
+    assert_within_tolerance(bits_of(Y), Y64, bound, "after a timeout check")
