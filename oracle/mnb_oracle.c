@@ -31,7 +31,7 @@
  *    followed by MatMul is the computation MatMulNBits replaces, i.e. the
  *    dequant map is (q - zp) * scale and the weight is used transposed.
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *  - INT4 packing: two 4-bit codes per byte along K; element k = 2j sits in
  *    the low nibble (bits 0..3) of byte j of the block, k = 2j + 1 in the
  *    high nibble.  INT8: one code per byte.  INT2 (the 2-bit weights of the
