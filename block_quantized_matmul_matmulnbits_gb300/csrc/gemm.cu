@@ -220,10 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nx = L.nx, nw = L.nw, np = L.np;
 
     const uint32_t bars = sbase + L.bar_off;
+    // With as many X slots as A slots, step k uses slot k % n of both rings and one
+    // commit per step releases both (a commit costs the single MMA thread several
+    // MMAs' worth of issue time); else each ring has its own release barrier.
+    const bool one_release = nx == nw;
     auto full_x = [&](int s) { return bars + 8u * s; };
     auto empty_x = [&](int s) { return bars + 8u * (nx + s); };
     auto full_w = [&](int s) { return bars + 8u * (2 * nx + s); };
-    auto empty_w = [&](int s) { return bars + 8u * (2 * nx + nw + s); };
+    auto empty_w = [&](int s) { return bars + 8u * (one_release ? nx + s : 2 * nx + nw + s); };
     const int b0 = 2 * nx + 2 * nw;
     auto full_p = [&](int j) { return bars + 8u * (b0 + j); };
     auto empty_p = [&](int j) { return bars + 8u * (b0 + np + j); };
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < nw; ++s) {
             mbar_init(full_w(s), kDqThreads);
-            mbar_init(empty_w(s), 1);
+            if (!one_release) mbar_init(empty_w(s), 1);  // else empty_w(s) is empty_x(s)
         }
         for (int j = 0; j < np; ++j) {
             mbar_init(full_p(j), 1);
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_mma(d_tmem, sw128_desc(wslot(sw) + 32u * j), sw128_desc(xslot(sx) + 32u * j), idesc,
                                (i > 0 || j > 0) ? 1u : 0u);
                     tc_commit(empty_x(sx));
-                    tc_commit(empty_w(sw));
+                    if (!one_release) tc_commit(empty_w(sw));
                 }
                 if (ok) tc_commit(acc_full(acc));
                 ++tl;
