@@ -79,6 +79,8 @@ def run_single(mnb, torch, inp, bias, K, bits, M, mode=0, flags=0):
     ((2048, 512), 1024, 2, (0, 3), 2),           # 2-bit
     ((4096, 1024, 1024), 4096, 4, (0, 15), 300),  # prefill: one tensor-core launch per member
     ((333, 17, 1000), 576, 8, (120, 136), 40),
+    ((100, 64, 250), 96, 4, (0, 15), 2),          # K % 64 == 32
+    ((100, 64, 250), 160, 8, None, 33),
 ])
 def test_multi_equals_single_calls_bitwise(env, Ns, K, bits, zp, M):
     torch, mnb = env

@@ -94,6 +94,8 @@ def run_q8x_gpu(mnb, torch, inp, bias=None, d=None):
     (64, 300, 1024, 4, (0, 15), 0),       # eight token tiles
     (300, 256, 512, 4, None, 32),         # a prefill-size M on the decode kernel
     (1, 4096, 11008, 4, (0, 15), 0),      # a large K (11008 int8 codes per staged token row): two-stage ring
+    (3, 300, 96, 4, (0, 15), 32),         # K % 64 == 32: the last 128-byte segment partly past the row
+    (9, 130, 160, 8, (120, 136), 0),      # INT8 with K % 64 == 32, two token tiles
 ])
 def test_q8x_matches_oracle(env, M, N, K, bits, zp, rank):
     torch, mnb = env
