@@ -54,10 +54,11 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreadsGemv = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kMaxRing = 4;                                // ring stages (2 or 4)
+constexpr int kMaxRing = 4;                                // most ring stages
 constexpr uint32_t kXStageMax = 64 * 1024;                 // largest X tile staged in shared memory
 constexpr uint32_t kXStageSmall = 24 * 1024;               // X tiles this small leave room for 3 CTAs per SM
 constexpr uint32_t kTwoPerSm = 113 * 1024;                 // shared memory of a CTA when two share an SM
+constexpr uint32_t kThreePerSm = 75 * 1024;                // ... and when three do
 constexpr int kGroup = 16;                                 // rows per stage / MMA tile
 constexpr int kMaxChunk = 1024;                            // K bytes per row and stage
 // Inside a stage's adapter region (1 KB: 16 FP16 rows of B, or 16 INT8 rows of
@@ -78,7 +79,7 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 __host__ __device__ inline uint32_t xs_pitch(int K) { return (uint32_t)K * 2u + 16u; }
 
 // Shared-memory layout, identical on host and device.  `ch` = K bytes per chunk,
-// `ring` = stages (2 or 4), `xbytes` = staged X (0 when X is read from global).
+// `ring` = stages (2 to 4), `xbytes` = staged X (0 when X is read from global).
 __host__ __device__ inline GemvLayout gemv_layout(int ch, int nblk, int tok, int ring, uint32_t xbytes) {
     GemvLayout L;
     L.w = 0;
@@ -106,14 +107,19 @@ inline int gemv_ctas_per_sm(int N, int nt, uint32_t xbytes, int sms) {
     return nt == 1 && xbytes > 0 && xbytes <= kXStageSmall && (N + kGroup - 1) / kGroup > 2 * sms ? 3 : 2;
 }
 
-// Ring stages: two when three CTAs share an SM (they still keep 96 KB of
-// weights in flight per SM) or when a CTA has at most two stages, else four.
-inline int gemv_ring(int nstages, int occ) { return nstages <= 2 || occ == 3 ? 2 : kMaxRing; }
+// Ring stages with two CTAs per SM: two when a CTA has at most two stages, else four.
+inline int gemv_ring(int nstages) { return nstages <= 2 ? 2 : kMaxRing; }
 
-// The ring for a CTA: two stages as well when four would not leave room for two
-// CTAs per SM next to a large staged X tile.
+// The ring for a CTA.  Two CTAs per SM: four stages, or two when four would not
+// leave room for both next to a large staged X tile.  Three CTAs per SM (small
+// stages): the deepest ring of up to four stages that fits a third of the SM.
 inline int gemv_pick_ring(int ch, int nblk, int tok, int nstages, int occ, uint32_t xbytes) {
-    const int ring = gemv_ring(nstages, occ);
+    if (occ == 3) {
+        for (int ring = kMaxRing; ring > 2; --ring)
+            if (ring <= nstages && gemv_layout(ch, nblk, tok, ring, xbytes).total <= kThreePerSm) return ring;
+        return 2;
+    }
+    const int ring = gemv_ring(nstages);
     return ring > 2 && gemv_layout(ch, nblk, tok, ring, xbytes).total > kTwoPerSm ? 2 : ring;
 }
 
@@ -180,6 +186,27 @@ struct GemvMaps {
     CUtensorMap m[kMaxSeg];
 };
 
+// Ring slot and pass parity of stage st.  Three-CTA kernels may run rings of
+// three stages and step a counter; the others have rings of two or four
+// stages and take them from st (both forms give the same slot and parity).
+template <int OCC>
+struct RingPosT {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void step(int ring) {
+        if constexpr (OCC == 3) {
+            if (++s == ring) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    }
+    __device__ __forceinline__ int slot(int st, int rmask) const { return OCC == 3 ? s : st & rmask; }
+    __device__ __forceinline__ uint32_t parity(int st, int ring) const {
+        return OCC == 3 ? ph : (uint32_t)(st / ring) & 1u;
+    }
+};
+
 template <int BITS, bool HAS_ZP, int NT, bool XS, int OCC, bool Q8X>
 __global__ void __launch_bounds__(kThreadsGemv, OCC)
     gemv_kernel(const __grid_constant__ GemvMaps maps, const __grid_constant__ GemvArgs a) {
@@ -230,15 +257,16 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
         // ------------------------------------------------------------ producer
         if (lane < 2) {
             bool ok = true;
-            for (int st = 0; ok && st < nstages; ++st) {
-                const int s = st & rmask;
+            RingPosT<OCC> rp;
+            for (int st = 0; ok && st < nstages; ++st, rp.step(ring)) {
+                const int s = rp.slot(st, rmask);
                 const int q = st / nchunk, c = st - q * nchunk;
                 const int sg = seg_of(g_begin + q);
                 const GemvSeg& pj = a.seg[sg];
                 const int ra = (g_begin + q - pj.g0) * kGroup, rows = min(kGroup, pj.N - ra);  // rows of projection sg
                 const uint64_t total_s = (uint64_t)pj.N * nblk * 2, total_z = (uint64_t)pj.N * nblk;
                 const uint32_t slot = sb + (uint32_t)s * L.stage;
-                if (!(ok = mbar_wait(empty(s), ((uint32_t)(st / ring) & 1u) ^ 1u, status))) break;
+                if (!(ok = mbar_wait(empty(s), rp.parity(st, ring) ^ 1u, status))) break;
                 // scales / zero points of the group's full rows as 16-byte aligned supersets;
                 // bytes past the last 16-byte boundary of an array come from lane 1
                 const uint64_t s0 = (uint64_t)ra * nblk * 2, s1 = (uint64_t)(ra + rows) * nblk * 2;
@@ -412,11 +440,12 @@ __global__ void __launch_bounds__(kThreadsGemv, OCC)
 
     bool ok = true;
     int q = 0, c = 0;  // group and chunk of stage st (counters: no divisions in the loop)
-    for (int st = 0; st < nstages; ++st) {
-        const int s = st & rmask;
+    RingPosT<OCC> rp;
+    for (int st = 0; st < nstages; ++st, rp.step(ring)) {
+        const int s = rp.slot(st, rmask);
         const GemvSeg& pj = a.seg[seg_of(g_begin + q)];
         const int ra = (g_begin + q - pj.g0) * kGroup, rows = min(kGroup, pj.N - ra);  // rows of this projection
-        if (ok) ok = mbar_wait(full(s), (uint32_t)(st / ring) & 1u, status);
+        if (ok) ok = mbar_wait(full(s), rp.parity(st, ring), status);
         const uint32_t soff = (uint32_t)s * L.stage;  // byte offset of the stage in `sm`
         const uint32_t s_al = ((uint32_t)ra * (uint32_t)nblk * 2u) & 15u;  // scale copy alignment offset
         const uint32_t z_al = ((uint32_t)ra * (uint32_t)nblk) & 15u;
@@ -892,7 +921,7 @@ cudaError_t gemv_q8x_launch(const GemvArgs& a_in, const mnb_plan_info& p, int bi
     GemvArgs a = a_in;
     const int rowbytes = a.K * bits / 8;
     const int nstages = (a.R + kGroup - 1) / kGroup * ((rowbytes + a.CH - 1) / a.CH);
-    a.ring = gemv_ring(nstages, 2);
+    a.ring = gemv_ring(nstages);
     a.xrows = a.Mt < 8 ? a.Mt : 8;
     size_t smem = gemv_layout(a.CH, a.K / 32, 8, a.ring, q8x_stage_bytes(8, a.K)).total;
     if (smem > 227 * 1024 && a.ring > 2) {  // large K: the staged codes leave room for two stages

@@ -135,6 +135,26 @@ def test_lm_head_int8(env, K, N):
     assert_within_tolerance(bits_of(Y), Y64, bound, f"lm_head K={K} N={N}")
 
 
+@pytest.mark.parametrize("M,K,N,bits,zp", [
+    (1, 2048, 23995, 4, (0, 15)),    # 5 stages per CTA: a ring of three
+    (2, 1536, 20007, 8, (120, 136)),  # two K chunks per row (1024 + 512 bytes), ring of three
+    (3, 576, 30001, 8, None),        # 13 small stages: a ring of four
+    (5, 1024, 20000, 4, None),       # three stages, ring of three
+    (1, 4096, 8000, 4, (0, 15)),     # large stages: a ring of two
+])
+def test_three_ctas_per_sm_rings(env, M, K, N, bits, zp):
+    """More than two row groups per SM and a small staged X put three CTAs on
+    an SM; the number of stages per CTA and the stage size then pick rings of
+    two, three or four stages (slots stepped by a counter).  Every output is
+    compared, ragged last groups included."""
+    torch, mnb = env
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=3300 + M, zp_range=zp)
+    Y, _, route = run_gpu(mnb, torch, inp)
+    assert route == mnb.ROUTE_GEMV
+    Y64, bound = oracle_ref(inp)
+    assert_within_tolerance(bits_of(Y), Y64, bound, f"three CTAs per SM M={M} K={K} N={N}")
+
+
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("rank", [32, 0])
 def test_mlp_up_decode_sampled_rows(env, M, rank):
