@@ -182,6 +182,12 @@ class Workload:
         # decode loops keep the weights constant: let each call stream them early
         self.h = mnb.mnb_create(N, K, bits, 32, 32, 0, 0, mnb.FLAG_EARLY_WEIGHTS)
 
+    def launches_per_call(self, sms, rank=None):
+        """Kernels one call launches: the matmul kernel, plus the LoRA down kernel
+        where the plan runs one."""
+        rank = self.cfg["rank"] if rank is None else rank
+        return 1 + self.mnb.mnb_plan(self.h, 1, self.cfg["M"], rank, sms)["lora_kernel"]
+
     def step(self, i, rank=None):
         c = self.copies[i % len(self.copies)]
         rank = self.cfg["rank"] if rank is None else rank
@@ -295,6 +301,30 @@ def e2e_decode(torch, wl, steps, chunk=240, lanes=4):
     return e0.elapsed_time(e1) / 1e3, M * K * 2, M * N * 2
 
 
+def measure_copy_gbs(torch, nbytes=1 << 30, reps=10):
+    """Device-to-device copy bandwidth of one 1 GiB buffer (bytes read + bytes
+    written, median of `reps` copies timed with CUDA events): the practical HBM
+    ceiling on this device, reported next to the roofline's peak."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        dst.copy_(src)
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(st)
+        dst.copy_(src)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    del src, dst
+    torch.cuda.empty_cache()
+    ts.sort()
+    return 2.0 * nbytes / ts[len(ts) // 2] / 1e9
+
+
 def run_gpu_arm(args, dist_ctx):
     import torch
 
@@ -312,6 +342,7 @@ def run_gpu_arm(args, dist_ctx):
     step_bytes = decode_bytes(cfg["M"], cfg["K"], cfg["N"], cfg["bits"], cfg["rank"])
     copies = max(8, math.ceil(4 * l2 / step_bytes))
     wl = Workload(torch, mnb, synth, cfg, copies)
+    launches_per_step = wl.launches_per_call(props.multi_processor_count)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -365,6 +396,8 @@ def run_gpu_arm(args, dist_ctx):
     except Exception as e:  # a prefill failure is reported in the line, not raised
         prefill = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
 
+    copy_gbs = measure_copy_gbs(torch) if only == "all" else None
+
     def rate(nbytes, steps, t):
         return nbytes * steps / t / 1e9 if t == t and t > 0 else None
 
@@ -388,7 +421,10 @@ def run_gpu_arm(args, dist_ctx):
         "roofline": {"bound": "hbm", "achieved": round(per_gbs, 2), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(per_gbs / hbm_peak, 4), "traffic": ncu_traffic("decode"),
                      "kernel": "decode pass (lora_down + PDL-overlapped gemv), per mnb_run call",
-                     "peak_source": f"{peak_src} HBM copy bandwidth"},
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "copy_ceiling": None if copy_gbs is None else {
+                         "value": round(copy_gbs, 1), "unit": "GB/s", "frac": round(per_gbs / copy_gbs, 4),
+                         "method": "1 GiB device-to-device copy on this GPU, read + write bytes, median of 10"}},
         "decode_base_only": {"value": round(base_gbs, 2), "unit": "GB/s", "bytes_per_step": base_bytes,
                              "ms_per_step": round(t_base / args.steps * 1e3, 6),
                              "frac": round(base_gbs / hbm_peak, 4), "traffic": ncu_traffic("decode_base")},
@@ -397,7 +433,7 @@ def run_gpu_arm(args, dist_ctx):
                 "steps": e2e_steps, "ms_per_step": round(t_e2e / e2e_steps * 1e3, 5),
                 "path": "pinned X host->device, mnb_run, Y device->host every step; 4 streams round-robin "
                         "(independent requests), recorded in CUDA graphs"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     return line
