@@ -514,13 +514,19 @@ def run_sweep(args):
                 "route": {1: "gemv", 2: "gemm"}.get(route, str(route))}
 
     rows = []
+
+    def wanted(name):
+        return args.sweep_filter is None or args.sweep_filter in name
+
     for name, (K, N, zpr, scr) in {"lm_head K=576 N=49152 INT8": (576, 49152, (120, 136), (0.001, 0.01)),
                                    "lm_head K=896 N=151936 INT8": (896, 151936, (120, 136), (0.001, 0.01))}.items():
+        if not wanted(name):
+            continue
         r = measure(1, K, N, 8, 0, zpr, scr, mnb.MODE_AUTO, synth.SEED_BASE + 4)
         rows.append({"workload": name, "M": 1, "rank": 0, "mode": "auto", **r})
         print(json.dumps(rows[-1]), flush=True)
     cross = {}
-    for rank in (0, 32):
+    for rank in ((0, 32) if wanted("K=4096 N=14336 INT4") else ()):
         for M in SWEEP_M:
             res = {}
             for mname, mode in (("gemv", mnb.MODE_FORCE_GEMV), ("gemm", mnb.MODE_FORCE_GEMM)):
@@ -826,6 +832,8 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: the lm_head shapes and the M sweep at K=4096, N=14336 "
                          "(both routes), one JSON line per point")
+    ap.add_argument("--sweep-filter", default=None,
+                    help="with --sweep: only the workloads whose name contains this text")
     ap.add_argument("--sweep-next", action="store_true",
                     help="instead of the bench line: the rows beyond the core path (adapter formats, int8 "
                          "activations, 2-bit weights, bias, fused QKV), one JSON line per point")
