@@ -33,7 +33,12 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_init_mu;
-bool g_prepared[kMaxDevices] = {};
+// Per device: the context the setup below was done in (0 = none yet), the
+// SM count and the status word's device address in that context.  A device
+// address and a kernel attribute belong to one context: when the current
+// context of the device changes (the primary context was reset and created
+// again, or the caller made another context current) the setup runs again.
+unsigned long long g_setup_ctx[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 unsigned int* g_status_ptr[kMaxDevices] = {};
 
@@ -52,33 +57,40 @@ int validate_desc(const mnb_desc* d) {
     return MNB_OK;
 }
 
-// One-time per-device setup: SM count and kernel attributes.  Returns MNB_OK
-// and the device's SM count, or MNB_ERR_NO_DEVICE / MNB_ERR_CUDA.
+// Per-device setup in the current context: SM count, kernel attributes and
+// the status word's address.  Returns MNB_OK and the device's SM count, or
+// MNB_ERR_NO_DEVICE / MNB_ERR_CUDA.
 int device_setup(int* sm_count, unsigned int** status = nullptr) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
         return MNB_ERR_NO_DEVICE;
     }
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MNB_ERR_NO_DEVICE;
+    }
+    if (major != 10) return MNB_ERR_NO_DEVICE;  // built for sm_103a only
+    unsigned long long ctx = 0;
+    if (mnb::current_context_id(&ctx) != cudaSuccess) return MNB_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_init_mu);
-    if (!g_prepared[dev]) {
-        int major = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if (g_setup_ctx[dev] != ctx) {
+        int sms = 0;
+        void* st = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return MNB_ERR_NO_DEVICE;
         }
-        if (major != 10) return MNB_ERR_NO_DEVICE;  // built for sm_103a only
-        void* st = nullptr;
         if (mnb::gemv_prepare() != cudaSuccess || mnb::gemm_prepare() != cudaSuccess ||
-            mnb::lora_down_prepare() != cudaSuccess ||
+            mnb::lora_down_prepare() != cudaSuccess || mnb::decode_prepare() != cudaSuccess ||
             cudaGetSymbolAddress(&st, mnb::g_status) != cudaSuccess) {
             cudaGetLastError();
             return MNB_ERR_CUDA;
         }
         g_status_ptr[dev] = static_cast<unsigned int*>(st);
         g_sm_count[dev] = sms;
-        g_prepared[dev] = true;
+        g_setup_ctx[dev] = ctx;
     }
     *sm_count = g_sm_count[dev];
     if (status) *status = g_status_ptr[dev];
@@ -86,6 +98,22 @@ int device_setup(int* sm_count, unsigned int** status = nullptr) {
 }
 
 int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Single-token decode kernel: rows split evenly over one CTA per SM, the
+// adapter (if any) in the same launch.
+void plan_decode(const mnb_desc& d, int rank, int sms, mnb_plan_info* p) {
+    int ctas, SR, ring;
+    size_t smem;
+    mnb::decode_geometry((int)d.N, (int)d.K, d.bits, rank > 0, sms, &ctas, &SR, &ring, &smem);
+    p->route = MNB_ROUTE_GEMV;
+    p->lora_kernel = 0;
+    p->grid_x = ctas;
+    p->grid_y = 1;
+    p->block_threads = 288;
+    p->rows_per_cta = (int)((d.N + ctas - 1) / ctas);
+    p->k_splits = SR;
+    p->tokens_per_cta = 1;
+}
 
 // Decode-kernel geometry: balanced row ranges, one CTA per SM and token group.
 void plan_gemv(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
@@ -118,7 +146,10 @@ void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
     p->tokens_per_cta = tok;
 }
 
-int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p) {
+// fused_ok: the call's variant can run on the single-token decode kernel (FP16 or
+// no adapter, FP16 activations, one projection).
+int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p,
+              bool fused_ok = true) {
     *p = mnb_plan_info{};
     const int64_t Mt = batch * M;
     if (Mt == 0 || d.N == 0) {
@@ -133,6 +164,10 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
     int route = M <= thr ? MNB_ROUTE_GEMV : MNB_ROUTE_GEMM;
     if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
     if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
+    if (route == MNB_ROUTE_GEMV && fused_ok && mnb::decode_supported(d.bits, Mt, (int)d.K)) {
+        plan_decode(d, rank, sms, p);
+        return MNB_OK;
+    }
     if (route == MNB_ROUTE_GEMV)
         plan_gemv(d, Mt, sms, p);
     else
@@ -187,10 +222,11 @@ struct Adapter {
     bool q8;
 };
 
-// q8x: the int8-activation base (decode kernel for every M).
+// q8x: the int8-activation base (decode kernel for every M).  noalloc: T goes
+// to the library's fixed scratch (mnb_run_noalloc); T_ws is then unused.
 int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const Adapter& ad,
              int32_t rank, const void* bias, void* Y, void* T_ws, int64_t batch, int64_t M, void* stream,
-             bool q8x = false) {
+             bool q8x = false, bool noalloc = false) {
     if (!h || batch < 0 || M < 0) return MNB_ERR_ARG;
     const mnb_desc& d = h->d;
     if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
@@ -203,7 +239,7 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     if (down == nullptr && up == nullptr) rank = 0;
     if (rank > 0) {
         if (rank > d.max_rank) return MNB_ERR_ARG;
-        if (!down || !up || !T_ws) return MNB_ERR_ARG;
+        if (!down || !up || (!T_ws && !noalloc)) return MNB_ERR_ARG;
         if (ad.q8 && (!ad.As || !ad.Bs)) return MNB_ERR_ARG;
     }
     if (Mt > 0 && d.N > 0) {
@@ -233,8 +269,15 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     if (Mt > 0 && d.N > 0) {
         const int rc = device_setup(&sms, &status);
         if (rc != MNB_OK) return rc;
+        if (noalloc && rank > 0) {
+            if (Mt > mnb::kNoallocMaxRows) return MNB_ERR_UNSUPPORTED;  // beyond the fixed scratch
+            __half* Tfix = nullptr;
+            const int rs = mnb::noalloc_scratch(&Tfix);
+            if (rs != MNB_OK) return rs;
+            T_ws = Tfix;
+        }
     }
-    make_plan(d, batch, M, rank, sms, &p);
+    make_plan(d, batch, M, rank, sms, &p, !q8x && !(rank > 0 && ad.q8));
     if (q8x && (p.route == MNB_ROUTE_GEMV || p.route == MNB_ROUTE_GEMM)) {
         plan_gemv(d, Mt, sms, &p);  // integer dots on the decode kernel, 8-token tiles
         p.tokens_per_cta = 8;
@@ -279,6 +322,27 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     // LoRA down kernel lets the matmul kernel start only after its own wait,
     // so behind it the matmul kernel reads X at once and waits only for T.
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
+    if (p.route == MNB_ROUTE_GEMV && p.tokens_per_cta == 1) {
+        // one launch: base and adapter on the single-token decode kernel
+        mnb::DecodeArgs a = {};
+        a.nseg = 1;
+        a.NR = (int)d.N;
+        a.seg[0] = mnb::DecSeg{0, (int)d.N, static_cast<const uint8_t*>(Wq), static_cast<const __half*>(scales),
+                               static_cast<const uint8_t*>(zp), biash, static_cast<__half*>(Y)};
+        a.X = Xh;
+        a.A = rank > 0 ? static_cast<const __half*>(ad.A) : nullptr;
+        a.B = rank > 0 ? static_cast<const __half*>(ad.B) : nullptr;
+        a.T = rank > 0 ? Th : nullptr;
+        a.K = (int)d.K;
+        a.bits = d.bits;
+        a.x_wait = early ? 1 : 0;
+        a.status = status;
+        e = mnb::decode_launch(a, rank, sms, early, st);
+        if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return MNB_ERR_CUDA;
+        h->last_route = p.route;
+        return MNB_OK;
+    }
     const bool lora_kernel = rank > 0;
     if (lora_kernel) {
         e = launch_down(Xh, Th, early, st);
@@ -338,6 +402,14 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
 }
 
 }  // namespace
+
+namespace mnb {
+int run_noalloc(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+                const void* B, int32_t rank, void* Y, int64_t batch, int64_t M, void* stream) {
+    return run_impl(h, X, Wq, scales, zp, Adapter{A, B, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, false},
+                    rank, nullptr, Y, nullptr, batch, M, stream, false, true);
+}
+}  // namespace mnb
 
 extern "C" {
 
@@ -449,6 +521,31 @@ int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
     mnb_plan_info p;
     make_plan(d, batch, M, 0, sms, &p);
+    if (p.route == MNB_ROUTE_GEMV && p.tokens_per_cta == 1) {
+        // one token row: one single-token decode launch over the nonempty members
+        mnb::DecodeArgs a = {};
+        int R = 0;
+        for (int i = 0; i < nproj; ++i) {
+            const mnb_projection& q = proj[i];
+            if (q.N == 0 || !q.Wq) continue;
+            a.seg[a.nseg++] = mnb::DecSeg{R, (int)q.N, static_cast<const uint8_t*>(q.Wq),
+                                          static_cast<const __half*>(q.scales), static_cast<const uint8_t*>(q.zp),
+                                          static_cast<const __half*>(q.bias), static_cast<__half*>(q.Y)};
+            R += (int)q.N;
+        }
+        a.NR = R;
+        a.X = static_cast<const __half*>(X);
+        a.K = (int)d.K;
+        a.bits = d.bits;
+        a.x_wait = early ? 1 : 0;
+        a.status = status;
+        e = mnb::decode_launch(a, 0, sms, early, st);
+        if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
+        if (e != cudaSuccess) return MNB_ERR_CUDA;
+        h->last_route = p.route;
+        return MNB_OK;
+    }
+    make_plan(d, batch, M, 0, sms, &p, false);
     if (p.route == MNB_ROUTE_GEMV) {
         // one launch over the nonempty members, each starting on a 16-row group
         mnb::GemvArgs a = {};
@@ -464,7 +561,7 @@ int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32
         a.G = G;
         mnb_desc dv = d;
         dv.N = (int64_t)G * 16;  // the launch geometry of the members' row space
-        make_plan(dv, batch, M, 0, sms, &p);
+        make_plan(dv, batch, M, 0, sms, &p, false);
         a.X = static_cast<const __half*>(X);
         a.Mt = (int)Mt;
         a.K = (int)d.K;
@@ -484,7 +581,7 @@ int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32
             mnb_desc dq = d;
             dq.N = q.N;
             mnb_plan_info pq;
-            make_plan(dq, batch, M, 0, sms, &pq);
+            make_plan(dq, batch, M, 0, sms, &pq, false);
             mnb::GemmArgs a = {};
             a.X = static_cast<const __half*>(X);
             a.Wq = static_cast<const uint8_t*>(q.Wq);

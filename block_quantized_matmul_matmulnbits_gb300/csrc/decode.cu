@@ -1,0 +1,672 @@
+// decode.cu -- single-token decode kernel: one launch computes
+//
+//     Y[n] = sum_k x[k] w[n, k]  (+ sum_r T[r] B[n, r],  T = fp16(x A))  (+ bias[n])
+//
+// for one token row x, the "fuse_down" decode path of "[WebGPU] Fuse rank-32
+// quantized LoRA with MatMulNBits" (onnxruntime PR 33370, commit message adding
+// MatMulNBitsLoRA: the base GEMV and the LoRA down projection T first, then the
+// base plus T * Bt^T), restated for sm_103a.  Both adapter projections are
+// fused into this one kernel, so the base weights are read exactly once and a
+// call is one launch.
+//
+// Design:
+//  * Rows are split evenly over the CTAs (one per SM): CTA c owns rows
+//    [c N / C, (c + 1) N / C), so every SM moves the same number of weight
+//    bytes.  Its rows are contiguous in memory: one producer lane streams them
+//    into shared memory in stages of up to SR rows (codes, scales, zero points
+//    and the adapter rows B[n, :], each a 1-D bulk copy), and when the CTA's
+//    whole share fits it is copied before anything else happens.  Weights are
+//    constant, so the copies start before the work queued ahead of this
+//    kernel has finished (programmatic dependent launch); only x waits for it.
+//  * The multiply runs on mma.sync m16n8k16 (FP16 in, FP32 accumulate) with 16
+//    weight rows as M.  A code is fed to the tensor core as the FP16 value
+//    q * 2^-24 (the code's bits placed in the mantissa of a subnormal half:
+//    exact), so unpacking is a mask (INT4) or a byte permute (INT8) and no
+//    dequant arithmetic runs per weight.  The eight MMA columns, which one
+//    token row would leave idle, each collect one (block, class) of codes:
+//    thread t of a quad owns block t of a group of four blocks, its A pairs
+//    go to columns 2t and 2t + 1, and only the threads supplying those
+//    columns carry x in their B fragment.  After a group of four blocks each
+//    thread holds, for its two rows, the block sums sum_k x q of its block, and
+//    applies the block's scale and zero point once, in FP32:
+//        y += s * (sum_k x q - zp * sum_k x).
+//    The scale and zero point of every (row, block) are restaged into a
+//    bank-conflict-free layout while the stage waits for x.
+//  * The adapter: the CTAs of a cluster of eight each take 1/8 of K, hold
+//    their slice of A in registers (prefetched with the weights), form T's
+//    partial sums on the tensor cores (movmatrix turns A's rows into the MMA's
+//    K-major operand) and exchange them through distributed shared memory;
+//    every CTA adds the eight partials in rank order, so T is bitwise
+//    reproducible, rounds T once to FP16 and adds sum_r T[r] B[n, r] (two
+//    MMAs per 16 rows) before the one rounding of each output.
+//  * Eight consumer warps split a stage's rounds; their partial sums are added
+//    in warp order (no atomics): results are deterministic.
+//  * Every mbarrier wait is bounded and reports through the status word.
+#include "common.cuh"
+#include "mnb_internal.h"
+
+namespace mnb {
+
+namespace {
+
+constexpr int kCW = 8;                     // consumer warps
+constexpr int kDecThreads = (kCW + 1) * 32;
+constexpr int kCl = 8;                     // cluster size of the adapter's T exchange
+constexpr int kRk = 32;                    // adapter rank
+constexpr int kBlkPerRound = 4;            // quantization blocks a warp covers per round
+constexpr int kMaxSR = 128;                // most rows per stage
+constexpr float kUnit = 1.0f / 16777216.f;  // a code q reaches the MMA as q * 2^-24
+
+__device__ __forceinline__ uint4 lds128_raw(const unsigned char* sm, uint32_t off) {
+    return *reinterpret_cast<const uint4*>(sm + off);
+}
+
+__host__ __device__ inline uint32_t al128(uint32_t x) { return (x + 127u) & ~127u; }
+
+// Shared memory plan, identical on host and device.  A stage slot holds SR
+// rows: codes [SR][rowbytes], scales and zero points as copied (a 16-byte
+// aligned superset), adapter rows [SR][32] FP16, and the restaged
+// {s_g, s_g+8, zp_g, zp_g+8} halves of each (16-row tile, block, g).
+struct DecLayout {
+    uint32_t sc, zp, b, rs, slot;           // offsets inside a slot, slot bytes
+    uint32_t xs, sxs, red, lora, tpart, t16, bars, total;
+};
+
+__host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, int nblk, int nblkR) {
+    DecLayout L;
+    L.sc = al128((uint32_t)SR * (uint32_t)rowbytes);
+    L.zp = al128(L.sc + (uint32_t)SR * (uint32_t)nblk * 2u + 32u);
+    L.b = al128(L.zp + (uint32_t)SR * (uint32_t)nblk + 32u);
+    L.rs = al128(L.b + (uint32_t)SR * 64u);
+    L.slot = al128(L.rs + (uint32_t)(SR / 16) * (uint32_t)nblkR * 64u);
+    uint32_t off = (uint32_t)ring * L.slot;
+    L.xs = off;  // x in the MMA's pair order, 64 bytes a block, then a 64-byte zero region
+    off = al128(off + (uint32_t)nblkR * 64u + 64u);
+    L.sxs = off;  // per block: sum of x, times 2^-E
+    off = al128(off + (uint32_t)nblkR * 4u);
+    L.red = off;  // two buffers [SR / 16][kCW][16] FP32
+    off += 2u * (uint32_t)(SR / 16) * kCW * 16u * 4u;
+    L.lora = off;  // two buffers [kMaxSR] FP32
+    off += 2u * kMaxSR * 4u;
+    L.tpart = off;  // [kCW][32] warp partials of T, then [32] the CTA's partial
+    off += (kCW + 1) * kRk * 4u;
+    L.t16 = off;  // T rounded to FP16
+    off += kRk * 2u;
+    L.bars = al128(off);
+    L.total = L.bars + 2u * (uint32_t)ring * 8u;
+    return L;
+}
+
+// Codes of a weight word as the subnormal FP16 pairs the MMA takes.
+// INT4 word = codes c0..c7 (c0 in bits 0..3): lo0 = (c0, c4), hi0 = 16 (c1, c5),
+// lo1 = (c2, c6), hi1 = 16 (c3, c7), each times 2^-24.
+// INT8 word = codes c0..c3: p0 = (c0, c1), p1 = (c2, c3), times 2^-24.
+template <int BITS>
+struct Unpack;
+
+template <>
+struct Unpack<4> {
+    static constexpr int kWordsPerBlock = 4;  // 16 bytes a block and row
+    static constexpr float kHiWeight = 1.f / 16.f;  // class 1 codes sit 4 bits higher: they read as 16 q
+    __device__ __forceinline__ static void pairs(uint32_t w, uint32_t a[4]) {
+        const uint32_t w8 = w >> 8;
+        a[0] = w & 0x000F000Fu;
+        a[1] = w & 0x00F000F0u;
+        a[2] = w8 & 0x000F000Fu;
+        a[3] = w8 & 0x00F000F0u;
+    }
+};
+
+template <>
+struct Unpack<8> {
+    static constexpr int kWordsPerBlock = 8;
+    static constexpr float kHiWeight = 1.f;
+    __device__ __forceinline__ static void pairs(uint32_t w, uint32_t a[2]) {
+        a[0] = prmt(w, 0u, 0x4140u);
+        a[1] = prmt(w, 0u, 0x4342u);
+    }
+};
+
+// Byte offset, inside a block's 64 bytes of staged x, of the pair that MMA
+// slot pair sp (0..3) of sub-block `sub` (8 consecutive codes) takes.  The
+// slot order follows the unpacking above, so the T projection reads the same
+// staged x as the base.
+template <int BITS>
+__device__ __forceinline__ uint32_t xs_pair_off(int sub, int sp) {
+    if constexpr (BITS == 4)  // sub-block = one word: slots (0,1)=(x0,x4) (2,3)=(x2,x6) (4,5)=(x1,x5) (6,7)=(x3,x7)
+        return (uint32_t)((sp >> 1) * 32 + sub * 8 + (sp & 1) * 4);
+    else  // sub-block = words 2 sub, 2 sub + 1: slots in natural order
+        return (uint32_t)((sp & 1) * 32 + (2 * sub + (sp >> 1)) * 4);
+}
+// K offset (0..7) inside a sub-block of MMA slot s.
+template <int BITS>
+__host__ __device__ constexpr int slot_k(int s) {
+    return BITS == 4 ? ((s & 1) * 4 + (s >> 2) + ((s >> 1) & 1) * 2) : s;
+}
+
+__device__ __forceinline__ void movmatrix_t(uint32_t& x) {
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;" : "+r"(x));
+}
+
+// Cluster barrier, per thread (not .aligned: the producer lane arrives early).
+__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+__device__ __forceinline__ float h2f_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
+__device__ __forceinline__ float h2f_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// The CTA's rows as a sequence of stages: at most SR rows, never across two
+// projections (each stage is contiguous in one projection's arrays).  Producer
+// and consumers step through the same sequence.
+struct StageIt {
+    int pos, seg;  // first row-space row of the stage, its projection
+    int ra, rs;    // its first row inside the projection, rows
+    __device__ __forceinline__ void settle(const DecodeArgs& a, int r1, int SR) {
+        while (seg + 1 < a.nseg && pos >= a.seg[seg + 1].row0) ++seg;
+        const int send = a.seg[seg].row0 + a.seg[seg].N;
+        rs = min(min(SR, r1 - pos), send - pos);
+        ra = pos - a.seg[seg].row0;
+    }
+    __device__ __forceinline__ void next(const DecodeArgs& a, int r1, int SR) {
+        pos += rs;
+        if (pos < r1) settle(a, r1, SR);
+    }
+};
+
+template <int BITS, bool HAS_ZP, bool LORA>
+__global__ void __launch_bounds__(kDecThreads, 2)
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
+    using U = Unpack<BITS>;
+    constexpr int kWB = U::kWordsPerBlock;
+    constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
+    extern __shared__ __align__(1024) unsigned char sm[];
+
+    const int K = a.K, NR = a.NR;
+    const int nblk = K >> 5;
+    const int nround = (nblk + kBlkPerRound - 1) / kBlkPerRound;
+    const int nblkR = nround * kBlkPerRound;
+    const int rowbytes = K * BITS / 8;
+    const int SR = a.SR, ring = a.ring;
+    const DecLayout L = dec_layout(SR, ring, rowbytes, nblk, nblkR);
+    const uint32_t sb = smem_u32(sm);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = gridDim.x;
+    const int r0 = (int)((long long)blockIdx.x * NR / C), r1 = (int)((long long)(blockIdx.x + 1) * NR / C);
+    unsigned int* status = a.status;
+
+    auto full = [&](int s) { return sb + L.bars + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return sb + L.bars + 8u * (uint32_t)(ring + s); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ring; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kCW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kCW) {
+        // ------------------------------------------------------------ producer
+        if (LORA) cl_arrive();  // the producer takes no part in T: arrive for the partials at once
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            StageIt it = {r0, 0, 0, 0};
+            if (r0 < r1) it.settle(a, r1, SR);
+            for (int st = 0; ok && it.pos < r1; ++st, ++issued, it.next(a, r1, SR)) {
+                const int s = st % ring;
+                const uint32_t par = (uint32_t)(st / ring) & 1u;
+                if (st >= ring && !(ok = mbar_wait(empty(s), par ^ 1u, status))) break;
+                const DecSeg& pj = a.seg[it.seg];
+                const int ra = it.ra, rs = it.rs;
+                const uint64_t total_s = (uint64_t)pj.N * nblk * 2, total_z = (uint64_t)pj.N * nblk;
+                unsigned char* slot = sm + (size_t)s * L.slot;
+                const uint32_t sslot = sb + (uint32_t)s * L.slot;
+                // scales / zero points of the stage's rows: the 16-byte aligned superset;
+                // bytes past the last 16-byte boundary of an array are stored here directly
+                const uint64_t s0 = (uint64_t)ra * nblk * 2, s1 = (uint64_t)(ra + rs) * nblk * 2;
+                const uint64_t s_lo = s0 & ~15ull, s_hi = min((s1 + 15) & ~15ull, total_s & ~15ull);
+                const uint64_t z0 = (uint64_t)ra * nblk, z1 = (uint64_t)(ra + rs) * nblk;
+                const uint64_t z_lo = z0 & ~15ull, z_hi = min((z1 + 15) & ~15ull, total_z & ~15ull);
+                for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
+                    slot[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(pj.S)[i];
+                if (HAS_ZP)
+                    for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) slot[L.zp + (uint32_t)(i - z_lo)] = pj.Z[i];
+                uint32_t bytes = (uint32_t)rs * (uint32_t)rowbytes;
+                if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
+                if (HAS_ZP && z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
+                if (LORA) bytes += (uint32_t)rs * 64u;
+                mbar_arrive_tx(full(s), bytes);
+                const uint8_t* src = pj.Wq + (size_t)ra * rowbytes;
+                const uint32_t cb = (uint32_t)rs * (uint32_t)rowbytes;
+                for (uint32_t off = 0; off < cb; off += 32768u)
+                    bulk_load(sslot + off, src + off, min(32768u, cb - off), full(s));
+                if (s_hi > s_lo)
+                    bulk_load(sslot + L.sc, reinterpret_cast<const uint8_t*>(pj.S) + s_lo, (uint32_t)(s_hi - s_lo),
+                              full(s));
+                if (HAS_ZP && z_hi > z_lo) bulk_load(sslot + L.zp, pj.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
+                if (LORA) bulk_load(sslot + L.b, a.B + (size_t)ra * kRk, (uint32_t)rs * 64u, full(s));
+            }
+            // no copy may still be in flight when the CTA exits (a consumer may have given up)
+            for (int st = issued > ring ? issued - ring : 0; st < issued; ++st)
+                mbar_wait(full(st % ring), (uint32_t)(st / ring) & 1u, status, false);
+        }
+        if (LORA) {  // the T exchange's two phases (see below)
+            cl_wait();
+            cl_arrive();
+            cl_wait();
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int ctid = threadIdx.x;  // 0 .. 255
+    constexpr uint32_t kNamed = 1;  // named barrier of the consumer warps
+
+    // The adapter's A slice, a weight: into registers before waiting for x.  CTA q of the
+    // cluster takes K steps (16 wide) [i S / 64, (i + 1) S / 64) with i = 8 q + warp; a step
+    // is 2 K sub-blocks x 4 rank sub-blocks of 8 x 8, each loaded in its natural fragment
+    // (row = K, thread (g, t) holds ranks 2t, 2t+1 of K row slot_k(g)) and transposed later.
+    constexpr int kMaxSteps = 4;
+    uint32_t areg[kMaxSteps][8];
+    int step0 = 0, nsteps = 0;
+    if constexpr (LORA) {
+        uint32_t qrank;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(qrank));
+        const int S = K / 16, wi = (int)qrank * kCW + warp;
+        step0 = (int)((long long)wi * S / (kCl * kCW));
+        nsteps = (int)((long long)(wi + 1) * S / (kCl * kCW)) - step0;
+#pragma unroll
+        for (int i = 0; i < kMaxSteps; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int kk = (step0 + i) * 16 + (j >> 2) * 8 + slot_k<BITS>(g);
+                areg[i][j] = i < nsteps ? __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t))
+                                        : 0u;
+            }
+    }
+
+    // Restage the scales and zero points of a stage in slot s: per 16-row tile, block
+    // and g, the halves {s_g, s_g+8, zp_g, zp_g+8}; zero past the rows or past K.  The
+    // scale and zero-point copies start at the 16-byte boundary below the first row's.
+    auto restage = [&](const StageIt& it, int s) {
+        const DecSeg& pj = a.seg[it.seg];
+        const int ra = it.ra, rs = it.rs;
+        const unsigned char* slot = sm + (size_t)s * L.slot;
+        const uint32_t s_al = ((uint32_t)ra * (uint32_t)nblk * 2u) & 15u, z_al = ((uint32_t)ra * (uint32_t)nblk) & 15u;
+        const __half* sc = reinterpret_cast<const __half*>(slot + L.sc + s_al);
+        const uint8_t* zq = slot + L.zp + z_al;
+        uint2* rsd = reinterpret_cast<uint2*>(sm + (size_t)s * L.slot + L.rs);
+        const int items = (rs + 15) / 16 * nblkR * 8;
+        for (int i = ctid; i < items; i += kCW * 32) {
+            const int gg = i & 7, b = (i >> 3) % nblkR, tl = (i >> 3) / nblkR;
+            const int ra_ = tl * 16 + gg, rb_ = ra_ + 8;
+            const bool kb = b < nblk;
+            uint32_t sa = 0, sbv = 0, za = 0, zb = 0;
+            if (kb && ra_ < rs) {
+                sa = __half_as_ushort(sc[ra_ * nblk + b]);
+                za = __half_as_ushort(__uint2half_rn(HAS_ZP ? (uint32_t)zq[ra_ * nblk + b] : kDefaultZp));
+            }
+            if (kb && rb_ < rs) {
+                sbv = __half_as_ushort(sc[rb_ * nblk + b]);
+                zb = __half_as_ushort(__uint2half_rn(HAS_ZP ? (uint32_t)zq[rb_ * nblk + b] : kDefaultZp));
+            }
+            rsd[(tl * nblkR + b) * 8 + gg] = make_uint2(sa | (sbv << 16), za | (zb << 16));
+        }
+        (void)pj;
+    };
+
+    bool ok = true;
+    StageIt it = {r0, 0, 0, 0};
+    if (r0 < r1) {
+        it.settle(a, r1, SR);
+        ok = mbar_wait(full(0), 0u, status);
+        restage(it, 0);
+    }
+    named_barrier_sync(kNamed, kCW * 32);
+
+    // ---- x: wait for the work that produces it, then stage it in the MMA's pair order
+    if (a.x_wait) pdl_wait();
+    {
+        const uint4* xg = reinterpret_cast<const uint4*>(a.X);
+        float* sxs = reinterpret_cast<float*>(sm + L.sxs);
+        for (int i0 = 0; i0 < nblkR * 4; i0 += kCW * 32) {  // one 8-code group per thread, 4 per block
+            const int i = i0 + ctid;  // every lane runs every iteration: the shuffles below
+            const int b = i >> 2, q = i & 3;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (b < nblk) v = __ldg(xg + i);
+            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+            const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+            float part = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            part += __shfl_xor_sync(0xffffffffu, part, 2);
+            if (b >= nblkR) continue;
+            if (q == 0) sxs[b] = part * kUnit;
+            unsigned char* xb = sm + L.xs + (uint32_t)b * 64u;
+            if constexpr (BITS == 4) {  // word q of the block: (x0,x4) (x2,x6) | (x1,x5) (x3,x7)
+                *reinterpret_cast<uint2*>(xb + q * 8) = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.y, v.w, 0x5410u));
+                *reinterpret_cast<uint2*>(xb + 32 + q * 8) = make_uint2(prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x7632u));
+            } else {  // words 2q, 2q+1: (x0,x1) (x4,x5) | (x2,x3) (x6,x7)
+                *reinterpret_cast<uint2*>(xb + q * 8) = make_uint2(v.x, v.z);
+                *reinterpret_cast<uint2*>(xb + 32 + q * 8) = make_uint2(v.y, v.w);
+            }
+        }
+        if (ctid < 16) reinterpret_cast<uint32_t*>(sm + L.xs + (uint32_t)nblkR * 64u)[ctid] = 0u;  // zero region
+    }
+    named_barrier_sync(kNamed, kCW * 32);
+
+    // ---- the adapter's partial T over this CTA's K slice (tensor cores), then the exchange
+    if constexpr (LORA) {
+        float tacc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tacc[j][e] = 0.f;
+        for (int i0 = 0; i0 < nsteps; i0 += kMaxSteps) {
+#pragma unroll
+            for (int i = 0; i < kMaxSteps; ++i) {
+                if (i0 + i >= nsteps) break;
+                uint32_t bfr[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (i0 == 0) {
+                        bfr[j] = areg[i][j];
+                    } else {
+                        const int kk = (step0 + i0 + i) * 16 + (j >> 2) * 8 + slot_k<BITS>(g);
+                        bfr[j] = __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t));
+                    }
+                    movmatrix_t(bfr[j]);
+                }
+                // x of the step's two sub-blocks for token row 0 (rows 1..15 of the MMA are empty)
+                const int k0 = (step0 + i0 + i) * 16;
+                const int blk = k0 >> 5, sub = (k0 & 31) >> 3;
+                const uint32_t xo = L.xs + (uint32_t)blk * 64u;
+                const uint32_t x0 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub, t)) : 0u;
+                const uint32_t x1 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub + 1, t)) : 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mma_16816(tacc[j], x0, 0u, x1, 0u, bfr[j], bfr[4 + j]);
+            }
+        }
+        // token row 0: thread (0, t) holds ranks 8j + 2t, 8j + 2t + 1
+        float* tpart = reinterpret_cast<float*>(sm + L.tpart);
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                tpart[warp * kRk + 8 * j + 2 * t] = tacc[j][0];
+                tpart[warp * kRk + 8 * j + 2 * t + 1] = tacc[j][1];
+            }
+        }
+        named_barrier_sync(kNamed, kCW * 32);
+        if (warp == 0) {  // the CTA's partial: warps added in order
+            float sum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) sum += tpart[w * kRk + lane];
+            tpart[kCW * kRk + lane] = sum;
+        }
+        cl_arrive();  // each writer releases its own writes
+    }
+
+    // ---- the stages.  Every warp takes rounds warp, warp + 8, ... of every 16-row tile
+    // of a stage, so a row's summation order depends on K alone, never on how rows
+    // were split into CTAs or stages.
+    float* red = reinterpret_cast<float*>(sm + L.red);
+    float* lorab = reinterpret_cast<float*>(sm + L.lora);
+    const float* sxs = reinterpret_cast<const float*>(sm + L.sxs);
+    // B operand streams: thread (g, t) carries x for column g, i.e. stream 0 when
+    // g == 2t (class 0 of block t) and stream 1 when g == 2t + 1; else the zero region.
+    const bool act0 = g == 2 * t, act1 = g == 2 * t + 1;
+    const uint32_t zero_off = L.xs + (uint32_t)nblkR * 64u;
+    const uint32_t xs0_base = act0 ? L.xs + (uint32_t)t * 64u : zero_off;
+    const uint32_t xs1_base = act1 ? L.xs + (uint32_t)t * 64u + 32u : zero_off;
+    const uint32_t xs0_step = act0 ? 256u : 0u, xs1_step = act1 ? 256u : 0u;  // 4 blocks a round
+    const int tiles_max = SR / 16;
+
+    for (int st = 0; it.pos < r1; ++st, it.next(a, r1, SR)) {
+        const int s = st % ring;
+        const uint32_t par = (uint32_t)(st / ring) & 1u;
+        const DecSeg& pj = a.seg[it.seg];
+        const int ra = it.ra, rs = it.rs;
+        const int ntile = (rs + 15) / 16;
+        if (st > 0) {
+            if (ok) ok = mbar_wait(full(s), par, status);
+            restage(it, s);
+            named_barrier_sync(kNamed, kCW * 32);
+        }
+        const uint32_t soff = (uint32_t)s * L.slot;
+        float* redb = red + (st & 1) * tiles_max * kCW * 16;
+        for (int tl = 0; tl < ntile; ++tl) {
+            // this warp's rounds of tile tl; two accumulators alternate so consecutive
+            // MMAs do not wait on each other
+            float v0 = 0.f, v1 = 0.f;  // rows g and g + 8 of the tile, units of 2^-24
+            const uint32_t wrow = soff + (uint32_t)(tl * 16 + g) * (uint32_t)rowbytes;
+            const uint32_t wrow8 = wrow + 8u * (uint32_t)rowbytes;
+            const uint32_t rsd_tile = soff + L.rs + (uint32_t)(tl * nblkR) * 64u + (uint32_t)g * 8u;
+            for (int rd = warp; ok && rd < nround; rd += kCW) {
+                const int blk = rd * kBlkPerRound + t;  // this thread's block
+                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                const uint32_t wo = (uint32_t)blk * (uint32_t)(kWB * 4);
+                const uint32_t x0o = xs0_base + (uint32_t)rd * xs0_step, x1o = xs1_base + (uint32_t)rd * xs1_step;
+#pragma unroll
+                for (int q = 0; q < kWB / 4; ++q) {  // 16 bytes of each row at a time
+                    const uint4 wa = lds128_raw(sm, wrow + wo + 16u * q), wb = lds128_raw(sm, wrow8 + wo + 16u * q);
+                    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
+                    if constexpr (BITS == 4) {
+                        // words 0..3: x pairs (2 per word and stream) from two 16-byte loads per stream
+                        const uint4 xa0 = lds128_raw(sm, x0o), xa1 = lds128_raw(sm, x0o + 16u);
+                        const uint4 xb0 = lds128_raw(sm, x1o), xb1 = lds128_raw(sm, x1o + 16u);
+                        const uint32_t X0[8] = {xa0.x, xa0.y, xa0.z, xa0.w, xa1.x, xa1.y, xa1.z, xa1.w};
+                        const uint32_t X1[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t pa[4], pb[4];
+                            U::pairs(wA[i], pa);
+                            U::pairs(wB[i], pb);
+                            mma_16816(d[0], pa[0], pb[0], pa[1], pb[1], X0[2 * i], X1[2 * i]);
+                            mma_16816(d[1], pa[2], pb[2], pa[3], pb[3], X0[2 * i + 1], X1[2 * i + 1]);
+                        }
+                    } else {
+                        // words 4q .. 4q+3: one x pair per word and stream
+                        const uint4 xa = lds128_raw(sm, x0o + 16u * q), xb = lds128_raw(sm, x1o + 16u * q);
+                        const uint32_t X0[4] = {xa.x, xa.y, xa.z, xa.w}, X1[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t pa[2], pb[2];
+                            U::pairs(wA[i], pa);
+                            U::pairs(wB[i], pb);
+                            mma_16816(d[i & 1], pa[0], pb[0], pa[1], pb[1], X0[i], X1[i]);
+                        }
+                    }
+                }
+                // columns 2t, 2t+1 of this thread = classes 0, 1 of block rd*4 + t for rows g, g+8
+                const uint2 rsv = *reinterpret_cast<const uint2*>(sm + rsd_tile + (uint32_t)blk * 64u);
+                const float sx = sxs[blk];
+                const float dd0 = d[0][0] + d[1][0], dd1 = d[0][1] + d[1][1];
+                const float dd2 = d[0][2] + d[1][2], dd3 = d[0][3] + d[1][3];
+                // sum_k x q of the block in units of 2^-24 (INT4: class 1, the high nibble, reads as 16 q)
+                float u0 = fmaf(U::kHiWeight, dd1, dd0), u1 = fmaf(U::kHiWeight, dd3, dd2);
+                u0 = fmaf(-h2f_lo(rsv.y), sx, u0);
+                u1 = fmaf(-h2f_hi(rsv.y), sx, u1);
+                v0 = fmaf(h2f_lo(rsv.x), u0, v0);
+                v1 = fmaf(h2f_hi(rsv.x), u1, v1);
+            }
+            // the quad's four blocks, then this warp's rows into the reduction buffer
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+            if (t == 0) {
+                redb[(tl * kCW + warp) * 16 + g] = v0;
+                redb[(tl * kCW + warp) * 16 + g + 8] = v1;
+            }
+        }
+        float* lorb = lorab + (st & 1) * kMaxSR;
+        if constexpr (LORA) {
+            if (st == 0) {
+                // T: every CTA's partial, added in rank order, rounded once
+                cl_wait();
+                if (warp == 0) {
+                    const uint32_t la = smem_u32(reinterpret_cast<float*>(sm + L.tpart) + kCW * kRk + lane);
+                    float tv = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kCl; ++q) tv += ld_peer_f32(la, (uint32_t)q);
+                    const __half th = __float2half_rn(tv);
+                    reinterpret_cast<__half*>(sm + L.t16)[lane] = th;
+                    if (blockIdx.x == 0) a.T[lane] = th;
+                }
+                cl_arrive();
+                named_barrier_sync(kNamed, kCW * 32);
+            }
+            if (warp < ntile) {
+                // sum_r B[n, r] T[r] for tile `warp`'s 16 rows: A = B rows (16 x 16 per MMA),
+                // B = T in column 0
+                const unsigned char* bs = sm + soff + L.b + (uint32_t)(warp * 16) * 64u;
+                const __half* th = reinterpret_cast<const __half*>(sm + L.t16);
+                float dl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kc = 0; kc < 2; ++kc) {
+                    const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
+                    const uint32_t b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
+                    const uint32_t b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
+                    const uint32_t b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
+                    const uint32_t b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
+                    const uint32_t t0 = g == 0 ? *reinterpret_cast<const uint32_t*>(th + 16 * kc + 2 * t) : 0u;
+                    const uint32_t t1 = g == 0 ? *reinterpret_cast<const uint32_t*>(th + 16 * kc + 2 * t + 8) : 0u;
+                    mma_16816(dl, b0r0, b0r8, b8r0, b8r8, t0, t1);
+                }
+                if (t == 0) {  // column 0: rows g, g + 8
+                    lorb[warp * 16 + g] = dl[0];
+                    lorb[warp * 16 + g + 8] = dl[2];
+                }
+            }
+        }
+        named_barrier_sync(kNamed, kCW * 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));  // every read of the slot is done
+        if (warp < ntile && lane < 16) {
+            const int row = warp * 16 + lane;
+            if (ok && row < rs) {
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kCW; ++w) v += redb[(warp * kCW + w) * 16 + lane];  // warp order
+                float y = v * (1.0f / kUnit);
+                if (LORA) y += lorb[row];
+                if (pj.bias) y += __half2float(pj.bias[ra + row]);
+                pj.Y[ra + row] = __float2half_rn(y);
+            }
+        }
+    }
+    if constexpr (LORA) {
+        if (r0 >= r1) {  // no rows: still take part in the exchange
+            cl_wait();
+            if (warp == 0 && blockIdx.x == 0) {
+                const uint32_t la = smem_u32(reinterpret_cast<float*>(sm + L.tpart) + kCW * kRk + lane);
+                float tv = 0.f;
+#pragma unroll
+                for (int q = 0; q < kCl; ++q) tv += ld_peer_f32(la, (uint32_t)q);
+                a.T[lane] = __float2half_rn(tv);
+            }
+            cl_arrive();
+        }
+        cl_wait();  // keep this CTA's partial alive until every peer has read it
+    }
+}
+
+template <int BITS, bool HAS_ZP, bool LORA>
+cudaError_t dec_launch_one(const DecodeArgs& a, int ctas, size_t smem, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (LORA) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = kCl;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, HAS_ZP, LORA>, a);
+}
+
+}  // namespace
+
+bool decode_supported(int bits, int64_t Mt, int K) {
+    return (bits == 4 || bits == 8) && Mt == 1 && K >= 32 && K <= 65536;
+}
+
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem) {
+    const int s = sms > 0 ? sms : 1;
+    int C = (N + 15) / 16;
+    if (C > s) C = s;
+    if (C < 1) C = 1;
+    if (lora) {
+        const int maxc = (s / kCl) * kCl > 0 ? (s / kCl) * kCl : kCl;
+        C = (C + kCl - 1) / kCl * kCl;
+        if (C > maxc) C = maxc;
+    }
+    const int nblk = K / 32, nround = (nblk + kBlkPerRound - 1) / kBlkPerRound, nblkR = nround * kBlkPerRound;
+    const int rowbytes = K * bits / 8;
+    const int rmax = (N + C - 1) / C;
+    // The whole share in one stage when it fits next to a second CTA of the next call
+    // (113 KB each); else a ring of 16- or 32-row stages in up to ~200 KB, one CTA per SM.
+    // stage rows: 16, 32, 64 or 128 (the tiles of a stage divide the eight warps)
+    int sr = 16;
+    while (sr < rmax) sr *= 2;
+    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR).total <= 113u * 1024u) {
+        *SR = sr;
+        *ring = 1;
+    } else {
+        const int sr2 = nround >= 8 ? 16 : 32;
+        int r = 1;
+        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR).total <= 200u * 1024u) ++r;
+        *SR = sr2;
+        *ring = r;
+    }
+    *ctas = C;
+    *smem = dec_layout(*SR, *ring, rowbytes, nblk, nblkR).total;
+}
+
+cudaError_t decode_prepare() {
+    cudaError_t e = cudaSuccess;
+#define MNB_DEC_SET(B, Z, L)                                                                                       \
+    if (e == cudaSuccess)                                                                                          \
+        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    MNB_DEC_SET(4, false, false) MNB_DEC_SET(4, true, false) MNB_DEC_SET(4, false, true) MNB_DEC_SET(4, true, true)
+    MNB_DEC_SET(8, false, false) MNB_DEC_SET(8, true, false) MNB_DEC_SET(8, false, true) MNB_DEC_SET(8, true, true)
+#undef MNB_DEC_SET
+    return e;
+}
+
+cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, cudaStream_t st) {
+    DecodeArgs a = a_in;
+    int C, SR, ring;
+    size_t smem;
+    const int bits = a.bits;
+    decode_geometry(a.NR, a.K, bits, rank > 0, sms, &C, &SR, &ring, &smem);
+    if (smem > 227 * 1024) return cudaErrorNotSupported;
+    a.SR = SR;
+    a.ring = ring;
+    const bool zp = a.seg[0].Z != nullptr, lora = rank > 0;
+    if (bits == 4) {
+        if (lora) return zp ? dec_launch_one<4, true, true>(a, C, smem, pdl, st) : dec_launch_one<4, false, true>(a, C, smem, pdl, st);
+        return zp ? dec_launch_one<4, true, false>(a, C, smem, pdl, st) : dec_launch_one<4, false, false>(a, C, smem, pdl, st);
+    }
+    if (lora) return zp ? dec_launch_one<8, true, true>(a, C, smem, pdl, st) : dec_launch_one<8, false, true>(a, C, smem, pdl, st);
+    return zp ? dec_launch_one<8, true, false>(a, C, smem, pdl, st) : dec_launch_one<8, false, false>(a, C, smem, pdl, st);
+}
+
+}  // namespace mnb

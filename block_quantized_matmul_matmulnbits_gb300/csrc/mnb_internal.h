@@ -17,6 +17,11 @@ constexpr unsigned int kStatusTimeout = 1u;
 
 // Host-side TMA descriptors (tensor_map.cu).
 cudaError_t tensor_map_prepare();
+// Process-unique identity of the calling thread's current context (the
+// device's primary context is made current first if none is).  Cached device
+// addresses and kernel attributes are valid only in the context they were
+// obtained in.
+cudaError_t current_context_id(unsigned long long* id);
 // Byte matrix [rows, rowbytes] (rowbytes % 256 == 0) seen as [rows][rowbytes/256][256]:
 // one box copies `box_rows` rows x `box_chunks` 256-byte pieces, rows `box_chunks*256`
 // bytes apart in shared memory.
@@ -70,6 +75,38 @@ cudaError_t gemv_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, boo
 // plan with 8 token rows per CTA.  cudaErrorNotSupported when K is too large to stage.
 cudaError_t gemv_q8x_launch(const GemvArgs& a, const mnb_plan_info& p, int bits, bool pdl, cudaStream_t st);
 
+// Single-token decode kernel (decode.cu): one token row, INT4 or INT8 weights,
+// up to kMaxSeg projections of the same x laid end to end in one row space
+// (rows [row0, row0 + N) belong to projection i), the optional FP16 rank-32
+// adapter (one projection only; T computed in the same launch) and biases.
+struct DecSeg {
+    int row0;            // first row of this projection in the row space
+    int N;               // its rows
+    const uint8_t* Wq;   // [N, K*bits/8]
+    const __half* S;     // [N, K/32]
+    const uint8_t* Z;    // [N, K/32] or nullptr (default 2^(bits-1)); all projections alike
+    const __half* bias;  // [N] or nullptr
+    __half* Y;           // [1, N]
+};
+struct DecodeArgs {
+    int nseg;            // projections (>= 1)
+    int NR;              // rows of the row space (sum of the projections' N)
+    DecSeg seg[kMaxSeg];
+    const __half* X;     // [1, K]
+    const __half* A;     // [K, 32] (adapter only)
+    const __half* B;     // [N, 32] (adapter only)
+    __half* T;           // [1, 32]: T on return (adapter only)
+    int K, bits;
+    int SR, ring;        // rows per stage and stage slots (set by the launcher)
+    int x_wait;          // X may be written by the work queued before this kernel
+    unsigned int* status;
+};
+bool decode_supported(int bits, int64_t Mt, int K);
+// CTAs, rows per stage, stage slots and shared memory of a launch.
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem);
+cudaError_t decode_prepare();
+cudaError_t decode_launch(const DecodeArgs& a, int rank, int sms, bool pdl, cudaStream_t st);
+
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.
 cudaError_t lora_down_prepare();
 cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st);
@@ -115,6 +152,17 @@ cudaError_t wait_check_launch(unsigned int* status, long long limit_cycles, cuda
 // Xq[m, k] / Xs[m, k/32]: the int8 activation codes and binary32 block scales the
 // int8-activation path computes (same device function), codes in K order.
 cudaError_t quantize_x_launch(const __half* X, int Mt, int K, int8_t* Xq, float* Xs, cudaStream_t st);
+
+// The fixed T scratch of mnb_run_noalloc (noalloc.cu): the most token rows it
+// holds, and its device address in the current context (looked up with
+// cudaGetSymbolAddress once per device and context).
+constexpr int64_t kNoallocMaxRows = 8192;
+int noalloc_scratch(__half** out);
+// mnb_run with T in that scratch instead of a caller buffer (api.cu): the
+// arguments, validation order and results of mnb_run; adapter calls with more
+// than kNoallocMaxRows token rows return MNB_ERR_UNSUPPORTED.
+int run_noalloc(mnb_handle h, const void* X, const void* Wq, const void* scales, const void* zp, const void* A,
+                const void* B, int32_t rank, void* Y, int64_t batch, int64_t M, void* stream);
 
 // W16[n, k] = fp16((q - zp) * scale) with the kernels' own dequant arithmetic.
 cudaError_t dequant_launch(const uint8_t* Wq, const __half* S, const uint8_t* Z, int N, int K, int bits,

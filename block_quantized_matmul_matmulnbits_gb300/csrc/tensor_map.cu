@@ -1,6 +1,8 @@
-// tensor_map.cu -- host-side TMA descriptor encoding shared by the kernels.
-// cuTensorMapEncodeTiled is fetched from the driver through the runtime, so
-// the library links only the (static) CUDA runtime.
+// tensor_map.cu -- host-side TMA descriptor encoding shared by the kernels,
+// and the identity of the current context.  The driver functions
+// (cuTensorMapEncodeTiled, cuCtxGetCurrent, cuCtxGetId) are fetched from the
+// driver through the runtime, so the library links only the (static) CUDA
+// runtime.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -13,16 +15,48 @@ namespace mnb {
 namespace {
 std::mutex g_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+cudaError_t driver_fn(const char* name, int version, void** fn) {
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    return q == cudaDriverEntryPointSuccess && *fn ? cudaSuccess : cudaErrorNotSupported;
+}
 }  // namespace
+
+cudaError_t current_context_id(unsigned long long* id) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_ctx_current || !g_ctx_id) {
+            void *a = nullptr, *b = nullptr;
+            cudaError_t e = driver_fn("cuCtxGetCurrent", 4000, &a);
+            if (e == cudaSuccess) e = driver_fn("cuCtxGetId", 12000, &b);
+            if (e != cudaSuccess) return e;
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+        }
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+    if (!ctx) {
+        // the runtime creates the device's primary context lazily: make it current
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaSetDevice(dev);
+        if (e != cudaSuccess) return e;
+        if (g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx) return cudaErrorUnknown;
+    }
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
 
 cudaError_t tensor_map_prepare() {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_encode) return cudaSuccess;
     void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    const cudaError_t e = driver_fn("cuTensorMapEncodeTiled", 12000, &fn);
     if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     return cudaSuccess;
 }

@@ -303,16 +303,17 @@ int mnb_lora_down(const void* X, const void* A, void* T, int64_t Mt, int64_t K, 
  * cudaMalloc / cudaFree are not allowed because they can synchronize the
  * device.  The pages have no counterpart to this entry point; it exists only
  * for such callers.
- *   Arguments and results are those of mnb_run, minus T_ws.  T lives in a
- *   fixed array inside the library's device memory (512 KiB on every GPU that
- *   loads the library, held until the process exits), so at most
- *   mnb_noalloc_max_rows() = 8192 token rows (batch * M) are accepted when an
- *   adapter is given; larger calls return MNB_ERR_UNSUPPORTED and launch
- *   nothing.  Without an adapter there is no limit.
+ *   Arguments, argument checks (in the same order) and results are those of
+ *   mnb_run, minus T_ws.  T lives in a fixed array inside the library's
+ *   device memory (512 KiB on every GPU that loads the library, held until
+ *   the process exits), so at most mnb_noalloc_max_rows() = 8192 token rows
+ *   (batch * M) are accepted when an adapter is given; larger calls return
+ *   MNB_ERR_UNSUPPORTED and launch nothing.  Without an adapter there is no
+ *   limit.
  *   No cudaMalloc, cudaFree or other allocating call is made.  The first call
- *   with an adapter on a device looks up the array's device address
- *   (cudaGetSymbolAddress) for that device; make that first call before any
- *   stream capture.
+ *   with an adapter in a context (per device; again after the device's
+ *   current context changed) looks up the array's device address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
  *   Every call shares the one array: calls whose kernels may overlap on the
  *   GPU (other streams, or other host threads without ordering) race on it. */
 int mnb_run_noalloc(mnb_handle h,

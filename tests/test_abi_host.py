@@ -1,9 +1,17 @@
 """Host-side checks of libmnb.so that need no GPU: the library loads, exports
 every entry point include/mnb.h declares, validates its arguments and makes
-the dispatch decision from the per-matrix row count.  No compute call here."""
+the dispatch decision from the per-matrix row count.  No compute call here.
+
+The argument checks pass made-up device addresses (0x1000, ...) that are never
+dereferenced because the call is rejected first.  They run in a child process
+that sees no GPU (CUDA_VISIBLE_DEVICES=""), so on a machine with a GPU a
+regression in the checks returns MNB_ERR_NO_DEVICE instead of launching a
+kernel on those addresses."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -17,6 +25,18 @@ from block_quantized_matmul_matmulnbits_gb300 import mnb
 def built():
     mnb_build.build()
     yield
+
+
+def run_without_gpu(fn):
+    """Run the module-level function `fn` of this file in a child process in
+    which no GPU is visible; its assertion failures fail the calling test."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    here = os.path.dirname(os.path.abspath(__file__))
+    mod = os.path.splitext(os.path.basename(fn.__code__.co_filename))[0]
+    code = (f"import sys; sys.path[:0] = [{here!r}, {ROOT!r}]; import {mod} as m; m.{fn.__name__}(); "
+            "print('child ok')")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-4000:] + r.stderr[-4000:]
 
 
 def declared_symbols():
@@ -77,7 +97,10 @@ def test_route_follows_per_matrix_rows_not_batch():
         assert mnb.mnb_plan(h, 2, 512, 0, 152)["route"] == mnb.ROUTE_GEMM
         assert mnb.mnb_plan(h, 0, 5, 0, 152)["route"] == mnb.ROUTE_NONE
         assert mnb.mnb_plan(h, 3, 0, 0, 152)["route"] == mnb.ROUTE_NONE
-        assert mnb.mnb_plan(h, 1, 1, 32, 152)["lora_kernel"] == 1
+        # one token row: the adapter runs inside the single-token decode kernel (one launch);
+        # more token rows: the LoRA down kernel first
+        assert mnb.mnb_plan(h, 1, 1, 32, 152)["lora_kernel"] == 0
+        assert mnb.mnb_plan(h, 1, 2, 32, 152)["lora_kernel"] == 1
         assert mnb.mnb_plan(h, 1, 1, 0, 152)["lora_kernel"] == 0
     finally:
         mnb.mnb_destroy(h)
@@ -109,7 +132,7 @@ def test_gemv_plan_balances_rows_over_sms():
     for N, K, bits in ((4096, 4096, 4), (14336, 4096, 4), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4)):
         h = mnb.mnb_create(N, K, bits)
         try:
-            p = mnb.mnb_plan(h, 1, 1, 0, 152)
+            p = mnb.mnb_plan(h, 1, 2, 0, 152)
             R, C, G = p["rows_per_cta"], p["grid_x"], -(-N // 16)
             # whole 16-row groups dealt out evenly: the largest share is ceil(G / C) groups
             assert C <= G and R == 16 * -(-G // C)
@@ -124,7 +147,44 @@ def test_gemv_plan_balances_rows_over_sms():
             mnb.mnb_destroy(h)
 
 
-def test_run_validation_needs_no_device():
+def test_single_token_plan_splits_rows_evenly():
+    # one token row: rows split evenly over one CTA per SM (any row count, not 16-row
+    # groups), a cluster-of-8 grid with an adapter, stages of 16..128 rows
+    for N, K, bits in ((4096, 4096, 4), (14336, 4096, 4), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4),
+                       (256, 256, 4), (5, 64, 8)):
+        h = mnb.mnb_create(N, K, bits)
+        try:
+            for rank in (0, 32):
+                p = mnb.mnb_plan(h, 1, 1, rank, 152)
+                C, R, SR = p["grid_x"], p["rows_per_cta"], p["k_splits"]
+                assert p["route"] == mnb.ROUTE_GEMV and p["tokens_per_cta"] == 1 and p["lora_kernel"] == 0
+                assert p["grid_y"] == 1 and p["block_threads"] == 288
+                assert 1 <= C <= 152 and R == -(-N // C)
+                assert C <= max(1, -(-N // 16)) or rank
+                if rank:
+                    assert C % 8 == 0
+                assert SR in (16, 32, 64, 128)
+                # shares differ by at most one row
+                shares = [(c + 1) * N // C - c * N // C for c in range(C)]
+                assert max(shares) - min(shares) <= 1 and sum(shares) == N
+        finally:
+            mnb.mnb_destroy(h)
+    # the headline decode shape: 4096 rows over 152 CTAs, 26 or 27 rows each, in one stage
+    h = mnb.mnb_create(4096, 4096, 4)
+    try:
+        p = mnb.mnb_plan(h, 1, 1, 32, 152)
+        assert p["grid_x"] == 152 and p["rows_per_cta"] == 27 and p["k_splits"] == 32
+    finally:
+        mnb.mnb_destroy(h)
+    # INT2, or the int8-activation entry point, keep the multi-token decode kernel
+    h = mnb.mnb_create(4096, 4096, 2)
+    try:
+        assert mnb.mnb_plan(h, 1, 1, 0, 152)["tokens_per_cta"] == 8
+    finally:
+        mnb.mnb_destroy(h)
+
+
+def check_run_validation_needs_no_device():
     h = mnb.mnb_create(64, 64, 4)
     try:
         def rc(**kw):
@@ -157,7 +217,7 @@ def test_run_validation_needs_no_device():
         mnb.mnb_destroy(h0)
 
 
-def test_qlora_validation_needs_no_device():
+def check_qlora_validation_needs_no_device():
     h = mnb.mnb_create(64, 64, 4)
     try:
         def rc(**kw):
@@ -179,7 +239,7 @@ def test_qlora_validation_needs_no_device():
         mnb.mnb_destroy(h)
 
 
-def test_multi_projection_validation_needs_no_device():
+def check_multi_projection_validation_needs_no_device():
     h = mnb.mnb_create(96, 64, 4)
     try:
         def rc(projs, M=1, X=0x1000):
@@ -203,7 +263,7 @@ def test_multi_projection_validation_needs_no_device():
         mnb.mnb_destroy(h)
 
 
-def test_dequant_and_lora_down_validation_needs_no_device():
+def check_dequant_and_lora_down_validation_needs_no_device():
     L = mnb.lib()
     assert L.mnb_check_wait_timeout(10, None) == mnb.MNB_ERR_ARG
     assert L.mnb_check_wait_timeout(5_000_000_000, None) == mnb.MNB_ERR_ARG
@@ -248,3 +308,19 @@ def test_gemm_plan_splits_k_only_when_tiles_are_few():
         assert mnb.mnb_plan(h, 1, 1, 0, 152)["k_splits"] == 8
     finally:
         mnb.mnb_destroy(h)
+
+
+def test_run_validation_needs_no_device():
+    run_without_gpu(check_run_validation_needs_no_device)
+
+
+def test_qlora_validation_needs_no_device():
+    run_without_gpu(check_qlora_validation_needs_no_device)
+
+
+def test_multi_projection_validation_needs_no_device():
+    run_without_gpu(check_multi_projection_validation_needs_no_device)
+
+
+def test_dequant_and_lora_down_validation_needs_no_device():
+    run_without_gpu(check_dequant_and_lora_down_validation_needs_no_device)
