@@ -185,6 +185,16 @@ __device__ __forceinline__ void mma_16816(float d[4], uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with C = 0: D = A * B (no accumulator input to clear first).
+__device__ __forceinline__ void mma_16816_z(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                            uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // D = A(16x32 u8, row) * B(32x8 s8, col), exact int32, C = 0: the integer dot
 // of the int8-activation path (weight codes unsigned, activation codes signed).
 __device__ __forceinline__ void mma_16832_u8s8(int d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

@@ -13,9 +13,11 @@
 //  * Rows are split evenly over the CTAs (one per SM): CTA c owns rows
 //    [c N / C, (c + 1) N / C), so every SM moves the same number of weight
 //    bytes.  Its rows are contiguous in memory: one producer lane streams them
-//    into shared memory in stages of up to SR rows (codes, scales, zero points
-//    and the adapter rows B[n, :], each a 1-D bulk copy), and when the CTA's
-//    whole share fits it is copied before anything else happens.  Weights are
+//    into shared memory in stages of up to SR rows (codes and adapter rows
+//    B[n, :] as 1-D bulk copies, scales and zero points as 2-D TMA boxes whose
+//    rows are 16 bytes wider than the data, so that reading one value from
+//    each of eight rows is free of bank conflicts), and when the CTA's whole
+//    share fits it is copied before anything else happens.  Weights are
 //    constant, so the copies start before the work queued ahead of this
 //    kernel has finished (programmatic dependent launch); only x waits for it.
 //  * The multiply runs on mma.sync m16n8k16 (FP16 in, FP32 accumulate) with 16
@@ -26,12 +28,11 @@
 //    token row would leave idle, each collect one (block, class) of codes:
 //    thread t of a quad owns block t of a group of four blocks, its A pairs
 //    go to columns 2t and 2t + 1, and only the threads supplying those
-//    columns carry x in their B fragment.  After a group of four blocks each
-//    thread holds, for its two rows, the block sums sum_k x q of its block, and
-//    applies the block's scale and zero point once, in FP32:
+//    columns carry x in their B fragment (x is staged per thread role, so a B
+//    fragment is one 16-byte load, zeros included).  After a group of four
+//    blocks each thread holds, for its two rows, the block sums sum_k x q of
+//    its block, and applies the block's scale and zero point once, in FP32:
 //        y += s * (sum_k x q - zp * sum_k x).
-//    The scale and zero point of every (row, block) are restaged into a
-//    bank-conflict-free layout while the stage waits for x.
 //  * The adapter: the CTAs of a cluster of eight each take 1/8 of K, hold
 //    their slice of A in registers (prefetched with the weights), form T's
 //    partial sums on the tensor cores (movmatrix turns A's rows into the MMA's
@@ -39,9 +40,16 @@
 //    every CTA adds the eight partials in rank order, so T is bitwise
 //    reproducible, rounds T once to FP16 and adds sum_r T[r] B[n, r] (two
 //    MMAs per 16 rows) before the one rounding of each output.
-//  * Eight consumer warps split a stage's rounds; their partial sums are added
-//    in warp order (no atomics): results are deterministic.
+//  * Eight consumer warps split every 16-row tile's rounds (warp w takes
+//    rounds w, w + 8, ...), so a row's summation order depends on K alone;
+//    partial sums are added in warp order (no atomics): results are
+//    deterministic and independent of how rows were split into CTAs.
 //  * Every mbarrier wait is bounded and reports through the status word.
+#include <cuda.h>
+
+#include <cstring>
+#include <type_traits>
+
 #include "common.cuh"
 #include "mnb_internal.h"
 
@@ -61,28 +69,72 @@ __device__ __forceinline__ uint4 lds128_raw(const unsigned char* sm, uint32_t of
     return *reinterpret_cast<const uint4*>(sm + off);
 }
 
+// Shared-memory loads at a 32-bit shared address plus an immediate offset.
+// Volatile: they stay after the barrier waits before them in program order.
+template <int OFF = 0>
+__device__ __forceinline__ uint4 lds128_s(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a), "n"(OFF));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16_s(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8_s(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32_s(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+
 __host__ __device__ inline uint32_t al128(uint32_t x) { return (x + 127u) & ~127u; }
 
+// How a stage's scales and zero points land in shared memory: rows `spitch` /
+// `zpitch` bytes apart.  With TMA boxes the rows carry 16 bytes of padding (the
+// box is wider than the tensor, the extra columns read as zero); with bulk
+// copies they are dense, starting at a 16-byte aligned superset.
+struct DecPitch {
+    int tma_s, tma_z;      // copied as 2-D TMA boxes (else 1-D bulk copies)
+    uint32_t spitch, zpitch;
+};
+
+__host__ __device__ inline DecPitch dec_pitch(int nblk) {
+    DecPitch p;
+    p.tma_s = nblk % 8 == 0 && nblk + 8 <= 256;    // 16-byte global rows, box within 256 elements
+    p.tma_z = nblk % 16 == 0 && nblk + 16 <= 256;
+    p.spitch = p.tma_s ? (uint32_t)(nblk + 8) * 2u : (uint32_t)nblk * 2u;
+    p.zpitch = p.tma_z ? (uint32_t)(nblk + 16) : (uint32_t)nblk;
+    return p;
+}
+
 // Shared memory plan, identical on host and device.  A stage slot holds SR
-// rows: codes [SR][rowbytes], scales and zero points as copied (a 16-byte
-// aligned superset), adapter rows [SR][32] FP16, and the restaged
-// {s_g, s_g+8, zp_g, zp_g+8} halves of each (16-row tile, block, g).
+// rows: codes [SR][rowbytes], scales [SR][spitch], zero points [SR][zpitch]
+// (each + 32 bytes for the aligned superset of a bulk copy) and adapter rows
+// [SR][32] FP16.
 struct DecLayout {
-    uint32_t sc, zp, b, rs, slot;           // offsets inside a slot, slot bytes
+    uint32_t sc, zp, b, slot;  // offsets inside a slot, slot bytes
     uint32_t xs, sxs, red, lora, tpart, t16, bars, total;
 };
 
 __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, int nblk, int nblkR) {
+    const DecPitch P = dec_pitch(nblk);
     DecLayout L;
     L.sc = al128((uint32_t)SR * (uint32_t)rowbytes);
-    L.zp = al128(L.sc + (uint32_t)SR * (uint32_t)nblk * 2u + 32u);
-    L.b = al128(L.zp + (uint32_t)SR * (uint32_t)nblk + 32u);
-    L.rs = al128(L.b + (uint32_t)SR * 64u);
-    L.slot = al128(L.rs + (uint32_t)(SR / 16) * (uint32_t)nblkR * 64u);
+    L.zp = al128(L.sc + (uint32_t)SR * P.spitch + 32u);
+    L.b = al128(L.zp + (uint32_t)SR * P.zpitch + 32u);
+    L.slot = al128(L.b + (uint32_t)SR * 64u);
     uint32_t off = (uint32_t)ring * L.slot;
-    L.xs = off;  // x in the MMA's pair order, 64 bytes a block, then a 64-byte zero region
-    off = al128(off + (uint32_t)nblkR * 64u + 64u);
-    L.sxs = off;  // per block: sum of x, times 2^-E
+    L.xs = off;  // x in the MMA's operand order: 128 bytes a block (two thread roles), then 64 zero bytes
+    off = al128(off + (uint32_t)nblkR * 128u + 64u);
+    L.sxs = off;  // per block: sum of x, times 2^-24
     off = al128(off + (uint32_t)nblkR * 4u);
     L.red = off;  // two buffers [SR / 16][kCW][16] FP32
     off += 2u * (uint32_t)(SR / 16) * kCW * 16u * 4u;
@@ -127,21 +179,34 @@ struct Unpack<8> {
     }
 };
 
-// Byte offset, inside a block's 64 bytes of staged x, of the pair that MMA
-// slot pair sp (0..3) of sub-block `sub` (8 consecutive codes) takes.  The
-// slot order follows the unpacking above, so the T projection reads the same
-// staged x as the base.
+// Staged x, per block (128 bytes): role 0 (threads carrying class 0) then role 1,
+// 64 bytes each, every B fragment (b0, b1) one 8-byte pair with the other role's
+// half zero.  INT4, word i (codes 8i .. 8i+7 of the block): role 0 at 16 i holds
+// {(x0, x4), 0, (x2, x6), 0}, role 1 at 64 + 16 i holds {0, (x1, x5), 0, (x3, x7)}.
+// INT8, word i (codes 4i .. 4i+3): role 0 at 8 i holds {(x0, x1), 0}, role 1 at
+// 64 + 8 i holds {0, (x2, x3)}.
+// Byte offset inside a block of the x pair that slot pair sp (0..3) of sub-block
+// `sub` (8 consecutive codes) takes in the T projection, whose slots follow the
+// same pairing.
 template <int BITS>
 __device__ __forceinline__ uint32_t xs_pair_off(int sub, int sp) {
     if constexpr (BITS == 4)  // sub-block = one word: slots (0,1)=(x0,x4) (2,3)=(x2,x6) (4,5)=(x1,x5) (6,7)=(x3,x7)
-        return (uint32_t)((sp >> 1) * 32 + sub * 8 + (sp & 1) * 4);
+        return (uint32_t)((sp >> 1) * 68 + sub * 16 + (sp & 1) * 8);
     else  // sub-block = words 2 sub, 2 sub + 1: slots in natural order
-        return (uint32_t)((sp & 1) * 32 + (2 * sub + (sp >> 1)) * 4);
+        return (uint32_t)((sp & 1) * 68 + (2 * sub + (sp >> 1)) * 8);
 }
 // K offset (0..7) inside a sub-block of MMA slot s.
 template <int BITS>
 __host__ __device__ constexpr int slot_k(int s) {
     return BITS == 4 ? ((s & 1) * 4 + (s >> 2) + ((s >> 1) & 1) * 2) : s;
+}
+
+// A load kept in program order with the other volatile asm (the prefetch before
+// griddepcontrol.wait stays before it).
+__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ void movmatrix_t(uint32_t& x) {
@@ -152,8 +217,15 @@ __device__ __forceinline__ void movmatrix_t(uint32_t& x) {
 __device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
-__device__ __forceinline__ float h2f_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu))); }
-__device__ __forceinline__ float h2f_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+__device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
+// A byte as an exact float, without the conversion unit: 2^23 + z read as binary32, minus 2^23.
+__device__ __forceinline__ float u8f(uint32_t z) { return __uint_as_float(0x4B000000u | z) - 8388608.f; }
+
+// TMA descriptors of the projections' scales and zero points (rows padded in shared memory).
+struct DecMaps {
+    CUtensorMap s[kMaxSeg];
+    CUtensorMap z[kMaxSeg];
+};
 
 // The CTA's rows as a sequence of stages: at most SR rows, never across two
 // projections (each stage is contiguous in one projection's arrays).  Producer
@@ -175,7 +247,7 @@ struct StageIt {
 
 template <int BITS, bool HAS_ZP, bool LORA>
 __global__ void __launch_bounds__(kDecThreads, 2)
-    decode_kernel(const __grid_constant__ DecodeArgs a) {
+    decode_kernel(const __grid_constant__ DecMaps maps, const __grid_constant__ DecodeArgs a) {
     using U = Unpack<BITS>;
     constexpr int kWB = U::kWordsPerBlock;
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
@@ -188,6 +260,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int rowbytes = K * BITS / 8;
     const int SR = a.SR, ring = a.ring;
     const DecLayout L = dec_layout(SR, ring, rowbytes, nblk, nblkR);
+    const DecPitch P = dec_pitch(nblk);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = gridDim.x;
@@ -221,32 +294,48 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                 if (st >= ring && !(ok = mbar_wait(empty(s), par ^ 1u, status))) break;
                 const DecSeg& pj = a.seg[it.seg];
                 const int ra = it.ra, rs = it.rs;
-                const uint64_t total_s = (uint64_t)pj.N * nblk * 2, total_z = (uint64_t)pj.N * nblk;
                 unsigned char* slot = sm + (size_t)s * L.slot;
                 const uint32_t sslot = sb + (uint32_t)s * L.slot;
-                // scales / zero points of the stage's rows: the 16-byte aligned superset;
-                // bytes past the last 16-byte boundary of an array are stored here directly
+                // dense copies: the 16-byte aligned superset of the stage's scales / zero
+                // points; bytes past the last 16-byte boundary of an array are stored here
+                const uint64_t total_s = (uint64_t)pj.N * nblk * 2, total_z = (uint64_t)pj.N * nblk;
                 const uint64_t s0 = (uint64_t)ra * nblk * 2, s1 = (uint64_t)(ra + rs) * nblk * 2;
                 const uint64_t s_lo = s0 & ~15ull, s_hi = min((s1 + 15) & ~15ull, total_s & ~15ull);
                 const uint64_t z0 = (uint64_t)ra * nblk, z1 = (uint64_t)(ra + rs) * nblk;
                 const uint64_t z_lo = z0 & ~15ull, z_hi = min((z1 + 15) & ~15ull, total_z & ~15ull);
-                for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
-                    slot[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(pj.S)[i];
-                if (HAS_ZP)
-                    for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) slot[L.zp + (uint32_t)(i - z_lo)] = pj.Z[i];
                 uint32_t bytes = (uint32_t)rs * (uint32_t)rowbytes;
-                if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
-                if (HAS_ZP && z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
+                if (P.tma_s) {
+                    bytes += (uint32_t)SR * P.spitch;  // a whole box always lands (rows past N read as zero)
+                } else {
+                    for (uint64_t i = max(s_hi, s_lo); i < s1; ++i)
+                        slot[L.sc + (uint32_t)(i - s_lo)] = reinterpret_cast<const uint8_t*>(pj.S)[i];
+                    if (s_hi > s_lo) bytes += (uint32_t)(s_hi - s_lo);
+                }
+                if (HAS_ZP) {
+                    if (P.tma_z) {
+                        bytes += (uint32_t)SR * P.zpitch;
+                    } else {
+                        for (uint64_t i = max(z_hi, z_lo); i < z1; ++i) slot[L.zp + (uint32_t)(i - z_lo)] = pj.Z[i];
+                        if (z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
+                    }
+                }
                 if (LORA) bytes += (uint32_t)rs * 64u;
                 mbar_arrive_tx(full(s), bytes);
                 const uint8_t* src = pj.Wq + (size_t)ra * rowbytes;
                 const uint32_t cb = (uint32_t)rs * (uint32_t)rowbytes;
                 for (uint32_t off = 0; off < cb; off += 32768u)
                     bulk_load(sslot + off, src + off, min(32768u, cb - off), full(s));
-                if (s_hi > s_lo)
+                if (P.tma_s)
+                    tma_load_2d(sslot + L.sc, &maps.s[it.seg], 0, ra, full(s));
+                else if (s_hi > s_lo)
                     bulk_load(sslot + L.sc, reinterpret_cast<const uint8_t*>(pj.S) + s_lo, (uint32_t)(s_hi - s_lo),
                               full(s));
-                if (HAS_ZP && z_hi > z_lo) bulk_load(sslot + L.zp, pj.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
+                if (HAS_ZP) {
+                    if (P.tma_z)
+                        tma_load_2d(sslot + L.zp, &maps.z[it.seg], 0, ra, full(s));
+                    else if (z_hi > z_lo)
+                        bulk_load(sslot + L.zp, pj.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
+                }
                 if (LORA) bulk_load(sslot + L.b, a.B + (size_t)ra * kRk, (uint32_t)rs * 64u, full(s));
             }
             // no copy may still be in flight when the CTA exits (a consumer may have given up)
@@ -284,79 +373,50 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int kk = (step0 + i) * 16 + (j >> 2) * 8 + slot_k<BITS>(g);
-                areg[i][j] = i < nsteps ? __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t))
-                                        : 0u;
+                areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
             }
     }
 
-    // Restage the scales and zero points of a stage in slot s: per 16-row tile, block
-    // and g, the halves {s_g, s_g+8, zp_g, zp_g+8}; zero past the rows or past K.  The
-    // scale and zero-point copies start at the 16-byte boundary below the first row's.
-    auto restage = [&](const StageIt& it, int s) {
-        const DecSeg& pj = a.seg[it.seg];
-        const int ra = it.ra, rs = it.rs;
-        const unsigned char* slot = sm + (size_t)s * L.slot;
-        const uint32_t s_al = ((uint32_t)ra * (uint32_t)nblk * 2u) & 15u, z_al = ((uint32_t)ra * (uint32_t)nblk) & 15u;
-        const __half* sc = reinterpret_cast<const __half*>(slot + L.sc + s_al);
-        const uint8_t* zq = slot + L.zp + z_al;
-        uint2* rsd = reinterpret_cast<uint2*>(sm + (size_t)s * L.slot + L.rs);
-        const int items = (rs + 15) / 16 * nblkR * 8;
-        for (int i = ctid; i < items; i += kCW * 32) {
-            const int gg = i & 7, b = (i >> 3) % nblkR, tl = (i >> 3) / nblkR;
-            const int ra_ = tl * 16 + gg, rb_ = ra_ + 8;
-            const bool kb = b < nblk;
-            uint32_t sa = 0, sbv = 0, za = 0, zb = 0;
-            if (kb && ra_ < rs) {
-                sa = __half_as_ushort(sc[ra_ * nblk + b]);
-                za = __half_as_ushort(__uint2half_rn(HAS_ZP ? (uint32_t)zq[ra_ * nblk + b] : kDefaultZp));
-            }
-            if (kb && rb_ < rs) {
-                sbv = __half_as_ushort(sc[rb_ * nblk + b]);
-                zb = __half_as_ushort(__uint2half_rn(HAS_ZP ? (uint32_t)zq[rb_ * nblk + b] : kDefaultZp));
-            }
-            rsd[(tl * nblkR + b) * 8 + gg] = make_uint2(sa | (sbv << 16), za | (zb << 16));
-        }
-        (void)pj;
-    };
-
-    bool ok = true;
-    StageIt it = {r0, 0, 0, 0};
-    if (r0 < r1) {
-        it.settle(a, r1, SR);
-        ok = mbar_wait(full(0), 0u, status);
-        restage(it, 0);
-    }
-    named_barrier_sync(kNamed, kCW * 32);
-
-    // ---- x: wait for the work that produces it, then stage it in the MMA's pair order
+    // ---- x: wait for the work that produces it, then stage it in the MMA's operand order
     if (a.x_wait) pdl_wait();
     {
         const uint4* xg = reinterpret_cast<const uint4*>(a.X);
         float* sxs = reinterpret_cast<float*>(sm + L.sxs);
-        for (int i0 = 0; i0 < nblkR * 4; i0 += kCW * 32) {  // one 8-code group per thread, 4 per block
-            const int i = i0 + ctid;  // every lane runs every iteration: the shuffles below
-            const int b = i >> 2, q = i & 3;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (b < nblk) v = __ldg(xg + i);
-            const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
-            const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
-            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
-            const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
-            float part = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
-            if (b >= nblkR) continue;
-            if (q == 0) sxs[b] = part * kUnit;
-            unsigned char* xb = sm + L.xs + (uint32_t)b * 64u;
-            if constexpr (BITS == 4) {  // word q of the block: (x0,x4) (x2,x6) | (x1,x5) (x3,x7)
-                *reinterpret_cast<uint2*>(xb + q * 8) = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.y, v.w, 0x5410u));
-                *reinterpret_cast<uint2*>(xb + 32 + q * 8) = make_uint2(prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x7632u));
-            } else {  // words 2q, 2q+1: (x0,x1) (x4,x5) | (x2,x3) (x6,x7)
-                *reinterpret_cast<uint2*>(xb + q * 8) = make_uint2(v.x, v.z);
-                *reinterpret_cast<uint2*>(xb + 32 + q * 8) = make_uint2(v.y, v.w);
+        constexpr int kXU = 4;  // 8-code groups in flight per thread
+        for (int i0 = 0; i0 < nblkR * 4; i0 += kXU * kCW * 32) {  // 4 groups a block
+            uint4 v[kXU];
+#pragma unroll
+            for (int u = 0; u < kXU; ++u) {
+                const int i = i0 + u * kCW * 32 + ctid;
+                v[u] = (i >> 2) < nblk ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kXU; ++u) {
+                if (i0 + u * kCW * 32 >= nblkR * 4) break;  // the same for every thread
+                const int i = i0 + u * kCW * 32 + ctid;  // every lane runs every step: the shuffles below
+                const int b = i >> 2, q = i & 3;
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v[u].x));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v[u].y));
+                const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&v[u].z));
+                const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&v[u].w));
+                float part = ((f0.x + f0.y) + (f1.x + f1.y)) + ((f2.x + f2.y) + (f3.x + f3.y));
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                if (b >= nblkR) continue;
+                if (q == 0) sxs[b] = part * kUnit;
+                unsigned char* xb = sm + L.xs + (uint32_t)b * 128u;
+                if constexpr (BITS == 4) {  // group q = word q: (x0,x4) (x2,x6) | (x1,x5) (x3,x7)
+                    *reinterpret_cast<uint4*>(xb + q * 16) =
+                        make_uint4(prmt(v[u].x, v[u].z, 0x5410u), 0u, prmt(v[u].y, v[u].w, 0x5410u), 0u);
+                    *reinterpret_cast<uint4*>(xb + 64 + q * 16) =
+                        make_uint4(0u, prmt(v[u].x, v[u].z, 0x7632u), 0u, prmt(v[u].y, v[u].w, 0x7632u));
+                } else {  // group q = words 2q, 2q+1: (x0,x1) (x4,x5) | (x2,x3) (x6,x7)
+                    *reinterpret_cast<uint4*>(xb + q * 16) = make_uint4(v[u].x, 0u, v[u].z, 0u);
+                    *reinterpret_cast<uint4*>(xb + 64 + q * 16) = make_uint4(0u, v[u].y, 0u, v[u].w);
+                }
             }
         }
-        if (ctid < 16) reinterpret_cast<uint32_t*>(sm + L.xs + (uint32_t)nblkR * 64u)[ctid] = 0u;  // zero region
+        if (ctid < 16) reinterpret_cast<uint32_t*>(sm + L.xs + (uint32_t)nblkR * 128u)[ctid] = 0u;  // zero region
     }
     named_barrier_sync(kNamed, kCW * 32);
 
@@ -385,7 +445,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                 // x of the step's two sub-blocks for token row 0 (rows 1..15 of the MMA are empty)
                 const int k0 = (step0 + i0 + i) * 16;
                 const int blk = k0 >> 5, sub = (k0 & 31) >> 3;
-                const uint32_t xo = L.xs + (uint32_t)blk * 64u;
+                const uint32_t xo = L.xs + (uint32_t)blk * 128u;
                 const uint32_t x0 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub, t)) : 0u;
                 const uint32_t x1 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub + 1, t)) : 0u;
 #pragma unroll
@@ -411,20 +471,20 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         cl_arrive();  // each writer releases its own writes
     }
 
-    // ---- the stages.  Every warp takes rounds warp, warp + 8, ... of every 16-row tile
-    // of a stage, so a row's summation order depends on K alone, never on how rows
-    // were split into CTAs or stages.
+    // ---- the stages
     float* red = reinterpret_cast<float*>(sm + L.red);
     float* lorab = reinterpret_cast<float*>(sm + L.lora);
-    const float* sxs = reinterpret_cast<const float*>(sm + L.sxs);
-    // B operand streams: thread (g, t) carries x for column g, i.e. stream 0 when
-    // g == 2t (class 0 of block t) and stream 1 when g == 2t + 1; else the zero region.
+    // This thread's x role: class 0 of block t when g == 2t, class 1 when g == 2t + 1,
+    // else the zero region.
     const bool act0 = g == 2 * t, act1 = g == 2 * t + 1;
-    const uint32_t zero_off = L.xs + (uint32_t)nblkR * 64u;
-    const uint32_t xs0_base = act0 ? L.xs + (uint32_t)t * 64u : zero_off;
-    const uint32_t xs1_base = act1 ? L.xs + (uint32_t)t * 64u + 32u : zero_off;
-    const uint32_t xs0_step = act0 ? 256u : 0u, xs1_step = act1 ? 256u : 0u;  // 4 blocks a round
+    const uint32_t xs_base = act0 ? L.xs + (uint32_t)t * 128u
+                           : act1 ? L.xs + (uint32_t)t * 128u + 64u
+                                  : L.xs + (uint32_t)nblkR * 128u;
+    const uint32_t xs_step = act0 || act1 ? (uint32_t)(kCW * kBlkPerRound * 128) : 0u;  // per round of this warp
     const int tiles_max = SR / 16;
+    bool ok = true;
+    StageIt it = {r0, 0, 0, 0};
+    if (r0 < r1) it.settle(a, r1, SR);
 
     for (int st = 0; it.pos < r1; ++st, it.next(a, r1, SR)) {
         const int s = st % ring;
@@ -432,76 +492,138 @@ __global__ void __launch_bounds__(kDecThreads, 2)
         const DecSeg& pj = a.seg[it.seg];
         const int ra = it.ra, rs = it.rs;
         const int ntile = (rs + 15) / 16;
-        if (st > 0) {
-            if (ok) ok = mbar_wait(full(s), par, status);
-            restage(it, s);
-            named_barrier_sync(kNamed, kCW * 32);
-        }
+        if (ok) ok = mbar_wait(full(s), par, status);
         const uint32_t soff = (uint32_t)s * L.slot;
+        // where row 0's scales / zero points start in the slot (dense copies: the aligned superset)
+        const uint32_t s_base = soff + L.sc + (P.tma_s ? 0u : (((uint32_t)ra * (uint32_t)nblk * 2u) & 15u));
+        const uint32_t z_base = soff + L.zp + (P.tma_z ? 0u : (((uint32_t)ra * (uint32_t)nblk) & 15u));
         float* redb = red + (st & 1) * tiles_max * kCW * 16;
-        for (int tl = 0; tl < ntile; ++tl) {
-            // this warp's rounds of tile tl; two accumulators alternate so consecutive
-            // MMAs do not wait on each other
-            float v0 = 0.f, v1 = 0.f;  // rows g and g + 8 of the tile, units of 2^-24
-            const uint32_t wrow = soff + (uint32_t)(tl * 16 + g) * (uint32_t)rowbytes;
-            const uint32_t wrow8 = wrow + 8u * (uint32_t)rowbytes;
-            const uint32_t rsd_tile = soff + L.rs + (uint32_t)(tl * nblkR) * 64u + (uint32_t)g * 8u;
-            for (int rd = warp; ok && rd < nround; rd += kCW) {
-                const int blk = rd * kBlkPerRound + t;  // this thread's block
-                float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                const uint32_t wo = (uint32_t)blk * (uint32_t)(kWB * 4);
-                const uint32_t x0o = xs0_base + (uint32_t)rd * xs0_step, x1o = xs1_base + (uint32_t)rd * xs1_step;
+        // This warp's rounds of NTL tiles at once (the x fragments serve both; their MMA
+        // chains are independent).  Per round: the block sums of the thread's block for
+        // rows g and g + 8 of each tile, then scale and zero point in FP32.
+        auto tiles = [&](auto ntl_c, int tl0) {
+            constexpr int NTL = decltype(ntl_c)::value;
+            float v[NTL][2];
+            // 32-bit shared addresses of this thread's words, scales and zero points in its
+            // first round, for rows g (A) and g + 8 (B) of each tile; all step by 32 blocks
+            uint32_t wA[NTL], wB[NTL], sA_[NTL], sB_[NTL], zA_[NTL], zB_[NTL];
+            const int blk0 = warp * kBlkPerRound + t;  // this thread's block in its first round
+#pragma unroll
+            for (int i = 0; i < NTL; ++i) {
+                v[i][0] = v[i][1] = 0.f;  // rows g and g + 8, units of 2^-24
+                const uint32_t row = (uint32_t)((tl0 + i) * 16 + g);
+                wA[i] = sb + soff + row * (uint32_t)rowbytes + (uint32_t)blk0 * (uint32_t)(kWB * 4);
+                wB[i] = wA[i] + 8u * (uint32_t)rowbytes;
+                sA_[i] = sb + s_base + row * P.spitch + (uint32_t)blk0 * 2u;
+                sB_[i] = sA_[i] + 8u * P.spitch;
+                zA_[i] = sb + z_base + row * P.zpitch + (uint32_t)blk0;
+                zB_[i] = zA_[i] + 8u * P.zpitch;
+            }
+            uint32_t xo = sb + xs_base + (uint32_t)warp * (uint32_t)(kBlkPerRound * 128) * ((act0 || act1) ? 1u : 0u);
+            uint32_t sxa = sb + L.sxs + (uint32_t)blk0 * 4u;
+            constexpr uint32_t kWStep = kCW * kBlkPerRound * kWB * 4, kSStep = kCW * kBlkPerRound * 2,
+                               kZStep = kCW * kBlkPerRound, kXStep = kCW * kBlkPerRound * 4;
+#pragma unroll 1
+            for (int rd = warp; rd < nround; rd += kCW) {
+                // two MMA chains per tile, whatever the tiles processed together (a row's
+                // arithmetic must not depend on it); a chain's first MMA starts from zero
+                constexpr int NCH = 2;
+                float d[NTL][NCH][4];
 #pragma unroll
                 for (int q = 0; q < kWB / 4; ++q) {  // 16 bytes of each row at a time
-                    const uint4 wa = lds128_raw(sm, wrow + wo + 16u * q), wb = lds128_raw(sm, wrow8 + wo + 16u * q);
-                    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w}, wB[4] = {wb.x, wb.y, wb.z, wb.w};
+                    uint4 wa[NTL], wb[NTL];
+#pragma unroll
+                    for (int i = 0; i < NTL; ++i) {
+                        wa[i] = q == 0 ? lds128_s<0>(wA[i]) : lds128_s<16>(wA[i]);
+                        wb[i] = q == 0 ? lds128_s<0>(wB[i]) : lds128_s<16>(wB[i]);
+                    }
                     if constexpr (BITS == 4) {
-                        // words 0..3: x pairs (2 per word and stream) from two 16-byte loads per stream
-                        const uint4 xa0 = lds128_raw(sm, x0o), xa1 = lds128_raw(sm, x0o + 16u);
-                        const uint4 xb0 = lds128_raw(sm, x1o), xb1 = lds128_raw(sm, x1o + 16u);
-                        const uint32_t X0[8] = {xa0.x, xa0.y, xa0.z, xa0.w, xa1.x, xa1.y, xa1.z, xa1.w};
-                        const uint32_t X1[8] = {xb0.x, xb0.y, xb0.z, xb0.w, xb1.x, xb1.y, xb1.z, xb1.w};
+                        // words 0..3: one 16-byte load each = the B pairs of its two MMAs
+                        const uint4 xw[4] = {lds128_s<0>(xo), lds128_s<16>(xo), lds128_s<32>(xo), lds128_s<48>(xo)};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t pa[4], pb[4];
-                            U::pairs(wA[i], pa);
-                            U::pairs(wB[i], pb);
-                            mma_16816(d[0], pa[0], pb[0], pa[1], pb[1], X0[2 * i], X1[2 * i]);
-                            mma_16816(d[1], pa[2], pb[2], pa[3], pb[3], X0[2 * i + 1], X1[2 * i + 1]);
-                        }
+                        for (int w = 0; w < 4; ++w)
+#pragma unroll
+                            for (int i = 0; i < NTL; ++i) {
+                                const uint32_t wa4[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
+                                const uint32_t wb4[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
+                                uint32_t pa[4], pb[4];
+                                U::pairs(wa4[w], pa);
+                                U::pairs(wb4[w], pb);
+                                if (w == 0) {
+                                    mma_16816_z(d[i][0], pa[0], pb[0], pa[1], pb[1], xw[w].x, xw[w].y);
+                                    mma_16816_z(d[i][1], pa[2], pb[2], pa[3], pb[3], xw[w].z, xw[w].w);
+                                } else {
+                                    mma_16816(d[i][0], pa[0], pb[0], pa[1], pb[1], xw[w].x, xw[w].y);
+                                    mma_16816(d[i][1], pa[2], pb[2], pa[3], pb[3], xw[w].z, xw[w].w);
+                                }
+                            }
                     } else {
-                        // words 4q .. 4q+3: one x pair per word and stream
-                        const uint4 xa = lds128_raw(sm, x0o + 16u * q), xb = lds128_raw(sm, x1o + 16u * q);
-                        const uint32_t X0[4] = {xa.x, xa.y, xa.z, xa.w}, X1[4] = {xb.x, xb.y, xb.z, xb.w};
+                        // words 4q .. 4q+3: an 8-byte B pair each
+                        const uint4 xa = q == 0 ? lds128_s<0>(xo) : lds128_s<32>(xo);
+                        const uint4 xb = q == 0 ? lds128_s<16>(xo) : lds128_s<48>(xo);
+                        const uint32_t X[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t pa[2], pb[2];
-                            U::pairs(wA[i], pa);
-                            U::pairs(wB[i], pb);
-                            mma_16816(d[i & 1], pa[0], pb[0], pa[1], pb[1], X0[i], X1[i]);
-                        }
+                        for (int w = 0; w < 4; ++w)
+#pragma unroll
+                            for (int i = 0; i < NTL; ++i) {
+                                const uint32_t wa4[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
+                                const uint32_t wb4[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
+                                uint32_t pa[2], pb[2];
+                                U::pairs(wa4[w], pa);
+                                U::pairs(wb4[w], pb);
+                                if (q == 0 && w < 2)
+                                    mma_16816_z(d[i][w & 1], pa[0], pb[0], pa[1], pb[1], X[2 * w], X[2 * w + 1]);
+                                else
+                                    mma_16816(d[i][w & 1], pa[0], pb[0], pa[1], pb[1], X[2 * w], X[2 * w + 1]);
+                            }
                     }
                 }
-                // columns 2t, 2t+1 of this thread = classes 0, 1 of block rd*4 + t for rows g, g+8
-                const uint2 rsv = *reinterpret_cast<const uint2*>(sm + rsd_tile + (uint32_t)blk * 64u);
-                const float sx = sxs[blk];
-                const float dd0 = d[0][0] + d[1][0], dd1 = d[0][1] + d[1][1];
-                const float dd2 = d[0][2] + d[1][2], dd3 = d[0][3] + d[1][3];
-                // sum_k x q of the block in units of 2^-24 (INT4: class 1, the high nibble, reads as 16 q)
-                float u0 = fmaf(U::kHiWeight, dd1, dd0), u1 = fmaf(U::kHiWeight, dd3, dd2);
-                u0 = fmaf(-h2f_lo(rsv.y), sx, u0);
-                u1 = fmaf(-h2f_hi(rsv.y), sx, u1);
-                v0 = fmaf(h2f_lo(rsv.x), u0, v0);
-                v1 = fmaf(h2f_hi(rsv.x), u1, v1);
+                // columns 2t, 2t+1 of this thread = classes 0, 1 of block 4 rd + t for rows g, g+8
+                const float sx = lds_f32_s(sxa);
+                const bool inK = rd * kBlkPerRound + t < nblk;  // past K: no scale (a dense copy holds other bytes)
+#pragma unroll
+                for (int i = 0; i < NTL; ++i) {
+                    const float sA = inK ? h2f(lds_u16_s(sA_[i])) : 0.f;
+                    const float sB = inK ? h2f(lds_u16_s(sB_[i])) : 0.f;
+                    const float zA = HAS_ZP ? u8f(lds_u8_s(zA_[i])) : (float)kDefaultZp;
+                    const float zB = HAS_ZP ? u8f(lds_u8_s(zB_[i])) : (float)kDefaultZp;
+                    const float dd0 = d[i][0][0] + d[i][1][0], dd1 = d[i][0][1] + d[i][1][1];
+                    const float dd2 = d[i][0][2] + d[i][1][2], dd3 = d[i][0][3] + d[i][1][3];
+                    // sum_k x q of the block in units of 2^-24 (INT4: class 1, the high nibble, reads as 16 q)
+                    const float u0 = fmaf(-zA, sx, fmaf(U::kHiWeight, dd1, dd0));
+                    const float u1 = fmaf(-zB, sx, fmaf(U::kHiWeight, dd3, dd2));
+                    v[i][0] = fmaf(sA, u0, v[i][0]);
+                    v[i][1] = fmaf(sB, u1, v[i][1]);
+                    wA[i] += kWStep;
+                    wB[i] += kWStep;
+                    sA_[i] += kSStep;
+                    sB_[i] += kSStep;
+                    zA_[i] += kZStep;
+                    zB_[i] += kZStep;
+                }
+                xo += xs_step;
+                sxa += kXStep;
             }
             // the quad's four blocks, then this warp's rows into the reduction buffer
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-            v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
-            v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
-            if (t == 0) {
-                redb[(tl * kCW + warp) * 16 + g] = v0;
-                redb[(tl * kCW + warp) * 16 + g + 8] = v1;
+#pragma unroll
+            for (int i = 0; i < NTL; ++i) {
+                float v0 = v[i][0], v1 = v[i][1];
+                v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+                v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+                v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+                v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+                if (t == 0) {
+                    redb[((tl0 + i) * kCW + warp) * 16 + g] = v0;
+                    redb[((tl0 + i) * kCW + warp) * 16 + g + 8] = v1;
+                }
+            }
+        };
+        if (ok) {
+            for (int tl0 = 0; tl0 < ntile; tl0 += 2) {
+                if (tl0 + 1 < ntile)
+                    tiles(std::integral_constant<int, 2>{}, tl0);
+                else
+                    tiles(std::integral_constant<int, 1>{}, tl0);
             }
         }
         float* lorb = lorab + (st & 1) * kMaxSR;
@@ -577,7 +699,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 }
 
 template <int BITS, bool HAS_ZP, bool LORA>
-cudaError_t dec_launch_one(const DecodeArgs& a, int ctas, size_t smem, bool pdl, cudaStream_t st) {
+cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, size_t smem, bool pdl,
+                           cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kDecThreads);
@@ -599,8 +722,14 @@ cudaError_t dec_launch_one(const DecodeArgs& a, int ctas, size_t smem, bool pdl,
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, HAS_ZP, LORA>, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, HAS_ZP, LORA>, maps, a);
 }
+
+constexpr int kMaxDev = 64;
+// Per device: clusters of kCl CTAs the GPU holds at once with two CTAs per SM (a
+// cluster needs kCl SMs of one GPC with room), halved: the clusters one call may
+// use so that the next call's clusters fit beside them.
+int g_cluster_cap[kMaxDev] = {};
 
 }  // namespace
 
@@ -608,31 +737,47 @@ bool decode_supported(int bits, int64_t Mt, int K) {
     return (bits == 4 || bits == 8) && Mt == 1 && K >= 32 && K <= 65536;
 }
 
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem) {
+int decode_cluster_cap() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+        cudaGetLastError();
+        return 0;
+    }
+    return g_cluster_cap[dev];
+}
+
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int cluster_cap, int* ctas, int* SR, int* ring,
+                     size_t* smem) {
     const int s = sms > 0 ? sms : 1;
     int C = (N + 15) / 16;
     if (C > s) C = s;
     if (C < 1) C = 1;
-    if (lora) {
-        const int maxc = (s / kCl) * kCl > 0 ? (s / kCl) * kCl : kCl;
-        C = (C + kCl - 1) / kCl * kCl;
-        if (C > maxc) C = maxc;
+    if (lora) {  // whole clusters of kCl CTAs, at most cluster_cap of them
+        int maxcl = s / kCl;
+        if (cluster_cap > 0 && cluster_cap < maxcl) maxcl = cluster_cap;
+        if (maxcl < 1) maxcl = 1;
+        C = (C + kCl - 1) / kCl;
+        if (C > maxcl) C = maxcl;
+        C *= kCl;
     }
     const int nblk = K / 32, nround = (nblk + kBlkPerRound - 1) / kBlkPerRound, nblkR = nround * kBlkPerRound;
     const int rowbytes = K * bits / 8;
     const int rmax = (N + C - 1) / C;
-    // The whole share in one stage when it fits next to a second CTA of the next call
-    // (113 KB each); else a ring of 16- or 32-row stages in up to ~200 KB, one CTA per SM.
-    // stage rows: 16, 32, 64 or 128 (the tiles of a stage divide the eight warps)
+    // The whole share in one stage when it fits in half an SM's shared memory: two CTAs
+    // per SM, so the next call's CTA prefetches its share while this one finishes.
+    // Larger shares stream through a ring of ~200 KB (one CTA per SM), in stages of at
+    // least ~24 KB (fewer per-stage barriers for short rows).
+    constexpr uint32_t kHalfSm = 112u * 1024u, kRing = 200u * 1024u;
     int sr = 16;
     while (sr < rmax) sr *= 2;
-    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR).total <= 113u * 1024u) {
+    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR).total <= kHalfSm) {
         *SR = sr;
         *ring = 1;
     } else {
-        const int sr2 = nround >= 8 ? 16 : 32;
+        int sr2 = 16;
+        while (sr2 < 64 && dec_layout(sr2, 1, rowbytes, nblk, nblkR).slot < 24u * 1024u) sr2 *= 2;
         int r = 1;
-        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR).total <= 200u * 1024u) ++r;
+        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR).total <= kRing) ++r;
         *SR = sr2;
         *ring = r;
     }
@@ -641,13 +786,37 @@ void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int*
 }
 
 cudaError_t decode_prepare() {
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = tensor_map_prepare();
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
 #define MNB_DEC_SET(B, Z, L)                                                                                       \
     if (e == cudaSuccess)                                                                                          \
-        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);  \
+    if (e == cudaSuccess) /* the largest carveout: two CTAs of up to ~112 KB per SM */                              \
+        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     MNB_DEC_SET(4, false, false) MNB_DEC_SET(4, true, false) MNB_DEC_SET(4, false, true) MNB_DEC_SET(4, true, true)
     MNB_DEC_SET(8, false, false) MNB_DEC_SET(8, true, false) MNB_DEC_SET(8, false, true) MNB_DEC_SET(8, true, true)
 #undef MNB_DEC_SET
+    if (e == cudaSuccess) {
+        // clusters that fit at once with two CTAs per SM (about half an SM of shared memory each)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kCl);
+        cfg.blockDim = dim3(kDecThreads);
+        cfg.dynamicSmemBytes = 110 * 1024;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int ncl = 0;
+        if (cudaOccupancyMaxActiveClusters(&ncl, decode_kernel<4, true, true>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            ncl = 0;
+        }
+        g_cluster_cap[dev] = ncl / 2;
+    }
     return e;
 }
 
@@ -656,17 +825,38 @@ cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, c
     int C, SR, ring;
     size_t smem;
     const int bits = a.bits;
-    decode_geometry(a.NR, a.K, bits, rank > 0, sms, &C, &SR, &ring, &smem);
+    decode_geometry(a.NR, a.K, bits, rank > 0, sms, decode_cluster_cap(), &C, &SR, &ring, &smem);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     a.SR = SR;
     a.ring = ring;
+    // scale / zero-point boxes of SR rows, each row padded to the shared-memory pitch
+    DecMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const int nblk = a.K / 32;
+    const DecPitch P = dec_pitch(nblk);
     const bool zp = a.seg[0].Z != nullptr, lora = rank > 0;
-    if (bits == 4) {
-        if (lora) return zp ? dec_launch_one<4, true, true>(a, C, smem, pdl, st) : dec_launch_one<4, false, true>(a, C, smem, pdl, st);
-        return zp ? dec_launch_one<4, true, false>(a, C, smem, pdl, st) : dec_launch_one<4, false, false>(a, C, smem, pdl, st);
+    for (int i = 0; i < a.nseg; ++i) {
+        cudaError_t e = cudaSuccess;
+        if (P.tma_s)
+            e = encode_2d(&maps.s[i], a.seg[i].S, 2, (uint64_t)nblk, (uint64_t)a.seg[i].N, (uint64_t)nblk * 2,
+                          P.spitch / 2u, (uint32_t)SR, false);
+        if (e == cudaSuccess && zp && P.tma_z)
+            e = encode_2d(&maps.z[i], a.seg[i].Z, 1, (uint64_t)nblk, (uint64_t)a.seg[i].N, (uint64_t)nblk,
+                          P.zpitch, (uint32_t)SR, false);
+        if (e != cudaSuccess) return e;
     }
-    if (lora) return zp ? dec_launch_one<8, true, true>(a, C, smem, pdl, st) : dec_launch_one<8, false, true>(a, C, smem, pdl, st);
-    return zp ? dec_launch_one<8, true, false>(a, C, smem, pdl, st) : dec_launch_one<8, false, false>(a, C, smem, pdl, st);
+    if (bits == 4) {
+        if (lora)
+            return zp ? dec_launch_one<4, true, true>(maps, a, C, smem, pdl, st)
+                      : dec_launch_one<4, false, true>(maps, a, C, smem, pdl, st);
+        return zp ? dec_launch_one<4, true, false>(maps, a, C, smem, pdl, st)
+                  : dec_launch_one<4, false, false>(maps, a, C, smem, pdl, st);
+    }
+    if (lora)
+        return zp ? dec_launch_one<8, true, true>(maps, a, C, smem, pdl, st)
+                  : dec_launch_one<8, false, true>(maps, a, C, smem, pdl, st);
+    return zp ? dec_launch_one<8, true, false>(maps, a, C, smem, pdl, st)
+              : dec_launch_one<8, false, false>(maps, a, C, smem, pdl, st);
 }
 
 }  // namespace mnb

@@ -102,8 +102,12 @@ struct DecodeArgs {
     unsigned int* status;
 };
 bool decode_supported(int bits, int64_t Mt, int K);
-// CTAs, rows per stage, stage slots and shared memory of a launch.
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem);
+// CTAs, rows per stage, stage slots and shared memory of a launch.  cluster_cap:
+// the adapter's clusters that fit on the GPU at once (0: unknown, SMs / 8).
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int cluster_cap, int* ctas, int* SR, int* ring,
+                     size_t* smem);
+// That number for the current device (0 before its setup).
+int decode_cluster_cap();
 cudaError_t decode_prepare();
 cudaError_t decode_launch(const DecodeArgs& a, int rank, int sms, bool pdl, cudaStream_t st);
 
