@@ -101,15 +101,15 @@ int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 // Single-token decode kernel: rows split evenly over one CTA per SM, the
 // adapter (if any) in the same launch.
-void plan_decode(const mnb_desc& d, int rank, int sms, int cluster_cap, mnb_plan_info* p) {
+void plan_decode(const mnb_desc& d, int rank, int sms, mnb_plan_info* p) {
     int ctas, SR, ring;
     size_t smem;
-    mnb::decode_geometry((int)d.N, (int)d.K, d.bits, rank > 0, sms, cluster_cap, &ctas, &SR, &ring, &smem);
+    mnb::decode_geometry((int)d.N, (int)d.K, d.bits, rank > 0, sms, &ctas, &SR, &ring, &smem);
     p->route = MNB_ROUTE_GEMV;
     p->lora_kernel = 0;
     p->grid_x = ctas;
     p->grid_y = 1;
-    p->block_threads = 288;
+    p->block_threads = rank > 0 ? 320 : 288;
     p->rows_per_cta = (int)((d.N + ctas - 1) / ctas);
     p->k_splits = SR;
     p->tokens_per_cta = 1;
@@ -149,7 +149,7 @@ void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
 // fused_ok: the call's variant can run on the single-token decode kernel (FP16 or
 // no adapter, FP16 activations, one projection).
 int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p,
-              bool fused_ok = true, int cluster_cap = 0) {
+              bool fused_ok = true) {
     *p = mnb_plan_info{};
     const int64_t Mt = batch * M;
     if (Mt == 0 || d.N == 0) {
@@ -164,8 +164,8 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
     int route = M <= thr ? MNB_ROUTE_GEMV : MNB_ROUTE_GEMM;
     if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
     if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
-    if (route == MNB_ROUTE_GEMV && fused_ok && mnb::decode_supported(d.bits, Mt, (int)d.K)) {
-        plan_decode(d, rank, sms, cluster_cap, p);
+    if (route == MNB_ROUTE_GEMV && fused_ok && mnb::decode_supported(d.bits, Mt, (int)d.K, d.N, rank > 0, sms)) {
+        plan_decode(d, rank, sms, p);
         return MNB_OK;
     }
     if (route == MNB_ROUTE_GEMV)
@@ -202,13 +202,12 @@ int mnb_plan(mnb_handle h, int64_t batch, int64_t M, int32_t rank, int32_t sm_co
     if (batch > 0 && M > INT32_MAX / batch) return MNB_ERR_UNSUPPORTED;
     if (rank != 0 && rank != 32) return MNB_ERR_UNSUPPORTED;
     if (rank > h->d.max_rank) return MNB_ERR_ARG;
-    int sms = sm_count, cap = 0;
-    if (sms <= 0) {  // the current device: also its cluster capacity
+    int sms = sm_count;
+    if (sms <= 0) {  // the current device
         const int rc = device_setup(&sms);
         if (rc != MNB_OK) return rc;
-        cap = mnb::decode_cluster_cap();
     }
-    return make_plan(h->d, batch, M, rank, sms, out, true, cap);
+    return make_plan(h->d, batch, M, rank, sms, out);
 }
 
 }  // extern "C"
@@ -278,7 +277,7 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
             T_ws = Tfix;
         }
     }
-    make_plan(d, batch, M, rank, sms, &p, !q8x && !(rank > 0 && ad.q8), sms > 0 ? mnb::decode_cluster_cap() : 0);
+    make_plan(d, batch, M, rank, sms, &p, !q8x && !(rank > 0 && ad.q8));
     if (q8x && (p.route == MNB_ROUTE_GEMV || p.route == MNB_ROUTE_GEMM)) {
         plan_gemv(d, Mt, sms, &p);  // integer dots on the decode kernel, 8-token tiles
         p.tokens_per_cta = 8;
@@ -612,6 +611,8 @@ int mnb_sync_status(mnb_handle h, void* stream) {
     unsigned int v = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&v, mnb::g_status, sizeof(v)) != cudaSuccess) return MNB_ERR_CUDA;
     if (v != 0 && cudaMemcpyToSymbol(mnb::g_status, &zero, sizeof(zero)) != cudaSuccess) return MNB_ERR_CUDA;
+    // a wait that gave up may have left an adapter exchange part way: start them afresh
+    if ((v & mnb::kStatusTimeout) && mnb::decode_reset_exchange() != cudaSuccess) return MNB_ERR_CUDA;
     return (v & mnb::kStatusTimeout) ? MNB_ERR_DEVICE_TIMEOUT : MNB_OK;
 }
 

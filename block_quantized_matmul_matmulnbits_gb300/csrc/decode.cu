@@ -33,13 +33,19 @@
 //    blocks each thread holds, for its two rows, the block sums sum_k x q of
 //    its block, and applies the block's scale and zero point once, in FP32:
 //        y += s * (sum_k x q - zp * sum_k x).
-//  * The adapter: the CTAs of a cluster of eight each take 1/8 of K, hold
-//    their slice of A in registers (prefetched with the weights), form T's
-//    partial sums on the tensor cores (movmatrix turns A's rows into the MMA's
-//    K-major operand) and exchange them through distributed shared memory;
-//    every CTA adds the eight partials in rank order, so T is bitwise
-//    reproducible, rounds T once to FP16 and adds sum_r T[r] B[n, r] (two
-//    MMAs per 16 rows) before the one rounding of each output.
+//  * The adapter runs on a warp of its own, beside the weight stream and the
+//    base dot products.  Every CTA takes an equal slice of K, holds its slice
+//    of A in registers (prefetched with the weights), forms the partial sums
+//    of T on the tensor cores (movmatrix turns A's rows into the MMA's K-major
+//    operand) and publishes them in global memory; after all CTAs of the
+//    launch have arrived (a counter; the launch is cooperative, so all of its
+//    CTAs are resident together) each CTA adds the partials in CTA order, so
+//    T is bitwise reproducible, rounds T once to FP16 and forms
+//    sum_r T[r] B[n, r] for its rows (two MMAs per 16 rows) from a copy of
+//    its B rows.  The consumers keep each row's base sum in FP32 and add the
+//    adapter term before the one rounding of the output, at the end.  No
+//    thread-block clusters: cluster placement put two CTAs of one launch on
+//    the same SM while others stayed idle.
 //  * Eight consumer warps split every 16-row tile's rounds (warp w takes
 //    rounds w, w + 8, ...), so a row's summation order depends on K alone;
 //    partial sums are added in warp order (no atomics): results are
@@ -47,6 +53,7 @@
 //  * Every mbarrier wait is bounded and reports through the status word.
 #include <cuda.h>
 
+#include <atomic>
 #include <cstring>
 #include <type_traits>
 
@@ -58,16 +65,52 @@ namespace mnb {
 namespace {
 
 constexpr int kCW = 8;                     // consumer warps
-constexpr int kDecThreads = (kCW + 1) * 32;
-constexpr int kCl = 8;                     // cluster size of the adapter's T exchange
 constexpr int kRk = 32;                    // adapter rank
+constexpr int kMaxLoraRows = 256;          // adapter: most rows per CTA (B rows and sums stay in shared memory)
+constexpr int kExSlots = 32;               // adapter exchange areas (calls in flight on different streams)
+constexpr int kExMaxC = 240;               // most CTAs of a launch (the count field of an exchange word)
 constexpr int kBlkPerRound = 4;            // quantization blocks a warp covers per round
 constexpr int kMaxSR = 128;                // most rows per stage
 constexpr float kUnit = 1.0f / 16777216.f;  // a code q reaches the MMA as q * 2^-24
 
-__device__ __forceinline__ uint4 lds128_raw(const unsigned char* sm, uint32_t off) {
-    return *reinterpret_cast<const uint4*>(sm + off);
+// Threads of a CTA: the consumer warps, the producer warp, and with an adapter the adapter warp.
+__host__ __device__ constexpr int dec_threads(bool lora) { return (kCW + (lora ? 2 : 1)) * 32; }
+
+// The adapter's exchange of partial T between the CTAs of one launch.  A launch
+// reads `gen` and works in generation gen & 1.  Each rank has kExSub 64-bit
+// words (each on its own 128-byte line, so few CTAs meet on one): CTA c adds
+// to word c % kExSub, atomically, its partial as a fixed-point number (units
+// of 2^-32) plus one count in the top byte.  Integer sums do not depend on the
+// order of the additions, so T is the same bits on every run; a CTA knows a
+// rank is complete when the counts of its words add up to the CTAs of the
+// launch.  CTA 0 then clears the other generation (used by the launch before,
+// to be used by the next) and advances `gen`.
+constexpr int kExSub = 4;
+struct LoraEx {
+    unsigned int gen;
+    unsigned int pad_[31];
+    unsigned long long acc[2][kRk][kExSub][16];  // [generation][rank][word], word 0 of each line
+};
+constexpr unsigned long long kExCount = 1ull << 56;  // one CTA's count in an exchange word
+// A partial (|v| < 2^22) as a signed multiple of 2^-32 plus one count.
+__device__ __forceinline__ unsigned long long ex_word(float v) {
+    long long q = __float2ll_rn(v * 4294967296.f);
+    const long long lim = 1ll << 54;
+    q = q > lim ? lim : (q < -lim ? -lim : q);
+    return (unsigned long long)q + kExCount;
 }
+__device__ __forceinline__ unsigned int ex_count(unsigned long long w) {
+    return (unsigned int)((w + (kExCount >> 1)) >> 56);
+}
+// The partials a word holds, in units of 2^-32.
+__device__ __forceinline__ long long ex_value(unsigned long long w) {
+    return (long long)(w - (unsigned long long)ex_count(w) * kExCount);
+}
+__device__ LoraEx g_lora_ex[kExSlots];
+
+__host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
+// Rows of the adapter's per-CTA buffers: the most rows a CTA owns, in whole 16-row tiles.
+__host__ __device__ inline int lora_rows(int NR, int C) { return round16((NR + C - 1) / C); }
 
 // Shared-memory loads at a 32-bit shared address plus an immediate offset.
 // Volatile: they stay after the barrier waits before them in program order.
@@ -116,21 +159,21 @@ __host__ __device__ inline DecPitch dec_pitch(int nblk) {
 }
 
 // Shared memory plan, identical on host and device.  A stage slot holds SR
-// rows: codes [SR][rowbytes], scales [SR][spitch], zero points [SR][zpitch]
-// (each + 32 bytes for the aligned superset of a bulk copy) and adapter rows
-// [SR][32] FP16.
+// rows: codes [SR][rowbytes], scales [SR][spitch] and zero points [SR][zpitch]
+// (each + 32 bytes for the aligned superset of a bulk copy).  With an adapter
+// (lrows > 0): the CTA's adapter rows B[n, :] [lrows][32] FP16, the adapter
+// term and the base sum of each row [lrows] FP32, and T [32] FP16.
 struct DecLayout {
-    uint32_t sc, zp, b, slot;  // offsets inside a slot, slot bytes
-    uint32_t xs, sxs, red, lora, tpart, t16, bars, total;
+    uint32_t sc, zp, slot;  // offsets inside a slot, slot bytes
+    uint32_t xs, sxs, red, bown, lorb, ybuf, t16, bars, total;
 };
 
-__host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, int nblk, int nblkR) {
+__host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, int nblk, int nblkR, int lrows) {
     const DecPitch P = dec_pitch(nblk);
     DecLayout L;
     L.sc = al128((uint32_t)SR * (uint32_t)rowbytes);
     L.zp = al128(L.sc + (uint32_t)SR * P.spitch + 32u);
-    L.b = al128(L.zp + (uint32_t)SR * P.zpitch + 32u);
-    L.slot = al128(L.b + (uint32_t)SR * 64u);
+    L.slot = al128(L.zp + (uint32_t)SR * P.zpitch + 32u);
     uint32_t off = (uint32_t)ring * L.slot;
     L.xs = off;  // x in the MMA's operand order: 128 bytes a block (two thread roles), then 64 zero bytes
     off = al128(off + (uint32_t)nblkR * 128u + 64u);
@@ -138,14 +181,16 @@ __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, 
     off = al128(off + (uint32_t)nblkR * 4u);
     L.red = off;  // two buffers [SR / 16][kCW][16] FP32
     off += 2u * (uint32_t)(SR / 16) * kCW * 16u * 4u;
-    L.lora = off;  // two buffers [kMaxSR] FP32
-    off += 2u * kMaxSR * 4u;
-    L.tpart = off;  // [kCW][32] warp partials of T, then [32] the CTA's partial
-    off += (kCW + 1) * kRk * 4u;
-    L.t16 = off;  // T rounded to FP16
-    off += kRk * 2u;
+    L.bown = al128(off);
+    off = L.bown + (uint32_t)lrows * 64u;
+    L.lorb = off;
+    off += (uint32_t)lrows * 4u;
+    L.ybuf = off;
+    off += (uint32_t)lrows * 4u;
+    L.t16 = off;
+    off += lrows > 0 ? kRk * 2u : 0u;
     L.bars = al128(off);
-    L.total = L.bars + 2u * (uint32_t)ring * 8u;
+    L.total = L.bars + (2u * (uint32_t)ring + 2u) * 8u;  // full and empty per slot, then B rows and adapter done
     return L;
 }
 
@@ -185,21 +230,6 @@ struct Unpack<8> {
 // {(x0, x4), 0, (x2, x6), 0}, role 1 at 64 + 16 i holds {0, (x1, x5), 0, (x3, x7)}.
 // INT8, word i (codes 4i .. 4i+3): role 0 at 8 i holds {(x0, x1), 0}, role 1 at
 // 64 + 8 i holds {0, (x2, x3)}.
-// Byte offset inside a block of the x pair that slot pair sp (0..3) of sub-block
-// `sub` (8 consecutive codes) takes in the T projection, whose slots follow the
-// same pairing.
-template <int BITS>
-__device__ __forceinline__ uint32_t xs_pair_off(int sub, int sp) {
-    if constexpr (BITS == 4)  // sub-block = one word: slots (0,1)=(x0,x4) (2,3)=(x2,x6) (4,5)=(x1,x5) (6,7)=(x3,x7)
-        return (uint32_t)((sp >> 1) * 68 + sub * 16 + (sp & 1) * 8);
-    else  // sub-block = words 2 sub, 2 sub + 1: slots in natural order
-        return (uint32_t)((sp & 1) * 68 + (2 * sub + (sp >> 1)) * 8);
-}
-// K offset (0..7) inside a sub-block of MMA slot s.
-template <int BITS>
-__host__ __device__ constexpr int slot_k(int s) {
-    return BITS == 4 ? ((s & 1) * 4 + (s >> 2) + ((s >> 1) & 1) * 2) : s;
-}
 
 // A load kept in program order with the other volatile asm (the prefetch before
 // griddepcontrol.wait stays before it).
@@ -213,9 +243,17 @@ __device__ __forceinline__ void movmatrix_t(uint32_t& x) {
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;" : "+r"(x));
 }
 
-// Cluster barrier, per thread (not .aligned: the producer lane arrives early).
-__device__ __forceinline__ void cl_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+// Global-memory accesses of the adapter exchange, at GPU scope.
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const unsigned int* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ float h2f(uint32_t bits16) { return __half2float(__ushort_as_half((unsigned short)bits16)); }
 // A byte as an exact float, without the conversion unit: 2^23 + z read as binary32, minus 2^23.
@@ -246,7 +284,7 @@ struct StageIt {
 };
 
 template <int BITS, bool HAS_ZP, bool LORA>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__global__ void __launch_bounds__(dec_threads(LORA), 2)
     decode_kernel(const __grid_constant__ DecMaps maps, const __grid_constant__ DecodeArgs a) {
     using U = Unpack<BITS>;
     constexpr int kWB = U::kWordsPerBlock;
@@ -259,21 +297,27 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int nblkR = nround * kBlkPerRound;
     const int rowbytes = K * BITS / 8;
     const int SR = a.SR, ring = a.ring;
-    const DecLayout L = dec_layout(SR, ring, rowbytes, nblk, nblkR);
+    const int C = gridDim.x;
+    const DecLayout L = dec_layout(SR, ring, rowbytes, nblk, nblkR, LORA ? lora_rows(NR, C) : 0);
     const DecPitch P = dec_pitch(nblk);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = gridDim.x;
     const int r0 = (int)((long long)blockIdx.x * NR / C), r1 = (int)((long long)(blockIdx.x + 1) * NR / C);
     unsigned int* status = a.status;
 
     auto full = [&](int s) { return sb + L.bars + 8u * (uint32_t)s; };
     auto empty = [&](int s) { return sb + L.bars + 8u * (uint32_t)(ring + s); };
+    const uint32_t bbar = sb + L.bars + 16u * (uint32_t)ring;  // adapter: the CTA's B rows landed
+    const uint32_t lready = bbar + 8u;                          // adapter: T B^T of the CTA's rows is in place
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ring; ++s) {
             mbar_init(full(s), 1);
             mbar_init(empty(s), kCW);
+        }
+        if (LORA) {
+            mbar_init(bbar, 1);
+            mbar_init(lready, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -282,7 +326,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
     if (warp == kCW) {
         // ------------------------------------------------------------ producer
-        if (LORA) cl_arrive();  // the producer takes no part in T: arrive for the partials at once
         if (lane == 0) {
             bool ok = true;
             int issued = 0;
@@ -319,7 +362,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                         if (z_hi > z_lo) bytes += (uint32_t)(z_hi - z_lo);
                     }
                 }
-                if (LORA) bytes += (uint32_t)rs * 64u;
                 mbar_arrive_tx(full(s), bytes);
                 const uint8_t* src = pj.Wq + (size_t)ra * rowbytes;
                 const uint32_t cb = (uint32_t)rs * (uint32_t)rowbytes;
@@ -336,18 +378,159 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                     else if (z_hi > z_lo)
                         bulk_load(sslot + L.zp, pj.Z + z_lo, (uint32_t)(z_hi - z_lo), full(s));
                 }
-                if (LORA) bulk_load(sslot + L.b, a.B + (size_t)ra * kRk, (uint32_t)rs * 64u, full(s));
             }
             // no copy may still be in flight when the CTA exits (a consumer may have given up)
             for (int st = issued > ring ? issued - ring : 0; st < issued; ++st)
                 mbar_wait(full(st % ring), (uint32_t)(st / ring) & 1u, status, false);
         }
-        if (LORA) {  // the T exchange's two phases (see below)
-            cl_wait();
-            cl_arrive();
-            cl_wait();
-        }
         return;
+    }
+
+    if constexpr (LORA) {
+        if (warp == kCW + 1) {
+            // -------------------------------------------------------- adapter
+            // T = fp16(x A) from every CTA's partial over an equal slice of K, then
+            // T B^T for this CTA's rows.  Its B rows and its slice of A are weights:
+            // copied before waiting for x.
+            const int g = lane >> 2, t = lane & 3;
+            const int nrows = r1 - r0;
+            if (lane == 0 && nrows > 0) {
+                mbar_arrive_tx(bbar, (uint32_t)nrows * 64u);
+                bulk_load(sb + L.bown, a.B + (size_t)r0 * kRk, (uint32_t)nrows * 64u, bbar);
+            }
+            // K steps (16 wide) [c S / C, (c + 1) S / C) of CTA c.  A step is 2 K
+            // sub-blocks x 4 rank sub-blocks of 8 x 8, each loaded in its natural
+            // fragment (thread (g, t) holds ranks 2t, 2t+1 of K row g) and transposed
+            // by movmatrix into the MMA's B fragment.
+            constexpr int kMaxSteps = 4;
+            const int S = K / 16;
+            const int step0 = (int)((long long)blockIdx.x * S / C);
+            const int nsteps = (int)((long long)(blockIdx.x + 1) * S / C) - step0;
+            uint32_t areg[kMaxSteps][8];
+#pragma unroll
+            for (int i = 0; i < kMaxSteps; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int kk = (step0 + i) * 16 + (j >> 2) * 8 + g;
+                    areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
+                }
+            // The area's generation: its last writer is the launch before this one on the
+            // area (kExSlots launches back), finished before this one starts.
+            LoraEx* ex = static_cast<LoraEx*>(a.ex);
+            const uint32_t gen = ld_relaxed_u32(&ex->gen);
+            const int gs = (int)(gen & 1u);
+            if (a.x_wait) pdl_wait();
+            float tacc[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tacc[j][e] = 0.f;
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(a.X);
+            for (int i0 = 0; i0 < nsteps; i0 += kMaxSteps) {
+                // x of the chunk's steps for token row 0 (rows 1..15 of the MMA are empty)
+                uint32_t xr[kMaxSteps][2];
+#pragma unroll
+                for (int i = 0; i < kMaxSteps; ++i) {
+                    const int k0 = (step0 + i0 + i) * 16;
+                    const bool on = g == 0 && i0 + i < nsteps;
+                    xr[i][0] = on ? xw[(k0 >> 1) + t] : 0u;
+                    xr[i][1] = on ? xw[(k0 >> 1) + 4 + t] : 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < kMaxSteps; ++i) {
+                    if (i0 + i >= nsteps) break;
+                    uint32_t bfr[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (i0 == 0) {
+                            bfr[j] = areg[i][j];
+                        } else {
+                            const int kk = (step0 + i0 + i) * 16 + (j >> 2) * 8 + g;
+                            bfr[j] = __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t));
+                        }
+                        movmatrix_t(bfr[j]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_16816(tacc[j], xr[i][0], 0u, xr[i][1], 0u, bfr[j], bfr[4 + j]);
+                }
+            }
+            // token row 0: thread (0, t) holds ranks 8j + 2t, 8j + 2t + 1: add them to the words
+            const int sub = (int)(blockIdx.x % kExSub);
+            if (g == 0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+                        atomicAdd(&ex->acc[gs][8 * j + 2 * t + e][sub][0], ex_word(tacc[j][e]));
+            }
+            // T[lane] once every CTA has added its partial (bounded wait: the launch is
+            // cooperative, so all of its CTAs are resident)
+            const long long t0 = clock64();
+            long long tq = 0;
+            auto poll = [&](int r) {  // the partials of rank r, once all are in (false: gave up)
+                for (;;) {
+                    unsigned long long w[kExSub];
+#pragma unroll
+                    for (int u = 0; u < kExSub; ++u) w[u] = ld_relaxed_u64(&ex->acc[gs][r][u][0]);
+                    unsigned int cnt = 0;
+                    long long q = 0;
+#pragma unroll
+                    for (int u = 0; u < kExSub; ++u) {
+                        cnt += ex_count(w[u]);
+                        q += ex_value(w[u]);
+                    }
+                    if (cnt >= (unsigned int)C) {
+                        tq = q;
+                        return true;
+                    }
+                    if (clock64() - t0 > kWaitCycles) return false;
+                    __nanosleep(200);
+                }
+            };
+            bool ok = poll(lane);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok && lane == 0) atomicOr(status, kStatusTimeout);
+            const __half th = __double2half((double)tq * 0x1p-32);  // T, rounded once
+            reinterpret_cast<__half*>(sm + L.t16)[lane] = th;
+            if (blockIdx.x == 0) a.T[lane] = th;
+            __syncwarp();
+            // sum_r B[n, r] T[r] for each 16-row tile: A = B rows (16 x 16 per MMA), B = T in column 0
+            if (nrows > 0 && !mbar_wait(bbar, 0u, status)) ok = false;
+            float* lorb = reinterpret_cast<float*>(sm + L.lorb);
+            const __half* th16 = reinterpret_cast<const __half*>(sm + L.t16);
+            for (int tl = 0; ok && tl * 16 < nrows; ++tl) {
+                const unsigned char* bs = sm + L.bown + (uint32_t)(tl * 16) * 64u;
+                float dl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kc = 0; kc < 2; ++kc) {
+                    const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
+                    const uint32_t b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
+                    const uint32_t b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
+                    const uint32_t b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
+                    const uint32_t b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
+                    const uint32_t t0r = g == 0 ? *reinterpret_cast<const uint32_t*>(th16 + 16 * kc + 2 * t) : 0u;
+                    const uint32_t t1r = g == 0 ? *reinterpret_cast<const uint32_t*>(th16 + 16 * kc + 2 * t + 8) : 0u;
+                    mma_16816(dl, b0r0, b0r8, b8r0, b8r8, t0r, t1r);
+                }
+                if (t == 0) {  // column 0: rows g, g + 8
+                    lorb[tl * 16 + g] = dl[0];
+                    lorb[tl * 16 + g + 8] = dl[2];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(lready);  // releases this warp's shared-memory writes
+            if (blockIdx.x == 0) {
+                // the other generation (the launch before this one on the area) for the next
+#pragma unroll
+                for (int u = 0; u < kExSub; ++u) ex->acc[gs ^ 1][lane][u][0] = 0ull;
+                __syncwarp();
+                if (lane == 0 && ok) {
+                    __threadfence();
+                    *reinterpret_cast<volatile unsigned int*>(&ex->gen) = gen + 1u;
+                }
+            }
+            return;
+        }
     }
 
     // ---------------------------------------------------------------- consumers
@@ -355,26 +538,12 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     const int ctid = threadIdx.x;  // 0 .. 255
     constexpr uint32_t kNamed = 1;  // named barrier of the consumer warps
 
-    // The adapter's A slice, a weight: into registers before waiting for x.  CTA q of the
-    // cluster takes K steps (16 wide) [i S / 64, (i + 1) S / 64) with i = 8 q + warp; a step
-    // is 2 K sub-blocks x 4 rank sub-blocks of 8 x 8, each loaded in its natural fragment
-    // (row = K, thread (g, t) holds ranks 2t, 2t+1 of K row slot_k(g)) and transposed later.
-    constexpr int kMaxSteps = 4;
-    uint32_t areg[kMaxSteps][8];
-    int step0 = 0, nsteps = 0;
-    if constexpr (LORA) {
-        uint32_t qrank;
-        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(qrank));
-        const int S = K / 16, wi = (int)qrank * kCW + warp;
-        step0 = (int)((long long)wi * S / (kCl * kCW));
-        nsteps = (int)((long long)(wi + 1) * S / (kCl * kCW)) - step0;
-#pragma unroll
-        for (int i = 0; i < kMaxSteps; ++i)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int kk = (step0 + i) * 16 + (j >> 2) * 8 + slot_k<BITS>(g);
-                areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
-            }
+    // The first stage's weights need no wait for earlier work: take them first.
+    bool ok = true;
+    StageIt it = {r0, 0, 0, 0};
+    if (r0 < r1) {
+        it.settle(a, r1, SR);
+        ok = mbar_wait(full(0), 0u, status);
     }
 
     // ---- x: wait for the work that produces it, then stage it in the MMA's operand order
@@ -420,60 +589,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     }
     named_barrier_sync(kNamed, kCW * 32);
 
-    // ---- the adapter's partial T over this CTA's K slice (tensor cores), then the exchange
-    if constexpr (LORA) {
-        float tacc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) tacc[j][e] = 0.f;
-        for (int i0 = 0; i0 < nsteps; i0 += kMaxSteps) {
-#pragma unroll
-            for (int i = 0; i < kMaxSteps; ++i) {
-                if (i0 + i >= nsteps) break;
-                uint32_t bfr[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    if (i0 == 0) {
-                        bfr[j] = areg[i][j];
-                    } else {
-                        const int kk = (step0 + i0 + i) * 16 + (j >> 2) * 8 + slot_k<BITS>(g);
-                        bfr[j] = __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t));
-                    }
-                    movmatrix_t(bfr[j]);
-                }
-                // x of the step's two sub-blocks for token row 0 (rows 1..15 of the MMA are empty)
-                const int k0 = (step0 + i0 + i) * 16;
-                const int blk = k0 >> 5, sub = (k0 & 31) >> 3;
-                const uint32_t xo = L.xs + (uint32_t)blk * 128u;
-                const uint32_t x0 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub, t)) : 0u;
-                const uint32_t x1 = g == 0 ? *reinterpret_cast<const uint32_t*>(sm + xo + xs_pair_off<BITS>(sub + 1, t)) : 0u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) mma_16816(tacc[j], x0, 0u, x1, 0u, bfr[j], bfr[4 + j]);
-            }
-        }
-        // token row 0: thread (0, t) holds ranks 8j + 2t, 8j + 2t + 1
-        float* tpart = reinterpret_cast<float*>(sm + L.tpart);
-        if (g == 0) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                tpart[warp * kRk + 8 * j + 2 * t] = tacc[j][0];
-                tpart[warp * kRk + 8 * j + 2 * t + 1] = tacc[j][1];
-            }
-        }
-        named_barrier_sync(kNamed, kCW * 32);
-        if (warp == 0) {  // the CTA's partial: warps added in order
-            float sum = 0.f;
-#pragma unroll
-            for (int w = 0; w < kCW; ++w) sum += tpart[w * kRk + lane];
-            tpart[kCW * kRk + lane] = sum;
-        }
-        cl_arrive();  // each writer releases its own writes
-    }
-
     // ---- the stages
     float* red = reinterpret_cast<float*>(sm + L.red);
-    float* lorab = reinterpret_cast<float*>(sm + L.lora);
     // This thread's x role: class 0 of block t when g == 2t, class 1 when g == 2t + 1,
     // else the zero region.
     const bool act0 = g == 2 * t, act1 = g == 2 * t + 1;
@@ -482,9 +599,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                                   : L.xs + (uint32_t)nblkR * 128u;
     const uint32_t xs_step = act0 || act1 ? (uint32_t)(kCW * kBlkPerRound * 128) : 0u;  // per round of this warp
     const int tiles_max = SR / 16;
-    bool ok = true;
-    StageIt it = {r0, 0, 0, 0};
-    if (r0 < r1) it.settle(a, r1, SR);
 
     for (int st = 0; it.pos < r1; ++st, it.next(a, r1, SR)) {
         const int s = st % ring;
@@ -626,46 +740,6 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                     tiles(std::integral_constant<int, 1>{}, tl0);
             }
         }
-        float* lorb = lorab + (st & 1) * kMaxSR;
-        if constexpr (LORA) {
-            if (st == 0) {
-                // T: every CTA's partial, added in rank order, rounded once
-                cl_wait();
-                if (warp == 0) {
-                    const uint32_t la = smem_u32(reinterpret_cast<float*>(sm + L.tpart) + kCW * kRk + lane);
-                    float tv = 0.f;
-#pragma unroll
-                    for (int q = 0; q < kCl; ++q) tv += ld_peer_f32(la, (uint32_t)q);
-                    const __half th = __float2half_rn(tv);
-                    reinterpret_cast<__half*>(sm + L.t16)[lane] = th;
-                    if (blockIdx.x == 0) a.T[lane] = th;
-                }
-                cl_arrive();
-                named_barrier_sync(kNamed, kCW * 32);
-            }
-            if (warp < ntile) {
-                // sum_r B[n, r] T[r] for tile `warp`'s 16 rows: A = B rows (16 x 16 per MMA),
-                // B = T in column 0
-                const unsigned char* bs = sm + soff + L.b + (uint32_t)(warp * 16) * 64u;
-                const __half* th = reinterpret_cast<const __half*>(sm + L.t16);
-                float dl[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int kc = 0; kc < 2; ++kc) {
-                    const uint32_t o = (uint32_t)(16 * kc + 2 * t) * 2u;
-                    const uint32_t b0r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o);
-                    const uint32_t b0r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o);
-                    const uint32_t b8r0 = *reinterpret_cast<const uint32_t*>(bs + g * 64 + o + 16);
-                    const uint32_t b8r8 = *reinterpret_cast<const uint32_t*>(bs + (g + 8) * 64 + o + 16);
-                    const uint32_t t0 = g == 0 ? *reinterpret_cast<const uint32_t*>(th + 16 * kc + 2 * t) : 0u;
-                    const uint32_t t1 = g == 0 ? *reinterpret_cast<const uint32_t*>(th + 16 * kc + 2 * t + 8) : 0u;
-                    mma_16816(dl, b0r0, b0r8, b8r0, b8r8, t0, t1);
-                }
-                if (t == 0) {  // column 0: rows g, g + 8
-                    lorb[warp * 16 + g] = dl[0];
-                    lorb[warp * 16 + g + 8] = dl[2];
-                }
-            }
-        }
         named_barrier_sync(kNamed, kCW * 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(s));  // every read of the slot is done
@@ -675,26 +749,28 @@ __global__ void __launch_bounds__(kDecThreads, 2)
                 float v = 0.f;
 #pragma unroll
                 for (int w = 0; w < kCW; ++w) v += redb[(warp * kCW + w) * 16 + lane];  // warp order
-                float y = v * (1.0f / kUnit);
-                if (LORA) y += lorb[row];
-                if (pj.bias) y += __half2float(pj.bias[ra + row]);
-                pj.Y[ra + row] = __float2half_rn(y);
+                const float y = v * (1.0f / kUnit);
+                if (LORA) {  // the adapter term comes at the end
+                    reinterpret_cast<float*>(sm + L.ybuf)[it.pos - r0 + row] = y;
+                } else {
+                    pj.Y[ra + row] = __float2half_rn(pj.bias ? y + __half2float(pj.bias[ra + row]) : y);
+                }
             }
         }
     }
     if constexpr (LORA) {
-        if (r0 >= r1) {  // no rows: still take part in the exchange
-            cl_wait();
-            if (warp == 0 && blockIdx.x == 0) {
-                const uint32_t la = smem_u32(reinterpret_cast<float*>(sm + L.tpart) + kCW * kRk + lane);
-                float tv = 0.f;
-#pragma unroll
-                for (int q = 0; q < kCl; ++q) tv += ld_peer_f32(la, (uint32_t)q);
-                a.T[lane] = __float2half_rn(tv);
+        // each row: base + T B^T (one adapter projection: one segment), + bias, rounded once
+        named_barrier_sync(kNamed, kCW * 32);
+        if (r0 < r1 && ok && mbar_wait(lready, 0u, status)) {
+            const DecSeg& pj = a.seg[0];
+            const float* ybuf = reinterpret_cast<const float*>(sm + L.ybuf);
+            const float* lorb = reinterpret_cast<const float*>(sm + L.lorb);
+            for (int row = ctid; row < r1 - r0; row += kCW * 32) {
+                float y = ybuf[row] + lorb[row];
+                if (pj.bias) y += __half2float(pj.bias[r0 + row]);
+                pj.Y[r0 + row] = __float2half_rn(y);
             }
-            cl_arrive();
         }
-        cl_wait();  // keep this CTA's partial alive until every peer has read it
     }
 }
 
@@ -703,7 +779,7 @@ cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, s
                            cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(kDecThreads);
+    cfg.blockDim = dim3(dec_threads(LORA));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -713,11 +789,9 @@ cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, s
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
-    if (LORA) {
-        attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = kCl;
-        attr[na].val.clusterDim.y = 1;
-        attr[na].val.clusterDim.z = 1;
+    if (LORA) {  // the adapter's CTAs wait for one another: all resident at once
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
         ++na;
     }
     cfg.attrs = attr;
@@ -726,43 +800,33 @@ cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, s
 }
 
 constexpr int kMaxDev = 64;
-// Per device: clusters of kCl CTAs the GPU holds at once with two CTAs per SM (a
-// cluster needs kCl SMs of one GPC with room), halved: the clusters one call may
-// use so that the next call's clusters fit beside them.
-int g_cluster_cap[kMaxDev] = {};
+// Per device (set up in its current context): the exchange areas' device address
+// and the next area to hand out.
+LoraEx* g_ex_base[kMaxDev] = {};
+std::atomic<unsigned int> g_ex_next[kMaxDev];
+
+int dec_ctas(int N, int sms) {
+    int C = (N + 15) / 16;
+    const int s = sms > 0 ? sms : 1;
+    if (C > s) C = s;
+    if (C > kExMaxC) C = kExMaxC;
+    return C < 1 ? 1 : C;
+}
 
 }  // namespace
 
-bool decode_supported(int bits, int64_t Mt, int K) {
-    return (bits == 4 || bits == 8) && Mt == 1 && K >= 32 && K <= 65536;
+bool decode_supported(int bits, int64_t Mt, int K, int64_t N, bool lora, int sms) {
+    if (!((bits == 4 || bits == 8) && Mt == 1 && K >= 32 && K <= 65536)) return false;
+    if (lora && (N > (int64_t)INT32_MAX || lora_rows((int)N, dec_ctas((int)N, sms)) > kMaxLoraRows)) return false;
+    return true;
 }
 
-int decode_cluster_cap() {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
-        cudaGetLastError();
-        return 0;
-    }
-    return g_cluster_cap[dev];
-}
-
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int cluster_cap, int* ctas, int* SR, int* ring,
-                     size_t* smem) {
-    const int s = sms > 0 ? sms : 1;
-    int C = (N + 15) / 16;
-    if (C > s) C = s;
-    if (C < 1) C = 1;
-    if (lora) {  // whole clusters of kCl CTAs, at most cluster_cap of them
-        int maxcl = s / kCl;
-        if (cluster_cap > 0 && cluster_cap < maxcl) maxcl = cluster_cap;
-        if (maxcl < 1) maxcl = 1;
-        C = (C + kCl - 1) / kCl;
-        if (C > maxcl) C = maxcl;
-        C *= kCl;
-    }
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem) {
+    const int C = dec_ctas(N, sms);
     const int nblk = K / 32, nround = (nblk + kBlkPerRound - 1) / kBlkPerRound, nblkR = nround * kBlkPerRound;
     const int rowbytes = K * bits / 8;
     const int rmax = (N + C - 1) / C;
+    const int lrows = lora ? lora_rows(N, C) : 0;
     // The whole share in one stage when it fits in half an SM's shared memory: two CTAs
     // per SM, so the next call's CTA prefetches its share while this one finishes.
     // Larger shares stream through a ring of ~200 KB (one CTA per SM), in stages of at
@@ -770,19 +834,19 @@ void decode_geometry(int N, int K, int bits, bool lora, int sms, int cluster_cap
     constexpr uint32_t kHalfSm = 112u * 1024u, kRing = 200u * 1024u;
     int sr = 16;
     while (sr < rmax) sr *= 2;
-    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR).total <= kHalfSm) {
+    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR, lrows).total <= kHalfSm) {
         *SR = sr;
         *ring = 1;
     } else {
         int sr2 = 16;
-        while (sr2 < 64 && dec_layout(sr2, 1, rowbytes, nblk, nblkR).slot < 24u * 1024u) sr2 *= 2;
+        while (sr2 < 64 && dec_layout(sr2, 1, rowbytes, nblk, nblkR, lrows).slot < 24u * 1024u) sr2 *= 2;
         int r = 1;
-        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR).total <= kRing) ++r;
+        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR, lrows).total <= kRing) ++r;
         *SR = sr2;
         *ring = r;
     }
     *ctas = C;
-    *smem = dec_layout(*SR, *ring, rowbytes, nblk, nblkR).total;
+    *smem = dec_layout(*SR, *ring, rowbytes, nblk, nblkR, lrows).total;
 }
 
 cudaError_t decode_prepare() {
@@ -797,27 +861,16 @@ cudaError_t decode_prepare() {
     MNB_DEC_SET(4, false, false) MNB_DEC_SET(4, true, false) MNB_DEC_SET(4, false, true) MNB_DEC_SET(4, true, true)
     MNB_DEC_SET(8, false, false) MNB_DEC_SET(8, true, false) MNB_DEC_SET(8, false, true) MNB_DEC_SET(8, true, true)
 #undef MNB_DEC_SET
-    if (e == cudaSuccess) {
-        // clusters that fit at once with two CTAs per SM (about half an SM of shared memory each)
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kCl);
-        cfg.blockDim = dim3(kDecThreads);
-        cfg.dynamicSmemBytes = 110 * 1024;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kCl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int ncl = 0;
-        if (cudaOccupancyMaxActiveClusters(&ncl, decode_kernel<4, true, true>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            ncl = 0;
-        }
-        g_cluster_cap[dev] = ncl / 2;
-    }
+    void* ex = nullptr;
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&ex, g_lora_ex);
+    if (e == cudaSuccess) g_ex_base[dev] = static_cast<LoraEx*>(ex);
     return e;
+}
+
+cudaError_t decode_reset_exchange() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || !g_ex_base[dev]) return cudaSuccess;
+    return cudaMemset(g_ex_base[dev], 0, sizeof(g_lora_ex));
 }
 
 cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, cudaStream_t st) {
@@ -825,10 +878,19 @@ cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, c
     int C, SR, ring;
     size_t smem;
     const int bits = a.bits;
-    decode_geometry(a.NR, a.K, bits, rank > 0, sms, decode_cluster_cap(), &C, &SR, &ring, &smem);
+    decode_geometry(a.NR, a.K, bits, rank > 0, sms, &C, &SR, &ring, &smem);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     a.SR = SR;
     a.ring = ring;
+    if (rank > 0) {
+        if (a.nseg != 1 || lora_rows(a.NR, C) > kMaxLoraRows) return cudaErrorNotSupported;
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev || !g_ex_base[dev])
+            return cudaErrorInvalidDevice;
+        // one exchange area per call, round robin: calls in flight at once on
+        // different streams use different areas
+        a.ex = g_ex_base[dev] + (g_ex_next[dev].fetch_add(1u, std::memory_order_relaxed) % kExSlots);
+    }
     // scale / zero-point boxes of SR rows, each row padded to the shared-memory pitch
     DecMaps maps;
     memset(&maps, 0, sizeof(maps));

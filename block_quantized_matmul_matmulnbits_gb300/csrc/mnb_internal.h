@@ -78,7 +78,8 @@ cudaError_t gemv_q8x_launch(const GemvArgs& a, const mnb_plan_info& p, int bits,
 // Single-token decode kernel (decode.cu): one token row, INT4 or INT8 weights,
 // up to kMaxSeg projections of the same x laid end to end in one row space
 // (rows [row0, row0 + N) belong to projection i), the optional FP16 rank-32
-// adapter (one projection only; T computed in the same launch) and biases.
+// adapter (one projection only; T computed in the same, cooperative, launch)
+// and biases.
 struct DecSeg {
     int row0;            // first row of this projection in the row space
     int N;               // its rows
@@ -100,15 +101,17 @@ struct DecodeArgs {
     int SR, ring;        // rows per stage and stage slots (set by the launcher)
     int x_wait;          // X may be written by the work queued before this kernel
     unsigned int* status;
+    void* ex;            // the adapter's exchange area (set by the launcher)
 };
-bool decode_supported(int bits, int64_t Mt, int K);
-// CTAs, rows per stage, stage slots and shared memory of a launch.  cluster_cap:
-// the adapter's clusters that fit on the GPU at once (0: unknown, SMs / 8).
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int cluster_cap, int* ctas, int* SR, int* ring,
-                     size_t* smem);
-// That number for the current device (0 before its setup).
-int decode_cluster_cap();
+// Whether a call runs on this kernel: bits 4 or 8, one token row, 32 <= K <= 65536;
+// with an adapter at most 256 rows per CTA (N rows over min(SMs, N / 16) CTAs).
+bool decode_supported(int bits, int64_t Mt, int K, int64_t N, bool lora, int sms);
+// CTAs, rows per stage, stage slots and shared memory of a launch.
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem);
 cudaError_t decode_prepare();
+// Clear the adapter exchange areas of the current device (after a device-side
+// timeout left one of them part way).
+cudaError_t decode_reset_exchange();
 cudaError_t decode_launch(const DecodeArgs& a, int rank, int sms, bool pdl, cudaStream_t st);
 
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.

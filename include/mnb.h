@@ -137,6 +137,10 @@ void mnb_destroy(mnb_handle h);
  * a nonempty weight.
  * Every row of X is independent: [batch, M] gives the same bits as one matrix
  * of batch*M rows routed the same way.  Results are deterministic run to run.
+ * A single-token call with an adapter is one cooperative launch whose CTAs add
+ * up T through one of 32 exchange areas of the library, handed out in turn per
+ * launch: at most 32 such launches may run at the same time (on different
+ * streams).
  * Errors: MNB_ERR_ARG, MNB_ERR_UNSUPPORTED, MNB_ERR_ALIGN, MNB_ERR_NO_DEVICE,
  * MNB_ERR_CUDA.  No allocation and no host synchronization happen here. */
 int mnb_run(mnb_handle h,
@@ -272,7 +276,8 @@ int mnb_last_route(mnb_handle h);
 /* Synchronize `stream`, then read and clear the library's device status word.
  * Returns MNB_OK, MNB_ERR_DEVICE_TIMEOUT when a bounded device-side wait of a
  * kernel gave up since the last call (that kernel's output is then
- * incomplete), or MNB_ERR_CUDA. */
+ * incomplete; the adapter exchange areas are then cleared, so no call may be
+ * in flight on another stream), or MNB_ERR_CUDA. */
 int mnb_sync_status(mnb_handle h, void* stream);
 
 /* Human-readable name of a status code (static string). */
