@@ -158,25 +158,41 @@ __host__ __device__ inline DecPitch dec_pitch(int nblk) {
     return p;
 }
 
+// A stage's rows [0, h) and [h, rs), h = ceil(rs / 2), land in two regions of
+// the slot; the MMA rows of a 16-row tile alternate between them (even MMA rows
+// from the first, odd from the second).  The two rows a quarter-warp reads with
+// one 16-byte load per thread (MMA rows 2p and 2p + 1) then never share banks,
+// which rows of one region would when packed rows are a multiple of 128 bytes:
+// the second region starts 64 bytes past a 128-byte boundary for INT4 (thread t
+// reads bytes [16 t, 16 t + 16) of a 64-byte round) and 16 bytes past it for
+// INT8 (bytes [32 t, 32 t + 16) or [32 t + 16, 32 t + 32) of a 128-byte round).
+__host__ __device__ inline int dec_half(int rs) { return (rs + 1) / 2; }
+
 // Shared memory plan, identical on host and device.  A stage slot holds SR
-// rows: codes [SR][rowbytes], scales [SR][spitch] and zero points [SR][zpitch]
+// rows: codes (two regions of SR / 2 rows, [SR/2][rowbytes] each), scales
+// [SR][spitch] and zero points [SR][zpitch]
 // (each + 32 bytes for the aligned superset of a bulk copy).  With an adapter
 // (lrows > 0): the CTA's adapter rows B[n, :] [lrows][32] FP16, the adapter
 // term and the base sum of each row [lrows] FP32, and T [32] FP16.
 struct DecLayout {
-    uint32_t sc, zp, slot;  // offsets inside a slot, slot bytes
+    uint32_t r1, sc, zp, slot;  // offsets inside a slot (second code region, scales, zero points), slot bytes
     uint32_t xs, sxs, red, bown, lorb, ybuf, t16, bars, total;
 };
 
-__host__ __device__ inline DecLayout dec_layout(int SR, int ring, int rowbytes, int nblk, int nblkR, int lrows) {
+__host__ __device__ inline DecLayout dec_layout(int SR, int ring, int bits, int rowbytes, int nblk, int nblkR,
+                                                int lrows) {
     const DecPitch P = dec_pitch(nblk);
     DecLayout L;
-    L.sc = al128((uint32_t)SR * (uint32_t)rowbytes);
+    const uint32_t half = (uint32_t)(SR / 2) * (uint32_t)rowbytes;
+    L.r1 = al128(half) + (bits == 4 ? 64u : 16u);
+    L.sc = al128(L.r1 + half);
     L.zp = al128(L.sc + (uint32_t)SR * P.spitch + 32u);
     L.slot = al128(L.zp + (uint32_t)SR * P.zpitch + 32u);
     uint32_t off = (uint32_t)ring * L.slot;
-    L.xs = off;  // x in the MMA's operand order: 128 bytes a block (two thread roles), then 64 zero bytes
-    off = al128(off + (uint32_t)nblkR * 128u + 64u);
+    // x in the MMA's operand order: 128 bytes a block (two thread roles), then 64 zero
+    // bytes starting 32 bytes into a line (their banks differ from both roles' reads)
+    L.xs = off;
+    off = al128(off + (uint32_t)nblkR * 128u + 96u);
     L.sxs = off;  // per block: sum of x, times 2^-24
     off = al128(off + (uint32_t)nblkR * 4u);
     L.red = off;  // two buffers [SR / 16][kCW][16] FP32
@@ -298,7 +314,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     const int rowbytes = K * BITS / 8;
     const int SR = a.SR, ring = a.ring;
     const int C = gridDim.x;
-    const DecLayout L = dec_layout(SR, ring, rowbytes, nblk, nblkR, LORA ? lora_rows(NR, C) : 0);
+    const DecLayout L = dec_layout(SR, ring, BITS, rowbytes, nblk, nblkR, LORA ? lora_rows(NR, C) : 0);
     const DecPitch P = dec_pitch(nblk);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -363,10 +379,13 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
                     }
                 }
                 mbar_arrive_tx(full(s), bytes);
+                // codes: rows [0, h) and [h, rs) into the two regions
                 const uint8_t* src = pj.Wq + (size_t)ra * rowbytes;
-                const uint32_t cb = (uint32_t)rs * (uint32_t)rowbytes;
-                for (uint32_t off = 0; off < cb; off += 32768u)
-                    bulk_load(sslot + off, src + off, min(32768u, cb - off), full(s));
+                const uint32_t c0 = (uint32_t)dec_half(rs) * (uint32_t)rowbytes, cb = (uint32_t)rs * (uint32_t)rowbytes;
+                for (uint32_t off = 0; off < c0; off += 32768u)
+                    bulk_load(sslot + off, src + off, min(32768u, c0 - off), full(s));
+                for (uint32_t off = c0; off < cb; off += 32768u)
+                    bulk_load(sslot + L.r1 + (off - c0), src + off, min(32768u, cb - off), full(s));
                 if (P.tma_s)
                     tma_load_2d(sslot + L.sc, &maps.s[it.seg], 0, ra, full(s));
                 else if (s_hi > s_lo)
@@ -585,7 +604,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
                 }
             }
         }
-        if (ctid < 16) reinterpret_cast<uint32_t*>(sm + L.xs + (uint32_t)nblkR * 128u)[ctid] = 0u;  // zero region
+        if (ctid < 16) reinterpret_cast<uint32_t*>(sm + L.xs + (uint32_t)nblkR * 128u + 32u)[ctid] = 0u;  // zero region
     }
     named_barrier_sync(kNamed, kCW * 32);
 
@@ -596,7 +615,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     const bool act0 = g == 2 * t, act1 = g == 2 * t + 1;
     const uint32_t xs_base = act0 ? L.xs + (uint32_t)t * 128u
                            : act1 ? L.xs + (uint32_t)t * 128u + 64u
-                                  : L.xs + (uint32_t)nblkR * 128u;
+                                  : L.xs + (uint32_t)nblkR * 128u + 32u;
     const uint32_t xs_step = act0 || act1 ? (uint32_t)(kCW * kBlkPerRound * 128) : 0u;  // per round of this warp
     const int tiles_max = SR / 16;
 
@@ -606,6 +625,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
         const DecSeg& pj = a.seg[it.seg];
         const int ra = it.ra, rs = it.rs;
         const int ntile = (rs + 15) / 16;
+        const int hh = dec_half(rs);
         if (ok) ok = mbar_wait(full(s), par, status);
         const uint32_t soff = (uint32_t)s * L.slot;
         // where row 0's scales / zero points start in the slot (dense copies: the aligned superset)
@@ -625,53 +645,119 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
 #pragma unroll
             for (int i = 0; i < NTL; ++i) {
                 v[i][0] = v[i][1] = 0.f;  // rows g and g + 8, units of 2^-24
-                const uint32_t row = (uint32_t)((tl0 + i) * 16 + g);
-                wA[i] = sb + soff + row * (uint32_t)rowbytes + (uint32_t)blk0 * (uint32_t)(kWB * 4);
-                wB[i] = wA[i] + 8u * (uint32_t)rowbytes;
+                // MMA rows g, g + 8: row (tl 8 + g / 2) resp. (tl 8 + g / 2 + 4) of region g & 1
+                const uint32_t rr = (uint32_t)((tl0 + i) * 8 + (g >> 1));
+                const uint32_t row = (g & 1 ? (uint32_t)hh : 0u) + rr;  // the stage row of MMA row g
+                wA[i] = sb + soff + (g & 1 ? L.r1 : 0u) + rr * (uint32_t)rowbytes + (uint32_t)blk0 * (uint32_t)(kWB * 4);
+                wB[i] = wA[i] + 4u * (uint32_t)rowbytes;
                 sA_[i] = sb + s_base + row * P.spitch + (uint32_t)blk0 * 2u;
-                sB_[i] = sA_[i] + 8u * P.spitch;
+                sB_[i] = sA_[i] + 4u * P.spitch;
                 zA_[i] = sb + z_base + row * P.zpitch + (uint32_t)blk0;
-                zB_[i] = zA_[i] + 8u * P.zpitch;
+                zB_[i] = zA_[i] + 4u * P.zpitch;
             }
             uint32_t xo = sb + xs_base + (uint32_t)warp * (uint32_t)(kBlkPerRound * 128) * ((act0 || act1) ? 1u : 0u);
             uint32_t sxa = sb + L.sxs + (uint32_t)blk0 * 4u;
             constexpr uint32_t kWStep = kCW * kBlkPerRound * kWB * 4, kSStep = kCW * kBlkPerRound * 2,
                                kZStep = kCW * kBlkPerRound, kXStep = kCW * kBlkPerRound * 4;
-#pragma unroll 1
-            for (int rd = warp; rd < nround; rd += kCW) {
-                // two MMA chains per tile, whatever the tiles processed together (a row's
-                // arithmetic must not depend on it); a chain's first MMA starts from zero
-                constexpr int NCH = 2;
-                float d[NTL][NCH][4];
+            // One round: columns 2t, 2t+1 of this thread = classes 0, 1 of block 4 rd + t for
+            // rows g, g+8.  Two MMA chains per tile, whatever the tiles processed together (a
+            // row's arithmetic must not depend on it); a chain's first MMA starts from zero.
+            // The round's scales, zero points and sum of x are loaded first, so that their
+            // latency passes under the MMAs.
+            auto epilogue = [&](float (&d)[NTL][2][4], const uint32_t (&sAr)[NTL], const uint32_t (&sBr)[NTL],
+                                const uint32_t (&zAr)[NTL], const uint32_t (&zBr)[NTL], float sx, bool inK) {
 #pragma unroll
-                for (int q = 0; q < kWB / 4; ++q) {  // 16 bytes of each row at a time
-                    uint4 wa[NTL], wb[NTL];
+                for (int i = 0; i < NTL; ++i) {
+                    const float sA = inK ? h2f(sAr[i]) : 0.f;  // past K: no scale (a dense copy holds other bytes)
+                    const float sB = inK ? h2f(sBr[i]) : 0.f;
+                    const float zA = HAS_ZP ? u8f(zAr[i]) : (float)kDefaultZp;
+                    const float zB = HAS_ZP ? u8f(zBr[i]) : (float)kDefaultZp;
+                    const float dd0 = d[i][0][0] + d[i][1][0], dd1 = d[i][0][1] + d[i][1][1];
+                    const float dd2 = d[i][0][2] + d[i][1][2], dd3 = d[i][0][3] + d[i][1][3];
+                    // sum_k x q of the block in units of 2^-24 (INT4: class 1, the high nibble, reads as 16 q)
+                    const float u0 = fmaf(-zA, sx, fmaf(U::kHiWeight, dd1, dd0));
+                    const float u1 = fmaf(-zB, sx, fmaf(U::kHiWeight, dd3, dd2));
+                    v[i][0] = fmaf(sA, u0, v[i][0]);
+                    v[i][1] = fmaf(sB, u1, v[i][1]);
+                }
+            };
+            auto meta = [&](uint32_t (&sAr)[NTL], uint32_t (&sBr)[NTL], uint32_t (&zAr)[NTL], uint32_t (&zBr)[NTL]) {
+#pragma unroll
+                for (int i = 0; i < NTL; ++i) {
+                    sAr[i] = lds_u16_s(sA_[i]);
+                    sBr[i] = lds_u16_s(sB_[i]);
+                    zAr[i] = HAS_ZP ? lds_u8_s(zA_[i]) : 0u;
+                    zBr[i] = HAS_ZP ? lds_u8_s(zB_[i]) : 0u;
+                    sA_[i] += kSStep;
+                    sB_[i] += kSStep;
+                    zA_[i] += kZStep;
+                    zB_[i] += kZStep;
+                }
+            };
+            if constexpr (BITS == 4) {
+                // 16 bytes of rows g and g + 8 per tile and round.  The next round's codes go
+                // into the same registers as soon as this round's last word is unpacked, so
+                // their loads pass under this round's last MMAs and epilogue.
+                uint4 ca[NTL], cb[NTL];
+                auto codes = [&]() {
 #pragma unroll
                     for (int i = 0; i < NTL; ++i) {
-                        wa[i] = q == 0 ? lds128_s<0>(wA[i]) : lds128_s<16>(wA[i]);
-                        wb[i] = q == 0 ? lds128_s<0>(wB[i]) : lds128_s<16>(wB[i]);
+                        ca[i] = lds128_s<0>(wA[i]);
+                        cb[i] = lds128_s<0>(wB[i]);
+                        wA[i] += kWStep;
+                        wB[i] += kWStep;
                     }
-                    if constexpr (BITS == 4) {
-                        // words 0..3: one 16-byte load each = the B pairs of its two MMAs
-                        const uint4 xw[4] = {lds128_s<0>(xo), lds128_s<16>(xo), lds128_s<32>(xo), lds128_s<48>(xo)};
+                };
+                if (warp < nround) codes();
+#pragma unroll 1
+                for (int rd = warp; rd < nround; rd += kCW) {
+                    uint32_t sAr[NTL], sBr[NTL], zAr[NTL], zBr[NTL];
+                    const float sx = lds_f32_s(sxa);
+                    meta(sAr, sBr, zAr, zBr);
+                    float d[NTL][2][4];
 #pragma unroll
-                        for (int w = 0; w < 4; ++w)
+                    for (int w = 0; w < 4; ++w) {
+                        // word w: one 16-byte x load = the B pairs of its two MMAs
+                        const uint4 xw = w == 0 ? lds128_s<0>(xo)
+                                       : w == 1 ? lds128_s<16>(xo)
+                                       : w == 2 ? lds128_s<32>(xo)
+                                                : lds128_s<48>(xo);
+                        uint32_t pa[NTL][4], pb[NTL][4];
 #pragma unroll
-                            for (int i = 0; i < NTL; ++i) {
-                                const uint32_t wa4[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
-                                const uint32_t wb4[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
-                                uint32_t pa[4], pb[4];
-                                U::pairs(wa4[w], pa);
-                                U::pairs(wb4[w], pb);
-                                if (w == 0) {
-                                    mma_16816_z(d[i][0], pa[0], pb[0], pa[1], pb[1], xw[w].x, xw[w].y);
-                                    mma_16816_z(d[i][1], pa[2], pb[2], pa[3], pb[3], xw[w].z, xw[w].w);
-                                } else {
-                                    mma_16816(d[i][0], pa[0], pb[0], pa[1], pb[1], xw[w].x, xw[w].y);
-                                    mma_16816(d[i][1], pa[2], pb[2], pa[3], pb[3], xw[w].z, xw[w].w);
-                                }
+                        for (int i = 0; i < NTL; ++i) {
+                            const uint32_t wa4[4] = {ca[i].x, ca[i].y, ca[i].z, ca[i].w};
+                            const uint32_t wb4[4] = {cb[i].x, cb[i].y, cb[i].z, cb[i].w};
+                            U::pairs(wa4[w], pa[i]);
+                            U::pairs(wb4[w], pb[i]);
+                        }
+                        if (w == 3 && rd + kCW < nround) codes();
+#pragma unroll
+                        for (int i = 0; i < NTL; ++i) {
+                            if (w == 0) {
+                                mma_16816_z(d[i][0], pa[i][0], pb[i][0], pa[i][1], pb[i][1], xw.x, xw.y);
+                                mma_16816_z(d[i][1], pa[i][2], pb[i][2], pa[i][3], pb[i][3], xw.z, xw.w);
+                            } else {
+                                mma_16816(d[i][0], pa[i][0], pb[i][0], pa[i][1], pb[i][1], xw.x, xw.y);
+                                mma_16816(d[i][1], pa[i][2], pb[i][2], pa[i][3], pb[i][3], xw.z, xw.w);
                             }
-                    } else {
+                        }
+                    }
+                    xo += xs_step;
+                    sxa += kXStep;
+                    epilogue(d, sAr, sBr, zAr, zBr, sx, rd * kBlkPerRound + t < nblk);
+                }
+            } else {
+#pragma unroll 1
+                for (int rd = warp; rd < nround; rd += kCW) {
+                    float d[NTL][2][4];
+#pragma unroll
+                    for (int q = 0; q < kWB / 4; ++q) {  // 16 bytes of each row at a time
+                        uint4 wa[NTL], wb[NTL];
+#pragma unroll
+                        for (int i = 0; i < NTL; ++i) {
+                            wa[i] = q == 0 ? lds128_s<0>(wA[i]) : lds128_s<16>(wA[i]);
+                            wb[i] = q == 0 ? lds128_s<0>(wB[i]) : lds128_s<16>(wB[i]);
+                        }
                         // words 4q .. 4q+3: an 8-byte B pair each
                         const uint4 xa = q == 0 ? lds128_s<0>(xo) : lds128_s<32>(xo);
                         const uint4 xb = q == 0 ? lds128_s<16>(xo) : lds128_s<48>(xo);
@@ -691,32 +777,18 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
                                     mma_16816(d[i][w & 1], pa[0], pb[0], pa[1], pb[1], X[2 * w], X[2 * w + 1]);
                             }
                     }
-                }
-                // columns 2t, 2t+1 of this thread = classes 0, 1 of block 4 rd + t for rows g, g+8
-                const float sx = lds_f32_s(sxa);
-                const bool inK = rd * kBlkPerRound + t < nblk;  // past K: no scale (a dense copy holds other bytes)
 #pragma unroll
-                for (int i = 0; i < NTL; ++i) {
-                    const float sA = inK ? h2f(lds_u16_s(sA_[i])) : 0.f;
-                    const float sB = inK ? h2f(lds_u16_s(sB_[i])) : 0.f;
-                    const float zA = HAS_ZP ? u8f(lds_u8_s(zA_[i])) : (float)kDefaultZp;
-                    const float zB = HAS_ZP ? u8f(lds_u8_s(zB_[i])) : (float)kDefaultZp;
-                    const float dd0 = d[i][0][0] + d[i][1][0], dd1 = d[i][0][1] + d[i][1][1];
-                    const float dd2 = d[i][0][2] + d[i][1][2], dd3 = d[i][0][3] + d[i][1][3];
-                    // sum_k x q of the block in units of 2^-24 (INT4: class 1, the high nibble, reads as 16 q)
-                    const float u0 = fmaf(-zA, sx, fmaf(U::kHiWeight, dd1, dd0));
-                    const float u1 = fmaf(-zB, sx, fmaf(U::kHiWeight, dd3, dd2));
-                    v[i][0] = fmaf(sA, u0, v[i][0]);
-                    v[i][1] = fmaf(sB, u1, v[i][1]);
-                    wA[i] += kWStep;
-                    wB[i] += kWStep;
-                    sA_[i] += kSStep;
-                    sB_[i] += kSStep;
-                    zA_[i] += kZStep;
-                    zB_[i] += kZStep;
+                    for (int i = 0; i < NTL; ++i) {
+                        wA[i] += kWStep;
+                        wB[i] += kWStep;
+                    }
+                    uint32_t sAr[NTL], sBr[NTL], zAr[NTL], zBr[NTL];
+                    const float sx = lds_f32_s(sxa);
+                    meta(sAr, sBr, zAr, zBr);
+                    xo += xs_step;
+                    sxa += kXStep;
+                    epilogue(d, sAr, sBr, zAr, zBr, sx, rd * kBlkPerRound + t < nblk);
                 }
-                xo += xs_step;
-                sxa += kXStep;
             }
             // the quad's four blocks, then this warp's rows into the reduction buffer
 #pragma unroll
@@ -744,8 +816,10 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(s));  // every read of the slot is done
         if (warp < ntile && lane < 16) {
-            const int row = warp * 16 + lane;
-            if (ok && row < rs) {
+            // MMA row `lane` of tile `warp`: row warp 8 + lane / 2 (+ 4 for lane >= 8) of region lane & 1
+            const int m = lane & 7, rr = warp * 8 + (m >> 1) + (lane >> 3) * 4;
+            const int row = (m & 1) ? hh + rr : rr;
+            if (ok && ((m & 1) ? row < rs : rr < hh)) {
                 float v = 0.f;
 #pragma unroll
                 for (int w = 0; w < kCW; ++w) v += redb[(warp * kCW + w) * 16 + lane];  // warp order
@@ -834,19 +908,19 @@ void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int*
     constexpr uint32_t kHalfSm = 112u * 1024u, kRing = 200u * 1024u;
     int sr = 16;
     while (sr < rmax) sr *= 2;
-    if (sr <= kMaxSR && dec_layout(sr, 1, rowbytes, nblk, nblkR, lrows).total <= kHalfSm) {
+    if (sr <= kMaxSR && dec_layout(sr, 1, bits, rowbytes, nblk, nblkR, lrows).total <= kHalfSm) {
         *SR = sr;
         *ring = 1;
     } else {
         int sr2 = 16;
-        while (sr2 < 64 && dec_layout(sr2, 1, rowbytes, nblk, nblkR, lrows).slot < 24u * 1024u) sr2 *= 2;
+        while (sr2 < 64 && dec_layout(sr2, 1, bits, rowbytes, nblk, nblkR, lrows).slot < 24u * 1024u) sr2 *= 2;
         int r = 1;
-        while (r < 16 && dec_layout(sr2, r + 1, rowbytes, nblk, nblkR, lrows).total <= kRing) ++r;
+        while (r < 16 && dec_layout(sr2, r + 1, bits, rowbytes, nblk, nblkR, lrows).total <= kRing) ++r;
         *SR = sr2;
         *ring = r;
     }
     *ctas = C;
-    *smem = dec_layout(*SR, *ring, rowbytes, nblk, nblkR, lrows).total;
+    *smem = dec_layout(*SR, *ring, bits, rowbytes, nblk, nblkR, lrows).total;
 }
 
 cudaError_t decode_prepare() {
