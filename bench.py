@@ -689,6 +689,12 @@ def run_next_rows(args):
         if want(name):
             us, nbytes, fl, route = single(M, K, 14336, 4, None, None, q8x=True, calls=100)
             report(name, us, nbytes, fl, route=route)
+    # int8 activations at a prefill size, next to the FP16 tensor-core path on the same shape
+    for q8x in (True, False):
+        name = f"M=1024 K=4096 N=4096 INT4 {'int8' if q8x else 'FP16'} activations, no adapter"
+        if want(name):
+            us, nbytes, fl, route = single(1024, K, 4096, 4, None, None, q8x=q8x, seed=synth.SEED_BASE + 2, calls=10)
+            report(name, us, nbytes, fl, route=route)
     for adapter in ("fp16", "int8"):
         name = f"M=1024 K=4096 N=4096 INT4, {adapter.upper()} rank-32 adapter"
         if want(name):

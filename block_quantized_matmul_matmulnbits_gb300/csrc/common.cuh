@@ -311,6 +311,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
 }
 
+// mbar_wait for a role whose wait is long and not on the critical path: between
+// probes the warp sleeps about `ns` nanoseconds, leaving its issue slots to the
+// warps that are working.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, unsigned int* status, uint32_t ns) {
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(ns);
+        if (mbar_try(bar, parity)) return true;
+        if (*reinterpret_cast<volatile unsigned int*>(status) & kStatusTimeout) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(

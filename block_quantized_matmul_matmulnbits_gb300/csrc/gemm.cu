@@ -55,6 +55,7 @@ constexpr int kThreads = 480;    // 15 warps
 constexpr int kDqWarp0 = 6;      // first dequant warp
 constexpr int kXWarp = 14;       // X producer
 constexpr int kDqThreads = 256;
+constexpr int kDqWarps = kDqThreads / 32;  // arrivals on the dequant barriers: one per warp
 constexpr int kEpiThreads = 128;
 constexpr int kWSlot = BM * 128; // dequantized FP16 A tile of one K step
 constexpr int kPBox = BM * 128;  // one packed-weight TMA box: 128 rows x 128 bytes
@@ -251,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty_x(s), 1);
         }
         for (int s = 0; s < nw; ++s) {
-            mbar_init(full_w(s), kDqThreads);
+            mbar_init(full_w(s), kDqWarps);
             if (!one_release) mbar_init(empty_w(s), 1);  // else empty_w(s) is empty_x(s)
         }
         for (int j = 0; j < np; ++j) {
             mbar_init(full_p(j), 1);
-            mbar_init(empty_p(j), kDqThreads);
+            mbar_init(empty_p(j), kDqWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full(i), 1);
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = u.i0; i < u.i1; i += kps, ++pstep) {
                     const int j = pstep % np;
                     const uint32_t ph = (uint32_t)(pstep / np) & 1u;
-                    if (!(ok = mbar_wait(empty_p(j), ph ^ 1u, status))) break;
+                    if (!(ok = mbar_wait_sleep(empty_p(j), ph ^ 1u, status, 64))) break;
                     // boxes holding this unit's K steps; rows past N and bytes past K read as zero
                     const int bytes = min(kps, u.i1 - i) * kStepBytes;
                     const int nbox = (bytes + 127) / 128;
@@ -320,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < nsteps; ++i, ++step) {
                     const int s = step % nx;
                     const uint32_t ph = (uint32_t)(step / nx) & 1u;
-                    if (!(ok = mbar_wait(empty_x(s), ph ^ 1u, status))) break;
+                    if (!(ok = mbar_wait_sleep(empty_x(s), ph ^ 1u, status, 64))) break;
                     if (i >= u.i1 - u.i0) {  // LoRA step: the dequant warps fill the slot
                         mbar_arrive(full_x(s));
                         continue;
@@ -380,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Unit u;
         while (next_unit(P, cursor, u)) {
             const int acc = tl & 1;
-            if (!mbar_wait(acc_full(acc), (uint32_t)(tl >> 1) & 1u, status)) break;
+            // the epilogue waits a whole tile: it sleeps, so as not to take issue slots from the dequant
+            if (!mbar_wait_sleep(acc_full(acc), (uint32_t)(tl >> 1) & 1u, status, 1000)) break;
             tc_fence_after();
             const int n = u.n0 + row;
             for (int c = 0; c < BN; c += 16) {
@@ -445,26 +447,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int i = i0 + v;
                     if (i >= u.i1) break;
                     const int local = i - u.i0;
+                    // the warp decides together (it arrives once per warp below)
                     if ((local & (kps - 1)) == 0) {
                         cur_p = pstep % np;
-                        if (!(ok = mbar_wait(full_p(cur_p), (uint32_t)(pstep / np) & 1u, status))) break;
+                        ok = __all_sync(0xffffffffu, mbar_wait_sleep(full_p(cur_p), (uint32_t)(pstep / np) & 1u, status, 32));
+                        if (!ok) break;
                         ++pstep;
                     }
                     const int s = step % nw;
                     const uint32_t ph = (uint32_t)(step / nw) & 1u;
-                    if (!(ok = mbar_wait(empty_w(s), ph ^ 1u, status))) break;  // the MMA is done with the slot
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(empty_w(s), ph ^ 1u, status, 32));  // the MMA is done with the slot
+                    if (!ok) break;
                     // invalid block (row past N, K tail): scale 0 makes its products 0
                     const DqConst dc = dq_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
                     Dq2Const d2 = {};
                     if constexpr (BITS == 2) d2 = dq2_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
-                    {  // refill this prefetch slot with step i + kPrefetch
-                        const int blk = 2 * (i + kPrefetch) + h;
-                        const bool ld = row_ok && blk < nblk && i + kPrefetch < u.i1;
-                        const int bc = ld ? blk : 0;
-                        sc[v] = (uint32_t)__ldg(srow + bc);
-                        if (HAS_ZP) zz[v] = (uint32_t)__ldg(zrow + bc);
-                        vmask = ld ? (vmask | (1u << v)) : (vmask & ~(1u << v));
-                    }
                     // this step's bytes of row r: box li*kStepBytes/128, 16-byte chunk c0 (+1)
                     const int li = (local & (kps - 1));
                     const int pb = li * kStepBytes;
@@ -496,16 +493,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      "r"(out[4 * c + 1]), "r"(out[4 * c + 2]), "r"(out[4 * c + 3])
                                      : "memory");
                     }
-                    fence_proxy_async();
-                    mbar_arrive(full_w(s));
-                    if ((local & (kps - 1)) == kps - 1 || i == u.i1 - 1) mbar_arrive(empty_p(cur_p));
+                    fence_proxy_async();  // this thread's writes, before the MMA reads them
+                    __syncwarp();
+                    if (dl == 0) {  // one arrival per warp: its lanes are ordered before lane 0 here
+                        mbar_arrive(full_w(s));
+                        if ((local & (kps - 1)) == kps - 1 || i == u.i1 - 1) mbar_arrive(empty_p(cur_p));
+                    }
+                    {  // refill this prefetch slot with step i + kPrefetch (after the fence, which
+                       // would otherwise wait for these loads)
+                        const int blk = 2 * (i + kPrefetch) + h;
+                        const bool ld = row_ok && blk < nblk && i + kPrefetch < u.i1;
+                        const int bc = ld ? blk : 0;
+                        sc[v] = (uint32_t)__ldg(srow + bc);
+                        if (HAS_ZP) zz[v] = (uint32_t)__ldg(zrow + bc);
+                        vmask = ld ? (vmask | (1u << v)) : (vmask & ~(1u << v));
+                    }
                     ++step;
                 }
             }
             if (ok && u.lora) {
                 const int s = step % nw, sx = step % nx;
-                if (!(ok = mbar_wait(empty_w(s), ((uint32_t)(step / nw) & 1u) ^ 1u, status))) break;
-                if (!(ok = mbar_wait(empty_x(sx), ((uint32_t)(step / nx) & 1u) ^ 1u, status))) break;
+                ok = __all_sync(0xffffffffu, mbar_wait(empty_w(s), ((uint32_t)(step / nw) & 1u) ^ 1u, status));
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu, mbar_wait(empty_x(sx), ((uint32_t)(step / nx) & 1u) ^ 1u, status));
+                if (!ok) break;
                 if (!waited) {
                     pdl_wait();  // T is written by the LoRA down kernel queued before this grid
                     waited = true;
@@ -545,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : "memory");
                 }
                 fence_proxy_async();
-                mbar_arrive(full_w(s));
+                __syncwarp();
+                if (dl == 0) mbar_arrive(full_w(s));
                 ++step;
             }
         }
