@@ -557,11 +557,24 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     const int ctid = threadIdx.x;  // 0 .. 255
     constexpr uint32_t kNamed = 1;  // named barrier of the consumer warps
 
-    // The first stage's weights need no wait for earlier work: take them first.
+    // The first stage's weights need no wait for earlier work: take them first.  So do the
+    // biases of the rows this thread writes first (the first stage's, or with an adapter the
+    // first row of the final pass).
     bool ok = true;
     StageIt it = {r0, 0, 0, 0};
+    float bias0 = 0.f;
     if (r0 < r1) {
         it.settle(a, r1, SR);
+        const DecSeg& pj = a.seg[it.seg];
+        if (pj.bias) {
+            if (LORA) {
+                if (ctid < r1 - r0) bias0 = __half2float(pj.bias[r0 + ctid]);
+            } else if (warp < (it.rs + 15) / 16 && lane < 16) {
+                const int m = lane & 7, rr = warp * 8 + (m >> 1) + (lane >> 3) * 4, hh = dec_half(it.rs);
+                const int row = (m & 1) ? hh + rr : rr;
+                if ((m & 1) ? row < it.rs : rr < hh) bias0 = __half2float(pj.bias[it.ra + row]);
+            }
+        }
         ok = mbar_wait(full(0), 0u, status);
     }
 
@@ -827,7 +840,8 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
                 if (LORA) {  // the adapter term comes at the end
                     reinterpret_cast<float*>(sm + L.ybuf)[it.pos - r0 + row] = y;
                 } else {
-                    pj.Y[ra + row] = __float2half_rn(pj.bias ? y + __half2float(pj.bias[ra + row]) : y);
+                    const float bn = st == 0 ? bias0 : (pj.bias ? __half2float(pj.bias[ra + row]) : 0.f);
+                    pj.Y[ra + row] = __float2half_rn(pj.bias ? y + bn : y);
                 }
             }
         }
@@ -841,7 +855,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
             const float* lorb = reinterpret_cast<const float*>(sm + L.lorb);
             for (int row = ctid; row < r1 - r0; row += kCW * 32) {
                 float y = ybuf[row] + lorb[row];
-                if (pj.bias) y += __half2float(pj.bias[r0 + row]);
+                if (pj.bias) y += row == ctid ? bias0 : __half2float(pj.bias[r0 + row]);
                 pj.Y[r0 + row] = __float2half_rn(y);
             }
         }
