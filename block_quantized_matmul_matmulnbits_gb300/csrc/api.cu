@@ -84,6 +84,7 @@ int device_setup(int* sm_count, unsigned int** status = nullptr) {
         }
         if (mnb::gemv_prepare() != cudaSuccess || mnb::gemm_prepare() != cudaSuccess ||
             mnb::lora_down_prepare() != cudaSuccess || mnb::decode_prepare() != cudaSuccess ||
+            mnb::decode_mt_prepare() != cudaSuccess ||
             cudaGetSymbolAddress(&st, mnb::g_status) != cudaSuccess) {
             cudaGetLastError();
             return MNB_ERR_CUDA;
@@ -113,6 +114,33 @@ void plan_decode(const mnb_desc& d, int rank, int sms, mnb_plan_info* p) {
     p->rows_per_cta = (int)((d.N + ctas - 1) / ctas);
     p->k_splits = SR;
     p->tokens_per_cta = 1;
+}
+
+// Decode kernel for 2 .. 16 token rows: rows split evenly over one CTA per SM,
+// the token rows as the MMA's N.
+void plan_decode_mt(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
+    int ctas, parts, ring;
+    size_t smem;
+    mnb::decode_mt_geometry((int)d.N, (int)d.K, d.bits, (int)Mt, true, sms, &ctas, &parts, &ring, &smem);
+    p->route = MNB_ROUTE_GEMV;
+    p->lora_kernel = 0;
+    p->grid_x = ctas;
+    p->grid_y = 1;
+    p->block_threads = 576;  // 16 consumer warps, the producer and the reducer
+    p->rows_per_cta = (int)((d.N + ctas - 1) / ctas);
+    p->k_splits = 16;
+    p->tokens_per_cta = Mt <= 8 ? 8 : 16;
+}
+
+// Which decode kernel streams the weights of a decode-route call: the
+// single-token kernel, the kernel for 2 .. 16 token rows, or (0) the general
+// multi-token kernel.  fused_ok: FP16 or no adapter, FP16 activations.
+enum { kDecGeneral = 0, kDecSingle = 1, kDecMulti = 2 };
+int decode_kind(const mnb_desc& d, int64_t Mt, int rank, int sms, bool fused_ok) {
+    if (!fused_ok) return kDecGeneral;
+    if (mnb::decode_supported(d.bits, Mt, (int)d.K, d.N, rank > 0, sms)) return kDecSingle;
+    if (mnb::decode_mt_supported(d.bits, Mt, (int)d.K, rank > 0)) return kDecMulti;
+    return kDecGeneral;
 }
 
 // Decode-kernel geometry: balanced row ranges, one CTA per SM and token group.
@@ -164,9 +192,16 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
     int route = M <= thr ? MNB_ROUTE_GEMV : MNB_ROUTE_GEMM;
     if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
     if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
-    if (route == MNB_ROUTE_GEMV && fused_ok && mnb::decode_supported(d.bits, Mt, (int)d.K, d.N, rank > 0, sms)) {
-        plan_decode(d, rank, sms, p);
-        return MNB_OK;
+    if (route == MNB_ROUTE_GEMV) {
+        const int kind = decode_kind(d, Mt, rank, sms, fused_ok);
+        if (kind == kDecSingle) {
+            plan_decode(d, rank, sms, p);
+            return MNB_OK;
+        }
+        if (kind == kDecMulti) {
+            plan_decode_mt(d, Mt, sms, p);
+            return MNB_OK;
+        }
     }
     if (route == MNB_ROUTE_GEMV)
         plan_gemv(d, Mt, sms, p);
@@ -322,8 +357,10 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     // LoRA down kernel lets the matmul kernel start only after its own wait,
     // so behind it the matmul kernel reads X at once and waits only for T.
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
-    if (p.route == MNB_ROUTE_GEMV && p.tokens_per_cta == 1) {
-        // one launch: base and adapter on the single-token decode kernel
+    const int kind = p.route == MNB_ROUTE_GEMV ? decode_kind(d, Mt, rank, sms, !q8x && !(rank > 0 && ad.q8)) : kDecGeneral;
+    if (kind != kDecGeneral) {
+        // one launch: the single-token decode kernel (base and adapter), or the
+        // decode kernel for 2 .. 16 token rows
         mnb::DecodeArgs a = {};
         a.nseg = 1;
         a.NR = (int)d.N;
@@ -335,9 +372,10 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
         a.T = rank > 0 ? Th : nullptr;
         a.K = (int)d.K;
         a.bits = d.bits;
+        a.Mt = (int)Mt;
         a.x_wait = early ? 1 : 0;
         a.status = status;
-        e = mnb::decode_launch(a, rank, sms, early, st);
+        e = kind == kDecSingle ? mnb::decode_launch(a, rank, sms, early, st) : mnb::decode_mt_launch(a, sms, early, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
         if (e != cudaSuccess) return MNB_ERR_CUDA;
         h->last_route = p.route;
@@ -521,8 +559,9 @@ int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
     mnb_plan_info p;
     make_plan(d, batch, M, 0, sms, &p);
-    if (p.route == MNB_ROUTE_GEMV && p.tokens_per_cta == 1) {
-        // one token row: one single-token decode launch over the nonempty members
+    const int kind = p.route == MNB_ROUTE_GEMV ? decode_kind(d, Mt, 0, sms, true) : kDecGeneral;
+    if (kind != kDecGeneral) {
+        // up to 16 token rows: one decode launch over the nonempty members
         mnb::DecodeArgs a = {};
         int R = 0;
         for (int i = 0; i < nproj; ++i) {
@@ -535,11 +574,12 @@ int mnb_run_multi(mnb_handle h, const void* X, const mnb_projection* proj, int32
         }
         a.NR = R;
         a.X = static_cast<const __half*>(X);
+        a.Mt = (int)Mt;
         a.K = (int)d.K;
         a.bits = d.bits;
         a.x_wait = early ? 1 : 0;
         a.status = status;
-        e = mnb::decode_launch(a, 0, sms, early, st);
+        e = kind == kDecSingle ? mnb::decode_launch(a, 0, sms, early, st) : mnb::decode_mt_launch(a, sms, early, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
         if (e != cudaSuccess) return MNB_ERR_CUDA;
         h->last_route = p.route;

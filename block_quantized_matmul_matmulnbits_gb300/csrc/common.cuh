@@ -328,6 +328,12 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, u
     }
 }
 
+// Bring `bytes` (a multiple of 16, from a 16-byte aligned address) into L2 without
+// waiting: later copies of the range then find it there.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(

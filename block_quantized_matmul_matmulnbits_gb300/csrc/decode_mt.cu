@@ -1,0 +1,699 @@
+// decode_mt.cu -- decode kernel for a few token rows (2 .. 16): one launch computes
+//
+//     Y[m, n] = sum_k X[m, k] w[n, k]  (+ bias[n])
+//
+// for every token row m, the decode ("fuse_down") path of "[WebGPU] Fuse rank-32
+// quantized LoRA with MatMulNBits" (onnxruntime PR 33370, commit message adding
+// MatMulNBitsLoRA: the decode mode is chosen from the per-matrix row count),
+// restated for sm_103a with the token rows as the MMA's N.
+//
+// Design:
+//  * Rows are split evenly over the CTAs (one per SM), as in the single-token
+//    kernel.  A producer warp streams the CTA's rows through a ring of slots: a
+//    16-row stage arrives as `kparts` slots, each a K range of the 16 rows (codes
+//    as one 3-D TMA box of 16 rows x the range's 128-byte segments, 128-byte
+//    swizzle: 16-byte chunk c of row r lands at c ^ (r & 7), so one 4-byte load
+//    per thread reads 8 rows x 4 words in 32 different banks; scales and zero
+//    points as 2-D TMA boxes with padded rows).  The whole share is prefetched
+//    into L2 once x is staged (before that it would only queue behind the x loads).
+//  * mma.sync m16n8k16 with 16 weight rows as M and 8 token rows as N.  A code
+//    reaches the tensor core as the FP16 value q * 2^-24 (exact), so unpacking is
+//    a mask (INT4) or a byte permute (INT8).  An INT4 word's low and high nibbles
+//    go to two MMAs (the high nibble reads as 16 q, its x is staged as x / 16),
+//    each covering one half of a block's codes for the quad's four words.  The
+//    MMAs of a block start from -zp * sum_k x, so they end at sum_k x (q - zp),
+//    and the thread applies y += s * that in FP32.
+//  * Warp w takes blocks w, w + 16, ... of every stage, for every token tile:
+//    a block's codes are unpacked once for all the token rows.  x is staged once
+//    per CTA by the thread that reads it: each thread keeps the B fragments of its
+//    blocks (16 bytes a block and token tile) and their sums of x (one MMA with
+//    all codes 1).
+//  * The consumer warps never wait for one another: each frees a slot when it has
+//    read it, and hands its partial sums of a stage to a reducer warp through a
+//    pair of barriers; the reducer adds the 16 warps' partials in a fixed order
+//    (no atomics) while the consumers work on the next stage.  Results are
+//    deterministic and independent of how the rows were split into CTAs.
+//  * Every mbarrier wait is bounded and reports through the status word.
+#include <cuda.h>
+
+#include <cstring>
+#include <type_traits>
+
+#include "common.cuh"
+#include "decode_common.cuh"
+#include "mnb_internal.h"
+
+namespace mnb {
+
+namespace {
+
+using namespace dec;
+
+constexpr int kMtCW = 16;                         // consumer warps
+constexpr int kMtThreads = (kMtCW + 2) * 32;      // + the producer and the reducer warps
+constexpr int kMtSR = 16;                         // rows per stage: one box
+constexpr int kMtMaxRing = 8;
+constexpr uint32_t kMtSmem = 227u * 1024u;        // shared memory of one CTA per SM
+constexpr uint32_t kXF = kMtCW * 512u;            // x fragments of one block and token tile, all warps
+constexpr uint32_t kQF = kMtCW * 64u;             // MMA starting values of one block and token tile, all warps
+constexpr int kTS = 20;                           // partials: floats between token rows
+
+// Shared-memory loads at a 32-bit address plus a constant offset (the assembler folds
+// the addition into the load); volatile: they stay after the barrier waits before them.
+__device__ __forceinline__ uint32_t lds32_dyn(uint32_t a, uint32_t off) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a + off));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16_dyn(uint32_t a, uint32_t off) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a + off));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds8_dyn(uint32_t a, uint32_t off) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a + off));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128_dyn(uint32_t a, uint32_t off) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a + off));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// Predicated shared-memory store and mbarrier arrival (no branch around them).
+__device__ __forceinline__ void sts128_if(bool p, uint32_t a, uint4 v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t"
+        "@q st.shared.v4.u32 [%1], {%2, %3, %4, %5};\n\t}" ::"r"((uint32_t)p),
+        "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_if(bool p, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %0, 0;\n\t"
+        "@q mbarrier.arrive.shared::cta.b64 _, [%1];\n\t}" ::"r"((uint32_t)p),
+        "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ uint4 ldg128_nc(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg64_nc(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+// Shared memory plan, identical on host and device.  Slot s holds a K range of one
+// 16-row stage: codes at s * codes (one box [segment][16 rows][128 B]), scales at
+// sc + s * 16 spitch, zero points at zp + s * 16 zpitch.  After the ring: the
+// threads' x fragments [block][token tile][warp][lane][16 B], the MMAs' starting
+// values [block][token tile][warp][t][4] FP32, the warps' partials of a stage
+// [warp][8 nt8 tokens (kTS floats apart)][16 rows] FP32, and the barriers full[ring],
+// empty[ring], "x staged", "partials written" and "partials added", and a flag: every
+// consumer's waits ended in time.
+struct MtLayout {
+    uint32_t codes, sc, zp;
+    uint32_t spitch, zpitch;
+    uint32_t xs, cq, red, rs, bars, total;  // rs: floats between two warps' partials
+};
+
+__host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8, int parts, bool zp) {
+    const int nblk = K / 32, nbp = nblk / parts;
+    const uint32_t rowbytes = (uint32_t)K * (uint32_t)bits / 8u / (uint32_t)parts;  // of a slot's K range
+    const DecPitch P = dec_pitch(nbp);
+    MtLayout L;
+    L.codes = 16u * rowbytes;  // a multiple of 2048: the boxes stay 1024-aligned
+    L.spitch = P.spitch;
+    L.zpitch = P.zpitch;
+    L.sc = (uint32_t)ring * L.codes;
+    L.zp = L.sc + (uint32_t)ring * (uint32_t)kMtSR * P.spitch;
+    L.xs = al128(L.zp + (zp ? (uint32_t)ring * (uint32_t)kMtSR * P.zpitch : 0u));
+    L.cq = L.xs + (uint32_t)nblk * (uint32_t)nt8 * 512u;
+    L.red = al128(L.cq + (uint32_t)nblk * (uint32_t)nt8 * 64u);
+    L.rs = (uint32_t)(8 * nt8 * kTS);
+    L.bars = al128(L.red + (uint32_t)kMtCW * L.rs * 4u);
+    L.total = L.bars + (2u * (uint32_t)ring + 4u) * 8u;  // + the "waits ended in time" flag
+    return L;
+}
+
+// The CTA's rows as 16-row stages that never straddle two projections.  The
+// current projection's bounds stay in registers: the kernel parameters (indexed by
+// a register) are read again only when the stages move to the next projection.
+struct MtRows {
+    int pos, r1;         // first row of the stage (row space), end of the CTA's rows
+    int seg, row0, end;  // current projection, its first row and end (row space)
+    int ra, rs;          // the stage's first row inside the projection, its rows
+    __device__ __forceinline__ void load(const DecodeArgs& a) {
+        while (seg + 1 < a.nseg && pos >= a.seg[seg + 1].row0) ++seg;  // empty projections start where the next does
+        row0 = a.seg[seg].row0;
+        end = row0 + a.seg[seg].N;
+    }
+    __device__ __forceinline__ void set() {
+        rs = min(min(kMtSR, r1 - pos), end - pos);
+        ra = pos - row0;
+    }
+    __device__ __forceinline__ void init(const DecodeArgs& a, int r0, int r1_) {
+        pos = r0;
+        r1 = r1_;
+        seg = 0;
+        if (pos < r1) {
+            load(a);
+            set();
+        }
+    }
+    // Next stage; true when it starts a new projection.
+    __device__ __forceinline__ bool next(const DecodeArgs& a) {
+        pos += rs;
+        if (pos >= r1) return false;
+        const bool moved = pos >= end;
+        if (moved) load(a);
+        set();
+        return moved;
+    }
+};
+
+// TMA descriptors per projection: codes (3-D, swizzled), scales and zero points.
+struct MtMaps {
+    CUtensorMap c[kMaxSeg];
+    CUtensorMap s[kMaxSeg];
+    CUtensorMap z[kMaxSeg];
+};
+
+template <int BITS, bool HAS_ZP, int NT8, int UB>
+__global__ void __launch_bounds__(kMtThreads, 1)
+    decode_mt_kernel(const __grid_constant__ MtMaps maps, const __grid_constant__ DecodeArgs a) {
+    using U = Unpack<BITS>;
+    constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
+    constexpr int kProducer = kMtCW, kReducer = kMtCW + 1;
+    extern __shared__ unsigned char sm_raw[];
+
+    const int K = a.K, NR = a.NR, Mt = a.Mt, H = a.kparts;
+    const int nblk = K >> 5, nj = nblk / kMtCW, njp = nj / H;  // blocks of a consumer warp: per stage, per slot
+    const int ring = a.ring;
+    const MtLayout L = mt_layout(ring, BITS, K, NT8, H, HAS_ZP);
+    const uint32_t sb = (smem_u32(sm_raw) + 1023u) & ~1023u;  // swizzled boxes want 1024-byte alignment
+    unsigned char* sm = sm_raw + (sb - smem_u32(sm_raw));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = gridDim.x;
+    const int r0 = (int)((long long)blockIdx.x * NR / C), r1 = (int)((long long)(blockIdx.x + 1) * NR / C);
+    unsigned int* status = a.status;
+
+    auto full = [&](int s) { return sb + L.bars + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return sb + L.bars + 8u * (uint32_t)(ring + s); };
+    const uint32_t xready = sb + L.bars + 16u * (uint32_t)ring;
+    const uint32_t pfull = xready + 8u, pfree = xready + 16u;  // the partials: written by all warps, added
+    float* red = reinterpret_cast<float*>(sm + L.red);
+    volatile int* in_time = reinterpret_cast<volatile int*>(sm + L.bars + 16u * (uint32_t)ring + 24u);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < ring; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kMtCW);
+        }
+        mbar_init(xready, kMtCW);
+        mbar_init(pfull, kMtCW);
+        mbar_init(pfree, 1);
+        *in_time = 1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == kProducer) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint32_t rowbytes = (uint32_t)K * BITS / 8u;
+            const int segp = (int)(rowbytes / 128u) / H, nbp = nblk / H;  // per slot
+            const uint32_t bytes = L.codes + (uint32_t)kMtSR * L.spitch + (HAS_ZP ? (uint32_t)kMtSR * L.zpitch : 0u);
+            bool ok = true;
+            int q = 0;  // slots issued
+            MtRows it;
+            it.init(a, r0, r1);
+            // Whole 16-row boxes land, rows past N reading as zero; the MMA rows of a
+            // shorter stage past its end read the next rows, and are not stored.
+            for (; ok && it.pos < r1; it.next(a)) {
+                for (int h = 0; h < H; ++h, ++q) {
+                    const int s = q % ring;
+                    const uint32_t par = (uint32_t)(q / ring) & 1u;
+                    if (q == ring) {
+                        // The ring is full: once x is staged, the rest of the share into
+                        // L2 at once, so that the refills come from L2 while HBM streams
+                        // the remainder at full rate.
+                        mbar_wait(xready, 0u, status);
+                        for (int sg = 0; sg < a.nseg; ++sg) {
+                            const DecSeg& pg = a.seg[sg];
+                            const int lo = max(r0, pg.row0), hi = min(r1, pg.row0 + pg.N);
+                            if (lo >= hi) continue;
+                            const size_t ra = (size_t)(lo - pg.row0), n = (size_t)(hi - lo);
+                            for (size_t off = 0; off < n * rowbytes; off += (1u << 20))
+                                prefetch_l2_bulk(pg.Wq + ra * rowbytes + off,
+                                                 (uint32_t)min((size_t)(1u << 20), n * rowbytes - off));
+                            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(pg.S) + ra * nblk * 2,
+                                             (uint32_t)(n * nblk * 2));
+                            if (HAS_ZP) prefetch_l2_bulk(pg.Z + ra * nblk, (uint32_t)(n * nblk));
+                        }
+                    }
+                    if (q >= ring && !(ok = mbar_wait(empty(s), par ^ 1u, status))) break;
+                    mbar_arrive_tx(full(s), bytes);
+                    tma_load_3d(sb + (uint32_t)s * L.codes, &maps.c[it.seg], 0, it.ra, h * segp, full(s));
+                    tma_load_2d(sb + L.sc + (uint32_t)s * kMtSR * L.spitch, &maps.s[it.seg], h * nbp, it.ra, full(s));
+                    if (HAS_ZP)
+                        tma_load_2d(sb + L.zp + (uint32_t)s * kMtSR * L.zpitch, &maps.z[it.seg], h * nbp, it.ra,
+                                    full(s));
+                }
+            }
+            // no copy may still be in flight when the CTA exits (a consumer may have given up)
+            for (int i = q > ring ? q - ring : 0; i < q; ++i)
+                mbar_wait(full(i % ring), (uint32_t)(i / ring) & 1u, status, false);
+        }
+        return;
+    }
+
+    if (warp == kReducer) {
+        // ------------------------------------------------------------ reducer
+        // Output o = lane + 32 i of a stage is token row o >> 4, row o & 15: the sum of
+        // the 16 warps' partials in warp order, one rounding.
+        if (r0 >= r1) return;
+        bool ok = true;
+        MtRows it;
+        it.init(a, r0, r1);
+        __half* Yp = a.seg[it.seg].Y;
+        const __half* bp = a.seg[it.seg].bias;
+        int Np = a.seg[it.seg].N;
+        uint32_t ph = 0u;
+        for (bool moved = false; it.pos < r1; moved = it.next(a), ph ^= 1u) {
+            if (moved) {
+                Yp = a.seg[it.seg].Y;
+                bp = a.seg[it.seg].bias;
+                Np = a.seg[it.seg].N;
+            }
+            if (ok) ok = mbar_wait(pfull, ph, status) && *in_time;
+            float y[NT8 * 4];
+#pragma unroll
+            for (int i = 0; i < NT8 * 4; ++i) {
+                const int o = lane + 32 * i;
+                const float* pr = red + (o >> 4) * kTS + (o & 15);
+                float acc = 0.f;
+#pragma unroll
+                for (int w = 0; w < kMtCW; ++w) acc += pr[w * (int)L.rs];
+                y[i] = acc;
+            }
+            __syncwarp();
+            mbar_arrive_if(lane == 0, pfree);  // every lane's reads are done
+#pragma unroll
+            for (int i = 0; i < NT8 * 4; ++i) {
+                const int o = lane + 32 * i, tok = o >> 4, m = o & 15;
+                if (ok && m < it.rs && tok < Mt) {
+                    float v = y[i] * (1.0f / kUnit);
+                    if (bp) v += __half2float(bp[it.ra + m]);
+                    Yp[(size_t)tok * Np + it.ra + m] = __float2half_rn(v);
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    if (r0 >= r1) {
+        mbar_arrive_if(lane == 0, xready);
+        return;
+    }
+    bool ok = true;
+
+    // This thread's x fragment of its j-th block (block warp + kMtCW j) and token tile
+    // jt at xf + (j NT8 + jt) kXF; at qf + (j NT8 + jt) kQF the MMA's starting
+    // accumulator for rows g, g + 8 and tokens 2t, 2t + 1 of the tile: (c0, c1, c0, c1),
+    // c = -8 sum_k x (INT4) or -128 sum_k x (INT8) without zero points, c = sum_k x
+    // with them (times the rows' -zp then), all times 2^-24.
+    const uint32_t xf = sb + L.xs + (uint32_t)warp * 512u + (uint32_t)lane * 16u;
+    const uint32_t qf = sb + L.cq + (uint32_t)warp * 64u + (uint32_t)t * 16u;
+
+    // ---- x of every token row: wait for the work that produces it, then stage it
+    if (a.x_wait) pdl_wait();
+    {
+        // A constant code of 1 (2^-24) and, for INT4 high nibbles, 16 (their x is x / 16):
+        // the MMA then gives sum_k x 2^-24 of the block for the tile's tokens.
+        constexpr uint32_t kOne = 0x00010001u, kHi = BITS == 4 ? 0x00100010u : kOne;
+        constexpr float kZs = HAS_ZP ? 1.f : -(float)kDefaultZp;
+        constexpr int kXU = 8;  // fragments in flight per thread
+        const __half2 k16 = __float2half2_rn(0.0625f);
+        const int npc = nj * NT8;
+        for (int i0 = 0; i0 < npc; i0 += kXU) {
+            uint4 v[kXU];
+#pragma unroll
+            for (int u = 0; u < kXU; ++u) {
+                const int i = i0 + u, j = i / NT8, tok = 8 * (i % NT8) + g;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < npc && tok < Mt) {
+                    const __half* p = a.X + (size_t)tok * K + (size_t)(warp + kMtCW * j) * 32;
+                    if constexpr (BITS == 4) {
+                        v[u] = ldg128_nc(p + 8 * t);  // word t: x[8t .. 8t + 7]
+                    } else {
+                        const uint2 lo = ldg64_nc(p + 4 * t), hi = ldg64_nc(p + 16 + 4 * t);  // words t, t + 4
+                        v[u] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kXU; ++u) {
+                const int i = i0 + u;
+                if (i >= npc) break;  // the same for every thread
+                uint4 o = v[u];
+                if constexpr (BITS == 4) {  // (x0, x4) (x2, x6) (x1, x5)/16 (x3, x7)/16
+                    const uint32_t h15 = prmt(o.x, o.z, 0x7632u), h37 = prmt(o.y, o.w, 0x7632u);
+                    const __half2 s15 = __hmul2(*reinterpret_cast<const __half2*>(&h15), k16);
+                    const __half2 s37 = __hmul2(*reinterpret_cast<const __half2*>(&h37), k16);
+                    o = make_uint4(prmt(o.x, o.z, 0x5410u), prmt(o.y, o.w, 0x5410u),
+                                   *reinterpret_cast<const uint32_t*>(&s15), *reinterpret_cast<const uint32_t*>(&s37));
+                }
+                sts128(xf + (uint32_t)i * kXF, o);
+                float d[4];
+                mma_16816_z(d, kOne, kOne, kOne, kOne, o.x, o.y);
+                mma_16816(d, kHi, kHi, kHi, kHi, o.z, o.w);
+                const uint32_t c0 = __float_as_uint(kZs * d[0]), c1 = __float_as_uint(kZs * d[1]);
+                sts128_if(g == 0, qf + (uint32_t)i * kQF, make_uint4(c0, c1, c0, c1));
+            }
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, xready);
+    }
+
+    // ---- the stages
+    // Codes of block b in the slot's box, row r: INT4 16 bytes at segment b >> 3, chunk
+    // b & 7; INT8 32 bytes at segment b >> 2, chunks 2 (b & 3) and 2 (b & 3) + 1; a
+    // segment is [16 rows][128 B], row r + 8 1024 bytes after row r.  Along this warp's
+    // blocks (b = warp + 16 j) the chunk is fixed and the segment steps by a constant;
+    // a slot starts at a multiple of 16 blocks.
+    const uint32_t ch0 = BITS == 4 ? (uint32_t)(warp & 7) : 2u * (uint32_t)(warp & 3);
+    const uint32_t c_off = (uint32_t)(BITS == 4 ? warp >> 3 : warp >> 2) * 2048u + (uint32_t)g * 128u +
+                           ((ch0 ^ (uint32_t)g) << 4) + 4u * (uint32_t)t;
+    const uint32_t c_hi = BITS == 4 ? 0u : (((ch0 + 1u) ^ (uint32_t)g) << 4) - ((ch0 ^ (uint32_t)g) << 4);  // word t + 4
+    constexpr uint32_t kCStep = (BITS == 4 ? kMtCW / 8 : kMtCW / 4) * 2048u;
+    constexpr uint32_t kSStep = 2u * kMtCW, kZStep = kMtCW;
+    // the slot cursor: index, phase, and this thread's codes, scales and zero points in it
+    int s = 0;
+    uint32_t par = 0u;
+    const uint32_t c_first = sb + c_off, s_first = sb + L.sc + (uint32_t)g * L.spitch + (uint32_t)warp * 2u;
+    const uint32_t z_first = sb + L.zp + (uint32_t)g * L.zpitch + (uint32_t)warp;
+    const uint32_t s8 = 8u * L.spitch, z8 = 8u * L.zpitch;
+    uint32_t cS = c_first, sS = s_first, zS = z_first;
+    // this thread's partials: rows g, g + 8 x tokens 8 jt + 2t, + 1
+    float* pw = red + warp * (int)L.rs + 2 * t * kTS + g;
+    uint32_t fph = 0u;  // phase of "partials added"
+    MtRows it;
+    it.init(a, r0, r1);
+    for (bool first = true; it.pos < r1; it.next(a), first = false) {
+        float v[NT8][4];
+#pragma unroll
+        for (int jt = 0; jt < NT8; ++jt) v[jt][0] = v[jt][1] = v[jt][2] = v[jt][3] = 0.f;
+        uint32_t xo = xf, qo = qf;  // the slots follow each other in K, and so do the fragments
+        for (int h = 0; h < H; ++h) {
+            // after a timeout the slot's stale bytes are read all the same (in bounds)
+            // and the reducer stores nothing
+            if (ok) ok = mbar_wait(full(s), par, status);
+            uint32_t cA = cS, sA = sS, zA = zS;
+#pragma unroll 1
+            for (int j = 0; j < njp; j += UB) {
+                // UB blocks: every load first, then the MMAs, then the FP32 block
+                // epilogues, so that the blocks' latencies overlap
+                uint32_t wa[UB][2], wb[UB][2], sc[UB][2];
+                [[maybe_unused]] uint32_t zq[UB][2];
+                uint4 xw[UB][NT8], cq[UB][NT8];
+#pragma unroll
+                for (int u = 0; u < UB; ++u) {
+                    wa[u][0] = lds32_dyn(cA, u * kCStep);
+                    wb[u][0] = lds32_dyn(cA, u * kCStep + 1024u);
+                    if constexpr (BITS == 8) {
+                        wa[u][1] = lds32_dyn(cA + c_hi, u * kCStep);
+                        wb[u][1] = lds32_dyn(cA + c_hi, u * kCStep + 1024u);
+                    }
+                    sc[u][0] = lds16_dyn(sA, u * kSStep);
+                    sc[u][1] = lds16_dyn(sA + s8, u * kSStep);
+                    if constexpr (HAS_ZP) {
+                        zq[u][0] = lds8_dyn(zA, u * kZStep);
+                        zq[u][1] = lds8_dyn(zA + z8, u * kZStep);
+                    }
+#pragma unroll
+                    for (int jt = 0; jt < NT8; ++jt) {
+                        xw[u][jt] = lds128_dyn(xo, (u * NT8 + jt) * kXF);
+                        cq[u][jt] = lds128_dyn(qo, (u * NT8 + jt) * kQF);
+                    }
+                }
+                float d[UB][NT8][4];
+#pragma unroll
+                for (int u = 0; u < UB; ++u) {
+#pragma unroll
+                    for (int jt = 0; jt < NT8; ++jt) {
+                        if constexpr (HAS_ZP) {  // start at -zp sum_k x
+                            const float zpA = u8f(zq[u][0]), zpB = u8f(zq[u][1]);
+                            d[u][jt][0] = -zpA * __uint_as_float(cq[u][jt].x);
+                            d[u][jt][1] = -zpA * __uint_as_float(cq[u][jt].y);
+                            d[u][jt][2] = -zpB * __uint_as_float(cq[u][jt].z);
+                            d[u][jt][3] = -zpB * __uint_as_float(cq[u][jt].w);
+                        } else {
+                            d[u][jt][0] = __uint_as_float(cq[u][jt].x);
+                            d[u][jt][1] = __uint_as_float(cq[u][jt].y);
+                            d[u][jt][2] = __uint_as_float(cq[u][jt].z);
+                            d[u][jt][3] = __uint_as_float(cq[u][jt].w);
+                        }
+                    }
+                    if constexpr (BITS == 4) {
+                        uint32_t pa[4], pb[4];
+                        U::pairs(wa[u][0], pa);
+                        U::pairs(wb[u][0], pb);
+#pragma unroll
+                        for (int jt = 0; jt < NT8; ++jt) {
+                            mma_16816(d[u][jt], pa[0], pb[0], pa[2], pb[2], xw[u][jt].x, xw[u][jt].y);  // low nibbles
+                            mma_16816(d[u][jt], pa[1], pb[1], pa[3], pb[3], xw[u][jt].z, xw[u][jt].w);  // high: 16 q, x / 16
+                        }
+                    } else {
+                        uint32_t pa0[2], pa1[2], pb0[2], pb1[2];
+                        U::pairs(wa[u][0], pa0);
+                        U::pairs(wa[u][1], pa1);
+                        U::pairs(wb[u][0], pb0);
+                        U::pairs(wb[u][1], pb1);
+#pragma unroll
+                        for (int jt = 0; jt < NT8; ++jt) {
+                            mma_16816(d[u][jt], pa0[0], pb0[0], pa0[1], pb0[1], xw[u][jt].x, xw[u][jt].y);  // words t
+                            mma_16816(d[u][jt], pa1[0], pb1[0], pa1[1], pb1[1], xw[u][jt].z, xw[u][jt].w);  // words t + 4
+                        }
+                    }
+                }
+                // y += s (sum_k x q - zp sum_k x), in units of 2^-24
+#pragma unroll
+                for (int u = 0; u < UB; ++u) {
+                    const float scA = h2f(sc[u][0]), scB = h2f(sc[u][1]);
+#pragma unroll
+                    for (int jt = 0; jt < NT8; ++jt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[jt][e] = fmaf(e < 2 ? scA : scB, d[u][jt][e], v[jt][e]);
+                }
+                cA += UB * kCStep;
+                sA += UB * kSStep;
+                zA += UB * kZStep;
+                xo += UB * NT8 * kXF;
+                qo += UB * NT8 * kQF;
+            }
+            __syncwarp();
+            mbar_arrive_if(lane == 0, empty(s));  // this warp's reads of the slot are done
+            if (++s == ring) {
+                s = 0;
+                par ^= 1u;
+                cS = c_first;
+                sS = s_first;
+                zS = z_first;
+            } else {
+                cS += L.codes;
+                sS += (uint32_t)kMtSR * L.spitch;
+                zS += (uint32_t)kMtSR * L.zpitch;
+            }
+        }
+        // hand this warp's partials to the reducer, once it has added the previous stage's
+        if (!first) {
+            if (ok) ok = mbar_wait(pfree, fph, status);
+            fph ^= 1u;
+        }
+        if (!ok) *in_time = 0;
+#pragma unroll
+        for (int jt = 0; jt < NT8; ++jt) {
+            float* pt = pw + 8 * jt * kTS;
+            pt[0] = v[jt][0];
+            pt[kTS] = v[jt][1];
+            pt[8] = v[jt][2];
+            pt[kTS + 8] = v[jt][3];
+        }
+        __threadfence_block();
+        __syncwarp();
+        mbar_arrive_if(lane == 0, pfull);
+    }
+}
+
+template <int BITS, bool HAS_ZP, int NT8, int UB>
+cudaError_t mt_launch_one(const MtMaps& maps, const DecodeArgs& a, int ctas, size_t smem, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kMtThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, decode_mt_kernel<BITS, HAS_ZP, NT8, UB>, maps, a);
+}
+
+// The kernels: bits x zero points x token tiles x blocks per loop step of a warp
+// (4, 2, 1 for one token tile; 2, 1 for two).
+template <int BITS, bool HAS_ZP>
+cudaError_t mt_launch_bz(int nt8, int ub, const MtMaps& maps, const DecodeArgs& a, int ctas, size_t smem, bool pdl,
+                         cudaStream_t st) {
+    if (nt8 == 1) {
+        if (ub == 4) return mt_launch_one<BITS, HAS_ZP, 1, 4>(maps, a, ctas, smem, pdl, st);
+        if (ub == 2) return mt_launch_one<BITS, HAS_ZP, 1, 2>(maps, a, ctas, smem, pdl, st);
+        return mt_launch_one<BITS, HAS_ZP, 1, 1>(maps, a, ctas, smem, pdl, st);
+    }
+    if (ub == 2) return mt_launch_one<BITS, HAS_ZP, 2, 2>(maps, a, ctas, smem, pdl, st);
+    return mt_launch_one<BITS, HAS_ZP, 2, 1>(maps, a, ctas, smem, pdl, st);
+}
+
+template <int BITS, bool HAS_ZP, int NT8, int UB>
+cudaError_t mt_set_one() {
+    return cudaFuncSetAttribute(decode_mt_kernel<BITS, HAS_ZP, NT8, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kMtSmem);
+}
+
+template <int BITS, bool HAS_ZP>
+cudaError_t mt_set_smem() {
+    cudaError_t e = mt_set_one<BITS, HAS_ZP, 1, 4>();
+    if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 1, 2>();
+    if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 1, 1>();
+    if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 2, 2>();
+    if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 2, 1>();
+    return e;
+}
+
+int mt_ctas(int N, int sms) {
+    int C = (N + 15) / 16;
+    const int s = sms > 0 ? sms : 1;
+    if (C > s) C = s;
+    return C < 1 ? 1 : C;
+}
+
+int mt_nt8(int Mt) { return Mt <= 8 ? 1 : 2; }
+
+// Blocks per loop step of a warp: the most (up to 4 for one token tile, 2 for two)
+// that divide the warp's blocks in a slot.
+int mt_ub(int nt8, int njp) {
+    const int top = nt8 == 1 ? 4 : 2;
+    for (int u = top; u > 1; u /= 2)
+        if (njp % u == 0) return u;
+    return 1;
+}
+
+// Slots per stage (K parts) and ring depth: among the plans whose slots give the
+// warps the most blocks per loop step, the one that keeps the most code bytes in
+// flight while the slowest warp works on one slot, (ring - 1) x slot; fewer parts on
+// a tie.
+struct MtGeo {
+    int parts, ring, ub;
+    uint32_t smem;
+};
+
+MtGeo mt_geo(int bits, int K, int Mt, bool zp) {
+    const int nt8 = mt_nt8(Mt), nj = K / 32 / kMtCW;
+    MtGeo best = {0, 0, 0, 0u};
+    uint64_t best_bytes = 0;
+    for (int parts = 1; parts <= 4; parts *= 2) {
+        if (nj % parts != 0) continue;
+        const int ub = mt_ub(nt8, nj / parts);
+        if (best.parts && ub < best.ub) continue;
+        for (int r = 2; r <= kMtMaxRing; ++r) {
+            const MtLayout L = mt_layout(r, bits, K, nt8, parts, zp);
+            if (L.total + 1024u > kMtSmem) break;
+            const uint64_t bytes = (uint64_t)(r - 1) * L.codes;
+            if (ub > best.ub || bytes > best_bytes) {
+                best_bytes = bytes;
+                best = {parts, r, ub, L.total + 1024u};
+            }
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+bool decode_mt_supported(int bits, int64_t Mt, int K, bool lora) {
+    if (lora || (bits != 4 && bits != 8) || Mt < 2 || Mt > 16) return false;
+    if (K <= 0 || K % 512 != 0 || K > 7680) return false;  // TMA boxes of scales / zero points, swizzled code rows
+    return mt_geo(bits, K, (int)Mt, true).parts > 0;        // with zero points: the larger plan
+}
+
+void decode_mt_geometry(int N, int K, int bits, int Mt, bool zp, int sms, int* ctas, int* parts, int* ring,
+                        size_t* smem) {
+    const MtGeo G = mt_geo(bits, K, Mt, zp);
+    *ctas = mt_ctas(N, sms);
+    *parts = G.parts;
+    *ring = G.ring;
+    *smem = G.smem;
+}
+
+cudaError_t decode_mt_prepare() {
+    cudaError_t e = tensor_map_prepare();
+    if (e == cudaSuccess) e = mt_set_smem<4, false>();
+    if (e == cudaSuccess) e = mt_set_smem<4, true>();
+    if (e == cudaSuccess) e = mt_set_smem<8, false>();
+    if (e == cudaSuccess) e = mt_set_smem<8, true>();
+    return e;
+}
+
+cudaError_t decode_mt_launch(const DecodeArgs& a_in, int sms, bool pdl, cudaStream_t st) {
+    DecodeArgs a = a_in;
+    const int bits = a.bits, K = a.K, nblk = K / 32;
+    const bool zp = a.seg[0].Z != nullptr;
+    if (!decode_mt_supported(bits, a.Mt, K, false)) return cudaErrorNotSupported;
+    const MtGeo G = mt_geo(bits, K, a.Mt, zp);
+    const int C = mt_ctas(a.NR, sms);
+    a.SR = kMtSR;
+    a.ring = G.ring;
+    a.kparts = G.parts;
+    const int nbp = nblk / G.parts;
+    const DecPitch P = dec_pitch(nbp);
+    const uint64_t rowbytes = (uint64_t)K * bits / 8;
+    MtMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int i = 0; i < a.nseg; ++i) {
+        cudaError_t e = encode_codes_sw128(&maps.c[i], a.seg[i].Wq, rowbytes, (uint64_t)a.seg[i].N, (uint32_t)kMtSR,
+                                           (uint32_t)(rowbytes / 128 / G.parts));
+        if (e == cudaSuccess)
+            e = encode_2d(&maps.s[i], a.seg[i].S, 2, (uint64_t)nblk, (uint64_t)a.seg[i].N, (uint64_t)nblk * 2,
+                          P.spitch / 2u, (uint32_t)kMtSR, false);
+        if (e == cudaSuccess && zp)
+            e = encode_2d(&maps.z[i], a.seg[i].Z, 1, (uint64_t)nblk, (uint64_t)a.seg[i].N, (uint64_t)nblk, P.zpitch,
+                          (uint32_t)kMtSR, false);
+        if (e != cudaSuccess) return e;
+    }
+    const int nt8 = mt_nt8(a.Mt);
+    const size_t smem = G.smem;
+    if (bits == 4)
+        return zp ? mt_launch_bz<4, true>(nt8, G.ub, maps, a, C, smem, pdl, st)
+                  : mt_launch_bz<4, false>(nt8, G.ub, maps, a, C, smem, pdl, st);
+    return zp ? mt_launch_bz<8, true>(nt8, G.ub, maps, a, C, smem, pdl, st)
+              : mt_launch_bz<8, false>(nt8, G.ub, maps, a, C, smem, pdl, st);
+}
+
+}  // namespace mnb

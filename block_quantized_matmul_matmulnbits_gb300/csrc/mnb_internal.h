@@ -22,6 +22,11 @@ cudaError_t tensor_map_prepare();
 // addresses and kernel attributes are valid only in the context they were
 // obtained in.
 cudaError_t current_context_id(unsigned long long* id);
+// Byte matrix [rows, rowbytes] (rowbytes % 128 == 0, <= 32 KB) as boxes of `box_rows`
+// rows x `box_segs` 128-byte segments, 128-byte swizzled: [box_segs][box_rows][128]
+// in shared memory (coordinates: 0, first row, first segment).
+cudaError_t encode_codes_sw128(CUtensorMap* map, const void* base, uint64_t rowbytes, uint64_t rows,
+                               uint32_t box_rows, uint32_t box_segs);
 // Byte matrix [rows, rowbytes] (rowbytes % 256 == 0) seen as [rows][rowbytes/256][256]:
 // one box copies `box_rows` rows x `box_chunks` 256-byte pieces, rows `box_chunks*256`
 // bytes apart in shared memory.
@@ -93,12 +98,14 @@ struct DecodeArgs {
     int nseg;            // projections (>= 1)
     int NR;              // rows of the row space (sum of the projections' N)
     DecSeg seg[kMaxSeg];
-    const __half* X;     // [1, K]
+    const __half* X;     // [Mt, K]
+    int Mt;              // token rows (1 for the single-token kernel)
     const __half* A;     // [K, 32] (adapter only)
     const __half* B;     // [N, 32] (adapter only)
     __half* T;           // [1, 32]: T on return (adapter only)
     int K, bits;
     int SR, ring;        // rows per stage and stage slots (set by the launcher)
+    int kparts;          // few-token kernel: a stage's K range arrives in this many slots
     int x_wait;          // X may be written by the work queued before this kernel
     unsigned int* status;
     void* ex;            // the adapter's exchange area (set by the launcher)
@@ -113,6 +120,17 @@ cudaError_t decode_prepare();
 // timeout left one of them part way).
 cudaError_t decode_reset_exchange();
 cudaError_t decode_launch(const DecodeArgs& a, int rank, int sms, bool pdl, cudaStream_t st);
+
+// Decode kernel for 2 .. 16 token rows (decode_mt.cu): the same row space (up to
+// kMaxSeg projections), no adapter.  Whether a call runs on it: bits 4 or 8,
+// 2 <= Mt <= 16, K % 512 == 0 and K <= 7680, and x of the token rows plus two
+// stage slots (with zero points) fitting in one SM's shared memory.
+bool decode_mt_supported(int bits, int64_t Mt, int K, bool lora);
+// CTAs, slots per 16-row stage (K parts), ring slots and shared memory of a launch.
+void decode_mt_geometry(int N, int K, int bits, int Mt, bool zp, int sms, int* ctas, int* parts, int* ring,
+                        size_t* smem);
+cudaError_t decode_mt_prepare();
+cudaError_t decode_mt_launch(const DecodeArgs& a, int sms, bool pdl, cudaStream_t st);
 
 // T = fp16(X * A), X [Mt, K], A [K, 32].  Deterministic split-K over a cluster.
 cudaError_t lora_down_prepare();

@@ -93,4 +93,22 @@ cudaError_t encode_rows_3d(CUtensorMap* map, const void* base, uint64_t rowbytes
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Rows of packed codes as 3-D boxes for a 128-byte swizzle: dims (128 bytes of a row,
+// row, 128-byte segment), box (128, box_rows, box_segs).  In shared memory a box is
+// [segment][box_rows][128 B] with chunk c of row r at c ^ (r & 7).
+cudaError_t encode_codes_sw128(CUtensorMap* map, const void* base, uint64_t rowbytes, uint64_t rows,
+                               uint32_t box_rows, uint32_t box_segs) {
+    if (!g_encode) return cudaErrorNotSupported;
+    if (rowbytes % 128 != 0 || rowbytes / 128 > 256 || box_segs == 0 || box_segs > rowbytes / 128)
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)rows, (cuuint64_t)(rowbytes / 128)};
+    const cuuint64_t strides[2] = {(cuuint64_t)rowbytes, 128};
+    const cuuint32_t box[3] = {128, box_rows, box_segs};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace mnb

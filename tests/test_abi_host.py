@@ -129,10 +129,11 @@ def test_k_zero_is_a_fill():
 
 
 def test_gemv_plan_balances_rows_over_sms():
+    # the general multi-token decode kernel (here: two token rows with an FP16 adapter)
     for N, K, bits in ((4096, 4096, 4), (14336, 4096, 4), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4)):
         h = mnb.mnb_create(N, K, bits)
         try:
-            p = mnb.mnb_plan(h, 1, 2, 0, 152)
+            p = mnb.mnb_plan(h, 1, 2, 32, 152)
             R, C, G = p["rows_per_cta"], p["grid_x"], -(-N // 16)
             # whole 16-row groups dealt out evenly: the largest share is ceil(G / C) groups
             assert C <= G and R == 16 * -(-G // C)
@@ -142,7 +143,34 @@ def test_gemv_plan_balances_rows_over_sms():
             cost = lambda c: -(-c // 152) * -(-G // c)
             assert all(cost(C) <= cost(c) for c in range(1, min(G, 3 * 152) + 1))
             assert p["block_threads"] == 288 and p["k_splits"] % 64 == 0 and 64 <= p["k_splits"] <= 1024
-            assert p["tokens_per_cta"] == 8
+            assert p["tokens_per_cta"] == 8 and p["lora_kernel"] == 1
+        finally:
+            mnb.mnb_destroy(h)
+
+
+def test_few_token_plan_splits_rows_evenly():
+    # 2 .. 16 token rows without an adapter, K a multiple of 512 up to 7680: the kernel
+    # with the token rows as the MMA's N, rows split evenly over one CTA per SM, one
+    # launch for up to 16 tokens; other shapes keep the general multi-token kernel
+    # (N, K, bits, most token rows on the kernel): x of 16 token rows and K = 4608
+    # leave no room for two stage slots, nor x of 8 token rows and INT8 rows of 7 KB;
+    # K % 512 != 0 or K > 7680 are outside the kernel's copies
+    for N, K, bits, mt_max in ((4096, 4096, 4, 16), (14336, 4096, 4, 16), (14336, 4096, 8, 16), (49152, 576, 8, 0),
+                               (4096, 4608, 4, 8), (4096, 7168, 4, 8), (4096, 6144, 8, 8), (4096, 7168, 8, 0),
+                               (1000, 96, 4, 0), (4096, 7680, 4, 0), (4096, 8192, 4, 0)):
+        h = mnb.mnb_create(N, K, bits)
+        try:
+            for M in (2, 5, 8, 9, 16):
+                p = mnb.mnb_plan(h, 1, M, 0, 152)
+                assert p["route"] == mnb.ROUTE_GEMV and p["lora_kernel"] == 0
+                if M <= mt_max:
+                    C = min(152, -(-N // 16))
+                    assert p["grid_x"] == C and p["grid_y"] == 1 and p["rows_per_cta"] == -(-N // C)
+                    assert p["tokens_per_cta"] == (8 if M <= 8 else 16) and p["k_splits"] == 16
+                else:
+                    assert p["k_splits"] % 64 == 0  # general kernel: K bytes per stage
+            # more than 16 token rows in one matrix: the prefill route (auto mode)
+            assert mnb.mnb_plan(h, 1, 17, 0, 152)["route"] == mnb.ROUTE_GEMM
         finally:
             mnb.mnb_destroy(h)
 

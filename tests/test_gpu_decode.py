@@ -168,6 +168,53 @@ def test_mlp_up_decode_sampled_rows(env, M, rank):
     assert_within_tolerance(got, Y64, bound, f"mlp_up M={M} rank={rank}")
 
 
+@pytest.mark.parametrize("M,N,K,bits,zp", [
+    (2, 1000, 512, 4, (0, 15)),       # one slot per stage, a ragged last stage
+    (6, 2077, 2048, 8, (120, 136)),   # INT8
+    (8, 3000, 4096, 4, None),         # K halves per slot, one token tile
+    (9, 2100, 4096, 4, (0, 15)),      # two token tiles (the second one token), K quarters per slot
+    (16, 1500, 4096, 8, (0, 255)),    # INT8, 16 token rows
+    (13, 700, 3072, 4, None),
+    (3, 37, 6144, 4, (0, 15)),        # three CTAs, stages of 12 and 13 rows
+])
+def test_few_token_kernel_matches_oracle(env, M, N, K, bits, zp):
+    """2 .. 16 token rows without an adapter run on the kernel with the token rows
+    as the MMA's N (its plan: 16-row stages, 8 or 16 token columns); every output
+    against the oracle."""
+    torch, mnb = env
+    h = mnb.mnb_create(N, K, bits)
+    try:
+        p = mnb.mnb_plan(h, 1, M, 0, torch.cuda.get_device_properties(0).multi_processor_count)
+    finally:
+        mnb.mnb_destroy(h)
+    assert p["k_splits"] == 16 and p["tokens_per_cta"] == (8 if M <= 8 else 16)
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=3400 + M, zp_range=zp)
+    Y, _, route = run_gpu(mnb, torch, inp)
+    assert route == mnb.ROUTE_GEMV
+    Y64, bound = oracle_ref(inp)
+    assert_within_tolerance(bits_of(Y), Y64, bound, f"few tokens M={M} N={N} K={K} bits={bits}")
+
+
+def test_few_token_exact_arithmetic_bitwise(env):
+    """X in {-1,0,1} (<= 8 nonzeros per row), power-of-two scales, 12 token rows, no
+    adapter: every product, block sum and partial sum of the few-token kernel is
+    exact, so it must match the oracle bit for bit."""
+    torch, mnb = env
+    rng = np.random.default_rng(405)
+    M, K, N = 12, 2048, 300
+    x = np.zeros((1, M, K))
+    for m in range(M):
+        idx = rng.choice(K, 8, replace=False)
+        x[0, m, idx] = rng.choice([-1.0, 1.0], 8)
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=405, zp_range=(0, 15))
+    inp.X = x.astype(np.float16).view(np.uint16)
+    inp.scales = np.ldexp(1.0, rng.integers(-8, -4, size=(N, K // 32))).astype(np.float16).view(np.uint16)
+    Y, _, route = run_gpu(mnb, torch, inp)
+    assert route == mnb.ROUTE_GEMV
+    Y16, _, _ = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, None, None, N, K, 4)
+    assert np.array_equal(bits_of(Y).reshape(M, N), Y16)
+
+
 # ------------------------------------------------------------------ edges
 
 @pytest.mark.parametrize("M,N,K,bits,zp", [(3, 1000, 96, 4, (0, 15)), (5, 17, 160, 8, (0, 255)), (1, 1, 32, 4, None),
