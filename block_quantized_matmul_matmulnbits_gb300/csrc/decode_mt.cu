@@ -56,7 +56,7 @@ constexpr int kMtMaxRing = 8;
 constexpr uint32_t kMtSmem = 227u * 1024u;        // shared memory of one CTA per SM
 constexpr uint32_t kXF = kMtCW * 512u;            // x fragments of one block and token tile, all warps
 constexpr uint32_t kQF = kMtCW * 64u;             // MMA starting values of one block and token tile, all warps
-constexpr int kTS = 20;                           // partials: floats between token rows
+constexpr int kPS = 20;                           // partials: floats between two outputs (16 warps + 4)
 
 // Shared-memory loads at a 32-bit address plus a constant offset (the assembler folds
 // the addition into the load); volatile: they stay after the barrier waits before them.
@@ -117,13 +117,13 @@ __device__ __forceinline__ uint2 ldg64_nc(const void* p) {
 // sc + s * 16 spitch, zero points at zp + s * 16 zpitch.  After the ring: the
 // threads' x fragments [block][token tile][warp][lane][16 B], the MMAs' starting
 // values [block][token tile][warp][t][4] FP32, the warps' partials of a stage
-// [warp][8 nt8 tokens (kTS floats apart)][16 rows] FP32, and the barriers full[ring],
+// [output (token row x 16 + row)][warp] FP32 (kPS floats an output), the barriers full[ring],
 // empty[ring], "x staged", "partials written" and "partials added", and a flag: every
 // consumer's waits ended in time.
 struct MtLayout {
     uint32_t codes, sc, zp;
     uint32_t spitch, zpitch;
-    uint32_t xs, cq, red, rs, bars, total;  // rs: floats between two warps' partials
+    uint32_t xs, cq, red, bars, total;
 };
 
 __host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8, int parts, bool zp) {
@@ -139,8 +139,7 @@ __host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8
     L.xs = al128(L.zp + (zp ? (uint32_t)ring * (uint32_t)kMtSR * P.zpitch : 0u));
     L.cq = L.xs + (uint32_t)nblk * (uint32_t)nt8 * 512u;
     L.red = al128(L.cq + (uint32_t)nblk * (uint32_t)nt8 * 64u);
-    L.rs = (uint32_t)(8 * nt8 * kTS);
-    L.bars = al128(L.red + (uint32_t)kMtCW * L.rs * 4u);
+    L.bars = al128(L.red + 16u * 8u * (uint32_t)nt8 * (uint32_t)kPS * 4u);
     L.total = L.bars + (2u * (uint32_t)ring + 4u) * 8u;  // + the "waits ended in time" flag
     return L;
 }
@@ -300,12 +299,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             float y[NT8 * 4];
 #pragma unroll
             for (int i = 0; i < NT8 * 4; ++i) {
-                const int o = lane + 32 * i;
-                const float* pr = red + (o >> 4) * kTS + (o & 15);
-                float acc = 0.f;
-#pragma unroll
-                for (int w = 0; w < kMtCW; ++w) acc += pr[w * (int)L.rs];
-                y[i] = acc;
+                const float4* pr = reinterpret_cast<const float4*>(red + (lane + 32 * i) * kPS);
+                const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];
+                y[i] = ((((((((((((((p0.x + p0.y) + p0.z) + p0.w) + p1.x) + p1.y) + p1.z) + p1.w) + p2.x) + p2.y) +
+                              p2.z) + p2.w) + p3.x) + p3.y) + p3.z) + p3.w;
             }
             __syncwarp();
             mbar_arrive_if(lane == 0, pfree);  // every lane's reads are done
@@ -408,7 +405,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     const uint32_t s8 = 8u * L.spitch, z8 = 8u * L.zpitch;
     uint32_t cS = c_first, sS = s_first, zS = z_first;
     // this thread's partials: rows g, g + 8 x tokens 8 jt + 2t, + 1
-    float* pw = red + warp * (int)L.rs + 2 * t * kTS + g;
+    float* pw = red + (32 * t + g) * kPS + warp;
     uint32_t fph = 0u;  // phase of "partials added"
     MtRows it;
     it.init(a, r0, r1);
@@ -526,11 +523,11 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         if (!ok) *in_time = 0;
 #pragma unroll
         for (int jt = 0; jt < NT8; ++jt) {
-            float* pt = pw + 8 * jt * kTS;
+            float* pt = pw + 128 * jt * kPS;
             pt[0] = v[jt][0];
-            pt[kTS] = v[jt][1];
-            pt[8] = v[jt][2];
-            pt[kTS + 8] = v[jt][3];
+            pt[16 * kPS] = v[jt][1];
+            pt[8 * kPS] = v[jt][2];
+            pt[24 * kPS] = v[jt][3];
         }
         __threadfence_block();
         __syncwarp();
