@@ -52,7 +52,7 @@ using namespace dec;
 constexpr int kMtCW = 16;                         // consumer warps
 constexpr int kMtThreads = (kMtCW + 2) * 32;      // + the producer and the reducer warps
 constexpr int kMtSR = 16;                         // rows per stage: one box
-constexpr int kMtMaxRing = 8;
+constexpr int kMtMaxRing = 12;
 constexpr uint32_t kMtSmem = 227u * 1024u;        // shared memory of one CTA per SM
 constexpr uint32_t kXF = kMtCW * 512u;            // x fragments of one block and token tile, all warps
 constexpr uint32_t kQF = kMtCW * 64u;             // MMA starting values of one block and token tile, all warps
@@ -99,6 +99,12 @@ __device__ __forceinline__ void mbar_arrive_if(bool p, uint32_t bar) {
         "r"(bar)
         : "memory");
 }
+// A register copy the compiler keeps where it stands.
+__device__ __forceinline__ float fmov_here(float x) {
+    float y;
+    asm volatile("mov.b32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ uint4 ldg128_nc(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -114,19 +120,21 @@ __device__ __forceinline__ uint2 ldg64_nc(const void* p) {
 
 // Shared memory plan, identical on host and device.  Slot s holds a K range of one
 // 16-row stage: codes at s * codes (one box [segment][16 rows][128 B]), scales at
-// sc + s * 16 spitch, zero points at zp + s * 16 zpitch.  After the ring: the
-// threads' x fragments [block][token tile][warp][lane][16 B], the MMAs' starting
-// values [block][token tile][warp][t][4] FP32, the warps' partials of a stage
-// [output (token row x 16 + row)][warp] FP32 (kPS floats an output), the barriers full[ring],
-// empty[ring], "x staged", "partials written" and "partials added", and a flag: every
-// consumer's waits ended in time.
+// sc + s * 16 spitch, zero points at zp + s * 16 zpitch.  After the ring (unless the
+// threads keep them in registers): the threads' x fragments [block][token tile]
+// [warp][lane][16 B] and the MMAs' starting values [block][token tile][warp][t][4]
+// FP32; then the warps' partials of a stage, in one buffer or (with x in registers,
+// where shared memory is plentiful) two, stage st in buffer st % buffers: [output
+// (token row x 16 + row)][warp] FP32 (kPS floats an output), the barriers
+// full[ring], empty[ring], "x staged", "partials written"[2] and "partials added"[2],
+// and a flag: every consumer's waits ended in time.
 struct MtLayout {
     uint32_t codes, sc, zp;
     uint32_t spitch, zpitch;
     uint32_t xs, cq, red, bars, total;
 };
 
-__host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8, int parts, bool zp) {
+__host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8, int parts, bool zp, bool xreg) {
     const int nblk = K / 32, nbp = nblk / parts;
     const uint32_t rowbytes = (uint32_t)K * (uint32_t)bits / 8u / (uint32_t)parts;  // of a slot's K range
     const DecPitch P = dec_pitch(nbp);
@@ -137,10 +145,10 @@ __host__ __device__ inline MtLayout mt_layout(int ring, int bits, int K, int nt8
     L.sc = (uint32_t)ring * L.codes;
     L.zp = L.sc + (uint32_t)ring * (uint32_t)kMtSR * P.spitch;
     L.xs = al128(L.zp + (zp ? (uint32_t)ring * (uint32_t)kMtSR * P.zpitch : 0u));
-    L.cq = L.xs + (uint32_t)nblk * (uint32_t)nt8 * 512u;
-    L.red = al128(L.cq + (uint32_t)nblk * (uint32_t)nt8 * 64u);
-    L.bars = al128(L.red + 16u * 8u * (uint32_t)nt8 * (uint32_t)kPS * 4u);
-    L.total = L.bars + (2u * (uint32_t)ring + 4u) * 8u;  // + the "waits ended in time" flag
+    L.cq = L.xs + (xreg ? 0u : (uint32_t)nblk * (uint32_t)nt8 * 512u);
+    L.red = al128(L.cq + (xreg ? 0u : (uint32_t)nblk * (uint32_t)nt8 * 64u));
+    L.bars = al128(L.red + (xreg ? 2u : 1u) * 16u * 8u * (uint32_t)nt8 * (uint32_t)kPS * 4u);
+    L.total = L.bars + (2u * (uint32_t)ring + 6u) * 8u;  // + the "waits ended in time" flag
     return L;
 }
 
@@ -187,6 +195,175 @@ struct MtMaps {
     CUtensorMap z[kMaxSeg];
 };
 
+// A CTA's shared-memory plan and barriers, as every role sees them.
+struct MtCtx {
+    MtLayout L;
+    uint32_t sb;  // shared base, 1024-aligned
+    unsigned char* sm;
+    int ring, H, nblk, r0, r1, nt8, nbuf;  // nbuf: buffers of partials
+    unsigned int* status;
+    __device__ __forceinline__ uint32_t full(int s) const { return sb + L.bars + 8u * (uint32_t)s; }
+    __device__ __forceinline__ uint32_t empty(int s) const { return sb + L.bars + 8u * (uint32_t)(ring + s); }
+    __device__ __forceinline__ uint32_t xready() const { return sb + L.bars + 16u * (uint32_t)ring; }
+    // buffer b of the partials: written by all consumer warps, then added
+    __device__ __forceinline__ uint32_t pfull(int b) const { return xready() + 8u + 8u * (uint32_t)b; }
+    __device__ __forceinline__ uint32_t pfree(int b) const { return xready() + 24u + 8u * (uint32_t)b; }
+    __device__ __forceinline__ float* red(int b) const {
+        return reinterpret_cast<float*>(sm + L.red) + b * (128 * nt8 * kPS);
+    }
+    __device__ __forceinline__ volatile int* in_time() const {
+        return reinterpret_cast<volatile int*>(sm + L.bars + 16u * (uint32_t)ring + 40u);
+    }
+};
+
+// The plan and the barriers (set up by thread 0); then the whole CTA meets and the
+// dependent launch is released.
+template <int BITS, bool HAS_ZP>
+__device__ __forceinline__ MtCtx mt_setup(const DecodeArgs& a, int nt8, bool xreg, unsigned char* sm_raw) {
+    MtCtx c;
+    c.ring = a.ring;
+    c.H = a.kparts;
+    c.nblk = a.K >> 5;
+    c.nt8 = nt8;
+    c.nbuf = xreg ? 2 : 1;
+    c.L = mt_layout(c.ring, BITS, a.K, nt8, c.H, HAS_ZP, xreg);
+    c.sb = (smem_u32(sm_raw) + 1023u) & ~1023u;  // swizzled boxes want 1024-byte alignment
+    c.sm = sm_raw + (c.sb - smem_u32(sm_raw));
+    const int C = gridDim.x;
+    c.r0 = (int)((long long)blockIdx.x * a.NR / C);
+    c.r1 = (int)((long long)(blockIdx.x + 1) * a.NR / C);
+    c.status = a.status;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < c.ring; ++s) {
+            mbar_init(c.full(s), 1);
+            mbar_init(c.empty(s), kMtCW);
+        }
+        mbar_init(c.xready(), kMtCW);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(c.pfull(b), kMtCW);
+            mbar_init(c.pfree(b), 1);
+        }
+        *c.in_time() = 1;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    return c;
+}
+
+// The producer (one thread): the CTA's stages as slots of K ranges through the ring.
+// Whole 16-row boxes land, rows past N reading as zero; the MMA rows of a shorter
+// stage past its end read the next rows, and are not stored.
+template <int BITS, bool HAS_ZP>
+__device__ __forceinline__ void mt_produce(const MtMaps& maps, const DecodeArgs& a, const MtCtx& c) {
+    const int K = a.K, H = c.H, ring = c.ring, nblk = c.nblk, r0 = c.r0, r1 = c.r1;
+    const MtLayout& L = c.L;
+    const uint32_t rowbytes = (uint32_t)K * BITS / 8u;
+    const int segp = (int)(rowbytes / 128u) / H, nbp = nblk / H;  // per slot
+    const uint32_t bytes = L.codes + (uint32_t)kMtSR * L.spitch + (HAS_ZP ? (uint32_t)kMtSR * L.zpitch : 0u);
+    bool ok = true;
+    int q = 0;  // slots issued
+    MtRows it;
+    it.init(a, r0, r1);
+    for (; ok && it.pos < r1; it.next(a)) {
+        for (int h = 0; h < H; ++h, ++q) {
+            const int s = q % ring;
+            const uint32_t par = (uint32_t)(q / ring) & 1u;
+            if (q == ring) {
+                // The ring is full: once x is staged, the rest of the share into L2 at
+                // once, so that the refills come from L2 while HBM streams the
+                // remainder at full rate.
+                mbar_wait(c.xready(), 0u, c.status);
+                for (int sg = 0; sg < a.nseg; ++sg) {
+                    const DecSeg& pg = a.seg[sg];
+                    const int lo = max(r0, pg.row0), hi = min(r1, pg.row0 + pg.N);
+                    if (lo >= hi) continue;
+                    const size_t ra = (size_t)(lo - pg.row0), n = (size_t)(hi - lo);
+                    for (size_t off = 0; off < n * rowbytes; off += (1u << 20))
+                        prefetch_l2_bulk(pg.Wq + ra * rowbytes + off,
+                                         (uint32_t)min((size_t)(1u << 20), n * rowbytes - off));
+                    prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(pg.S) + ra * nblk * 2, (uint32_t)(n * nblk * 2));
+                    if (HAS_ZP) prefetch_l2_bulk(pg.Z + ra * nblk, (uint32_t)(n * nblk));
+                }
+            }
+            if (q >= ring && !(ok = mbar_wait(c.empty(s), par ^ 1u, c.status))) break;
+            mbar_arrive_tx(c.full(s), bytes);
+            tma_load_3d(c.sb + (uint32_t)s * L.codes, &maps.c[it.seg], 0, it.ra, h * segp, c.full(s));
+            tma_load_2d(c.sb + L.sc + (uint32_t)s * kMtSR * L.spitch, &maps.s[it.seg], h * nbp, it.ra, c.full(s));
+            if (HAS_ZP)
+                tma_load_2d(c.sb + L.zp + (uint32_t)s * kMtSR * L.zpitch, &maps.z[it.seg], h * nbp, it.ra, c.full(s));
+        }
+    }
+    // no copy may still be in flight when the CTA exits (a consumer may have given up)
+    for (int i = q > ring ? q - ring : 0; i < q; ++i) mbar_wait(c.full(i % ring), (uint32_t)(i / ring) & 1u, c.status, false);
+}
+
+// The reducer (one warp): output o = lane + 32 i of a stage is token row o >> 4, row
+// o & 15, the sum of the 16 warps' partials in warp order, one rounding.
+template <int NT8>
+__device__ __forceinline__ void mt_reduce(const DecodeArgs& a, const MtCtx& c, int lane) {
+    if (c.r0 >= c.r1) return;
+    bool ok = true;
+    MtRows it;
+    it.init(a, c.r0, c.r1);
+    __half* Yp = a.seg[it.seg].Y;
+    const __half* bp = a.seg[it.seg].bias;
+    int Np = a.seg[it.seg].N;
+    bool moved = false;
+    for (int st = 0; it.pos < c.r1; moved = it.next(a), ++st) {
+        if (moved) {
+            Yp = a.seg[it.seg].Y;
+            bp = a.seg[it.seg].bias;
+            Np = a.seg[it.seg].N;
+        }
+        const int b = st % c.nbuf, use = st / c.nbuf;  // stage st's buffer, in its use-th use
+        if (ok) ok = mbar_wait(c.pfull(b), (uint32_t)use & 1u, c.status) && *c.in_time();
+        const float* red = c.red(b);
+        float y[NT8 * 4];
+#pragma unroll
+        for (int i = 0; i < NT8 * 4; ++i) {
+            const float4* pr = reinterpret_cast<const float4*>(red + (lane + 32 * i) * kPS);
+            const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];
+            y[i] = ((((((((((((((p0.x + p0.y) + p0.z) + p0.w) + p1.x) + p1.y) + p1.z) + p1.w) + p2.x) + p2.y) +
+                          p2.z) + p2.w) + p3.x) + p3.y) + p3.z) + p3.w;
+        }
+        __syncwarp();
+        mbar_arrive_if(lane == 0, c.pfree(b));  // every lane's reads are done
+#pragma unroll
+        for (int i = 0; i < NT8 * 4; ++i) {
+            const int o = lane + 32 * i, tok = o >> 4, m = o & 15;
+            if (ok && m < it.rs && tok < a.Mt) {
+                float v = y[i] * (1.0f / kUnit);
+                if (bp) v += __half2float(bp[it.ra + m]);
+                Yp[(size_t)tok * Np + it.ra + m] = __float2half_rn(v);
+            }
+        }
+    }
+}
+
+// A consumer warp hands its partials of stage st (thread (g, t): rows g, g + 8 x
+// tokens 8 jt + 2t, + 1; offset pw in a buffer) to the reducer, once the reducer has
+// added the stage that used the same buffer before.
+template <int NT8>
+__device__ __forceinline__ void mt_hand_over(const MtCtx& c, int pw, const float (&v)[NT8][4], int st, bool& ok,
+                                             int lane) {
+    const int b = st % c.nbuf, use = st / c.nbuf;
+    if (use > 0 && ok) ok = mbar_wait(c.pfree(b), (uint32_t)(use - 1) & 1u, c.status);
+    if (!ok) *c.in_time() = 0;
+    float* pt0 = c.red(b) + pw;
+#pragma unroll
+    for (int jt = 0; jt < NT8; ++jt) {
+        float* pt = pt0 + 128 * jt * kPS;
+        pt[0] = v[jt][0];
+        pt[16 * kPS] = v[jt][1];
+        pt[8 * kPS] = v[jt][2];
+        pt[24 * kPS] = v[jt][3];
+    }
+    __threadfence_block();
+    __syncwarp();
+    mbar_arrive_if(lane == 0, c.pfull(b));
+}
+
 template <int BITS, bool HAS_ZP, int NT8, int UB>
 __global__ void __launch_bounds__(kMtThreads, 1)
     decode_mt_kernel(const __grid_constant__ MtMaps maps, const __grid_constant__ DecodeArgs a) {
@@ -194,135 +371,26 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
     constexpr int kProducer = kMtCW, kReducer = kMtCW + 1;
     extern __shared__ unsigned char sm_raw[];
-
-    const int K = a.K, NR = a.NR, Mt = a.Mt, H = a.kparts;
-    const int nblk = K >> 5, nj = nblk / kMtCW, njp = nj / H;  // blocks of a consumer warp: per stage, per slot
-    const int ring = a.ring;
-    const MtLayout L = mt_layout(ring, BITS, K, NT8, H, HAS_ZP);
-    const uint32_t sb = (smem_u32(sm_raw) + 1023u) & ~1023u;  // swizzled boxes want 1024-byte alignment
-    unsigned char* sm = sm_raw + (sb - smem_u32(sm_raw));
+    const MtCtx c = mt_setup<BITS, HAS_ZP>(a, NT8, false, sm_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int C = gridDim.x;
-    const int r0 = (int)((long long)blockIdx.x * NR / C), r1 = (int)((long long)(blockIdx.x + 1) * NR / C);
-    unsigned int* status = a.status;
-
-    auto full = [&](int s) { return sb + L.bars + 8u * (uint32_t)s; };
-    auto empty = [&](int s) { return sb + L.bars + 8u * (uint32_t)(ring + s); };
-    const uint32_t xready = sb + L.bars + 16u * (uint32_t)ring;
-    const uint32_t pfull = xready + 8u, pfree = xready + 16u;  // the partials: written by all warps, added
-    float* red = reinterpret_cast<float*>(sm + L.red);
-    volatile int* in_time = reinterpret_cast<volatile int*>(sm + L.bars + 16u * (uint32_t)ring + 24u);
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < ring; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), kMtCW);
-        }
-        mbar_init(xready, kMtCW);
-        mbar_init(pfull, kMtCW);
-        mbar_init(pfree, 1);
-        *in_time = 1;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    pdl_launch_dependents();
-
     if (warp == kProducer) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint32_t rowbytes = (uint32_t)K * BITS / 8u;
-            const int segp = (int)(rowbytes / 128u) / H, nbp = nblk / H;  // per slot
-            const uint32_t bytes = L.codes + (uint32_t)kMtSR * L.spitch + (HAS_ZP ? (uint32_t)kMtSR * L.zpitch : 0u);
-            bool ok = true;
-            int q = 0;  // slots issued
-            MtRows it;
-            it.init(a, r0, r1);
-            // Whole 16-row boxes land, rows past N reading as zero; the MMA rows of a
-            // shorter stage past its end read the next rows, and are not stored.
-            for (; ok && it.pos < r1; it.next(a)) {
-                for (int h = 0; h < H; ++h, ++q) {
-                    const int s = q % ring;
-                    const uint32_t par = (uint32_t)(q / ring) & 1u;
-                    if (q == ring) {
-                        // The ring is full: once x is staged, the rest of the share into
-                        // L2 at once, so that the refills come from L2 while HBM streams
-                        // the remainder at full rate.
-                        mbar_wait(xready, 0u, status);
-                        for (int sg = 0; sg < a.nseg; ++sg) {
-                            const DecSeg& pg = a.seg[sg];
-                            const int lo = max(r0, pg.row0), hi = min(r1, pg.row0 + pg.N);
-                            if (lo >= hi) continue;
-                            const size_t ra = (size_t)(lo - pg.row0), n = (size_t)(hi - lo);
-                            for (size_t off = 0; off < n * rowbytes; off += (1u << 20))
-                                prefetch_l2_bulk(pg.Wq + ra * rowbytes + off,
-                                                 (uint32_t)min((size_t)(1u << 20), n * rowbytes - off));
-                            prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(pg.S) + ra * nblk * 2,
-                                             (uint32_t)(n * nblk * 2));
-                            if (HAS_ZP) prefetch_l2_bulk(pg.Z + ra * nblk, (uint32_t)(n * nblk));
-                        }
-                    }
-                    if (q >= ring && !(ok = mbar_wait(empty(s), par ^ 1u, status))) break;
-                    mbar_arrive_tx(full(s), bytes);
-                    tma_load_3d(sb + (uint32_t)s * L.codes, &maps.c[it.seg], 0, it.ra, h * segp, full(s));
-                    tma_load_2d(sb + L.sc + (uint32_t)s * kMtSR * L.spitch, &maps.s[it.seg], h * nbp, it.ra, full(s));
-                    if (HAS_ZP)
-                        tma_load_2d(sb + L.zp + (uint32_t)s * kMtSR * L.zpitch, &maps.z[it.seg], h * nbp, it.ra,
-                                    full(s));
-                }
-            }
-            // no copy may still be in flight when the CTA exits (a consumer may have given up)
-            for (int i = q > ring ? q - ring : 0; i < q; ++i)
-                mbar_wait(full(i % ring), (uint32_t)(i / ring) & 1u, status, false);
-        }
+        if (lane == 0) mt_produce<BITS, HAS_ZP>(maps, a, c);
         return;
     }
-
     if (warp == kReducer) {
-        // ------------------------------------------------------------ reducer
-        // Output o = lane + 32 i of a stage is token row o >> 4, row o & 15: the sum of
-        // the 16 warps' partials in warp order, one rounding.
-        if (r0 >= r1) return;
-        bool ok = true;
-        MtRows it;
-        it.init(a, r0, r1);
-        __half* Yp = a.seg[it.seg].Y;
-        const __half* bp = a.seg[it.seg].bias;
-        int Np = a.seg[it.seg].N;
-        uint32_t ph = 0u;
-        for (bool moved = false; it.pos < r1; moved = it.next(a), ph ^= 1u) {
-            if (moved) {
-                Yp = a.seg[it.seg].Y;
-                bp = a.seg[it.seg].bias;
-                Np = a.seg[it.seg].N;
-            }
-            if (ok) ok = mbar_wait(pfull, ph, status) && *in_time;
-            float y[NT8 * 4];
-#pragma unroll
-            for (int i = 0; i < NT8 * 4; ++i) {
-                const float4* pr = reinterpret_cast<const float4*>(red + (lane + 32 * i) * kPS);
-                const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];
-                y[i] = ((((((((((((((p0.x + p0.y) + p0.z) + p0.w) + p1.x) + p1.y) + p1.z) + p1.w) + p2.x) + p2.y) +
-                              p2.z) + p2.w) + p3.x) + p3.y) + p3.z) + p3.w;
-            }
-            __syncwarp();
-            mbar_arrive_if(lane == 0, pfree);  // every lane's reads are done
-#pragma unroll
-            for (int i = 0; i < NT8 * 4; ++i) {
-                const int o = lane + 32 * i, tok = o >> 4, m = o & 15;
-                if (ok && m < it.rs && tok < Mt) {
-                    float v = y[i] * (1.0f / kUnit);
-                    if (bp) v += __half2float(bp[it.ra + m]);
-                    Yp[(size_t)tok * Np + it.ra + m] = __float2half_rn(v);
-                }
-            }
-        }
+        mt_reduce<NT8>(a, c, lane);
         return;
     }
+    const int K = a.K, Mt = a.Mt, H = c.H, ring = c.ring, r0 = c.r0, r1 = c.r1;
+    const int nj = c.nblk / kMtCW, njp = nj / H;  // blocks of a warp: per stage, per slot
+    const MtLayout& L = c.L;
+    const uint32_t sb = c.sb;
+    unsigned int* status = c.status;
 
     // ---------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
     if (r0 >= r1) {
-        mbar_arrive_if(lane == 0, xready);
+        mbar_arrive_if(lane == 0, c.xready());
         return;
     }
     bool ok = true;
@@ -382,7 +450,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
             }
         }
         __syncwarp();
-        mbar_arrive_if(lane == 0, xready);
+        mbar_arrive_if(lane == 0, c.xready());
     }
 
     // ---- the stages
@@ -405,11 +473,10 @@ __global__ void __launch_bounds__(kMtThreads, 1)
     const uint32_t s8 = 8u * L.spitch, z8 = 8u * L.zpitch;
     uint32_t cS = c_first, sS = s_first, zS = z_first;
     // this thread's partials: rows g, g + 8 x tokens 8 jt + 2t, + 1
-    float* pw = red + (32 * t + g) * kPS + warp;
-    uint32_t fph = 0u;  // phase of "partials added"
+    const int pw = (32 * t + g) * kPS + warp;  // this thread's partials in a buffer
     MtRows it;
     it.init(a, r0, r1);
-    for (bool first = true; it.pos < r1; it.next(a), first = false) {
+    for (int st = 0; it.pos < r1; it.next(a), ++st) {
         float v[NT8][4];
 #pragma unroll
         for (int jt = 0; jt < NT8; ++jt) v[jt][0] = v[jt][1] = v[jt][2] = v[jt][3] = 0.f;
@@ -417,7 +484,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
         for (int h = 0; h < H; ++h) {
             // after a timeout the slot's stale bytes are read all the same (in bounds)
             // and the reducer stores nothing
-            if (ok) ok = mbar_wait(full(s), par, status);
+            if (ok) ok = mbar_wait(c.full(s), par, status);
             uint32_t cA = cS, sA = sS, zA = zS;
 #pragma unroll 1
             for (int j = 0; j < njp; j += UB) {
@@ -502,7 +569,7 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 qo += UB * NT8 * kQF;
             }
             __syncwarp();
-            mbar_arrive_if(lane == 0, empty(s));  // this warp's reads of the slot are done
+            mbar_arrive_if(lane == 0, c.empty(s));  // this warp's reads of the slot are done
             if (++s == ring) {
                 s = 0;
                 par ^= 1u;
@@ -515,23 +582,218 @@ __global__ void __launch_bounds__(kMtThreads, 1)
                 zS += (uint32_t)kMtSR * L.zpitch;
             }
         }
-        // hand this warp's partials to the reducer, once it has added the previous stage's
-        if (!first) {
-            if (ok) ok = mbar_wait(pfree, fph, status);
-            fph ^= 1u;
-        }
-        if (!ok) *in_time = 0;
+        mt_hand_over<NT8>(c, pw, v, st, ok, lane);
+    }
+}
+
+// The same consumers for one token tile at K = 4096 with x kept in registers: each
+// thread holds the B fragments of its 8 blocks and their MMA starting values for
+// the whole launch, so a block costs two code loads and half a scale load from
+// shared memory.  Warp w takes the block pairs (2w, 2w + 1) + 32 k, k = 0 .. 3: one
+// 4-byte load reads the scales of a pair, one 2-byte load its zero points.  H slots
+// a stage (K halves or the whole K).
+template <int BITS, bool HAS_ZP, int H>
+__global__ void __launch_bounds__(kMtThreads, 1)
+    decode_mt_xr_kernel(const __grid_constant__ MtMaps maps, const __grid_constant__ DecodeArgs a) {
+    using U = Unpack<BITS>;
+    constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
+    constexpr int kProducer = kMtCW, kReducer = kMtCW + 1;
+    constexpr int NJ = 8, PPS = NJ / 2 / H, GP = BITS == 4 ? 2 : 1;  // blocks of a warp per stage, pairs per slot, pairs per step
+    constexpr uint32_t kPair = (BITS == 4 ? 4u : 8u) * 2048u;  // codes: 32 blocks further, in a slot's box
+    extern __shared__ unsigned char sm_raw[];
+    const MtCtx c = mt_setup<BITS, HAS_ZP>(a, 1, true, sm_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp == kProducer) {
+        if (lane == 0) mt_produce<BITS, HAS_ZP>(maps, a, c);
+        return;
+    }
+    if (warp == kReducer) {
+        mt_reduce<1>(a, c, lane);
+        return;
+    }
+    const int K = a.K, Mt = a.Mt, ring = c.ring, r0 = c.r0, r1 = c.r1;
+    const MtLayout& L = c.L;
+    const uint32_t sb = c.sb;
+    unsigned int* status = c.status;
+    const int g = lane >> 2, t = lane & 3;
+    if (r0 >= r1) {
+        mbar_arrive_if(lane == 0, c.xready());
+        return;
+    }
+    bool ok = true;
+
+    // ---- x of the token rows: fragment j is block 2 warp + (j & 1) + 32 (j >> 1), token row g
+    uint32_t xw[NJ][4];
+    float sx0[NJ], sx1[NJ];  // the MMA's starting values for tokens 2t, 2t + 1 (see the other kernel)
+    if (a.x_wait) pdl_wait();
+    {
+        constexpr uint32_t kOne = 0x00010001u, kHi = BITS == 4 ? 0x00100010u : kOne;
+        constexpr float kZs = HAS_ZP ? 1.f : -(float)kDefaultZp;
+        const __half2 k16 = __float2half2_rn(0.0625f);
+        const __half* xr = a.X + (size_t)g * K + (size_t)(2 * warp) * 32 + (BITS == 4 ? 8 * t : 4 * t);
+        uint4 v[NJ];
 #pragma unroll
-        for (int jt = 0; jt < NT8; ++jt) {
-            float* pt = pw + 128 * jt * kPS;
-            pt[0] = v[jt][0];
-            pt[16 * kPS] = v[jt][1];
-            pt[8 * kPS] = v[jt][2];
-            pt[24 * kPS] = v[jt][3];
+        for (int j = 0; j < NJ; ++j) {
+            const __half* p = xr + ((j & 1) + 32 * (j >> 1)) * 32;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (g < Mt) {
+                if constexpr (BITS == 4) {
+                    v[j] = ldg128_nc(p);  // word t: x[8t .. 8t + 7]
+                } else {
+                    const uint2 lo = ldg64_nc(p), hi = ldg64_nc(p + 16);  // words t, t + 4
+                    v[j] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                }
+            }
         }
-        __threadfence_block();
-        __syncwarp();
-        mbar_arrive_if(lane == 0, pfull);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            uint4 o = v[j];
+            if constexpr (BITS == 4) {  // (x0, x4) (x2, x6) (x1, x5)/16 (x3, x7)/16
+                const uint32_t h15 = prmt(o.x, o.z, 0x7632u), h37 = prmt(o.y, o.w, 0x7632u);
+                const __half2 s15 = __hmul2(*reinterpret_cast<const __half2*>(&h15), k16);
+                const __half2 s37 = __hmul2(*reinterpret_cast<const __half2*>(&h37), k16);
+                o = make_uint4(prmt(o.x, o.z, 0x5410u), prmt(o.y, o.w, 0x5410u),
+                               *reinterpret_cast<const uint32_t*>(&s15), *reinterpret_cast<const uint32_t*>(&s37));
+            }
+            xw[j][0] = o.x;
+            xw[j][1] = o.y;
+            xw[j][2] = o.z;
+            xw[j][3] = o.w;
+            float d[4];
+            mma_16816_z(d, kOne, kOne, kOne, kOne, o.x, o.y);
+            mma_16816(d, kHi, kHi, kHi, kHi, o.z, o.w);
+            sx0[j] = kZs * d[0];
+            sx1[j] = kZs * d[1];
+        }
+    }
+    mbar_arrive_if(lane == 0, c.xready());
+
+    // ---- the stages
+    // Codes of block b in the slot's box (segment [16 rows][128 B], row r + 8 1024 bytes
+    // after row r): INT4 16 bytes at segment b >> 3, chunk b & 7; INT8 32 bytes at
+    // segment b >> 2, chunks 2 (b & 3) and 2 (b & 3) + 1.  Block e of this warp's pair
+    // (b = 2 warp + e + 32 k): this thread's word at off[e][0] (and word t + 4 at
+    // off[e][1]) plus k kPair.
+    const uint32_t w2 = 2u * (uint32_t)warp, gg = (uint32_t)g;
+    uint32_t off[2][2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        if constexpr (BITS == 4) {
+            const uint32_t ch = (w2 & 7u) + (uint32_t)e;
+            off[e][0] = (w2 >> 3) * 2048u + gg * 128u + ((ch ^ gg) << 4) + 4u * (uint32_t)t;
+            off[e][1] = off[e][0];
+        } else {
+            const uint32_t ch = 2u * (w2 & 3u) + 2u * (uint32_t)e;
+            off[e][0] = (w2 >> 2) * 2048u + gg * 128u + ((ch ^ gg) << 4) + 4u * (uint32_t)t;
+            off[e][1] = (w2 >> 2) * 2048u + gg * 128u + (((ch + 1u) ^ gg) << 4) + 4u * (uint32_t)t;
+        }
+    }
+    const uint32_t s_off = gg * L.spitch + 2u * w2, z_off = gg * L.zpitch + w2;
+    const uint32_t s8 = 8u * L.spitch, z8 = 8u * L.zpitch;
+    // the slot cursor: index, phase, and the slot's codes, scales and zero points
+    int s = 0;
+    uint32_t par = 0u;
+    uint32_t cS = sb, sS = sb + L.sc + s_off, zS = sb + L.zp + z_off;
+    const int pw = (32 * t + g) * kPS + warp;  // this thread's partials in a buffer
+    MtRows it;
+    it.init(a, r0, r1);
+    for (int st = 0; it.pos < r1; it.next(a), ++st) {
+        float v[1][4] = {{0.f, 0.f, 0.f, 0.f}};  // rows g, g + 8 x tokens 2t, 2t + 1
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            // after a timeout the slot's stale bytes are read all the same (in bounds)
+            // and the reducer stores nothing
+            if (ok) ok = mbar_wait(c.full(s), par, status);
+            const uint32_t c0 = cS + off[0][0], c1 = cS + off[1][0];
+            [[maybe_unused]] const uint32_t c0h = cS + off[0][1], c1h = cS + off[1][1];
+#pragma unroll
+            for (int k0 = 0; k0 < PPS; k0 += GP) {
+                uint32_t wa[GP][2][2], wb[GP][2][2], scA[GP], scB[GP];
+                [[maybe_unused]] uint32_t zqA[GP], zqB[GP];
+#pragma unroll
+                for (int kk = 0; kk < GP; ++kk) {
+                    const uint32_t kp = (uint32_t)(k0 + kk);
+                    wa[kk][0][0] = lds32_dyn(c0, kp * kPair);
+                    wb[kk][0][0] = lds32_dyn(c0, kp * kPair + 1024u);
+                    wa[kk][1][0] = lds32_dyn(c1, kp * kPair);
+                    wb[kk][1][0] = lds32_dyn(c1, kp * kPair + 1024u);
+                    if constexpr (BITS == 8) {
+                        wa[kk][0][1] = lds32_dyn(c0h, kp * kPair);
+                        wb[kk][0][1] = lds32_dyn(c0h, kp * kPair + 1024u);
+                        wa[kk][1][1] = lds32_dyn(c1h, kp * kPair);
+                        wb[kk][1][1] = lds32_dyn(c1h, kp * kPair + 1024u);
+                    }
+                    scA[kk] = lds32_dyn(sS, kp * 64u);
+                    scB[kk] = lds32_dyn(sS + s8, kp * 64u);
+                    if constexpr (HAS_ZP) {
+                        zqA[kk] = lds16_dyn(zS, kp * 32u);
+                        zqB[kk] = lds16_dyn(zS + z8, kp * 32u);
+                    }
+                }
+                float d[GP][2][4];
+#pragma unroll
+                for (int kk = 0; kk < GP; ++kk)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = 2 * (h * PPS + k0 + kk) + e;
+                        if constexpr (HAS_ZP) {  // start at -zp sum_k x
+                            const float zA = u8f((zqA[kk] >> (8 * e)) & 0xFFu), zB = u8f((zqB[kk] >> (8 * e)) & 0xFFu);
+                            d[kk][e][0] = -zA * sx0[j];
+                            d[kk][e][1] = -zA * sx1[j];
+                            d[kk][e][2] = -zB * sx0[j];
+                            d[kk][e][3] = -zB * sx1[j];
+                        } else {  // copied here, not once outside the loop (that would hold 32 more registers)
+                            d[kk][e][0] = fmov_here(sx0[j]);
+                            d[kk][e][1] = fmov_here(sx1[j]);
+                            d[kk][e][2] = fmov_here(sx0[j]);
+                            d[kk][e][3] = fmov_here(sx1[j]);
+                        }
+                        if constexpr (BITS == 4) {
+                            uint32_t pa[4], pb[4];
+                            U::pairs(wa[kk][e][0], pa);
+                            U::pairs(wb[kk][e][0], pb);
+                            mma_16816(d[kk][e], pa[0], pb[0], pa[2], pb[2], xw[j][0], xw[j][1]);  // low nibbles
+                            mma_16816(d[kk][e], pa[1], pb[1], pa[3], pb[3], xw[j][2], xw[j][3]);  // high: 16 q, x / 16
+                        } else {
+                            uint32_t pa0[2], pa1[2], pb0[2], pb1[2];
+                            U::pairs(wa[kk][e][0], pa0);
+                            U::pairs(wa[kk][e][1], pa1);
+                            U::pairs(wb[kk][e][0], pb0);
+                            U::pairs(wb[kk][e][1], pb1);
+                            mma_16816(d[kk][e], pa0[0], pb0[0], pa0[1], pb0[1], xw[j][0], xw[j][1]);  // words t
+                            mma_16816(d[kk][e], pa1[0], pb1[0], pa1[1], pb1[1], xw[j][2], xw[j][3]);  // words t + 4
+                        }
+                    }
+                // y += s (sum_k x q - zp sum_k x), in units of 2^-24
+#pragma unroll
+                for (int kk = 0; kk < GP; ++kk) {
+                    const float2 sa = __half22float2(*reinterpret_cast<const __half2*>(&scA[kk]));
+                    const float2 sbb = __half22float2(*reinterpret_cast<const __half2*>(&scB[kk]));
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float ssA = e ? sa.y : sa.x, ssB = e ? sbb.y : sbb.x;
+                        v[0][0] = fmaf(ssA, d[kk][e][0], v[0][0]);
+                        v[0][1] = fmaf(ssA, d[kk][e][1], v[0][1]);
+                        v[0][2] = fmaf(ssB, d[kk][e][2], v[0][2]);
+                        v[0][3] = fmaf(ssB, d[kk][e][3], v[0][3]);
+                    }
+                }
+            }
+            __syncwarp();
+            mbar_arrive_if(lane == 0, c.empty(s));  // this warp's reads of the slot are done
+            if (++s == ring) {
+                s = 0;
+                par ^= 1u;
+                cS = sb;
+                sS = sb + L.sc + s_off;
+                zS = sb + L.zp + z_off;
+            } else {
+                cS += L.codes;
+                sS += (uint32_t)kMtSR * L.spitch;
+                zS += (uint32_t)kMtSR * L.zpitch;
+            }
+        }
+        mt_hand_over<1>(c, pw, v, st, ok, lane);
     }
 }
 
@@ -568,6 +830,25 @@ cudaError_t mt_launch_bz(int nt8, int ub, const MtMaps& maps, const DecodeArgs& 
     return mt_launch_one<BITS, HAS_ZP, 2, 1>(maps, a, ctas, smem, pdl, st);
 }
 
+template <int BITS, bool HAS_ZP, int H>
+cudaError_t mt_launch_xr(const MtMaps& maps, const DecodeArgs& a, int ctas, size_t smem, bool pdl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kMtThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, decode_mt_xr_kernel<BITS, HAS_ZP, H>, maps, a);
+}
+
 template <int BITS, bool HAS_ZP, int NT8, int UB>
 cudaError_t mt_set_one() {
     return cudaFuncSetAttribute(decode_mt_kernel<BITS, HAS_ZP, NT8, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -581,6 +862,12 @@ cudaError_t mt_set_smem() {
     if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 1, 1>();
     if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 2, 2>();
     if (e == cudaSuccess) e = mt_set_one<BITS, HAS_ZP, 2, 1>();
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_mt_xr_kernel<BITS, HAS_ZP, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMtSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_mt_xr_kernel<BITS, HAS_ZP, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMtSmem);
     return e;
 }
 
@@ -611,16 +898,20 @@ struct MtGeo {
     uint32_t smem;
 };
 
+// x in registers: one token tile at K = 4096, one or two slots a stage.
+bool mt_xreg(int K, int Mt) { return K == 4096 && mt_nt8(Mt) == 1; }
+
 MtGeo mt_geo(int bits, int K, int Mt, bool zp) {
     const int nt8 = mt_nt8(Mt), nj = K / 32 / kMtCW;
+    const bool xreg = mt_xreg(K, Mt);
     MtGeo best = {0, 0, 0, 0u};
     uint64_t best_bytes = 0;
-    for (int parts = 1; parts <= 4; parts *= 2) {
+    for (int parts = 1; parts <= (xreg ? 2 : 4); parts *= 2) {
         if (nj % parts != 0) continue;
         const int ub = mt_ub(nt8, nj / parts);
         if (best.parts && ub < best.ub) continue;
         for (int r = 2; r <= kMtMaxRing; ++r) {
-            const MtLayout L = mt_layout(r, bits, K, nt8, parts, zp);
+            const MtLayout L = mt_layout(r, bits, K, nt8, parts, zp, xreg);
             if (L.total + 1024u > kMtSmem) break;
             const uint64_t bytes = (uint64_t)(r - 1) * L.codes;
             if (ub > best.ub || bytes > best_bytes) {
@@ -686,6 +977,14 @@ cudaError_t decode_mt_launch(const DecodeArgs& a_in, int sms, bool pdl, cudaStre
     }
     const int nt8 = mt_nt8(a.Mt);
     const size_t smem = G.smem;
+    if (mt_xreg(K, a.Mt)) {
+        if (bits == 4) {
+            if (zp) return G.parts == 2 ? mt_launch_xr<4, true, 2>(maps, a, C, smem, pdl, st) : mt_launch_xr<4, true, 1>(maps, a, C, smem, pdl, st);
+            return G.parts == 2 ? mt_launch_xr<4, false, 2>(maps, a, C, smem, pdl, st) : mt_launch_xr<4, false, 1>(maps, a, C, smem, pdl, st);
+        }
+        if (zp) return G.parts == 2 ? mt_launch_xr<8, true, 2>(maps, a, C, smem, pdl, st) : mt_launch_xr<8, true, 1>(maps, a, C, smem, pdl, st);
+        return G.parts == 2 ? mt_launch_xr<8, false, 2>(maps, a, C, smem, pdl, st) : mt_launch_xr<8, false, 1>(maps, a, C, smem, pdl, st);
+    }
     if (bits == 4)
         return zp ? mt_launch_bz<4, true>(nt8, G.ub, maps, a, C, smem, pdl, st)
                   : mt_launch_bz<4, false>(nt8, G.ub, maps, a, C, smem, pdl, st);
