@@ -541,16 +541,20 @@ def run_sweep(args):
         rows.append({"workload": name, "M": 1, "rank": 0, "mode": "auto", **r})
         print(json.dumps(rows[-1]), flush=True)
     cross = {}
-    for rank in ((0, 32) if wanted("K=4096 N=14336 INT4") else ()):
-        for M in SWEEP_M:
+    ms = SWEEP_M if args.sweep_m is None else tuple(int(v) for v in args.sweep_m.split(","))
+    ranks = (0, 32) if args.sweep_rank is None else (args.sweep_rank,)
+    modes = tuple((m, r) for m, r in (("gemv", mnb.MODE_FORCE_GEMV), ("gemm", mnb.MODE_FORCE_GEMM))
+                  if args.sweep_mode in (None, m))
+    for rank in (ranks if wanted("K=4096 N=14336 INT4") else ()):
+        for M in ms:
             res = {}
-            for mname, mode in (("gemv", mnb.MODE_FORCE_GEMV), ("gemm", mnb.MODE_FORCE_GEMM)):
+            for mname, mode in modes:
                 if mname == "gemv" and M > 64:
                     continue  # the decode kernel re-reads the weights per 16 tokens
                 res[mname] = measure(M, 4096, 14336, 4, rank, None, None, mode, synth.SEED_BASE + 5)
                 rows.append({"workload": "K=4096 N=14336 INT4", "M": M, "rank": rank, "mode": mname, **res[mname]})
                 print(json.dumps(rows[-1]), flush=True)
-            if "gemv" in res and res["gemm"]["us"] < res["gemv"]["us"] and rank not in cross:
+            if "gemv" in res and "gemm" in res and res["gemm"]["us"] < res["gemv"]["us"] and rank not in cross:
                 cross[rank] = M
     summary = {"sweep": "lm_head + K=4096 N=14336 M sweep", "peaks": {"hbm_GBps": hbm_peak, "tensor_TFps": bf16_peak,
                                                                      "source": peak_src},
@@ -855,6 +859,11 @@ def main(argv=None):
                          "(both routes), one JSON line per point")
     ap.add_argument("--sweep-filter", default=None,
                     help="with --sweep: only the workloads whose name contains this text")
+    ap.add_argument("--sweep-m", default=None, help="with --sweep: only these M of the N=14336 sweep (comma list)")
+    ap.add_argument("--sweep-rank", type=int, choices=[0, 32], default=None,
+                    help="with --sweep: only this adapter rank of the N=14336 sweep")
+    ap.add_argument("--sweep-mode", choices=["gemv", "gemm"], default=None,
+                    help="with --sweep: only this route of the N=14336 sweep")
     ap.add_argument("--sweep-next", action="store_true",
                     help="instead of the bench line: the rows beyond the core path (adapter formats, int8 "
                          "activations, 2-bit weights, bias, fused QKV), one JSON line per point")

@@ -101,9 +101,11 @@ typedef struct {
     int32_t block_threads;  /* threads per CTA of the main kernel */
     int32_t rows_per_cta;   /* GEMV: most output rows a CTA owns (whole 16-row groups, dealt out
                                evenly); GEMM: output rows per tile */
-    int32_t k_splits;       /* GEMV: K bytes per row and pipeline stage; GEMM: CTAs (one cluster)
-                               sharing a tile along K, 1 = persistent CTAs over tiles */
-    int32_t tokens_per_cta; /* GEMV: token rows per CTA (8 or 16); GEMM: token tile */
+    int32_t k_splits;       /* GEMV: rows per pipeline stage (single- and few-token decode
+                               kernels, a whole row each) or K bytes per row and stage (general
+                               multi-token kernel); GEMM: CTAs (one cluster) sharing a tile
+                               along K, 1 = persistent CTAs over tiles */
+    int32_t tokens_per_cta; /* GEMV: token columns per CTA (1, 8 or 16); GEMM: token tile */
 } mnb_plan_info;
 
 /* Validate `desc` and create a handle.  Host memory only: no device call is
