@@ -200,6 +200,7 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
         }
         if (kind == kDecMulti) {
             plan_decode_mt(d, Mt, sms, p);
+            p->lora_kernel = rank > 0 ? 1 : 0;
             return MNB_OK;
         }
     }
@@ -360,7 +361,13 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     const int kind = p.route == MNB_ROUTE_GEMV ? decode_kind(d, Mt, rank, sms, !q8x && !(rank > 0 && ad.q8)) : kDecGeneral;
     if (kind != kDecGeneral) {
         // one launch: the single-token decode kernel (base and adapter), or the
-        // decode kernel for 2 .. 16 token rows
+        // decode kernel for 2 .. 16 token rows (behind the LoRA down kernel with an
+        // adapter: X is then complete when it starts, only T is waited for)
+        const bool down = kind == kDecMulti && rank > 0;
+        if (down) {
+            e = launch_down(Xh, Th, early, st);
+            if (e != cudaSuccess) return MNB_ERR_CUDA;
+        }
         mnb::DecodeArgs a = {};
         a.nseg = 1;
         a.NR = (int)d.N;
@@ -373,9 +380,10 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
         a.K = (int)d.K;
         a.bits = d.bits;
         a.Mt = (int)Mt;
-        a.x_wait = early ? 1 : 0;
+        a.x_wait = early && !down ? 1 : 0;
         a.status = status;
-        e = kind == kDecSingle ? mnb::decode_launch(a, rank, sms, early, st) : mnb::decode_mt_launch(a, sms, early, st);
+        e = kind == kDecSingle ? mnb::decode_launch(a, rank, sms, early, st)
+                               : mnb::decode_mt_launch(a, sms, early || down, st);
         if (e == cudaErrorNotSupported) return MNB_ERR_UNSUPPORTED;
         if (e != cudaSuccess) return MNB_ERR_CUDA;
         h->last_route = p.route;

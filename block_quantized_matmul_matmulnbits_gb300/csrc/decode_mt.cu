@@ -1,11 +1,12 @@
 // decode_mt.cu -- decode kernel for a few token rows (2 .. 16): one launch computes
 //
-//     Y[m, n] = sum_k X[m, k] w[n, k]  (+ bias[n])
+//     Y[m, n] = sum_k X[m, k] w[n, k]  (+ sum_r T[m, r] B[n, r])  (+ bias[n])
 //
 // for every token row m, the decode ("fuse_down") path of "[WebGPU] Fuse rank-32
 // quantized LoRA with MatMulNBits" (onnxruntime PR 33370, commit message adding
-// MatMulNBitsLoRA: the decode mode is chosen from the per-matrix row count),
-// restated for sm_103a with the token rows as the MMA's N.
+// MatMulNBitsLoRA: the decode mode is chosen from the per-matrix row count; the base
+// GEMV and T = X A first, then base plus T B^T), restated for sm_103a with the token
+// rows as the MMA's N.  T comes from the LoRA down kernel launched just before.
 //
 // Design:
 //  * Rows are split evenly over the CTAs (one per SM), as in the single-token
@@ -299,11 +300,38 @@ __device__ __forceinline__ void mt_produce(const MtMaps& maps, const DecodeArgs&
 }
 
 // The reducer (one warp): output o = lane + 32 i of a stage is token row o >> 4, row
-// o & 15, the sum of the 16 warps' partials in warp order, one rounding.
+// o & 15, the sum of the 16 warps' partials in warp order (plus, with an adapter,
+// sum_r T[tok, r] B[n, r]), one rounding.  The adapter term comes from two MMAs per
+// token tile (16 rows of B x T of 8 token rows, FP32 accumulation), which the warp
+// stores in the partials' unit (times 2^-24, exact) as a 17th partial of each output.
+// T is the previous launch's output (the LoRA down kernel): read after the wait for it.
 template <int NT8>
 __device__ __forceinline__ void mt_reduce(const DecodeArgs& a, const MtCtx& c, int lane) {
     if (c.r0 >= c.r1) return;
+    const bool lora = a.B != nullptr;
+    const int g = lane >> 2, t = lane & 3;
     bool ok = true;
+    // T fragments (the MMA's B operand): token row 8 jt + g, ranks 16 ks + 2t, + 1 and + 8, + 9
+    uint32_t tf[NT8][2][2];
+#pragma unroll
+    for (int jt = 0; jt < NT8; ++jt)
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) tf[jt][ks][0] = tf[jt][ks][1] = 0u;
+    if (lora) {
+        pdl_wait();
+#pragma unroll
+        for (int jt = 0; jt < NT8; ++jt) {
+            const int tok = 8 * jt + g;
+            if (tok < a.Mt) {
+                const __half* tr = a.T + (size_t)tok * 32 + 2 * t;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    tf[jt][ks][0] = ldg_nc_u32(tr + 16 * ks);
+                    tf[jt][ks][1] = ldg_nc_u32(tr + 16 * ks + 8);
+                }
+            }
+        }
+    }
     MtRows it;
     it.init(a, c.r0, c.r1);
     __half* Yp = a.seg[it.seg].Y;
@@ -316,16 +344,54 @@ __device__ __forceinline__ void mt_reduce(const DecodeArgs& a, const MtCtx& c, i
             bp = a.seg[it.seg].bias;
             Np = a.seg[it.seg].N;
         }
+        // the stage's adapter rows (the MMA's A operand: rows g, g + 8, ranks as T's),
+        // loaded before the wait for the partials so that their latency passes under it
+        uint32_t bf[2][4];
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) bf[ks][e] = 0u;
+        if (lora) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int r = g + 8 * hr;
+                if (r < it.rs) {
+                    const __half* br = a.B + (size_t)(it.ra + r) * 32 + 2 * t;
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        bf[ks][hr] = ldg_nc_u32(br + 16 * ks);
+                        bf[ks][2 + hr] = ldg_nc_u32(br + 16 * ks + 8);
+                    }
+                }
+            }
+        }
         const int b = st % c.nbuf, use = st / c.nbuf;  // stage st's buffer, in its use-th use
         if (ok) ok = mbar_wait(c.pfull(b), (uint32_t)use & 1u, c.status) && *c.in_time();
-        const float* red = c.red(b);
+        float* red = c.red(b);
+        if (lora) {
+#pragma unroll
+            for (int jt = 0; jt < NT8; ++jt) {
+                float d[4];
+                mma_16816_z(d, bf[0][0], bf[0][1], bf[0][2], bf[0][3], tf[jt][0][0], tf[jt][0][1]);
+                mma_16816(d, bf[1][0], bf[1][1], bf[1][2], bf[1][3], tf[jt][1][0], tf[jt][1][1]);
+                // d: rows g, g + 8 x token rows 8 jt + 2t, + 1; output o = token row x 16 + row
+                float* pl = red + ((8 * jt + 2 * t) * 16 + g) * kPS + kMtCW;
+                pl[0] = d[0] * kUnit;
+                pl[16 * kPS] = d[1] * kUnit;
+                pl[8 * kPS] = d[2] * kUnit;
+                pl[24 * kPS] = d[3] * kUnit;
+            }
+            __syncwarp();
+        }
         float y[NT8 * 4];
 #pragma unroll
         for (int i = 0; i < NT8 * 4; ++i) {
-            const float4* pr = reinterpret_cast<const float4*>(red + (lane + 32 * i) * kPS);
+            const float* po = red + (lane + 32 * i) * kPS;
+            const float4* pr = reinterpret_cast<const float4*>(po);
             const float4 p0 = pr[0], p1 = pr[1], p2 = pr[2], p3 = pr[3];
             y[i] = ((((((((((((((p0.x + p0.y) + p0.z) + p0.w) + p1.x) + p1.y) + p1.z) + p1.w) + p2.x) + p2.y) +
                           p2.z) + p2.w) + p3.x) + p3.y) + p3.z) + p3.w;
+            if (lora) y[i] += po[kMtCW];
         }
         __syncwarp();
         mbar_arrive_if(lane == 0, c.pfree(b));  // every lane's reads are done
@@ -926,7 +992,8 @@ MtGeo mt_geo(int bits, int K, int Mt, bool zp) {
 }  // namespace
 
 bool decode_mt_supported(int bits, int64_t Mt, int K, bool lora) {
-    if (lora || (bits != 4 && bits != 8) || Mt < 2 || Mt > 16) return false;
+    (void)lora;  // an FP16 rank-32 adapter: T from the LoRA down kernel, T B^T by the reducer warp
+    if ((bits != 4 && bits != 8) || Mt < 2 || Mt > 16) return false;
     if (K <= 0 || K % 512 != 0 || K > 7680) return false;  // TMA boxes of scales / zero points, swizzled code rows
     return mt_geo(bits, K, (int)Mt, true).parts > 0;        // with zero points: the larger plan
 }
@@ -953,7 +1020,7 @@ cudaError_t decode_mt_launch(const DecodeArgs& a_in, int sms, bool pdl, cudaStre
     DecodeArgs a = a_in;
     const int bits = a.bits, K = a.K, nblk = K / 32;
     const bool zp = a.seg[0].Z != nullptr;
-    if (!decode_mt_supported(bits, a.Mt, K, false)) return cudaErrorNotSupported;
+    if (!decode_mt_supported(bits, a.Mt, K, a.B != nullptr)) return cudaErrorNotSupported;
     const MtGeo G = mt_geo(bits, K, a.Mt, zp);
     const int C = mt_ctas(a.NR, sms);
     a.SR = kMtSR;

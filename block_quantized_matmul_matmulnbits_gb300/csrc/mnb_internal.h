@@ -122,7 +122,9 @@ cudaError_t decode_reset_exchange();
 cudaError_t decode_launch(const DecodeArgs& a, int rank, int sms, bool pdl, cudaStream_t st);
 
 // Decode kernel for 2 .. 16 token rows (decode_mt.cu): the same row space (up to
-// kMaxSeg projections), no adapter.  Whether a call runs on it: bits 4 or 8,
+// kMaxSeg projections); with an FP16 rank-32 adapter (one projection) B [N, 32] and
+// T [Mt, 32] from the LoRA down kernel launched just before (read after
+// griddepcontrol.wait).  Whether a call runs on it: bits 4 or 8,
 // 2 <= Mt <= 16, K % 512 == 0 and K <= 7680, and x of the token rows plus two
 // stage slots (with zero points) fitting in one SM's shared memory.
 bool decode_mt_supported(int bits, int64_t Mt, int K, bool lora);

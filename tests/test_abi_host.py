@@ -129,8 +129,9 @@ def test_k_zero_is_a_fill():
 
 
 def test_gemv_plan_balances_rows_over_sms():
-    # the general multi-token decode kernel (here: two token rows with an FP16 adapter)
-    for N, K, bits in ((4096, 4096, 4), (14336, 4096, 4), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4)):
+    # the general multi-token decode kernel (here: two token rows with an FP16 adapter;
+    # INT2 weights at K = 4096, where INT4 / INT8 run on the few-token kernel)
+    for N, K, bits in ((4096, 4096, 2), (14336, 4096, 2), (49152, 576, 8), (151936, 896, 8), (1000, 96, 4)):
         h = mnb.mnb_create(N, K, bits)
         try:
             p = mnb.mnb_plan(h, 1, 2, 32, 152)
@@ -161,6 +162,8 @@ def test_few_token_plan_splits_rows_evenly():
         h = mnb.mnb_create(N, K, bits)
         try:
             for M in (2, 5, 8, 9, 16):
+                # an FP16 adapter keeps the kernel (the LoRA down kernel runs first)
+                assert mnb.mnb_plan(h, 1, M, 32, 152)["k_splits"] == mnb.mnb_plan(h, 1, M, 0, 152)["k_splits"]
                 p = mnb.mnb_plan(h, 1, M, 0, 152)
                 assert p["route"] == mnb.ROUTE_GEMV and p["lora_kernel"] == 0
                 if M <= mt_max:

@@ -195,6 +195,30 @@ def test_few_token_kernel_matches_oracle(env, M, N, K, bits, zp):
     assert_within_tolerance(bits_of(Y), Y64, bound, f"few tokens M={M} N={N} K={K} bits={bits}")
 
 
+@pytest.mark.parametrize("M,N,K,bits,zp,partial", [
+    (3, 1000, 512, 4, (0, 15), False),
+    (8, 2077, 4096, 4, None, True),     # x in registers; ranks 16..31 zero
+    (12, 700, 2048, 8, (120, 136), False),
+    (16, 1500, 4096, 4, (0, 15), False),
+])
+def test_few_token_kernel_with_adapter(env, M, N, K, bits, zp, partial):
+    """An FP16 rank-32 adapter on the few-token kernel: T from the LoRA down kernel,
+    T B^T added by the reducer warp before the one rounding; every output against
+    the oracle."""
+    torch, mnb = env
+    h = mnb.mnb_create(N, K, bits)
+    try:
+        p = mnb.mnb_plan(h, 1, M, 32, torch.cuda.get_device_properties(0).multi_processor_count)
+    finally:
+        mnb.mnb_destroy(h)
+    assert p["k_splits"] == 16 and p["lora_kernel"] == 1
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=bits, seed=3500 + M, zp_range=zp, rank=32, partial=partial)
+    Y, _, route = run_gpu(mnb, torch, inp)
+    assert route == mnb.ROUTE_GEMV
+    Y64, bound = oracle_ref(inp)
+    assert_within_tolerance(bits_of(Y), Y64, bound, f"few tokens + adapter M={M} N={N} K={K} bits={bits}")
+
+
 def test_few_token_exact_arithmetic_bitwise(env):
     """X in {-1,0,1} (<= 8 nonzeros per row), power-of-two scales, 12 token rows, no
     adapter: every product, block sum and partial sum of the few-token kernel is
