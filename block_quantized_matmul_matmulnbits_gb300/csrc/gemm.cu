@@ -13,21 +13,32 @@
 //    shapes) the K range of a tile is split over the S CTAs of a thread-block
 //    cluster; their partial tiles are added in rank order through distributed
 //    shared memory (deterministic, no atomics).
+//  * The K loop runs in stages of xk 64-wide K steps (xk = 2 when a CTA takes
+//    whole rows of an even number of K steps, else 1).  A stage is one X slot
+//    in shared memory plus xk dequantized A steps in tensor memory, with one
+//    barrier each for "X landed", "A written" and "MMAs done": the single MMA
+//    thread spends a few hundred cycles on every wait and every commit, as
+//    much as on issuing several MMAs, so it waits twice and commits once per
+//    stage instead of per K step.
 //  * Two producer warps, so that the weight stream runs ahead of X: warp 0
-//    copies the packed weights of 128 rows in super-stages of 256 bytes per
-//    row (two TMA boxes of 128 rows x 128 bytes, 128-byte swizzle), warp 14
-//    the X tile [BN x 64] FP16 of each 64-wide K step (TMA, 128-byte swizzle).
-//    Few large boxes: one TMA copy costs about as much to issue as a small
-//    one, so per-row copies of a few hundred bytes cannot feed an SM.
+//    copies the packed weights of 128 rows in super-stages of 128 or 256
+//    bytes per row (TMA boxes of 128 rows x 128 bytes, 128-byte swizzle),
+//    warp 14 the X tile of a stage: [BN x 64] FP16 per K step, xk of them in
+//    one 3-D box (TMA, 128-byte swizzle).  Few large boxes: one TMA copy
+//    costs about as much as a small one, so per-row copies of a few hundred
+//    bytes cannot feed an SM.
 //  * Warps 6..13 dequantize: exact (q - zp), one rounding by the FP16 scale --
 //    the DequantizeLinear map of "Fuse DQ->MatMulNBits for shared initializers
-//    and skip outer-scope weights" (PR 33800) -- into the canonical K-major
-//    128B-swizzled FP16 operand layout, fence the generic->async proxy and
-//    arrive on the stage's barrier.
-//  * Warp 1 allocates tensor memory (two 128 x BN FP32 accumulators) and one
-//    lane issues tcgen05.mma.kind::f16 (A = dequantized weights, B = X, both
-//    from shared memory descriptors), committing each stage back to the
-//    producer.
+//    and skip outer-scope weights" (PR 33800) -- straight into tensor memory
+//    (tcgen05.st: a warp writes its own quarter of the 128 rows, one row per
+//    lane, half of the step's K each), then arrive on the stage's barrier
+//    once its xk steps are written.
+//    The A operand never passes through shared memory: per K step that saves
+//    writing and reading 16 KB there, next to the 32 KB of X the MMA reads.
+//  * Warp 1 allocates tensor memory (one or two 128 x BN FP32 accumulators and
+//    the A steps of the stage ring) and one lane issues tcgen05.mma.kind::f16
+//    (A from tensor memory, B = X from a shared memory descriptor), committing
+//    each stage back to both producers with one commit.
 //  * The LoRA term is one more K step (in the last K split of a tile) with A =
 //    B_lora[n, 0:32] (FP16, or dequantized from an INT8 block-32 up weight)
 //    and B = T[m, 0:32], written into the ring by the dequant
@@ -57,7 +68,7 @@ constexpr int kXWarp = 14;       // X producer
 constexpr int kDqThreads = 256;
 constexpr int kDqWarps = kDqThreads / 32;  // arrivals on the dequant barriers: one per warp
 constexpr int kEpiThreads = 128;
-constexpr int kWSlot = BM * 128; // dequantized FP16 A tile of one K step
+constexpr int kACols = BK / 2;    // tensor-memory columns of one dequantized A stage (128 rows x 64 FP16)
 constexpr int kPBox = BM * 128;  // one packed-weight TMA box: 128 rows x 128 bytes
 constexpr int kMaxSplit = 8;
 constexpr uint32_t kSmemBudget = 232448;
@@ -85,13 +96,27 @@ __host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// tcgen05.mma.kind::f16 with A in tensor memory ([a_tmem]: rows in lanes, K along
+// the columns, two FP16 values a 32-bit column) and B from a shared-memory descriptor.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes (one per
+// thread), waited for.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -119,34 +144,45 @@ __host__ __device__ inline uint32_t g_align(uint32_t x, uint32_t a) { return (x 
 // The split-K partial tile (128 x BN FP32) reuses the ring from offset 0: a
 // CTA of a split runs one unit, and once its accumulator is complete every
 // copy into the ring has landed and every read of it has finished.
-// Three rings: X tiles (nx slots), dequantized A tiles (nw slots of 16 KB),
-// packed-weight super-stages (np slots).  X has its own ring so that its
-// loads run ahead of the MMA instead of waiting for a slot of the A ring.
+// Two rings in shared memory: stages (nx slots of xk K steps of X) and
+// packed-weight super-stages (np slots).  The stages' dequantized A steps
+// (nw = nx xk) live in tensor memory beside the accumulators: columns
+// [0, nacc BN) hold one or two 128 x BN FP32 accumulators, A step t of the
+// ring starts at column a_col + 32 t.
 struct GemmLayout {
     uint32_t xslot;    // bytes of one X slot (BN rows x 128 B, 1024-aligned)
     int nx, nw, np;    // slots of the X, A and packed rings
     int pboxes;        // TMA boxes per packed super-stage (128 packed bytes of each row per box)
     uint32_t pstage;   // bytes of one packed super-stage
-    uint32_t w_off, p_off, red_bytes, bar_off, total;
+    int nacc;          // accumulators (two: a tile's epilogue runs under the next tile's MMAs)
+    uint32_t a_col, tmem_cols;
+    uint32_t p_off, red_bytes, bar_off, total;
 };
 
-__host__ __device__ inline GemmLayout gemm_layout(int BN) {
+__host__ __device__ inline GemmLayout gemm_layout(int BN, int xk) {
     GemmLayout L;
-    L.xslot = g_align((uint32_t)BN * 128u, 1024u);
+    L.xslot = g_align((uint32_t)(xk * BN) * 128u, 1024u);
     // Small token tiles (decode shapes) are bound by the weight stream: deep
     // packed ring, large super-stages.  Large tiles keep four X slots and four
     // A slots (the dequant runs up to four steps ahead of the MMA).
     L.pboxes = BN <= 64 ? 2 : 1;
     L.pstage = (uint32_t)(L.pboxes * kPBox);
     L.np = BN <= 64 ? 4 : 2;
-    L.nw = 4;
+    // 512 columns of tensor memory: two accumulators where four A stages still fit
+    L.nacc = 2 * BN + 4 * kACols <= 512 ? 2 : 1;
+    L.a_col = g_align((uint32_t)(L.nacc * BN), 32u);
+    L.tmem_cols = 512u;
     L.red_bytes = (uint32_t)BM * BN * 4u;
-    const uint32_t fixed = L.np * L.pstage + L.nw * (uint32_t)kWSlot + 512u + 1024u;
+    // One ring of stages: stage s holds xk K steps of X (an X slot) and their xk
+    // dequantized A steps (tensor memory), filled and released together.
+    const uint32_t fixed = L.np * L.pstage + 512u + 1024u;
     int nx = fixed < kSmemBudget ? (int)((kSmemBudget - fixed) / L.xslot) : 0;
+    const int nx_tmem = (int)((512u - L.a_col) / kACols) / xk;
+    if (nx > nx_tmem) nx = nx_tmem;
     if (nx > 12) nx = 12;
     L.nx = nx;
-    L.w_off = (uint32_t)nx * L.xslot;
-    L.p_off = L.w_off + (uint32_t)L.nw * kWSlot;
+    L.nw = nx * xk;
+    L.p_off = (uint32_t)nx * L.xslot;
     L.bar_off = L.p_off + (uint32_t)L.np * L.pstage;
     L.total = L.bar_off + 512u + 1024u;
     return L;
@@ -159,7 +195,7 @@ struct GemmParams {
     int tiles;      // total tiles
     int ksteps;     // 64-wide K steps of a full row
     int split;      // CTAs (one cluster) sharing a tile along K; 1 = persistent over tiles
-    int tmem_cols;  // allocated tensor-memory columns (power of two >= 2 BN)
+    int xk;         // K steps per X copy: 2 = one 3-D box of two 64-wide K slices (split 1, even K steps)
     int x_wait;     // X may be written by the work queued before this grid: wait for it
 };
 
@@ -217,19 +253,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base_raw = smem_u32(smem_raw);
     const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
     unsigned char* sptr = smem_raw + (sbase - base_raw);
-    const GemmLayout L = gemm_layout(P.BN);
-    const int nx = L.nx, nw = L.nw, np = L.np;
+    const GemmLayout L = gemm_layout(P.BN, P.xk);
+    const int nx = L.nx, np = L.np;
 
     const uint32_t bars = sbase + L.bar_off;
-    // With as many X slots as A slots, step k uses slot k % n of both rings and one
-    // commit per step releases both (a commit costs the single MMA thread several
-    // MMAs' worth of issue time); else each ring has its own release barrier.
-    const bool one_release = nx == nw;
+    // Stage s: full_x (X landed), full_w (its A steps written), empty (the MMAs
+    // are done with both).  The single MMA thread then waits twice and commits
+    // once per stage: each of those costs it a few hundred cycles, as much as
+    // issuing several MMAs.
     auto full_x = [&](int s) { return bars + 8u * s; };
     auto empty_x = [&](int s) { return bars + 8u * (nx + s); };
     auto full_w = [&](int s) { return bars + 8u * (2 * nx + s); };
-    auto empty_w = [&](int s) { return bars + 8u * (one_release ? nx + s : 2 * nx + nw + s); };
-    const int b0 = 2 * nx + 2 * nw;
+    const int b0 = 3 * nx;
     auto full_p = [&](int j) { return bars + 8u * (b0 + j); };
     auto empty_p = [&](int j) { return bars + 8u * (b0 + np + j); };
     auto acc_full = [&](int a) { return bars + 8u * (b0 + 2 * np + a); };
@@ -237,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain = bars + 8u * (b0 + 2 * np + 4);
     const uint32_t tmem_slot = drain + 8u;
     auto xslot = [&](int s) { return sbase + (uint32_t)s * L.xslot; };
-    auto wslot = [&](int s) { return sbase + L.w_off + (uint32_t)s * kWSlot; };
 
     const GemmArgs& a = P.a;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,10 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < nx; ++s) {
             mbar_init(full_x(s), 1);
             mbar_init(empty_x(s), 1);
-        }
-        for (int s = 0; s < nw; ++s) {
             mbar_init(full_w(s), kDqWarps);
-            if (!one_release) mbar_init(empty_w(s), 1);  // else empty_w(s) is empty_x(s)
         }
         for (int j = 0; j < np; ++j) {
             mbar_init(full_p(j), 1);
@@ -268,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot),
-                     "r"(P.tmem_cols)
+                     "r"(L.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -279,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
 
     const int nblk = a.K / 32;
-    const uint32_t x_bytes = (uint32_t)BN * 128u;
+    const int xk = P.xk;
+    const uint32_t x_tile = (uint32_t)BN * 128u;  // one K step of X in a slot
+    const uint32_t x_bytes = (uint32_t)xk * x_tile;
 
     if (warp == 0) {
         // ---------------------------------------------------------------- packed-weight producer
@@ -313,16 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- X producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
-            int step = 0, cursor = blockIdx.x;
+            int step = 0, cursor = blockIdx.x;  // step: X stages (xk K steps each, or the LoRA step)
             bool ok = true, x_ready = P.x_wait == 0;
             Unit u;
             while (ok && next_unit(P, cursor, u)) {
-                const int nsteps = (u.i1 - u.i0) + (u.lora ? 1 : 0);
-                for (int i = 0; i < nsteps; ++i, ++step) {
+                const int nkx = (u.i1 - u.i0) / xk;  // K stages (xk divides the range)
+                const int nst = nkx + (u.lora ? 1 : 0);
+                for (int i = 0; i < nst; ++i, ++step) {
                     const int s = step % nx;
                     const uint32_t ph = (uint32_t)(step / nx) & 1u;
                     if (!(ok = mbar_wait_sleep(empty_x(s), ph ^ 1u, status, 64))) break;
-                    if (i >= u.i1 - u.i0) {  // LoRA step: the dequant warps fill the slot
+                    if (i >= nkx) {  // LoRA step: the dequant warps fill the slot
                         mbar_arrive(full_x(s));
                         continue;
                     }
@@ -331,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x_ready = true;
                     }
                     mbar_arrive_tx(full_x(s), x_bytes);
-                    tma_load_2d(xslot(s), &tmX, (u.i0 + i) * BK, u.m0, full_x(s));
+                    if (xk == 1)
+                        tma_load_2d(xslot(s), &tmX, (u.i0 + i) * BK, u.m0, full_x(s));
+                    else  // [K slice][token row][128 B]: one 128B-swizzled tile per K step
+                        tma_load_3d(xslot(s), &tmX, 0, u.m0, u.i0 + i * xk, full_x(s));
                 }
             }
             for (int j = 1; j <= nx && step - j >= 0; ++j) {
@@ -344,27 +381,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(BM, BN);
-            int step = 0, tl = 0, cursor = blockIdx.x;
+            int xs = 0, tl = 0, cursor = blockIdx.x;  // xs: stages
             bool ok = true;
             Unit u;
             while (ok && next_unit(P, cursor, u)) {
-                const int acc = tl & 1;
-                if (!(ok = mbar_wait(acc_empty(acc), ((uint32_t)(tl >> 1) & 1u) ^ 1u, status))) break;
+                const int acc = tl % L.nacc, use = tl / L.nacc;
+                if (!(ok = mbar_wait(acc_empty(acc), ((uint32_t)use & 1u) ^ 1u, status))) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                const int nsteps = (u.i1 - u.i0) + (u.lora ? 1 : 0);
-                for (int i = 0; i < nsteps; ++i, ++step) {
-                    const int sx = step % nx, sw = step % nw;
-                    if (!(ok = mbar_wait(full_x(sx), (uint32_t)(step / nx) & 1u, status))) break;
-                    if (!(ok = mbar_wait(full_w(sw), (uint32_t)(step / nw) & 1u, status))) break;
+                const int nkx = (u.i1 - u.i0) / xk;
+                const int nst = nkx + (u.lora ? 1 : 0);
+                for (int i = 0; i < nst; ++i, ++xs) {
+                    const int sx = xs % nx;
+                    const uint32_t ph = (uint32_t)(xs / nx) & 1u;
+                    if (!(ok = mbar_wait(full_x(sx), ph, status))) break;
+                    if (!(ok = mbar_wait(full_w(sx), ph, status))) break;
                     tc_fence_after();
-                    const bool lora_step = i >= u.i1 - u.i0;
-                    const int kk = lora_step ? 2 : BK / 16;  // the LoRA step covers K = 32
-                    for (int j = 0; j < kk; ++j)
-                        tc_mma(d_tmem, sw128_desc(wslot(sw) + 32u * j), sw128_desc(xslot(sx) + 32u * j), idesc,
-                               (i > 0 || j > 0) ? 1u : 0u);
-                    tc_commit(empty_x(sx));
-                    if (!one_release) tc_commit(empty_w(sw));
+                    // K = 16 a MMA: 8 columns of A, 32 bytes of an X row (2 in the descriptor's address field)
+                    uint32_t a_tmem = tmem_base + L.a_col + (uint32_t)(sx * xk * kACols);
+                    uint64_t bd = sw128_desc(xslot(sx));
+                    if (i >= nkx) {  // the LoRA step: K = 32
+                        tc_mma_ta(d_tmem, a_tmem, bd, idesc, 1u);
+                        tc_mma_ta(d_tmem, a_tmem + 8u, bd + 2u, idesc, 1u);
+                    } else {
+                        for (int sub = 0; sub < xk; ++sub) {
+#pragma unroll
+                            for (int j = 0; j < BK / 16; ++j)
+                                tc_mma_ta(d_tmem, a_tmem + 8u * j, bd + 2u * j, idesc, (i | sub | j) ? 1u : 0u);
+                            a_tmem += kACols;
+                            bd += x_tile >> 4;
+                        }
+                    }
+                    tc_commit(empty_x(sx));  // the X slot and the stage's A steps
                 }
                 if (ok) tc_commit(acc_full(acc));
                 ++tl;
@@ -380,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tl = 0, cursor = blockIdx.x;
         Unit u;
         while (next_unit(P, cursor, u)) {
-            const int acc = tl & 1;
+            const int acc = tl % L.nacc, use = tl / L.nacc;
             // the epilogue waits a whole tile: it sleeps, so as not to take issue slots from the dequant
-            if (!mbar_wait_sleep(acc_full(acc), (uint32_t)(tl >> 1) & 1u, status, 1000)) break;
+            if (!mbar_wait_sleep(acc_full(acc), (uint32_t)use & 1u, status, 1000)) break;
             tc_fence_after();
             const int n = u.n0 + row;
             for (int c = 0; c < BN; c += 16) {
@@ -409,16 +457,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- dequant
-        // thread -> (row r, block h of the step): a quarter warp takes 8
-        // consecutive rows with one h, so its swizzled 16-byte reads of the
-        // packed box and writes of the A tile hit 8 distinct bank groups
+        // thread -> (row r, block h of the step): a warp owns the 32 rows of its
+        // tensor-memory lane quarter (warp % 4) and one block of every step (warps
+        // 6..9 the first, 10..13 the second); a quarter warp's swizzled 16-byte
+        // reads of the packed box hit 8 distinct bank groups
         const int d = threadIdx.x - kDqWarp0 * 32;  // 0..255
-        const int dl = d & 31;
-        const int r = (d >> 5) * 16 + (dl & 7) + ((dl >> 4) << 3);
-        const int h = (dl >> 3) & 1;
+        const int dl = lane;
+        const int r = (warp & 3) * 32 + lane;
+        const int h = (warp - kDqWarp0) >> 2;
+        const uint32_t a_lane = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + L.a_col + (uint32_t)h * 16u;
         constexpr int kPrefetch = 6;                // scale / zero-point loads in flight
         constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
-        int step = 0, pstep = 0, cursor = blockIdx.x;
+        int pstep = 0, xs = 0, cursor = blockIdx.x;  // xs: stages
         bool ok = true, waited = false;
         Unit u;
         while (ok && next_unit(P, cursor, u)) {
@@ -454,10 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         ++pstep;
                     }
-                    const int s = step % nw;
-                    const uint32_t ph = (uint32_t)(step / nw) & 1u;
-                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(empty_w(s), ph ^ 1u, status, 32));  // the MMA is done with the slot
-                    if (!ok) break;
+                    const int sx = xs % nx, sub = local % xk;
+                    if (sub == 0) {  // the MMA is done with the stage
+                        ok = __all_sync(0xffffffffu, mbar_wait_sleep(empty_x(sx), ((uint32_t)(xs / nx) & 1u) ^ 1u, status, 32));
+                        if (!ok) break;
+                    }
+                    const int s = sx * xk + sub;  // A step of the ring
                     // invalid block (row past N, K tail): scale 0 makes its products 0
                     const DqConst dc = dq_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
                     Dq2Const d2 = {};
@@ -485,20 +537,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], dc, &out[2 * w]);
                     }
-                    const uint32_t wrow = wslot(s);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t dst = wrow + swz128(r, 4 * h + c);
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(out[4 * c]),
-                                     "r"(out[4 * c + 1]), "r"(out[4 * c + 2]), "r"(out[4 * c + 3])
-                                     : "memory");
-                    }
-                    fence_proxy_async();  // this thread's writes, before the MMA reads them
+                    // the block's 32 FP16 values: 16 columns of row r in A step s
+                    tmem_st16(a_lane + (uint32_t)(s * kACols), out);
+                    const bool last_sub = sub == xk - 1;
+                    if (last_sub) tc_fence_before();  // the stores, before the MMA thread is told
                     __syncwarp();
                     if (dl == 0) {  // one arrival per warp: its lanes are ordered before lane 0 here
-                        mbar_arrive(full_w(s));
+                        if (last_sub) mbar_arrive(full_w(sx));
                         if ((local & (kps - 1)) == kps - 1 || i == u.i1 - 1) mbar_arrive(empty_p(cur_p));
                     }
+                    if (last_sub) ++xs;
                     {  // refill this prefetch slot with step i + kPrefetch (after the fence, which
                        // would otherwise wait for these loads)
                         const int blk = 2 * (i + kPrefetch) + h;
@@ -508,43 +556,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (HAS_ZP) zz[v] = (uint32_t)__ldg(zrow + bc);
                         vmask = ld ? (vmask | (1u << v)) : (vmask & ~(1u << v));
                     }
-                    ++step;
                 }
             }
             if (ok && u.lora) {
-                const int s = step % nw, sx = step % nx;
-                ok = __all_sync(0xffffffffu, mbar_wait(empty_w(s), ((uint32_t)(step / nw) & 1u) ^ 1u, status));
-                if (!ok) break;
-                ok = __all_sync(0xffffffffu, mbar_wait(empty_x(sx), ((uint32_t)(step / nx) & 1u) ^ 1u, status));
+                const int sx = xs % nx, s = sx * xk;
+                ok = __all_sync(0xffffffffu, mbar_wait(empty_x(sx), ((uint32_t)(xs / nx) & 1u) ^ 1u, status));
                 if (!ok) break;
                 if (!waited) {
                     pdl_wait();  // T is written by the LoRA down kernel queued before this grid
                     waited = true;
                 }
-                if (h == 0 && a.Bq) {  // A operand from the INT8 up weight: one block per row
-                    const size_t nn = (size_t)(row_ok ? n : 0);
-                    const uint4* brow = reinterpret_cast<const uint4*>(a.Bq + nn * 32);
-                    const uint4 p0 = __ldg(brow), p1 = __ldg(brow + 1);
-                    const uint16_t sbits = row_ok ? reinterpret_cast<const uint16_t*>(a.Bs)[nn] : (uint16_t)0;
-                    const DqConst bc = dq_const(a.Bz ? (uint32_t)a.Bz[nn] : 128u, sbits);  // scale 0: row past N
-                    const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                if (h == 0) {  // A operand: row r's 32 adapter values in columns 0..15 of stage s
                     uint32_t o[16];
+                    if (a.Bq) {  // from the INT8 up weight: one block per row
+                        const size_t nn = (size_t)(row_ok ? n : 0);
+                        const uint4* brow = reinterpret_cast<const uint4*>(a.Bq + nn * 32);
+                        const uint4 p0 = __ldg(brow), p1 = __ldg(brow + 1);
+                        const uint16_t sbits = row_ok ? reinterpret_cast<const uint16_t*>(a.Bs)[nn] : (uint16_t)0;
+                        const DqConst bc = dq_const(a.Bz ? (uint32_t)a.Bz[nn] : 128u, sbits);  // scale 0: row past N
+                        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], bc, &o[2 * w]);
+                        for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], bc, &o[2 * w]);
+                    } else {  // B_lora[n, 0:32]
+                        const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)(row_ok ? n : 0) * 32);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(wslot(s) + swz128(r, c)),
-                                     "r"(o[4 * c]), "r"(o[4 * c + 1]), "r"(o[4 * c + 2]), "r"(o[4 * c + 3])
-                                     : "memory");
-                } else if (h == 0) {  // A operand: B_lora[n, 0:32] in chunks 0..3 of row r
-                    const uint4* brow = reinterpret_cast<const uint4*>(a.B + (size_t)(row_ok ? n : 0) * 32);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 v = row_ok ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(wslot(s) + swz128(r, c)),
-                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                     : "memory");
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = row_ok ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
+                            o[4 * c] = v.x;
+                            o[4 * c + 1] = v.y;
+                            o[4 * c + 2] = v.z;
+                            o[4 * c + 3] = v.w;
+                        }
                     }
+                    tmem_st16(a_lane + (uint32_t)(s * kACols), o);  // h == 0: columns 0..15
                 }
                 for (int idx = d; idx < BN * 4; idx += kDqThreads) {  // B operand: T[m, 0:32]
                     const int tr = idx >> 2, c = idx & 3;
@@ -555,10 +599,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  "r"(v.y), "r"(v.z), "r"(v.w)
                                  : "memory");
                 }
-                fence_proxy_async();
+                fence_proxy_async();  // T in the X slot, before the MMA reads it
+                tc_fence_before();    // the adapter rows in tensor memory, likewise
                 __syncwarp();
-                if (dl == 0) mbar_arrive(full_w(s));
-                ++step;
+                if (dl == 0) mbar_arrive(full_w(sx));
+                ++xs;
             }
         }
     }
@@ -605,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(P.tmem_cols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(L.tmem_cols)
                      : "memory");
     }
 }
@@ -686,17 +731,19 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
     P.tiles = P.tiles_m * ((a.N + BM - 1) / BM);
     P.ksteps = (a.K + BK - 1) / BK;
     P.split = p.k_splits > 1 ? p.k_splits : 1;
-    int cols = 32;
-    while (cols < 2 * P.BN) cols *= 2;
-    P.tmem_cols = cols;
     P.x_wait = x_wait ? 1 : 0;
-    const GemmLayout L = gemm_layout(P.BN);
+    // Two K steps of X a copy where a whole row is one unit and its K steps pair
+    // up: a copy costs the SM's TMA about the same time whatever its size, and one
+    // 64-wide step of a 256-token tile is too little to keep the MMA fed.
+    P.xk = (P.split == 1 && a.K % (2 * BK) == 0 && a.K * 2 / 128 <= 256 && gemm_layout(P.BN, 2).nx >= 2) ? 2 : 1;
+    const GemmLayout L = gemm_layout(P.BN, P.xk);
     if (L.nx < 2 || L.total > kSmemBudget || (P.split > 1 && L.red_bytes > L.bar_off))
         return cudaErrorInvalidConfiguration;
 
-    CUtensorMap tx;
-    cudaError_t e = encode_2d(&tx, a.X, 2, (uint64_t)a.K, (uint64_t)a.Mt, (uint64_t)a.K * 2, (uint32_t)BK,
-                              (uint32_t)P.BN, true);
+    CUtensorMap tx;  // X [Mt x K] FP16: 2-D boxes of BN rows x 64, or 3-D boxes of two such K slices
+    cudaError_t e = P.xk == 1 ? encode_2d(&tx, a.X, 2, (uint64_t)a.K, (uint64_t)a.Mt, (uint64_t)a.K * 2, (uint32_t)BK,
+                                          (uint32_t)P.BN, true)
+                              : encode_codes_sw128(&tx, a.X, (uint64_t)a.K * 2, (uint64_t)a.Mt, (uint32_t)P.BN, 2u);
     if (e != cudaSuccess) return e;
     CUtensorMap tw;  // packed weights [N rows x K*bits/8 bytes], boxes of 128 rows x 128 bytes
     e = encode_2d(&tw, a.Wq, 1, (uint64_t)a.K * a.bits / 8, (uint64_t)a.N, (uint64_t)a.K * a.bits / 8, 128u, (uint32_t)BM,
