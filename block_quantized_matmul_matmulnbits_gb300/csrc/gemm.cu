@@ -108,7 +108,8 @@ __device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint
 }
 
 // 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes (one per
-// thread), waited for.
+// thread); the registers are read at issue, the write completes asynchronously
+// (tmem_wait_st).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -116,8 +117,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t v[16]) 
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
         "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -540,7 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the block's 32 FP16 values: 16 columns of row r in A step s
                     tmem_st16(a_lane + (uint32_t)(s * kACols), out);
                     const bool last_sub = sub == xk - 1;
-                    if (last_sub) tc_fence_before();  // the stores, before the MMA thread is told
+                    if (last_sub) {  // the stage's stores complete, before the MMA thread is told
+                        tmem_wait_st();
+                        tc_fence_before();
+                    }
                     __syncwarp();
                     if (dl == 0) {  // one arrival per warp: its lanes are ordered before lane 0 here
                         if (last_sub) mbar_arrive(full_w(sx));
@@ -600,7 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : "memory");
                 }
                 fence_proxy_async();  // T in the X slot, before the MMA reads it
-                tc_fence_before();    // the adapter rows in tensor memory, likewise
+                tmem_wait_st();       // the adapter rows in tensor memory, likewise
+                tc_fence_before();
                 __syncwarp();
                 if (dl == 0) mbar_arrive(full_w(sx));
                 ++xs;
@@ -609,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- teardown
+    tmem_wait_st();  // a role that stopped early may have stores in flight
     tc_fence_before();
     __syncthreads();
     if (P.split > 1) {
