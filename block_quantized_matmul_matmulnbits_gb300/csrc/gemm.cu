@@ -126,6 +126,14 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  : "memory");
 }
 
+// A 2-D TMA store of a shared-memory tile (async proxy; bulk group of this thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(src)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -158,10 +166,12 @@ struct GemmLayout {
     uint32_t pstage;   // bytes of one packed super-stage
     int nacc;          // accumulators (two: a tile's epilogue runs under the next tile's MMAs)
     uint32_t a_col, tmem_cols;
-    uint32_t p_off, red_bytes, bar_off, total;
+    uint32_t p_off, y_off, red_bytes, bar_off, total;
 };
 
-__host__ __device__ inline GemmLayout gemm_layout(int BN, int xk) {
+// ystage: the epilogue stages the FP16 output tile in shared memory, a
+// [BN tokens][32 rows] part per epilogue warp, each written with one TMA store.
+__host__ __device__ inline GemmLayout gemm_layout(int BN, int xk, int ystage) {
     GemmLayout L;
     L.xslot = g_align((uint32_t)(xk * BN) * 128u, 1024u);
     // Small token tiles (decode shapes) are bound by the weight stream: deep
@@ -177,7 +187,8 @@ __host__ __device__ inline GemmLayout gemm_layout(int BN, int xk) {
     L.red_bytes = (uint32_t)BM * BN * 4u;
     // One ring of stages: stage s holds xk K steps of X (an X slot) and their xk
     // dequantized A steps (tensor memory), filled and released together.
-    const uint32_t fixed = L.np * L.pstage + 512u + 1024u;
+    const uint32_t ybytes = ystage ? (uint32_t)(BM * BN * 2) : 0u;
+    const uint32_t fixed = L.np * L.pstage + ybytes + 512u + 1024u;
     int nx = fixed < kSmemBudget ? (int)((kSmemBudget - fixed) / L.xslot) : 0;
     const int nx_tmem = (int)((512u - L.a_col) / kACols) / xk;
     if (nx > nx_tmem) nx = nx_tmem;
@@ -185,7 +196,8 @@ __host__ __device__ inline GemmLayout gemm_layout(int BN, int xk) {
     L.nx = nx;
     L.nw = nx * xk;
     L.p_off = (uint32_t)nx * L.xslot;
-    L.bar_off = L.p_off + (uint32_t)L.np * L.pstage;
+    L.y_off = L.p_off + (uint32_t)L.np * L.pstage;
+    L.bar_off = L.y_off + ybytes;
     L.total = L.bar_off + 512u + 1024u;
     return L;
 }
@@ -198,6 +210,7 @@ struct GemmParams {
     int ksteps;     // 64-wide K steps of a full row
     int split;      // CTAs (one cluster) sharing a tile along K; 1 = persistent over tiles
     int xk;         // K steps per X copy: 2 = one 3-D box of two 64-wide K slices (split 1, even K steps)
+    int ystage;     // output tile through shared memory and a TMA store (split 1, N % 8 == 0)
     int x_wait;     // X may be written by the work queued before this grid: wait for it
 };
 
@@ -250,12 +263,13 @@ __device__ __forceinline__ float4 ld_peer_f32x4(uint32_t local_addr, uint32_t ra
 
 template <int BITS, bool HAS_ZP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmParams P) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                const __grid_constant__ CUtensorMap tmY, const GemmParams P) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t base_raw = smem_u32(smem_raw);
     const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
     unsigned char* sptr = smem_raw + (sbase - base_raw);
-    const GemmLayout L = gemm_layout(P.BN, P.xk);
+    const GemmLayout L = gemm_layout(P.BN, P.xk, P.ystage);
     const int nx = L.nx, np = L.np;
 
     const uint32_t bars = sbase + L.bar_off;
@@ -431,10 +445,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         Unit u;
         while (next_unit(P, cursor, u)) {
             const int acc = tl % L.nacc, use = tl / L.nacc;
-            // the epilogue waits a whole tile: it sleeps, so as not to take issue slots from the dequant
-            if (!mbar_wait_sleep(acc_full(acc), (uint32_t)use & 1u, status, 1000)) break;
+            // the epilogue waits a whole tile: it sleeps, so as not to take issue slots from the
+            // dequant; the warp decides together (it synchronises below)
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(acc_full(acc), (uint32_t)use & 1u, status, 1000))) break;
             tc_fence_after();
             const int n = u.n0 + row;
+            if (P.ystage) {
+                // This warp's 32 rows of the output tile, [BN tokens][32 rows] FP16 in shared
+                // memory (64 contiguous bytes a token), then one TMA store by lane 0; rows
+                // past N and tokens past Mt are clipped by the store.  Only the warp
+                // synchronises, so a wait given up by one warp blocks no other.
+                const uint32_t ystg = sbase + L.y_off + (uint32_t)(q * BN * 64);
+                const float bn = a.bias && n < a.N ? __half2float(a.bias[n]) : 0.f;
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const __half h = __float2half_rn(__uint_as_float(v[j]) + bn);
+                        asm volatile("st.shared.u16 [%0], %1;" ::"r"(ystg + (uint32_t)(((c + j) * 32 + lane) * 2)),
+                                     "h"(__half_as_ushort(h))
+                                     : "memory");
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(acc_empty(acc));  // tensor memory read: the next tile's MMAs may start
+                fence_proxy_async();          // the staged rows, before the TMA reads them
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmY, ystg, u.n0 + q * 32, u.m0);
+                    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+                }
+                __syncwarp();  // the staging rows are free again
+                ++tl;
+                continue;
+            }
             for (int c = 0; c < BN; c += 16) {
                 uint32_t v[16];
                 tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c), v);
@@ -457,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(acc_empty(acc));
             ++tl;
         }
+        if (P.ystage && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // the output writes, complete
     } else {
         // ---------------------------------------------------------------- dequant
         // thread -> (row r, block h of the step): a warp owns the 32 rows of its
@@ -671,7 +717,8 @@ cudaError_t set_attr() {
 }
 
 template <int BITS, bool HAS_ZP>
-cudaError_t launch(const CUtensorMap& tx, const CUtensorMap& tw, const GemmParams& P, int grid, size_t smem, bool pdl,
+cudaError_t launch(const CUtensorMap& tx, const CUtensorMap& tw, const CUtensorMap& ty, const GemmParams& P, int grid,
+                   size_t smem, bool pdl,
                    cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
@@ -694,7 +741,7 @@ cudaError_t launch(const CUtensorMap& tx, const CUtensorMap& tw, const GemmParam
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<BITS, HAS_ZP>, tx, tw, P);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<BITS, HAS_ZP>, tx, tw, ty, P);
 }
 
 }  // namespace
@@ -739,11 +786,12 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
     P.ksteps = (a.K + BK - 1) / BK;
     P.split = p.k_splits > 1 ? p.k_splits : 1;
     P.x_wait = x_wait ? 1 : 0;
+    P.ystage = P.split == 1 && a.N % 8 == 0 ? 1 : 0;  // TMA store: 16-byte row pitch
     // Two K steps of X a copy where a whole row is one unit and its K steps pair
     // up: a copy costs the SM's TMA about the same time whatever its size, and one
     // 64-wide step of a 256-token tile is too little to keep the MMA fed.
-    P.xk = (P.split == 1 && a.K % (2 * BK) == 0 && a.K * 2 / 128 <= 256 && gemm_layout(P.BN, 2).nx >= 2) ? 2 : 1;
-    const GemmLayout L = gemm_layout(P.BN, P.xk);
+    P.xk = (P.split == 1 && a.K % (2 * BK) == 0 && a.K * 2 / 128 <= 256 && gemm_layout(P.BN, 2, P.ystage).nx >= 2) ? 2 : 1;
+    const GemmLayout L = gemm_layout(P.BN, P.xk, P.ystage);
     if (L.nx < 2 || L.total > kSmemBudget || (P.split > 1 && L.red_bytes > L.bar_off))
         return cudaErrorInvalidConfiguration;
 
@@ -756,15 +804,21 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
     e = encode_2d(&tw, a.Wq, 1, (uint64_t)a.K * a.bits / 8, (uint64_t)a.N, (uint64_t)a.K * a.bits / 8, 128u, (uint32_t)BM,
                   true);
     if (e != cudaSuccess) return e;
+    CUtensorMap ty = tw;  // Y [Mt x N] FP16, boxes of BN tokens x 32 rows (unused without ystage)
+    if (P.ystage) {
+        e = encode_2d(&ty, a.Y, 2, (uint64_t)a.N, (uint64_t)a.Mt, (uint64_t)a.N * 2, 32u, (uint32_t)P.BN, false);
+        if (e != cudaSuccess) return e;
+    }
     const int grid = p.grid_x;
     const bool zp = a.Z != nullptr;
     if (a.bits == 2)
-        return zp ? launch<2, true>(tx, tw, P, grid, L.total, pdl, st)
-                  : launch<2, false>(tx, tw, P, grid, L.total, pdl, st);
+        return zp ? launch<2, true>(tx, tw, ty, P, grid, L.total, pdl, st)
+                  : launch<2, false>(tx, tw, ty, P, grid, L.total, pdl, st);
     if (a.bits == 4)
-        return zp ? launch<4, true>(tx, tw, P, grid, L.total, pdl, st)
-                  : launch<4, false>(tx, tw, P, grid, L.total, pdl, st);
-    return zp ? launch<8, true>(tx, tw, P, grid, L.total, pdl, st) : launch<8, false>(tx, tw, P, grid, L.total, pdl, st);
+        return zp ? launch<4, true>(tx, tw, ty, P, grid, L.total, pdl, st)
+                  : launch<4, false>(tx, tw, ty, P, grid, L.total, pdl, st);
+    return zp ? launch<8, true>(tx, tw, ty, P, grid, L.total, pdl, st)
+              : launch<8, false>(tx, tw, ty, P, grid, L.total, pdl, st);
 }
 
 }  // namespace mnb
