@@ -514,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (warp & 3) * 32 + lane;
         const int h = (warp - kDqWarp0) >> 2;
         const uint32_t a_lane = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + L.a_col + (uint32_t)h * 16u;
-        constexpr int kPrefetch = 6;                // scale / zero-point loads in flight
+        constexpr int kPrefetch = 6;                // scale / zero-point loads in flight (steps; even)
+        static_assert(kPrefetch % 2 == 0, "steps are dequantized in pairs");
         constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
         int pstep = 0, xs = 0, cursor = blockIdx.x;  // xs: stages
         bool ok = true, waited = false;
@@ -539,11 +540,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 vmask |= ld ? (1u << v) : 0u;
             }
             int cur_p = 0;
+            // One row's block h of step v of the prefetch window (packed super-stage cur_p).
+            auto dq_step = [&](int v, int local, uint32_t(&out)[16]) {
+                // invalid block (row past N, K tail): scale 0 makes its products 0
+                const uint16_t sv = ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0;
+                // this step's bytes of row r: box li*kStepBytes/128, 16-byte chunk c0 (+1)
+                const int li = (local & (kps - 1));
+                const int pb = li * kStepBytes;
+                const int c0 = ((pb & 127) >> 4) + (BITS == 2 ? 0 : h * (kStepBytes / 32));
+                const unsigned char* prow =
+                    sptr + L.p_off + (uint32_t)cur_p * L.pstage + (uint32_t)(pb >> 7) * kPBox + (uint32_t)r * 128u;
+                if constexpr (BITS == 2) {  // the step's 16 bytes are one chunk; block h is its half h
+                    const Dq2Const d2 = dq2_const(zz[v], sv);
+                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
+                    dq_int2_natural(h ? pk.z : pk.x, d2, &out[0]);
+                    dq_int2_natural(h ? pk.w : pk.y, d2, &out[8]);
+                } else if constexpr (BITS == 4) {
+                    const DqConst dc = dq_const(zz[v], sv);
+                    const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
+                    const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) dq_int4_natural(wv[w], dc, &out[4 * w]);
+                } else {
+                    const DqConst dc = dq_const(zz[v], sv);
+                    const uint4 p0 = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
+                    const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((c0 + 1) ^ (r & 7)) << 4));
+                    const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], dc, &out[2 * w]);
+                }
+            };
+            // Steps in pairs: one stage (xk = 2) or two (xk = 1).  A pair's two blocks are
+            // independent, so their loads and arithmetic overlap, and their stores are
+            // waited for once.  Pairs start at even unit-local steps, so a packed
+            // super-stage (an even number of steps) never changes inside one.
             for (int i0 = u.i0; ok && i0 < u.i1; i0 += kPrefetch) {
 #pragma unroll
-                for (int v = 0; v < kPrefetch; ++v) {
+                for (int v = 0; v < kPrefetch; v += 2) {
                     const int i = i0 + v;
                     if (i >= u.i1) break;
+                    const bool two = i + 1 < u.i1;  // always with xk = 2 (an even number of steps)
                     const int local = i - u.i0;
                     // the warp decides together (it arrives once per warp below)
                     if ((local & (kps - 1)) == 0) {
@@ -552,60 +588,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         ++pstep;
                     }
-                    const int sx = xs % nx, sub = local % xk;
-                    if (sub == 0) {  // the MMA is done with the stage
-                        ok = __all_sync(0xffffffffu, mbar_wait_sleep(empty_x(sx), ((uint32_t)(xs / nx) & 1u) ^ 1u, status, 32));
-                        if (!ok) break;
-                    }
-                    const int s = sx * xk + sub;  // A step of the ring
-                    // invalid block (row past N, K tail): scale 0 makes its products 0
-                    const DqConst dc = dq_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
-                    Dq2Const d2 = {};
-                    if constexpr (BITS == 2) d2 = dq2_const(zz[v], ((vmask >> v) & 1u) ? (uint16_t)sc[v] : (uint16_t)0);
-                    // this step's bytes of row r: box li*kStepBytes/128, 16-byte chunk c0 (+1)
-                    const int li = (local & (kps - 1));
-                    const int pb = li * kStepBytes;
-                    const int c0 = ((pb & 127) >> 4) + (BITS == 2 ? 0 : h * (kStepBytes / 32));
-                    const unsigned char* prow =
-                        sptr + L.p_off + (uint32_t)cur_p * L.pstage + (uint32_t)(pb >> 7) * kPBox + (uint32_t)r * 128u;
-                    uint32_t out[16];
-                    if constexpr (BITS == 2) {  // the step's 16 bytes are one chunk; block h is its half h
-                        const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
-                        dq_int2_natural(h ? pk.z : pk.x, d2, &out[0]);
-                        dq_int2_natural(h ? pk.w : pk.y, d2, &out[8]);
-                    } else if constexpr (BITS == 4) {
-                        const uint4 pk = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
-                        const uint32_t wv[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) dq_int4_natural(wv[w], dc, &out[4 * w]);
-                    } else {
-                        const uint4 p0 = *reinterpret_cast<const uint4*>(prow + ((c0 ^ (r & 7)) << 4));
-                        const uint4 p1 = *reinterpret_cast<const uint4*>(prow + (((c0 + 1) ^ (r & 7)) << 4));
-                        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], dc, &out[2 * w]);
-                    }
-                    // the block's 32 FP16 values: 16 columns of row r in A step s
-                    tmem_st16(a_lane + (uint32_t)(s * kACols), out);
-                    const bool last_sub = sub == xk - 1;
-                    if (last_sub) {  // the stage's stores complete, before the MMA thread is told
-                        tmem_wait_st();
-                        tc_fence_before();
-                    }
+                    const bool split2 = xk == 1 && two;  // the second step is a stage of its own
+                    const int sx0 = xs % nx, sx1 = split2 ? (xs + 1) % nx : sx0;
+                    const int s0 = sx0 * xk, s1 = split2 ? sx1 : s0 + 1;  // A steps of the ring
+                    // the MMA is done with the stage(s)
+                    ok = __all_sync(0xffffffffu, mbar_wait_sleep(empty_x(sx0), ((uint32_t)(xs / nx) & 1u) ^ 1u, status, 32));
+                    if (ok && split2)
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait_sleep(empty_x(sx1), ((uint32_t)((xs + 1) / nx) & 1u) ^ 1u, status, 32));
+                    if (!ok) break;
+                    uint32_t out0[16], out1[16];
+                    dq_step(v, local, out0);
+                    if (two) dq_step(v + 1, local + 1, out1);
+                    // each block's 32 FP16 values: 16 columns of row r in its A step
+                    tmem_st16(a_lane + (uint32_t)(s0 * kACols), out0);
+                    if (two) tmem_st16(a_lane + (uint32_t)(s1 * kACols), out1);
+                    tmem_wait_st();  // the stores complete, before the MMA thread is told
+                    tc_fence_before();
                     __syncwarp();
                     if (dl == 0) {  // one arrival per warp: its lanes are ordered before lane 0 here
-                        if (last_sub) mbar_arrive(full_w(sx));
-                        if ((local & (kps - 1)) == kps - 1 || i == u.i1 - 1) mbar_arrive(empty_p(cur_p));
+                        mbar_arrive(full_w(sx0));
+                        if (split2) mbar_arrive(full_w(sx1));
+                        if (!two || ((local + 1) & (kps - 1)) == kps - 1 || i + 1 == u.i1 - 1)
+                            mbar_arrive(empty_p(cur_p));  // the packed super-stage is consumed
                     }
-                    if (last_sub) ++xs;
-                    {  // refill this prefetch slot with step i + kPrefetch (after the fence, which
-                       // would otherwise wait for these loads)
-                        const int blk = 2 * (i + kPrefetch) + h;
-                        const bool ld = row_ok && blk < nblk && i + kPrefetch < u.i1;
+                    xs += split2 ? 2 : 1;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {  // refill the prefetch slots with steps i + t + kPrefetch
+                        const int it = i + t + kPrefetch;
+                        const int blk = 2 * it + h;
+                        const bool ld = row_ok && blk < nblk && it < u.i1;
                         const int bc = ld ? blk : 0;
-                        sc[v] = (uint32_t)__ldg(srow + bc);
-                        if (HAS_ZP) zz[v] = (uint32_t)__ldg(zrow + bc);
-                        vmask = ld ? (vmask | (1u << v)) : (vmask & ~(1u << v));
+                        sc[v + t] = (uint32_t)__ldg(srow + bc);
+                        if (HAS_ZP) zz[v + t] = (uint32_t)__ldg(zrow + bc);
+                        vmask = ld ? (vmask | (1u << (v + t))) : (vmask & ~(1u << (v + t)));
                     }
                 }
             }
