@@ -273,14 +273,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nx = L.nx, np = L.np;
 
     const uint32_t bars = sbase + L.bar_off;
-    // Stage s: full_x (X landed), full_w (its A steps written), empty (the MMAs
-    // are done with both).  The single MMA thread then waits twice and commits
-    // once per stage: each of those costs it a few hundred cycles, as much as
-    // issuing several MMAs.
+    // Stage s: full_x (X landed and its A steps written: the X producer's
+    // arrival with the copy's bytes, one arrival per dequant warp), empty_x (the
+    // MMAs are done with both).  The single MMA thread then waits once and
+    // commits once per stage: each of those costs it a few hundred cycles, as
+    // much as issuing several MMAs.
     auto full_x = [&](int s) { return bars + 8u * s; };
     auto empty_x = [&](int s) { return bars + 8u * (nx + s); };
-    auto full_w = [&](int s) { return bars + 8u * (2 * nx + s); };
-    const int b0 = 3 * nx;
+    const int b0 = 2 * nx;
     auto full_p = [&](int j) { return bars + 8u * (b0 + j); };
     auto empty_p = [&](int j) { return bars + 8u * (b0 + np + j); };
     auto acc_full = [&](int a) { return bars + 8u * (b0 + 2 * np + a); };
@@ -298,9 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nx; ++s) {
-            mbar_init(full_x(s), 1);
+            mbar_init(full_x(s), 1 + kDqWarps);
             mbar_init(empty_x(s), 1);
-            mbar_init(full_w(s), kDqWarps);
         }
         for (int j = 0; j < np; ++j) {
             mbar_init(full_p(j), 1);
@@ -397,7 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = f16_idesc(BM, BN);
-            int xs = 0, tl = 0, cursor = blockIdx.x;  // xs: stages
+            int sx = 0, tl = 0, cursor = blockIdx.x;  // sx: ring slot of the stage, ph: its phase
+            uint32_t ph = 0;
             bool ok = true;
             Unit u;
             while (ok && next_unit(P, cursor, u)) {
@@ -407,11 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 const int nkx = (u.i1 - u.i0) / xk;
                 const int nst = nkx + (u.lora ? 1 : 0);
-                for (int i = 0; i < nst; ++i, ++xs) {
-                    const int sx = xs % nx;
-                    const uint32_t ph = (uint32_t)(xs / nx) & 1u;
+                for (int i = 0; i < nst; ++i) {
                     if (!(ok = mbar_wait(full_x(sx), ph, status))) break;
-                    if (!(ok = mbar_wait(full_w(sx), ph, status))) break;
                     tc_fence_after();
                     // K = 16 a MMA: 8 columns of A, 32 bytes of an X row (2 in the descriptor's address field)
                     uint32_t a_tmem = tmem_base + L.a_col + (uint32_t)(sx * xk * kACols);
@@ -429,6 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     tc_commit(empty_x(sx));  // the X slot and the stage's A steps
+                    if (++sx == nx) {
+                        sx = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (ok) tc_commit(acc_full(acc));
                 ++tl;
@@ -607,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (dl == 0) {  // one arrival per warp: its lanes are ordered before lane 0 here
-                        mbar_arrive(full_w(sx0));
-                        if (split2) mbar_arrive(full_w(sx1));
+                        mbar_arrive(full_x(sx0));
+                        if (split2) mbar_arrive(full_x(sx1));
                         if (!two || ((local + 1) & (kps - 1)) == kps - 1 || i + 1 == u.i1 - 1)
                             mbar_arrive(empty_p(cur_p));  // the packed super-stage is consumed
                     }
@@ -670,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_st();       // the adapter rows in tensor memory, likewise
                 tc_fence_before();
                 __syncwarp();
-                if (dl == 0) mbar_arrive(full_w(sx));
+                if (dl == 0) mbar_arrive(full_x(sx));
                 ++xs;
             }
         }
