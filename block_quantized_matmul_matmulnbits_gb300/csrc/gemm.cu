@@ -16,10 +16,15 @@
 //  * The K loop runs in stages of xk 64-wide K steps (xk = 2 when a CTA takes
 //    whole rows of an even number of K steps, else 1).  A stage is one X slot
 //    in shared memory plus xk dequantized A steps in tensor memory, with one
-//    barrier each for "X landed", "A written" and "MMAs done": the single MMA
-//    thread spends a few hundred cycles on every wait and every commit, as
-//    much as on issuing several MMAs, so it waits twice and commits once per
-//    stage instead of per K step.
+//    "full" barrier (the X copy's bytes and every dequant warp's arrival) and
+//    one "empty" barrier (the MMAs are done): the single MMA thread spends a
+//    few hundred cycles on every wait and every commit, as much as on issuing
+//    several MMAs, so it waits once and commits once per stage instead of
+//    twice each per K step.
+//  * Each dequant thread takes its block of both K steps of a stage together:
+//    two independent chains of loads and arithmetic, one tensor-memory store
+//    wait.  The dequant warps are few (two a scheduler) and latency-bound, so
+//    that overlap, not the arithmetic, sets their rate.
 //  * Two producer warps, so that the weight stream runs ahead of X: warp 0
 //    copies the packed weights of 128 rows in super-stages of 128 or 256
 //    bytes per row (TMA boxes of 128 rows x 128 bytes, 128-byte swizzle),
