@@ -100,6 +100,9 @@ int device_setup(int* sm_count, unsigned int** status = nullptr) {
 
 int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// Idle SMs beside a prefill grid from which the LoRA down projection runs there.
+constexpr int kIdleDownCtas = 8;
+
 // Single-token decode kernel: rows split evenly over one CTA per SM, the
 // adapter (if any) in the same launch.
 void plan_decode(const mnb_desc& d, int rank, int sms, mnb_plan_info* p) {
@@ -292,16 +295,17 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     const uint8_t* Bq8 = rank > 0 && ad.q8 ? static_cast<const uint8_t*>(ad.Bq) : nullptr;
     const __half* Bs8 = Bq8 ? static_cast<const __half*>(ad.Bs) : nullptr;
     const uint8_t* Bz8 = Bq8 ? static_cast<const uint8_t*>(ad.Bz) : nullptr;
-    auto launch_down = [&](const __half* Xh, __half* Th, bool early, cudaStream_t st) {
+    unsigned int* status = nullptr;  // the device's status word (set up below)
+    auto launch_down = [&](const __half* Xh, __half* Th, bool early, cudaStream_t st, int max_ctas = 0) {
         return ad.q8 ? mnb::lora_down_q8_launch(Xh, static_cast<const uint8_t*>(ad.Aq),
                                                 static_cast<const __half*>(ad.As),
                                                 static_cast<const uint8_t*>(ad.Az), Th, (int)Mt, (int)d.K, early, st)
-                     : mnb::lora_down_launch(Xh, static_cast<const __half*>(ad.A), Th, (int)Mt, (int)d.K, early, st);
+                     : mnb::lora_down_launch(Xh, static_cast<const __half*>(ad.A), Th, (int)Mt, (int)d.K, early, st,
+                                             max_ctas, status);
     };
 
     mnb_plan_info p;
     int sms = 0;
-    unsigned int* status = nullptr;
     if (Mt > 0 && d.N > 0) {
         const int rc = device_setup(&sms, &status);
         if (rc != MNB_OK) return rc;
@@ -391,7 +395,11 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     }
     const bool lora_kernel = rank > 0;
     if (lora_kernel) {
-        e = launch_down(Xh, Th, early, st);
+        // A prefill grid well short of the SM count leaves SMs idle: the down
+        // projection runs there, beside the prefill kernel (which needs T only for
+        // its last stage), instead of first holding SMs that kernel waits for.
+        const int idle = p.route == MNB_ROUTE_GEMM && p.k_splits <= 1 ? sms - p.grid_x : 0;
+        e = launch_down(Xh, Th, early, st, idle >= kIdleDownCtas ? idle : 0);
         if (e != cudaSuccess) return MNB_ERR_CUDA;
     }
     const bool pdl = lora_kernel || early;

@@ -256,12 +256,129 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
     cluster_sync_all();  // keep every CTA's shared memory alive until all peers have read it
 }
 
+// The same projection for the SMs a prefill grid leaves idle (FP16 A, more than
+// 16 token rows): no cluster -- its CTAs could not be placed together there -- so a
+// CTA takes all of K for groups of 64 token rows, gridDim.x groups apart.  K runs
+// in pieces of 256, double-buffered: X by four TMA boxes of 64 rows x 64 K
+// (128-byte swizzle) on an mbarrier, A by cp.async into padded rows, the copies of
+// piece p + 1 in flight while piece p is multiplied.  One CTA sums a row's whole K
+// in a fixed order, so T is the same bits every run.
+constexpr int kRPiece = 256;                          // K per piece
+constexpr int kRXBytes = kTok * kRPiece * 2;          // X of a piece: 4 boxes of 8 KB
+constexpr int kRABytes = kRPiece * kPitchA * 2;       // A of a piece, padded rows
+constexpr int kRBuf = kRXBytes + kRABytes;
+static_assert(kRABytes % 1024 == 0, "the next buffer's X boxes stay 1024-aligned");
+constexpr int kRowsSmem = 2 * kRBuf + 64 + 1024;      // two buffers, two barriers, alignment
+
+__global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                              const __half* __restrict__ A, __half* __restrict__ T,
+                                                              int Mt, int K, unsigned int* status) {
+    extern __shared__ unsigned char lds_raw[];
+    const uint32_t base_raw = smem_u32(lds_raw);
+    const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
+    unsigned char* sptr = lds_raw + (sbase - base_raw);
+    const uint32_t bars = sbase + 2u * kRBuf;
+    auto xbuf = [&](int b) { return sbase + (uint32_t)(b * kRBuf); };
+    auto abuf = [&](int b) { return reinterpret_cast<__half*>(sptr + b * kRBuf + kRXBytes); };
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wrow = warp * 16;  // this warp's 16 token rows of the group
+    const int npiece = K / kRPiece;
+    if (tid == 0) {
+        mbar_init(bars, 1);
+        mbar_init(bars + 8u, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
+    }
+    __syncthreads();
+    bool waited = false, ok = true;
+    int pc = 0;  // pieces staged so far: buffer pc & 1, its barrier's phase (pc >> 1) & 1
+    for (int grp = blockIdx.x; ok && grp * kTok < Mt; grp += gridDim.x) {
+        const int tokb = grp * kTok;
+        // issue the copies of K piece p into buffer b (A first: a weight, not behind the wait)
+        auto stage = [&](int p, int b) {
+            const int kb = p * kRPiece;
+            __half* a_s = abuf(b);
+            for (int idx = tid; idx < kRPiece * 4; idx += blockDim.x) {
+                const int row = idx >> 2, c = idx & 3;
+                cp_async16(smem_u32(a_s + row * kPitchA + c * 8), A + (size_t)(kb + row) * 32 + c * 8, 16);
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+            if (!waited) {
+                pdl_wait();
+                pdl_launch_dependents();  // the work before this kernel is complete: X is readable
+                waited = true;
+            }
+            if (tid == 0) {  // rows past Mt read as zero
+                const uint32_t bar = bars + 8u * (uint32_t)b;
+                mbar_arrive_tx(bar, (uint32_t)kRXBytes);
+#pragma unroll
+                for (int q = 0; q < kRPiece / 64; ++q)
+                    tma_load_2d(xbuf(b) + (uint32_t)(q * kTok * 128), &tmX, kb + 64 * q, tokb, bar);
+            }
+        };
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+        stage(0, pc & 1);
+        for (int p = 0; p < npiece; ++p, ++pc) {
+            const int b = pc & 1;
+            if (p + 1 < npiece) {
+                stage(p + 1, (pc + 1) & 1);
+                asm volatile("cp.async.wait_group 1;" ::: "memory");  // A of piece p has landed
+            } else {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            }
+            ok = mbar_wait(bars + 8u * (uint32_t)b, (uint32_t)(pc >> 1) & 1u, status, false);  // X of piece p
+            ok = __syncthreads_and(ok) != 0;  // the block decides together
+            if (!ok) break;
+            const __half* a_s = abuf(b);
+            const int mat = lane >> 3, row8 = lane & 7;
+            const int xr = wrow + (mat & 1) * 8 + row8;  // this lane's X row for ldmatrix
+#pragma unroll 4
+            for (int kk = 0; kk < kRPiece; kk += 16) {
+                uint32_t a0, a1, a2, a3;  // X rows wrow .. +15, K columns kk .. kk+15 (box kk / 64, swizzled)
+                const int chunk = ((kk & 63) >> 3) + (mat >> 1);
+                ldsm_x4(xbuf(b) + (uint32_t)((kk >> 6) * kTok * 128 + xr * 128 + ((chunk ^ (xr & 7)) << 4)), a0, a1,
+                        a2, a3);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(smem_u32(a_s + (kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8), b0, b1,
+                              b2, b3);
+                    mma_16816(acc[2 * h], a0, a1, a2, a3, b0, b1);
+                    mma_16816(acc[2 * h + 1], a0, a1, a2, a3, b2, b3);
+                }
+            }
+            __syncthreads();  // the buffer is refilled by the stage after next
+        }
+        if (!ok) break;
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int r = nt * 8 + 2 * t;
+            const int m0 = tokb + wrow + g, m1 = m0 + 8;
+            if (m0 < Mt)
+                *reinterpret_cast<__half2*>(&T[(size_t)m0 * 32 + r]) = __floats2half2_rn(acc[nt][0], acc[nt][1]);
+            if (m1 < Mt)
+                *reinterpret_cast<__half2*>(&T[(size_t)m1 * 32 + r]) = __floats2half2_rn(acc[nt][2], acc[nt][3]);
+        }
+    }
+    if (!waited) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
+}
+
 }  // namespace
 
 cudaError_t lora_down_prepare() {
     cudaError_t e = cudaFuncSetAttribute(lora_down_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(lora_down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lora_down_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem);
     return e;
 }
 
@@ -293,7 +410,25 @@ cudaError_t launch_down(const __half* X, const DownWeight& W, bool q8, __half* T
 
 }  // namespace
 
-cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st) {
+cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st,
+                             int max_ctas, unsigned int* status) {
+    if (max_ctas > 0 && status && Mt > 16 && K % kRPiece == 0) {  // the rows kernel on at most max_ctas SMs
+        CUtensorMap tx;  // X [Mt x K] FP16, boxes of 64 rows x 64 K, 128-byte swizzle
+        cudaError_t e = encode_2d(&tx, X, 2, (uint64_t)K, (uint64_t)Mt, (uint64_t)K * 2, 64u, (uint32_t)kTok, true);
+        if (e != cudaSuccess) return e;
+        const int groups = (Mt + kTok - 1) / kTok;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(groups < max_ctas ? groups : max_ctas);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = kRowsSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        return cudaLaunchKernelEx(&cfg, lora_down_rows_kernel, tx, A, T, Mt, K, status);
+    }
     return launch_down(X, DownWeight{A, nullptr, nullptr, nullptr}, false, T, Mt, K, pdl, st);
 }
 
