@@ -136,3 +136,34 @@ def test_prefill_deterministic_and_guarded(env):
     assert torch.all(Ybuf[:pad] == 7.0) and torch.all(Ybuf[pad + 200 * 260:] == 7.0)
     Y64, bound = oracle_ref(inp)
     assert_within_tolerance(bits_of(Y), Y64, bound, "guarded prefill")
+
+
+@pytest.mark.parametrize("M", [100, 64])
+def test_prefill_adapter_down_on_idle_sms_exact(env, M):
+    """A one-wave prefill grid well short of the SM count (80 weight tiles): the LoRA down
+    projection runs on the idle SMs, one CTA summing all of K for a group of 64 token rows
+    (M=100: a full group and a ragged one).  Exact arithmetic, so T and Y match the oracle
+    bit for bit."""
+    torch, mnb = env
+    rng = np.random.default_rng(605 + M)
+    K, N = 512, 10240
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    h = mnb.mnb_create(N, K, 4, 32, 32)
+    try:
+        p = mnb.mnb_plan(h, 1, M, 32, sms)
+    finally:
+        mnb.mnb_destroy(h)
+    assert p["route"] == mnb.ROUTE_GEMM and p["k_splits"] <= 1 and sms - p["grid_x"] >= 8
+    x = np.zeros((1, M, K))
+    for m in range(M):
+        idx = rng.choice(K, 8, replace=False)
+        x[0, m, idx] = rng.choice([-1.0, 1.0], 8)
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=605 + M, zp_range=(0, 15), rank=32)
+    inp.X = x.astype(np.float16).view(np.uint16)
+    inp.scales = np.ldexp(1.0, rng.integers(-8, -4, size=(N, K // 32))).astype(np.float16).view(np.uint16)
+    inp.A = (rng.integers(-3, 4, size=(K, 32)) / 16.0).astype(np.float16).view(np.uint16)
+    inp.B = (rng.integers(-3, 4, size=(N, 32)) / 16.0).astype(np.float16).view(np.uint16)
+    Y, _, route = run_gpu(mnb, torch, inp)
+    assert route == mnb.ROUTE_GEMM
+    Y16, _, _ = oracle.run(inp.X2d, inp.Wq, inp.scales, inp.zp, inp.A, inp.B, N, K, 4)
+    assert np.array_equal(bits_of(Y).reshape(M, N), Y16)
