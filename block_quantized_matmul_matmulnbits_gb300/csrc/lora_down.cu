@@ -23,6 +23,12 @@
 // after its own griddepcontrol.wait: the matmul kernel queued after it then
 // starts only once the work before this kernel has completed, so it may read
 // X at once and waits (griddepcontrol.wait) only for T.
+//
+// Ahead of a prefill grid that leaves SMs idle, a second kernel takes the same
+// projection onto those SMs only (lora_down_rows_kernel, below): a cluster's
+// CTAs could not be placed together on scattered idle SMs, so each CTA sums all
+// of K for its groups of 64 token rows, with X fed by TMA.  It then runs beside
+// the prefill kernel, which needs T only at its last stage.
 #include "common.cuh"
 #include "mnb_internal.h"
 
