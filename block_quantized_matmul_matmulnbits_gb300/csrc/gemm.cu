@@ -216,6 +216,7 @@ struct GemmParams {
     int split;      // CTAs (one cluster) sharing a tile along K; 1 = persistent over tiles
     int xk;         // K steps per X copy: 2 = one 3-D box of two 64-wide K slices (split 1, even K steps)
     int ystage;     // output tile through shared memory and a TMA store (split 1, N % 8 == 0)
+    int tpre;       // T of a CTA's first tile staged early by the epilogue warps (ystage, rank > 0)
     int x_wait;     // X may be written by the work queued before this grid: wait for it
 };
 
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acc_empty = [&](int a) { return bars + 8u * (b0 + 2 * np + 2 + a); };
     const uint32_t drain = bars + 8u * (b0 + 2 * np + 4);
     const uint32_t tmem_slot = drain + 8u;
+    const uint32_t t_ready = drain + 16u;  // T of the first unit staged (tpre)
     auto xslot = [&](int s) { return sbase + (uint32_t)s * L.xslot; };
 
     const GemmArgs& a = P.a;
@@ -315,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acc_empty(i), kEpiThreads);
         }
         mbar_init(drain, 1);
+        mbar_init(t_ready, kEpiThreads / 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t a_tmem = tmem_base + L.a_col + (uint32_t)(sx * xk * kACols);
                     uint64_t bd = sw128_desc(xslot(sx));
                     if (i >= nkx) {  // the LoRA step: K = 32
+                        if (P.tpre && tl == 0) bd = sw128_desc(sbase + L.y_off);  // T staged by the epilogue warps
                         tc_mma_ta(d_tmem, a_tmem, bd, idesc, 1u);
                         tc_mma_ta(d_tmem, a_tmem + 8u, bd + 2u, idesc, 1u);
                     } else {
@@ -451,6 +455,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         Unit u;
         while (next_unit(P, cursor, u)) {
             const int acc = tl % L.nacc, use = tl / L.nacc;
+            if (P.tpre && tl == 0 && u.lora) {
+                // T of the CTA's first tile into the output staging, unused until this tile's
+                // epilogue, while the K loop runs: the LoRA stage then copies nothing
+                pdl_wait();  // T is written by the LoRA down kernel queued before this grid
+                const uint32_t tst = sbase + L.y_off;
+                for (int idx = threadIdx.x - 64; idx < BN * 4; idx += kEpiThreads) {  // warps 2..5
+                    const int tr = idx >> 2, c = idx & 3;
+                    const int m = u.m0 + tr;
+                    const uint4 v = m < a.Mt ? *reinterpret_cast<const uint4*>(a.T + (size_t)m * 32 + c * 8)
+                                             : make_uint4(0, 0, 0, 0);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(tst + swz128(tr, c)), "r"(v.x),
+                                 "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
+                }
+                fence_proxy_async();  // before the MMA reads it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(t_ready);
+            }
             // the epilogue waits a whole tile: it sleeps, so as not to take issue slots from the
             // dequant; the warp decides together (it synchronises below)
             if (!__all_sync(0xffffffffu, mbar_wait_sleep(acc_full(acc), (uint32_t)use & 1u, status, 1000))) break;
@@ -523,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kPrefetch = 6;                // scale / zero-point loads in flight (steps; even)
         static_assert(kPrefetch % 2 == 0, "steps are dequantized in pairs");
         constexpr uint32_t kDefaultZp = 1u << (BITS - 1);
-        int pstep = 0, xs = 0, cursor = blockIdx.x;  // xs: stages
+        int pstep = 0, xs = 0, du = 0, cursor = blockIdx.x;  // xs: stages, du: units
         bool ok = true, waited = false;
         Unit u;
         while (ok && next_unit(P, cursor, u)) {
@@ -635,7 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sx = xs % nx, s = sx * xk;
                 ok = __all_sync(0xffffffffu, mbar_wait(empty_x(sx), ((uint32_t)(xs / nx) & 1u) ^ 1u, status));
                 if (!ok) break;
-                if (!waited) {
+                const bool t_staged = P.tpre && du == 0;  // T already in the output staging
+                if (!waited && !t_staged) {
                     pdl_wait();  // T is written by the LoRA down kernel queued before this grid
                     waited = true;
                 }
@@ -663,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tmem_st16(a_lane + (uint32_t)(s * kACols), o);  // h == 0: columns 0..15
                 }
-                for (int idx = d; idx < BN * 4; idx += kDqThreads) {  // B operand: T[m, 0:32]
+                for (int idx = t_staged ? BN * 4 : d; idx < BN * 4; idx += kDqThreads) {  // B operand: T[m, 0:32]
                     const int tr = idx >> 2, c = idx & 3;
                     const int m = u.m0 + tr;
                     const uint4 v = m < a.Mt ? *reinterpret_cast<const uint4*>(a.T + (size_t)m * 32 + c * 8)
@@ -675,10 +698,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async();  // T in the X slot, before the MMA reads it
                 tmem_wait_st();       // the adapter rows in tensor memory, likewise
                 tc_fence_before();
+                if (t_staged) {  // T staged by the epilogue warps (their arrival orders it before ours)
+                    ok = __all_sync(0xffffffffu, mbar_wait(t_ready, 0, status));
+                    if (!ok) break;
+                }
                 __syncwarp();
                 if (dl == 0) mbar_arrive(full_x(sx));
                 ++xs;
             }
+            ++du;
         }
     }
 
@@ -809,6 +837,7 @@ cudaError_t gemm_launch(const GemmArgs& a, const mnb_plan_info& p, bool pdl, boo
     P.split = p.k_splits > 1 ? p.k_splits : 1;
     P.x_wait = x_wait ? 1 : 0;
     P.ystage = P.split == 1 && a.N % 8 == 0 ? 1 : 0;  // TMA store: 16-byte row pitch
+    P.tpre = P.ystage && a.rank > 0 ? 1 : 0;
     // Two K steps of X a copy where a whole row is one unit and its K steps pair
     // up: a copy costs the SM's TMA about the same time whatever its size, and one
     // 64-wide step of a 256-token tile is too little to keep the MMA fed.
