@@ -265,16 +265,18 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
 // The same projection for the SMs a prefill grid leaves idle (FP16 A, more than
 // 16 token rows): no cluster -- its CTAs could not be placed together there -- so a
 // CTA takes all of K for groups of 64 token rows, gridDim.x groups apart.  K runs
-// in pieces of 256, double-buffered: X by four TMA boxes of 64 rows x 64 K
-// (128-byte swizzle) on an mbarrier, A by cp.async into padded rows, the copies of
-// piece p + 1 in flight while piece p is multiplied.  One CTA sums a row's whole K
+// in pieces of 256 through a ring of four buffers: X by four TMA boxes of 64 rows x
+// 64 K (128-byte swizzle) on an mbarrier, A by cp.async into padded rows, the
+// copies of pieces p + 1 .. p + 3 in flight while piece p is multiplied (a CTA
+// streams its rows from HBM alone, so it needs many bytes in flight).  One CTA sums a row's whole K
 // in a fixed order, so T is the same bits every run.
 constexpr int kRPiece = 256;                          // K per piece
 constexpr int kRXBytes = kTok * kRPiece * 2;          // X of a piece: 4 boxes of 8 KB
 constexpr int kRABytes = kRPiece * kPitchA * 2;       // A of a piece, padded rows
 constexpr int kRBuf = kRXBytes + kRABytes;
 static_assert(kRABytes % 1024 == 0, "the next buffer's X boxes stay 1024-aligned");
-constexpr int kRowsSmem = 2 * kRBuf + 64 + 1024;      // two buffers, two barriers, alignment
+constexpr int kRBufs = 4;                             // ring of K pieces
+constexpr int kRowsSmem = kRBufs * kRBuf + 64 + 1024;  // buffers, barriers, alignment
 
 __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX,
                                                               const __half* __restrict__ A, __half* __restrict__ T,
@@ -283,21 +285,20 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
     const uint32_t base_raw = smem_u32(lds_raw);
     const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
     unsigned char* sptr = lds_raw + (sbase - base_raw);
-    const uint32_t bars = sbase + 2u * kRBuf;
+    const uint32_t bars = sbase + (uint32_t)(kRBufs * kRBuf);
     auto xbuf = [&](int b) { return sbase + (uint32_t)(b * kRBuf); };
     auto abuf = [&](int b) { return reinterpret_cast<__half*>(sptr + b * kRBuf + kRXBytes); };
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wrow = warp * 16;  // this warp's 16 token rows of the group
     const int npiece = K / kRPiece;
     if (tid == 0) {
-        mbar_init(bars, 1);
-        mbar_init(bars + 8u, 1);
+        for (int b = 0; b < kRBufs; ++b) mbar_init(bars + 8u * (uint32_t)b, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmX)) : "memory");
     }
     __syncthreads();
     bool waited = false, ok = true;
-    int pc = 0;  // pieces staged so far: buffer pc & 1, its barrier's phase (pc >> 1) & 1
+    int pc = 0;  // pieces consumed so far: piece pc is in buffer pc % kRBufs, its barrier's phase (pc / kRBufs) & 1
     for (int grp = blockIdx.x; ok && grp * kTok < Mt; grp += gridDim.x) {
         const int tokb = grp * kTok;
         // issue the copies of K piece p into buffer b (A first: a weight, not behind the wait)
@@ -327,16 +328,23 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-        stage(0, pc & 1);
+        for (int p = 0; p < kRBufs - 1 && p < npiece; ++p) stage(p, (pc + p) % kRBufs);
         for (int p = 0; p < npiece; ++p, ++pc) {
-            const int b = pc & 1;
-            if (p + 1 < npiece) {
-                stage(p + 1, (pc + 1) & 1);
-                asm volatile("cp.async.wait_group 1;" ::: "memory");  // A of piece p has landed
-            } else {
+            const int b = pc % kRBufs;
+            // the buffer of piece p + 3 was last read by piece p - 1 (the block passed the
+            // barrier at the end of that piece)
+            if (p + kRBufs - 1 < npiece) stage(p + kRBufs - 1, (pc + kRBufs - 1) % kRBufs);
+            // A of piece p has landed once at most the groups committed after it are pending
+            const int ahead = min(kRBufs - 1, npiece - 1 - p);
+            if (ahead >= 3)
+                asm volatile("cp.async.wait_group 3;" ::: "memory");
+            else if (ahead == 2)
+                asm volatile("cp.async.wait_group 2;" ::: "memory");
+            else if (ahead == 1)
+                asm volatile("cp.async.wait_group 1;" ::: "memory");
+            else
                 asm volatile("cp.async.wait_group 0;" ::: "memory");
-            }
-            ok = mbar_wait(bars + 8u * (uint32_t)b, (uint32_t)(pc >> 1) & 1u, status, false);  // X of piece p
+            ok = mbar_wait(bars + 8u * (uint32_t)b, (uint32_t)(pc / kRBufs) & 1u, status, false);  // X of piece p
             ok = __syncthreads_and(ok) != 0;  // the block decides together
             if (!ok) break;
             const __half* a_s = abuf(b);
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
                     mma_16816(acc[2 * h + 1], a0, a1, a2, a3, b2, b3);
                 }
             }
-            __syncthreads();  // the buffer is refilled by the stage after next
+            __syncthreads();  // this buffer is refilled kRBufs - 1 pieces on
         }
         if (!ok) break;
         const int g = lane >> 2, t = lane & 3;
