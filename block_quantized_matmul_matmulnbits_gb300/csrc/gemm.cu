@@ -160,13 +160,13 @@ __host__ __device__ inline uint32_t g_align(uint32_t x, uint32_t a) { return (x 
 // CTA of a split runs one unit, and once its accumulator is complete every
 // copy into the ring has landed and every read of it has finished.
 // Two rings in shared memory: stages (nx slots of xk K steps of X) and
-// packed-weight super-stages (np slots).  The stages' dequantized A steps
-// (nw = nx xk) live in tensor memory beside the accumulators: columns
-// [0, nacc BN) hold one or two 128 x BN FP32 accumulators, A step t of the
-// ring starts at column a_col + 32 t.
+// packed-weight super-stages (np slots), then (ystage) the output staging.  The
+// stages' dequantized A steps (nw = nx xk) live in tensor memory beside the
+// accumulators: columns [0, nacc BN) hold one or two 128 x BN FP32
+// accumulators, A step t of the ring starts at column a_col + 32 t.
 struct GemmLayout {
     uint32_t xslot;    // bytes of one X slot (BN rows x 128 B, 1024-aligned)
-    int nx, nw, np;    // slots of the X, A and packed rings
+    int nx, nw, np;    // stages (X slots), their A steps in tensor memory, packed super-stages
     int pboxes;        // TMA boxes per packed super-stage (128 packed bytes of each row per box)
     uint32_t pstage;   // bytes of one packed super-stage
     int nacc;          // accumulators (two: a tile's epilogue runs under the next tile's MMAs)
@@ -180,8 +180,7 @@ __host__ __device__ inline GemmLayout gemm_layout(int BN, int xk, int ystage) {
     GemmLayout L;
     L.xslot = g_align((uint32_t)(xk * BN) * 128u, 1024u);
     // Small token tiles (decode shapes) are bound by the weight stream: deep
-    // packed ring, large super-stages.  Large tiles keep four X slots and four
-    // A slots (the dequant runs up to four steps ahead of the MMA).
+    // packed ring, large super-stages.  Large tiles give the space to the stages.
     L.pboxes = BN <= 64 ? 2 : 1;
     L.pstage = (uint32_t)(L.pboxes * kPBox);
     L.np = BN <= 64 ? 4 : 2;
