@@ -299,7 +299,8 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     auto launch_down = [&](const __half* Xh, __half* Th, bool early, cudaStream_t st, int max_ctas = 0) {
         return ad.q8 ? mnb::lora_down_q8_launch(Xh, static_cast<const uint8_t*>(ad.Aq),
                                                 static_cast<const __half*>(ad.As),
-                                                static_cast<const uint8_t*>(ad.Az), Th, (int)Mt, (int)d.K, early, st)
+                                                static_cast<const uint8_t*>(ad.Az), Th, (int)Mt, (int)d.K, early, st,
+                                                max_ctas, status)
                      : mnb::lora_down_launch(Xh, static_cast<const __half*>(ad.A), Th, (int)Mt, (int)d.K, early, st,
                                              max_ctas, status);
     };

@@ -273,14 +273,18 @@ __global__ void __launch_bounds__(128) lora_down_kernel(const __half* __restrict
 constexpr int kRPiece = 256;                          // K per piece
 constexpr int kRXBytes = kTok * kRPiece * 2;          // X of a piece: 4 boxes of 8 KB
 constexpr int kRABytes = kRPiece * kPitchA * 2;       // A of a piece, padded rows
+constexpr int kRPitchR = kRPiece + 8;                 // INT8 A: halfs per dequantized rank row of a piece
+static_assert(32 * kRPitchR * 2 <= kRABytes, "a dequantized INT8 A piece fits the FP16 one's space");
+constexpr int kRQItems = 32 * kRPiece / 16 / 128;     // INT8 A: 16-code items per thread and piece
 constexpr int kRBuf = kRXBytes + kRABytes;
 static_assert(kRABytes % 1024 == 0, "the next buffer's X boxes stay 1024-aligned");
 constexpr int kRBufs = 4;                             // ring of K pieces
 constexpr int kRowsSmem = kRBufs * kRBuf + 64 + 1024;  // buffers, barriers, alignment
 
-__global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX,
-                                                              const __half* __restrict__ A, __half* __restrict__ T,
-                                                              int Mt, int K, unsigned int* status) {
+template <bool Q8>
+__global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX, const DownWeight W,
+                                                              __half* __restrict__ T, int Mt, int K,
+                                                              unsigned int* status) {
     extern __shared__ unsigned char lds_raw[];
     const uint32_t base_raw = smem_u32(lds_raw);
     const uint32_t sbase = (base_raw + 1023u) & ~1023u;  // 1024-aligned: swizzle atoms
@@ -301,13 +305,50 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
     int pc = 0;  // pieces consumed so far: piece pc is in buffer pc % kRBufs, its barrier's phase (pc / kRBufs) & 1
     for (int grp = blockIdx.x; ok && grp * kTok < Mt; grp += gridDim.x) {
         const int tokb = grp * kTok;
-        // issue the copies of K piece p into buffer b (A first: a weight, not behind the wait)
+        // INT8 A of piece p: this thread's kRQItems items of 16 codes (rank idx / 16, codes
+        // 16 (idx % 16) .. of the piece), loaded into registers, then dequantized (exact
+        // q - zp, one rounding) into the rank-major tile [32][kRPitchR] of buffer b
+        uint4 qv[kRQItems];
+        uint32_t qs[kRQItems], qz[kRQItems];
+        auto q8_load = [&](int p) {
+            const int kb = p * kRPiece, nblk = K / 32;
+#pragma unroll
+            for (int j = 0; j < kRQItems; ++j) {
+                const int idx = j * 128 + tid, r = idx >> 4, c = idx & 15;
+                const int b = r * nblk + (kb + 16 * c) / 32;
+                qv[j] = __ldg(reinterpret_cast<const uint4*>(W.Aq + (size_t)r * K + kb + 16 * c));
+                qs[j] = reinterpret_cast<const uint16_t*>(W.As)[b];
+                qz[j] = W.Az ? (uint32_t)W.Az[b] : 128u;
+            }
+        };
+        auto q8_store = [&](int b) {
+            __half* a_s = abuf(b);
+#pragma unroll
+            for (int j = 0; j < kRQItems; ++j) {
+                const int idx = j * 128 + tid, r = idx >> 4, c = idx & 15;
+                const DqConst dc = dq_const(qz[j], (uint16_t)qs[j]);
+                uint32_t d[8];
+                dq_int8_natural(qv[j].x, dc, &d[0]);
+                dq_int8_natural(qv[j].y, dc, &d[2]);
+                dq_int8_natural(qv[j].z, dc, &d[4]);
+                dq_int8_natural(qv[j].w, dc, &d[6]);
+                uint4* dst = reinterpret_cast<uint4*>(a_s + r * kRPitchR + 16 * c);
+                dst[0] = make_uint4(d[0], d[1], d[2], d[3]);
+                dst[1] = make_uint4(d[4], d[5], d[6], d[7]);
+            }
+        };
+        // issue the copies of K piece p into buffer b (A first: a weight, not behind the
+        // wait; INT8 A only loaded here, dequantized by q8_store)
         auto stage = [&](int p, int b) {
             const int kb = p * kRPiece;
-            __half* a_s = abuf(b);
-            for (int idx = tid; idx < kRPiece * 4; idx += blockDim.x) {
-                const int row = idx >> 2, c = idx & 3;
-                cp_async16(smem_u32(a_s + row * kPitchA + c * 8), A + (size_t)(kb + row) * 32 + c * 8, 16);
+            if constexpr (Q8) {
+                q8_load(p);
+            } else {
+                __half* a_s = abuf(b);
+                for (int idx = tid; idx < kRPiece * 4; idx += blockDim.x) {
+                    const int row = idx >> 2, c = idx & 3;
+                    cp_async16(smem_u32(a_s + row * kPitchA + c * 8), W.A + (size_t)(kb + row) * 32 + c * 8, 16);
+                }
             }
             asm volatile("cp.async.commit_group;" ::: "memory");
             if (!waited) {
@@ -328,12 +369,17 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-        for (int p = 0; p < kRBufs - 1 && p < npiece; ++p) stage(p, (pc + p) % kRBufs);
+        for (int p = 0; p < kRBufs - 1 && p < npiece; ++p) {
+            stage(p, (pc + p) % kRBufs);
+            if constexpr (Q8) q8_store((pc + p) % kRBufs);
+        }
+        if constexpr (Q8) __syncthreads();  // the prologue's dequantized A
         for (int p = 0; p < npiece; ++p, ++pc) {
             const int b = pc % kRBufs;
             // the buffer of piece p + 3 was last read by piece p - 1 (the block passed the
             // barrier at the end of that piece)
-            if (p + kRBufs - 1 < npiece) stage(p + kRBufs - 1, (pc + kRBufs - 1) % kRBufs);
+            const bool ahead3 = p + kRBufs - 1 < npiece;
+            if (ahead3) stage(p + kRBufs - 1, (pc + kRBufs - 1) % kRBufs);
             // A of piece p has landed once at most the groups committed after it are pending
             const int ahead = min(kRBufs - 1, npiece - 1 - p);
             if (ahead >= 3)
@@ -359,12 +405,20 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(smem_u32(a_s + (kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8), b0, b1,
-                              b2, b3);
+                    if constexpr (Q8)  // rank rows h*16 .. +15, K columns kk .. kk+15
+                        ldsm_x4(smem_u32(a_s + (h * 16 + (mat >> 1) * 8 + row8) * kRPitchR + kk + (mat & 1) * 8), b0,
+                                b1, b2, b3);
+                    else
+                        ldsm_x4_t(smem_u32(a_s + (kk + (mat & 1) * 8 + row8) * kPitchA + h * 16 + (mat >> 1) * 8), b0,
+                                  b1, b2, b3);
                     mma_16816(acc[2 * h], a0, a1, a2, a3, b0, b1);
                     mma_16816(acc[2 * h + 1], a0, a1, a2, a3, b2, b3);
                 }
             }
+            // INT8 A of piece p + 3, loaded before this piece's MMAs, into the buffer piece
+            // p - 1 left (read by every thread before the block passed the last barrier)
+            if constexpr (Q8)
+                if (ahead3) q8_store((pc + kRBufs - 1) % kRBufs);
             __syncthreads();  // this buffer is refilled kRBufs - 1 pieces on
         }
         if (!ok) break;
@@ -392,7 +446,9 @@ cudaError_t lora_down_prepare() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(lora_down_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLoraSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(lora_down_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem);
+        e = cudaFuncSetAttribute(lora_down_rows_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lora_down_rows_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsSmem);
     return e;
 }
 
@@ -424,31 +480,47 @@ cudaError_t launch_down(const __half* X, const DownWeight& W, bool q8, __half* T
 
 }  // namespace
 
+namespace {
+
+// The rows kernel on at most max_ctas SMs (the caller checked Mt > 16, K % kRPiece == 0).
+cudaError_t launch_rows(const __half* X, const DownWeight& W, bool q8, __half* T, int Mt, int K, bool pdl,
+                        int max_ctas, unsigned int* status, cudaStream_t st) {
+    CUtensorMap tx;  // X [Mt x K] FP16, boxes of 64 rows x 64 K, 128-byte swizzle
+    cudaError_t e = encode_2d(&tx, X, 2, (uint64_t)K, (uint64_t)Mt, (uint64_t)K * 2, 64u, (uint32_t)kTok, true);
+    if (e != cudaSuccess) return e;
+    const int groups = (Mt + kTok - 1) / kTok;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups < max_ctas ? groups : max_ctas);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kRowsSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return q8 ? cudaLaunchKernelEx(&cfg, lora_down_rows_kernel<true>, tx, W, T, Mt, K, status)
+              : cudaLaunchKernelEx(&cfg, lora_down_rows_kernel<false>, tx, W, T, Mt, K, status);
+}
+
+bool use_rows(int max_ctas, const unsigned int* status, int Mt, int K) {
+    return max_ctas > 0 && status && Mt > 16 && K % kRPiece == 0;
+}
+
+}  // namespace
+
 cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st,
                              int max_ctas, unsigned int* status) {
-    if (max_ctas > 0 && status && Mt > 16 && K % kRPiece == 0) {  // the rows kernel on at most max_ctas SMs
-        CUtensorMap tx;  // X [Mt x K] FP16, boxes of 64 rows x 64 K, 128-byte swizzle
-        cudaError_t e = encode_2d(&tx, X, 2, (uint64_t)K, (uint64_t)Mt, (uint64_t)K * 2, 64u, (uint32_t)kTok, true);
-        if (e != cudaSuccess) return e;
-        const int groups = (Mt + kTok - 1) / kTok;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(groups < max_ctas ? groups : max_ctas);
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = kRowsSmem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = pdl ? 1 : 0;
-        return cudaLaunchKernelEx(&cfg, lora_down_rows_kernel, tx, A, T, Mt, K, status);
-    }
-    return launch_down(X, DownWeight{A, nullptr, nullptr, nullptr}, false, T, Mt, K, pdl, st);
+    const DownWeight W{A, nullptr, nullptr, nullptr};
+    if (use_rows(max_ctas, status, Mt, K)) return launch_rows(X, W, false, T, Mt, K, pdl, max_ctas, status, st);
+    return launch_down(X, W, false, T, Mt, K, pdl, st);
 }
 
 cudaError_t lora_down_q8_launch(const __half* X, const uint8_t* Aq, const __half* As, const uint8_t* Az, __half* T,
-                                int Mt, int K, bool pdl, cudaStream_t st) {
-    return launch_down(X, DownWeight{nullptr, Aq, As, Az}, true, T, Mt, K, pdl, st);
+                                int Mt, int K, bool pdl, cudaStream_t st, int max_ctas, unsigned int* status) {
+    const DownWeight W{nullptr, Aq, As, Az};
+    if (use_rows(max_ctas, status, Mt, K)) return launch_rows(X, W, true, T, Mt, K, pdl, max_ctas, status, st);
+    return launch_down(X, W, true, T, Mt, K, pdl, st);
 }
 
 }  // namespace mnb

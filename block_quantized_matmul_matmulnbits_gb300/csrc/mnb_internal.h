@@ -138,13 +138,14 @@ cudaError_t decode_mt_launch(const DecodeArgs& a, int sms, bool pdl, cudaStream_
 cudaError_t lora_down_prepare();
 // max_ctas > 0 (Mt > 16, K % 256 == 0, a status word for its bounded waits): at most
 // that many CTAs and no cluster, each taking all of K for its token rows, so that they
-// fit on the SMs a following prefill kernel leaves idle.
+// fit on the SMs a following prefill kernel leaves idle (both down-weight formats).
 cudaError_t lora_down_launch(const __half* X, const __half* A, __half* T, int Mt, int K, bool pdl, cudaStream_t st,
                              int max_ctas = 0, unsigned int* status = nullptr);
 // The same with an INT8 down weight: Aq [32, K] (block-32 rows along K), As / Az [32, K/32]
 // (Az nullptr: 128); A[k, r] = fp16((Aq[r, k] - zp) * scale).
 cudaError_t lora_down_q8_launch(const __half* X, const uint8_t* Aq, const __half* As, const uint8_t* Az, __half* T,
-                                int Mt, int K, bool pdl, cudaStream_t st);
+                                int Mt, int K, bool pdl, cudaStream_t st, int max_ctas = 0,
+                                unsigned int* status = nullptr);
 
 struct GemmArgs {
     const __half* X;

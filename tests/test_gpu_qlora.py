@@ -181,3 +181,40 @@ def test_qlora_empty_adapter_is_base_bitwise(env):
     finally:
         mnb.mnb_destroy(h)
     assert torch.equal(Y0, Y1)
+
+
+def test_qlora_down_on_idle_sms_exact_bitwise(env):
+    """A one-wave prefill grid (80 weight tiles) leaves SMs idle: the INT8 down weight's
+    projection runs there, each CTA dequantizing the adapter codes of a K piece while it
+    multiplies the one before.  Exact arithmetic: T and Y match the oracle bit for bit."""
+    torch, mnb = env
+    rng = np.random.default_rng(960)
+    M, K, N = 100, 1024, 10240
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    h = mnb.mnb_create(N, K, 4, 32, 32)
+    try:
+        p = mnb.mnb_plan(h, 1, M, 32, sms)
+    finally:
+        mnb.mnb_destroy(h)
+    assert p["route"] == mnb.ROUTE_GEMM and p["k_splits"] <= 1 and sms - p["grid_x"] >= 8
+    x = np.zeros((1, M, K))
+    for m in range(M):
+        idx = rng.choice(K, 8, replace=False)
+        x[0, m, idx] = rng.choice([-1.0, 1.0], 8)
+    inp = synth.make_inputs(M=M, K=K, N=N, bits=4, seed=960, zp_range=(0, 15))
+    inp.X = x.astype(np.float16).view(np.uint16)
+    inp.scales = np.ldexp(1.0, rng.integers(-8, -4, size=(N, K // 32))).astype(np.float16).view(np.uint16)
+    ql = synth.make_qlora(K=K, N=N, seed=961)
+    ql.Aq = (ql.A_zp[:, :, None] + rng.integers(-3, 4, size=ql.Aq.shape)).astype(np.uint8)
+    ql.Bq = (ql.B_zp[:, :, None] + rng.integers(-3, 4, size=ql.Bq.shape)).astype(np.uint8)
+    ql.A_scales = np.full(ql.A_scales.shape, 0x2C00, np.uint16)  # 1/16
+    ql.B_scales = np.full(ql.B_scales.shape, 0x2C00, np.uint16)
+    Y, T, route = run_qlora_gpu(mnb, torch, inp, ql)
+    assert route == mnb.ROUTE_GEMM
+    Y16, _, _ = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq,
+                                 ql.B_scales, ql.B_zp, N, K, 4)
+    assert np.array_equal(bits_of(Y).reshape(M, N), Y16)
+    a16 = oracle.dequant_f16(ql.Aq, ql.A_scales, ql.A_zp, 32, K, 8)
+    T64 = oracle.lora_down(inp.X2d, np.ascontiguousarray(a16.T))
+    got = bits_of(T).view(np.float16).astype(np.float64).reshape(M, 32)
+    assert np.array_equal(got, T64)
