@@ -275,14 +275,16 @@ constexpr int kRXBytes = kTok * kRPiece * 2;          // X of a piece: 4 boxes o
 constexpr int kRABytes = kRPiece * kPitchA * 2;       // A of a piece, padded rows
 constexpr int kRPitchR = kRPiece + 8;                 // INT8 A: halfs per dequantized rank row of a piece
 static_assert(32 * kRPitchR * 2 <= kRABytes, "a dequantized INT8 A piece fits the FP16 one's space");
-constexpr int kRQItems = 32 * kRPiece / 16 / 128;     // INT8 A: 16-code items per thread and piece
+constexpr int kRThreads = 256;                        // 8 warps: 4 row tiles x 2 halves of a piece's K
+constexpr int kRQItems = 32 * kRPiece / 16 / kRThreads;  // INT8 A: 16-code items per thread and piece
 constexpr int kRBuf = kRXBytes + kRABytes;
 static_assert(kRABytes % 1024 == 0, "the next buffer's X boxes stay 1024-aligned");
 constexpr int kRBufs = 4;                             // ring of K pieces
-constexpr int kRowsSmem = kRBufs * kRBuf + 64 + 1024;  // buffers, barriers, alignment
+constexpr int kRRed = 4 * 32 * 16 * 4;                // the second K half's accumulators, [row tile][lane][16]
+constexpr int kRowsSmem = kRBufs * kRBuf + 64 + kRRed + 1024;  // buffers, barriers, reduction, alignment
 
 template <bool Q8>
-__global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX, const DownWeight W,
+__global__ void __launch_bounds__(kRThreads) lora_down_rows_kernel(const __grid_constant__ CUtensorMap tmX, const DownWeight W,
                                                               __half* __restrict__ T, int Mt, int K,
                                                               unsigned int* status) {
     extern __shared__ unsigned char lds_raw[];
@@ -293,7 +295,9 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
     auto xbuf = [&](int b) { return sbase + (uint32_t)(b * kRBuf); };
     auto abuf = [&](int b) { return reinterpret_cast<__half*>(sptr + b * kRBuf + kRXBytes); };
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int wrow = warp * 16;  // this warp's 16 token rows of the group
+    const int wrow = (warp & 3) * 16;  // this warp's 16 token rows of the group
+    const int kh = warp >> 2;          // and its half of every piece's K
+    float* red = reinterpret_cast<float*>(sptr + kRBufs * kRBuf + 64);
     const int npiece = K / kRPiece;
     if (tid == 0) {
         for (int b = 0; b < kRBufs; ++b) mbar_init(bars + 8u * (uint32_t)b, 1);
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
             const int kb = p * kRPiece, nblk = K / 32;
 #pragma unroll
             for (int j = 0; j < kRQItems; ++j) {
-                const int idx = j * 128 + tid, r = idx >> 4, c = idx & 15;
+                const int idx = j * kRThreads + tid, r = idx >> 4, c = idx & 15;
                 const int b = r * nblk + (kb + 16 * c) / 32;
                 qv[j] = __ldg(reinterpret_cast<const uint4*>(W.Aq + (size_t)r * K + kb + 16 * c));
                 qs[j] = reinterpret_cast<const uint16_t*>(W.As)[b];
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
             __half* a_s = abuf(b);
 #pragma unroll
             for (int j = 0; j < kRQItems; ++j) {
-                const int idx = j * 128 + tid, r = idx >> 4, c = idx & 15;
+                const int idx = j * kRThreads + tid, r = idx >> 4, c = idx & 15;
                 const DqConst dc = dq_const(qz[j], (uint16_t)qs[j]);
                 uint32_t d[8];
                 dq_int8_natural(qv[j].x, dc, &d[0]);
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
             const int mat = lane >> 3, row8 = lane & 7;
             const int xr = wrow + (mat & 1) * 8 + row8;  // this lane's X row for ldmatrix
 #pragma unroll 4
-            for (int kk = 0; kk < kRPiece; kk += 16) {
+            for (int kk = kh * (kRPiece / 2); kk < (kh + 1) * (kRPiece / 2); kk += 16) {
                 uint32_t a0, a1, a2, a3;  // X rows wrow .. +15, K columns kk .. kk+15 (box kk / 64, swizzled)
                 const int chunk = ((kk & 63) >> 3) + (mat >> 1);
                 ldsm_x4(xbuf(b) + (uint32_t)((kk >> 6) * kTok * 128 + xr * 128 + ((chunk ^ (xr & 7)) << 4)), a0, a1,
@@ -422,6 +426,19 @@ __global__ void __launch_bounds__(128) lora_down_rows_kernel(const __grid_consta
             __syncthreads();  // this buffer is refilled kRBufs - 1 pieces on
         }
         if (!ok) break;
+        // the second K halves' sums to the first halves' warps, added in that order
+        if (kh == 1) {
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) red[((warp & 3) * 32 + lane) * 16 + nt * 4 + e] = acc[nt][e];
+        }
+        __syncthreads();
+        if (kh == 1) continue;  // (the next group's first barrier waits for the readers below)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] += red[((warp & 3) * 32 + lane) * 16 + nt * 4 + e];
         const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
@@ -491,7 +508,7 @@ cudaError_t launch_rows(const __half* X, const DownWeight& W, bool q8, __half* T
     const int groups = (Mt + kTok - 1) / kTok;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(groups < max_ctas ? groups : max_ctas);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(kRThreads);
     cfg.dynamicSmemBytes = kRowsSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
