@@ -137,11 +137,13 @@ void plan_decode_mt(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
 
 // Which decode kernel streams the weights of a decode-route call: the
 // single-token kernel, the kernel for 2 .. 16 token rows, or (0) the general
-// multi-token kernel.  fused_ok: FP16 or no adapter, FP16 activations.
+// multi-token kernel.  fused_ok: FP16 activations; q8_adapter: an INT8 adapter
+// (the single-token kernel takes it, the kernel for 2 .. 16 rows does not).
 enum { kDecGeneral = 0, kDecSingle = 1, kDecMulti = 2 };
-int decode_kind(const mnb_desc& d, int64_t Mt, int rank, int sms, bool fused_ok) {
+int decode_kind(const mnb_desc& d, int64_t Mt, int rank, int sms, bool fused_ok, bool q8_adapter = false) {
     if (!fused_ok) return kDecGeneral;
     if (mnb::decode_supported(d.bits, Mt, (int)d.K, d.N, rank > 0, sms)) return kDecSingle;
+    if (rank > 0 && q8_adapter) return kDecGeneral;
     if (mnb::decode_mt_supported(d.bits, Mt, (int)d.K, rank > 0)) return kDecMulti;
     return kDecGeneral;
 }
@@ -180,7 +182,7 @@ void plan_gemm(const mnb_desc& d, int64_t Mt, int sms, mnb_plan_info* p) {
 // fused_ok: the call's variant can run on the single-token decode kernel (FP16 or
 // no adapter, FP16 activations, one projection).
 int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mnb_plan_info* p,
-              bool fused_ok = true) {
+              bool fused_ok = true, bool q8_adapter = false) {
     *p = mnb_plan_info{};
     const int64_t Mt = batch * M;
     if (Mt == 0 || d.N == 0) {
@@ -196,7 +198,7 @@ int make_plan(const mnb_desc& d, int64_t batch, int64_t M, int rank, int sms, mn
     if (d.mode == MNB_MODE_FORCE_GEMV) route = MNB_ROUTE_GEMV;
     if (d.mode == MNB_MODE_FORCE_GEMM) route = MNB_ROUTE_GEMM;
     if (route == MNB_ROUTE_GEMV) {
-        const int kind = decode_kind(d, Mt, rank, sms, fused_ok);
+        const int kind = decode_kind(d, Mt, rank, sms, fused_ok, q8_adapter);
         if (kind == kDecSingle) {
             plan_decode(d, rank, sms, p);
             return MNB_OK;
@@ -318,7 +320,7 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
             T_ws = Tfix;
         }
     }
-    make_plan(d, batch, M, rank, sms, &p, !q8x && !(rank > 0 && ad.q8));
+    make_plan(d, batch, M, rank, sms, &p, !q8x, rank > 0 && ad.q8);
     if (q8x && (p.route == MNB_ROUTE_GEMV || p.route == MNB_ROUTE_GEMM)) {
         plan_gemv(d, Mt, sms, &p);  // integer dots on the decode kernel, 8-token tiles
         p.tokens_per_cta = 8;
@@ -363,7 +365,7 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
     // LoRA down kernel lets the matmul kernel start only after its own wait,
     // so behind it the matmul kernel reads X at once and waits only for T.
     const bool early = (d.flags & MNB_FLAG_EARLY_WEIGHTS) != 0;
-    const int kind = p.route == MNB_ROUTE_GEMV ? decode_kind(d, Mt, rank, sms, !q8x && !(rank > 0 && ad.q8)) : kDecGeneral;
+    const int kind = p.route == MNB_ROUTE_GEMV ? decode_kind(d, Mt, rank, sms, !q8x, rank > 0 && ad.q8) : kDecGeneral;
     if (kind != kDecGeneral) {
         // one launch: the single-token decode kernel (base and adapter), or the
         // decode kernel for 2 .. 16 token rows (behind the LoRA down kernel with an
@@ -379,8 +381,16 @@ int run_impl(mnb_handle h, const void* X, const void* Wq, const void* scales, co
         a.seg[0] = mnb::DecSeg{0, (int)d.N, static_cast<const uint8_t*>(Wq), static_cast<const __half*>(scales),
                                static_cast<const uint8_t*>(zp), biash, static_cast<__half*>(Y)};
         a.X = Xh;
-        a.A = rank > 0 ? static_cast<const __half*>(ad.A) : nullptr;
-        a.B = rank > 0 ? static_cast<const __half*>(ad.B) : nullptr;
+        a.A = rank > 0 && !ad.q8 ? static_cast<const __half*>(ad.A) : nullptr;
+        a.B = rank > 0 && !ad.q8 ? static_cast<const __half*>(ad.B) : nullptr;
+        if (rank > 0 && ad.q8) {  // INT8 adapter: single-token kernel only
+            a.Aq = static_cast<const uint8_t*>(ad.Aq);
+            a.As = static_cast<const __half*>(ad.As);
+            a.Az = static_cast<const uint8_t*>(ad.Az);
+            a.Bq = Bq8;
+            a.Bs = Bs8;
+            a.Bz = Bz8;
+        }
         a.T = rank > 0 ? Th : nullptr;
         a.K = (int)d.K;
         a.bits = d.bits;

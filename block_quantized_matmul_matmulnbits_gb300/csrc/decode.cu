@@ -132,11 +132,14 @@ __host__ __device__ inline int dec_half(int rs) { return (rs + 1) / 2; }
 // term and the base sum of each row [lrows] FP32, and T [32] FP16.
 struct DecLayout {
     uint32_t r1, sc, zp, slot;  // offsets inside a slot (second code region, scales, zero points), slot bytes
-    uint32_t xs, sxs, red, bown, lorb, ybuf, t16, bars, total;
+    uint32_t xs, sxs, red, bown, lorb, ybuf, t16, braw, astg, bars, total;
 };
 
+// lq8: an INT8 adapter, whose B rows' codes [lrows][32] (then each row's scale and zero
+// point as one word [lrows]) land in braw before they are dequantized into bown, and
+// whose A slice is dequantized into astg [64][32] (k-major).
 __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int bits, int rowbytes, int nblk, int nblkR,
-                                                int lrows) {
+                                                int lrows, bool lq8 = false) {
     const DecPitch P = dec_pitch(nblk);
     DecLayout L;
     const uint32_t half = (uint32_t)(SR / 2) * (uint32_t)rowbytes;
@@ -161,6 +164,10 @@ __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int bits, int 
     off += (uint32_t)lrows * 4u;
     L.t16 = off;
     off += lrows > 0 ? kRk * 2u : 0u;
+    L.braw = al128(off);
+    off = L.braw + (lq8 ? (uint32_t)lrows * 36u : 0u);
+    L.astg = al128(off);
+    off = L.astg + (lq8 ? 64u * kRk * 2u : 0u);
     L.bars = al128(off);
     L.total = L.bars + (2u * (uint32_t)ring + 2u) * 8u;  // full and empty per slot, then B rows and adapter done
     return L;
@@ -189,7 +196,22 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-template <int BITS, bool HAS_ZP, bool LORA>
+// The adapter's FP16 A pair (A[k][c], A[k][c + 1]) from the INT8 down weight Aq [32, K]
+// (rank rows, block-32 along K): each value fp16((q - zp) * scale), rounded once.
+__device__ __forceinline__ uint32_t q8_apair(const DecodeArgs& a, int k, int c) {
+    const int nblk = a.K >> 5;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int r = c + e, b = r * nblk + (k >> 5);
+        const int q = (int)a.Aq[(size_t)r * a.K + k], zp = a.Az ? (int)a.Az[b] : 128;
+        const __half v = __hmul(__int2half_rn(q - zp), __ushort_as_half(reinterpret_cast<const uint16_t*>(a.As)[b]));
+        w |= (uint32_t)__half_as_ushort(v) << (16 * e);
+    }
+    return w;
+}
+
+template <int BITS, bool HAS_ZP, bool LORA, bool Q8L>
 __global__ void __launch_bounds__(dec_threads(LORA), 2)
     decode_kernel(const __grid_constant__ DecMaps maps, const __grid_constant__ DecodeArgs a) {
     using U = Unpack<BITS>;
@@ -204,7 +226,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     const int rowbytes = K * BITS / 8;
     const int SR = a.SR, ring = a.ring;
     const int C = gridDim.x;
-    const DecLayout L = dec_layout(SR, ring, BITS, rowbytes, nblk, nblkR, LORA ? lora_rows(NR, C) : 0);
+    const DecLayout L = dec_layout(SR, ring, BITS, rowbytes, nblk, nblkR, LORA ? lora_rows(NR, C) : 0, Q8L);
     const DecPitch P = dec_pitch(nblk);
     const uint32_t sb = smem_u32(sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,8 +326,21 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
             const int g = lane >> 2, t = lane & 3;
             const int nrows = r1 - r0;
             if (lane == 0 && nrows > 0) {
-                mbar_arrive_tx(bbar, (uint32_t)nrows * 64u);
-                bulk_load(sb + L.bown, a.B + (size_t)r0 * kRk, (uint32_t)nrows * 64u, bbar);
+                if constexpr (Q8L) {  // the rows' INT8 codes, dequantized into B rows once T is under way
+                    mbar_arrive_tx(bbar, (uint32_t)nrows * 32u);
+                    bulk_load(sb + L.braw, a.Bq + (size_t)r0 * kRk, (uint32_t)nrows * 32u, bbar);
+                } else {
+                    mbar_arrive_tx(bbar, (uint32_t)nrows * 64u);
+                    bulk_load(sb + L.bown, a.B + (size_t)r0 * kRk, (uint32_t)nrows * 64u, bbar);
+                }
+            }
+            if constexpr (Q8L) {  // each B row's scale and zero point, read while nothing waits on them
+                uint32_t* bsz = reinterpret_cast<uint32_t*>(sm + L.braw + (uint32_t)lora_rows(NR, C) * 32u);
+                for (int rr = lane; rr < nrows; rr += 32) {
+                    const int n = r0 + rr;
+                    bsz[rr] = (uint32_t)reinterpret_cast<const uint16_t*>(a.Bs)[n] |
+                              ((a.Bz ? (uint32_t)a.Bz[n] : 128u) << 16);
+                }
             }
             // K steps (16 wide) [c S / C, (c + 1) S / C) of CTA c.  A step is 2 K
             // sub-blocks x 4 rank sub-blocks of 8 x 8, each loaded in its natural
@@ -316,12 +351,49 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
             const int step0 = (int)((long long)blockIdx.x * S / C);
             const int nsteps = (int)((long long)(blockIdx.x + 1) * S / C) - step0;
             uint32_t areg[kMaxSteps][8];
+            if constexpr (Q8L) {
+                // lane r: rank r's codes of the first kMaxSteps steps (16-byte loads, all in
+                // flight together), dequantized into the k-major FP16 tile astg
+                __half* ast = reinterpret_cast<__half*>(sm + L.astg);
+                const int k_lo = step0 * 16, ns = nsteps < kMaxSteps ? nsteps : kMaxSteps;
+                uint4 qv[kMaxSteps];
+                uint32_t qs[kMaxSteps], qz[kMaxSteps];
+#pragma unroll
+                for (int i = 0; i < kMaxSteps; ++i) {
+                    const int k = k_lo + 16 * (i < ns ? i : 0), b = lane * (K >> 5) + (k >> 5);
+                    qv[i] = __ldg(reinterpret_cast<const uint4*>(a.Aq + (size_t)lane * K + k));
+                    qs[i] = reinterpret_cast<const uint16_t*>(a.As)[b];
+                    qz[i] = a.Az ? (uint32_t)a.Az[b] : 128u;
+                }
+#pragma unroll
+                for (int i = 0; i < kMaxSteps; ++i) {
+                    if (i >= ns) break;
+                    const DqConst dc = dq_const(qz[i], (uint16_t)qs[i]);
+                    const uint32_t wv[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        uint32_t d[2];
+                        dq_int8_natural(wv[w], dc, d);  // codes 4w .. 4w+3 of the step
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            ast[(i * 16 + 4 * w + e) * kRk + lane] =
+                                __ushort_as_half((uint16_t)(d[e >> 1] >> (16 * (e & 1))));
+                    }
+                }
+                __syncwarp();
+            }
 #pragma unroll
             for (int i = 0; i < kMaxSteps; ++i)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int kk = (step0 + i) * 16 + (j >> 2) * 8 + g;
-                    areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
+                    if constexpr (Q8L)
+                        areg[i][j] = i < nsteps ? *reinterpret_cast<const uint32_t*>(
+                                                      reinterpret_cast<const __half*>(sm + L.astg) +
+                                                      (i * 16 + (j >> 2) * 8 + g) * kRk + (j & 3) * 8 + 2 * t)
+                                                : 0u;
+                    else
+                        areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
                 }
             // The area's generation: its last writer is the launch before this one on the
             // area (kExSlots launches back), finished before this one starts.
@@ -355,7 +427,10 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
                             bfr[j] = areg[i][j];
                         } else {
                             const int kk = (step0 + i0 + i) * 16 + (j >> 2) * 8 + g;
-                            bfr[j] = __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t));
+                            if constexpr (Q8L)
+                                bfr[j] = q8_apair(a, kk, (j & 3) * 8 + 2 * t);
+                            else
+                                bfr[j] = __ldg(reinterpret_cast<const uint32_t*>(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t));
                         }
                         movmatrix_t(bfr[j]);
                     }
@@ -371,6 +446,26 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
 #pragma unroll
                     for (int e = 0; e < 2; ++e)
                         atomicAdd(&ex->acc[gs][8 * j + 2 * t + e][sub][0], ex_word(tacc[j][e]));
+            }
+            if constexpr (Q8L) {
+                // the B rows from their INT8 codes while the other CTAs' partials arrive:
+                // row n's 32 values fp16((q - zp) * scale) (one block a row), into bown
+                if (nrows > 0 && mbar_wait(bbar, 0u, status)) {
+                    const uint32_t* bsz = reinterpret_cast<const uint32_t*>(sm + L.braw + (uint32_t)lora_rows(NR, C) * 32u);
+                    for (int rr = lane; rr < nrows; rr += 32) {
+                        const uint4* src = reinterpret_cast<const uint4*>(sm + L.braw + (uint32_t)rr * 32u);
+                        const uint4 p0 = src[0], p1 = src[1];
+                        const DqConst dc = dq_const(bsz[rr] >> 16, (uint16_t)(bsz[rr] & 0xFFFFu));
+                        const uint32_t wv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                        uint32_t o[16];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) dq_int8_natural(wv[w], dc, &o[2 * w]);
+                        uint4* dst = reinterpret_cast<uint4*>(sm + L.bown + (uint32_t)rr * 64u);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    }
+                }
+                __syncwarp();
             }
             // T[lane] once every CTA has added its partial (bounded wait: the launch is
             // cooperative, so all of its CTAs are resident)
@@ -752,7 +847,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     }
 }
 
-template <int BITS, bool HAS_ZP, bool LORA>
+template <int BITS, bool HAS_ZP, bool LORA, bool Q8L = false>
 cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, size_t smem, bool pdl,
                            cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
@@ -774,7 +869,7 @@ cudaError_t dec_launch_one(const DecMaps& maps, const DecodeArgs& a, int ctas, s
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, HAS_ZP, LORA>, maps, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, HAS_ZP, LORA, Q8L>, maps, a);
 }
 
 constexpr int kMaxDev = 64;
@@ -799,7 +894,8 @@ bool decode_supported(int bits, int64_t Mt, int K, int64_t N, bool lora, int sms
     return true;
 }
 
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem) {
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem,
+                     bool lq8) {
     const int C = dec_ctas(N, sms);
     const int nblk = K / 32, nround = (nblk + kBlkPerRound - 1) / kBlkPerRound, nblkR = nround * kBlkPerRound;
     const int rowbytes = K * bits / 8;
@@ -812,32 +908,36 @@ void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int*
     constexpr uint32_t kHalfSm = 112u * 1024u, kRing = 200u * 1024u;
     int sr = 16;
     while (sr < rmax) sr *= 2;
-    if (sr <= kMaxSR && dec_layout(sr, 1, bits, rowbytes, nblk, nblkR, lrows).total <= kHalfSm) {
+    if (sr <= kMaxSR && dec_layout(sr, 1, bits, rowbytes, nblk, nblkR, lrows, lq8).total <= kHalfSm) {
         *SR = sr;
         *ring = 1;
     } else {
         int sr2 = 16;
-        while (sr2 < 64 && dec_layout(sr2, 1, bits, rowbytes, nblk, nblkR, lrows).slot < 24u * 1024u) sr2 *= 2;
+        while (sr2 < 64 && dec_layout(sr2, 1, bits, rowbytes, nblk, nblkR, lrows, lq8).slot < 24u * 1024u) sr2 *= 2;
         int r = 1;
-        while (r < 16 && dec_layout(sr2, r + 1, bits, rowbytes, nblk, nblkR, lrows).total <= kRing) ++r;
+        while (r < 16 && dec_layout(sr2, r + 1, bits, rowbytes, nblk, nblkR, lrows, lq8).total <= kRing) ++r;
         *SR = sr2;
         *ring = r;
     }
     *ctas = C;
-    *smem = dec_layout(*SR, *ring, bits, rowbytes, nblk, nblkR, lrows).total;
+    *smem = dec_layout(*SR, *ring, bits, rowbytes, nblk, nblkR, lrows, lq8).total;
 }
 
 cudaError_t decode_prepare() {
     cudaError_t e = tensor_map_prepare();
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-#define MNB_DEC_SET(B, Z, L)                                                                                       \
-    if (e == cudaSuccess)                                                                                          \
-        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);  \
-    if (e == cudaSuccess) /* the largest carveout: two CTAs of up to ~112 KB per SM */                              \
-        e = cudaFuncSetAttribute(decode_kernel<B, Z, L>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    MNB_DEC_SET(4, false, false) MNB_DEC_SET(4, true, false) MNB_DEC_SET(4, false, true) MNB_DEC_SET(4, true, true)
-    MNB_DEC_SET(8, false, false) MNB_DEC_SET(8, true, false) MNB_DEC_SET(8, false, true) MNB_DEC_SET(8, true, true)
+#define MNB_DEC_SET(B, Z, L, Q)                                                                                    \
+    if (e == cudaSuccess)                                                                                            \
+        e = cudaFuncSetAttribute(decode_kernel<B, Z, L, Q>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024); \
+    if (e == cudaSuccess) /* the largest carveout: two CTAs of up to ~112 KB per SM */                                \
+        e = cudaFuncSetAttribute(decode_kernel<B, Z, L, Q>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    MNB_DEC_SET(4, false, false, false) MNB_DEC_SET(4, true, false, false)
+    MNB_DEC_SET(4, false, true, false) MNB_DEC_SET(4, true, true, false)
+    MNB_DEC_SET(4, false, true, true) MNB_DEC_SET(4, true, true, true)
+    MNB_DEC_SET(8, false, false, false) MNB_DEC_SET(8, true, false, false)
+    MNB_DEC_SET(8, false, true, false) MNB_DEC_SET(8, true, true, false)
+    MNB_DEC_SET(8, false, true, true) MNB_DEC_SET(8, true, true, true)
 #undef MNB_DEC_SET
     void* ex = nullptr;
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&ex, g_lora_ex);
@@ -856,7 +956,8 @@ cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, c
     int C, SR, ring;
     size_t smem;
     const int bits = a.bits;
-    decode_geometry(a.NR, a.K, bits, rank > 0, sms, &C, &SR, &ring, &smem);
+    const bool q8l = rank > 0 && a.Aq != nullptr;  // INT8 adapter
+    decode_geometry(a.NR, a.K, bits, rank > 0, sms, &C, &SR, &ring, &smem, q8l);
     if (smem > 227 * 1024) return cudaErrorNotSupported;
     a.SR = SR;
     a.ring = ring;
@@ -886,12 +987,18 @@ cudaError_t decode_launch(const DecodeArgs& a_in, int rank, int sms, bool pdl, c
         if (e != cudaSuccess) return e;
     }
     if (bits == 4) {
+        if (q8l)
+            return zp ? dec_launch_one<4, true, true, true>(maps, a, C, smem, pdl, st)
+                      : dec_launch_one<4, false, true, true>(maps, a, C, smem, pdl, st);
         if (lora)
             return zp ? dec_launch_one<4, true, true>(maps, a, C, smem, pdl, st)
                       : dec_launch_one<4, false, true>(maps, a, C, smem, pdl, st);
         return zp ? dec_launch_one<4, true, false>(maps, a, C, smem, pdl, st)
                   : dec_launch_one<4, false, false>(maps, a, C, smem, pdl, st);
     }
+    if (q8l)
+        return zp ? dec_launch_one<8, true, true, true>(maps, a, C, smem, pdl, st)
+                  : dec_launch_one<8, false, true, true>(maps, a, C, smem, pdl, st);
     if (lora)
         return zp ? dec_launch_one<8, true, true>(maps, a, C, smem, pdl, st)
                   : dec_launch_one<8, false, true>(maps, a, C, smem, pdl, st);

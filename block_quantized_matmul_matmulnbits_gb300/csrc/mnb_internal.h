@@ -100,8 +100,16 @@ struct DecodeArgs {
     DecSeg seg[kMaxSeg];
     const __half* X;     // [Mt, K]
     int Mt;              // token rows (1 for the single-token kernel)
-    const __half* A;     // [K, 32] (adapter only)
-    const __half* B;     // [N, 32] (adapter only)
+    const __half* A;     // [K, 32] (FP16 adapter)
+    const __half* B;     // [N, 32] (FP16 adapter)
+    // INT8 adapter (single-token kernel; A and B unused): Aq [32, K] with As / Az
+    // [32, K/32], Bq [N, 32] with Bs / Bz [N] (Az / Bz nullptr: 128)
+    const uint8_t* Aq;
+    const __half* As;
+    const uint8_t* Az;
+    const uint8_t* Bq;
+    const __half* Bs;
+    const uint8_t* Bz;
     __half* T;           // [1, 32]: T on return (adapter only)
     int K, bits;
     int SR, ring;        // rows per stage and stage slots (set by the launcher)
@@ -114,7 +122,9 @@ struct DecodeArgs {
 // with an adapter at most 256 rows per CTA (N rows over min(SMs, N / 16) CTAs).
 bool decode_supported(int bits, int64_t Mt, int K, int64_t N, bool lora, int sms);
 // CTAs, rows per stage, stage slots and shared memory of a launch.
-void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem);
+// lq8: an INT8 adapter (its B rows' codes staged before they are dequantized).
+void decode_geometry(int N, int K, int bits, bool lora, int sms, int* ctas, int* SR, int* ring, size_t* smem,
+                     bool lq8 = false);
 cudaError_t decode_prepare();
 // Clear the adapter exchange areas of the current device (after a device-side
 // timeout left one of them part way).

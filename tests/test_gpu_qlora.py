@@ -115,7 +115,7 @@ def test_qlora_4096_sampled_with_bias(env, M):
     assert_within_tolerance(got, Y64, bound, f"qlora 4096 M={M}")
 
 
-@pytest.mark.parametrize("M", [5, 300])
+@pytest.mark.parametrize("M", [1, 5, 300])
 def test_qlora_exact_arithmetic_bitwise(env, M):
     """Sparse {-1,0,1} X, power-of-two scales everywhere and adapter codes near
     their zero points: every value and partial sum is exact in FP16/FP32, so
@@ -135,11 +135,15 @@ def test_qlora_exact_arithmetic_bitwise(env, M):
     ql.Bq = (ql.B_zp[:, :, None] + rng.integers(-3, 4, size=ql.Bq.shape)).astype(np.uint8)
     ql.A_scales = np.full(ql.A_scales.shape, 0x2C00, np.uint16)  # 1/16
     ql.B_scales = np.full(ql.B_scales.shape, 0x2C00, np.uint16)
-    Y, _, route = run_qlora_gpu(mnb, torch, inp, ql)
+    Y, T, route = run_qlora_gpu(mnb, torch, inp, ql)
     assert route == (mnb.ROUTE_GEMV if M <= 16 else mnb.ROUTE_GEMM)
     Y16, _, _ = oracle.run_qlora(inp.X2d, inp.Wq, inp.scales, inp.zp, ql.Aq, ql.A_scales, ql.A_zp, ql.Bq,
                                  ql.B_scales, ql.B_zp, N, K, 4)
     assert np.array_equal(bits_of(Y).reshape(M, N), Y16)
+    if M == 1:  # the single-token kernel (adapter dequantized in its adapter warp): T exact too
+        a16 = oracle.dequant_f16(ql.Aq, ql.A_scales, ql.A_zp, 32, K, 8)
+        T64 = oracle.lora_down(inp.X2d, np.ascontiguousarray(a16.T))
+        assert np.array_equal(bits_of(T).view(np.float16).astype(np.float64).reshape(M, 32), T64)
 
 
 @pytest.mark.parametrize("M", [2, 64])
