@@ -42,7 +42,10 @@
 //    CTAs are resident together) each CTA adds the partials in CTA order, so
 //    T is bitwise reproducible, rounds T once to FP16 and forms
 //    sum_r T[r] B[n, r] for its rows (two MMAs per 16 rows) from a copy of
-//    its B rows.  The consumers keep each row's base sum in FP32 and add the
+//    its B rows.  An INT8 adapter (block-32 Aq [32, K], Bq [N, 32]) is
+//    dequantized by the same warp (exact q - zp, one rounding by the FP16
+//    scale): its A slice into a k-major FP16 tile before x arrives, its B rows
+//    while the other CTAs' partials of T arrive.  The consumers keep each row's base sum in FP32 and add the
 //    adapter term before the one rounding of the output, at the end.  No
 //    thread-block clusters: cluster placement put two CTAs of one launch on
 //    the same SM while others stayed idle.
