@@ -132,7 +132,8 @@ __host__ __device__ inline int dec_half(int rs) { return (rs + 1) / 2; }
 // [SR][spitch] and zero points [SR][zpitch]
 // (each + 32 bytes for the aligned superset of a bulk copy).  With an adapter
 // (lrows > 0): the CTA's adapter rows B[n, :] [lrows][32] FP16, the adapter
-// term and the base sum of each row [lrows] FP32, and T [32] FP16.
+// term and the base sum of each row [lrows] FP32, T [32] FP16, and the first
+// 64 K rows of the CTA's slice of A, astg [64][32] FP16 (k-major).
 struct DecLayout {
     uint32_t r1, sc, zp, slot;  // offsets inside a slot (second code region, scales, zero points), slot bytes
     uint32_t xs, sxs, red, bown, lorb, ybuf, t16, braw, astg, bars, total;
@@ -140,7 +141,7 @@ struct DecLayout {
 
 // lq8: an INT8 adapter, whose B rows' codes [lrows][32] (then each row's scale and zero
 // point as one word [lrows]) land in braw before they are dequantized into bown, and
-// whose A slice is dequantized into astg [64][32] (k-major).
+// whose A slice is dequantized into astg (an FP16 A slice is copied there as is).
 __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int bits, int rowbytes, int nblk, int nblkR,
                                                 int lrows, bool lq8 = false) {
     const DecPitch P = dec_pitch(nblk);
@@ -169,10 +170,11 @@ __host__ __device__ inline DecLayout dec_layout(int SR, int ring, int bits, int 
     off += lrows > 0 ? kRk * 2u : 0u;
     L.braw = al128(off);
     off = L.braw + (lq8 ? (uint32_t)lrows * 36u : 0u);
-    L.astg = al128(off);
-    off = L.astg + (lq8 ? 64u * kRk * 2u : 0u);
+    L.astg = al128(off);  // the adapter's first 64 K rows of A, k-major FP16
+    off = L.astg + (lrows > 0 ? 64u * kRk * 2u : 0u);
     L.bars = al128(off);
-    L.total = L.bars + (2u * (uint32_t)ring + 2u) * 8u;  // full and empty per slot, then B rows and adapter done
+    // full and empty per slot, then B rows, adapter done and the A slice
+    L.total = L.bars + (2u * (uint32_t)ring + 3u) * 8u;
     return L;
 }
 
@@ -240,6 +242,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
     auto empty = [&](int s) { return sb + L.bars + 8u * (uint32_t)(ring + s); };
     const uint32_t bbar = sb + L.bars + 16u * (uint32_t)ring;  // adapter: the CTA's B rows landed
     const uint32_t lready = bbar + 8u;                          // adapter: T B^T of the CTA's rows is in place
+    const uint32_t abar = bbar + 16u;                           // adapter (FP16 A): its slice of A landed
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ring; ++s) {
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
         if (LORA) {
             mbar_init(bbar, 1);
             mbar_init(lready, 1);
+            mbar_init(abar, 1);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -354,11 +358,24 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
             const int step0 = (int)((long long)blockIdx.x * S / C);
             const int nsteps = (int)((long long)(blockIdx.x + 1) * S / C) - step0;
             uint32_t areg[kMaxSteps][8];
+            const int ns = nsteps < kMaxSteps ? nsteps : kMaxSteps;  // steps staged in astg
+            bool a_ok = true;
+            if constexpr (!Q8L) {
+                // FP16 A: the slice's first ns steps (16 K rows of 32 ranks each, contiguous
+                // in A) in one bulk copy.  Per-lane 4-byte loads here were measured to slow
+                // the consumer warps of the previous call on the SM, whose rounds run
+                // while this CTA starts.
+                if (lane == 0 && ns > 0) {
+                    mbar_arrive_tx(abar, (uint32_t)ns * 16u * kRk * 2u);
+                    bulk_load(sb + L.astg, a.A + (size_t)step0 * 16 * kRk, (uint32_t)ns * 16u * kRk * 2u, abar);
+                }
+                a_ok = ns == 0 || mbar_wait(abar, 0u, status);
+            }
             if constexpr (Q8L) {
                 // lane r: rank r's codes of the first kMaxSteps steps (16-byte loads, all in
                 // flight together), dequantized into the k-major FP16 tile astg
                 __half* ast = reinterpret_cast<__half*>(sm + L.astg);
-                const int k_lo = step0 * 16, ns = nsteps < kMaxSteps ? nsteps : kMaxSteps;
+                const int k_lo = step0 * 16;
                 uint4 qv[kMaxSteps];
                 uint32_t qs[kMaxSteps], qz[kMaxSteps];
 #pragma unroll
@@ -388,16 +405,11 @@ __global__ void __launch_bounds__(dec_threads(LORA), 2)
 #pragma unroll
             for (int i = 0; i < kMaxSteps; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int kk = (step0 + i) * 16 + (j >> 2) * 8 + g;
-                    if constexpr (Q8L)
-                        areg[i][j] = i < nsteps ? *reinterpret_cast<const uint32_t*>(
+                for (int j = 0; j < 8; ++j)  // K row (j / 4) 8 + g of step i, ranks (j % 4) 8 + 2t, + 1
+                    areg[i][j] = i < ns && a_ok ? *reinterpret_cast<const uint32_t*>(
                                                       reinterpret_cast<const __half*>(sm + L.astg) +
                                                       (i * 16 + (j >> 2) * 8 + g) * kRk + (j & 3) * 8 + 2 * t)
                                                 : 0u;
-                    else
-                        areg[i][j] = i < nsteps ? ldg_nc_u32(a.A + (size_t)kk * kRk + (j & 3) * 8 + 2 * t) : 0u;
-                }
             // The area's generation: its last writer is the launch before this one on the
             // area (kExSlots launches back), finished before this one starts.
             LoraEx* ex = static_cast<LoraEx*>(a.ex);
