@@ -34,13 +34,14 @@
 //    its block, and applies the block's scale and zero point once, in FP32:
 //        y += s * (sum_k x q - zp * sum_k x).
 //  * The adapter runs on a warp of its own, beside the weight stream and the
-//    base dot products.  Every CTA takes an equal slice of K, holds its slice
-//    of A in registers (prefetched with the weights), forms the partial sums
-//    of T on the tensor cores (movmatrix turns A's rows into the MMA's K-major
-//    operand) and publishes them in global memory; after all CTAs of the
-//    launch have arrived (a counter; the launch is cooperative, so all of its
-//    CTAs are resident together) each CTA adds the partials in CTA order, so
-//    T is bitwise reproducible, rounds T once to FP16 and forms
+//    base dot products.  Every CTA takes an equal slice of K, copies its slice
+//    of A into shared memory with the weights (one bulk copy), forms the
+//    partial sums of T on the tensor cores (movmatrix turns A's rows into the
+//    MMA's K-major operand) and adds them to per-rank words in global memory
+//    as fixed-point integers with a count; once the counts show every CTA of
+//    the launch (the launch is cooperative, so all of its CTAs are resident
+//    together) each CTA reads T (integer sums: the same bits whatever the
+//    order of the additions), rounds T once to FP16 and forms
 //    sum_r T[r] B[n, r] for its rows (two MMAs per 16 rows) from a copy of
 //    its B rows.  An INT8 adapter (block-32 Aq [32, K], Bq [N, 32]) is
 //    dequantized by the same warp (exact q - zp, one rounding by the FP16
