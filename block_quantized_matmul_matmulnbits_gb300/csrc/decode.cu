@@ -90,8 +90,10 @@ __host__ __device__ constexpr int dec_threads(bool lora) { return (kCW + (lora ?
 // order of the additions, so T is the same bits on every run; a CTA knows a
 // rank is complete when the counts of its words add up to the CTAs of the
 // launch.  CTA 0 then clears the other generation (used by the launch before,
-// to be used by the next) and advances `gen`.
-constexpr int kExSub = 4;
+// to be used by the next) and advances `gen`.  Two words a rank: one makes the
+// adds to a word queue up (4.85 us per call at 4096 x 4096), more make every
+// poll read more (4.76 with four, 5.58 with eight, 4.72 to 4.74 with two).
+constexpr int kExSub = 2;
 struct LoraEx {
     unsigned int gen;
     unsigned int pad_[31];
